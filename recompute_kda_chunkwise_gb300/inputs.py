@@ -1,0 +1,111 @@
+"""Seeded synthetic inputs for KDA forward + backward.
+
+This module holds no arithmetic of the method: it only draws random tensors
+with the shapes, dtypes and distributions of the workloads measured in
+"KDA Memory with Recompute: FLA vs cuDNN Frontend FROST" (section "Sources and
+measurement configuration": D128, bf16 Q/K/V/raw gate/raw beta/dO, fp32
+A_log = dt_bias = 0, equal-length packed sequences) and the small fp32 preset
+of "KDA at the production shape ..." (section 2, b=10 t=512 h=12 K=V=64).
+Both the CUDA path and the oracle consume exactly these tensors.
+
+Recipe: a torch.Generator on the requested device, seeded with the workload's
+seed, draws in this fixed order: Q, K, V, raw gate, raw beta, dO (each in
+fp32, then cast to the workload dtype), then -- only when ``param_std`` > 0 --
+A_log and dt_bias (fp32). Otherwise A_log and dt_bias are zeros. The raw gate
+is N(gate_mean, gate_std); everything else is N(0, 1).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+
+import torch
+
+_DTYPES = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    lengths: tuple          # tokens per packed sequence
+    H: int
+    D: int
+    dtype: str = "bf16"    # "bf16" or "f32"
+    seed: int = 0
+    gate_mean: float = 0.0
+    gate_std: float = 1.0
+    param_std: float = 0.0  # std of A_log / dt_bias draws (0 -> zeros)
+    scale: float = 1.0
+    extra: dict = field(default_factory=dict, compare=False, hash=False)
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.lengths)
+
+    @property
+    def total_tokens(self) -> int:
+        return int(sum(self.lengths))
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+def _equal(n, t):
+    return tuple([t] * n)
+
+
+# The five workloads (seed = 20260 + index; the H sweep of workload 4 uses
+# sub-seeds 202641 and 202642).
+WORKLOADS = {
+    "tiny_t256_h2_d64_bf16": Workload("tiny_t256_h2_d64_bf16", _equal(1, 256), 2, 64, "bf16", 20261),
+    "b10_t512_h12_d64_f32": Workload("b10_t512_h12_d64_f32", _equal(10, 512), 12, 64, "f32", 20262),
+    "mbs8_8k_h16_d128_bf16": Workload("mbs8_8k_h16_d128_bf16", _equal(8, 8192), 16, 128, "bf16", 20263),
+    "mbs2_8k_h96_d128_bf16_gate2": Workload("mbs2_8k_h96_d128_bf16_gate2", _equal(2, 8192), 96, 128,
+                                            "bf16", 20264, gate_std=2.0),
+    "mbs1_8k_h64_d128_bf16_gate2": Workload("mbs1_8k_h64_d128_bf16_gate2", _equal(1, 8192), 64, 128,
+                                            "bf16", 202641, gate_std=2.0),
+    "mbs1_8k_h128_d128_bf16_gate2": Workload("mbs1_8k_h128_d128_bf16_gate2", _equal(1, 8192), 128, 128,
+                                             "bf16", 202642, gate_std=2.0),
+    "mbs1_128k_h96_d128_bf16": Workload("mbs1_128k_h96_d128_bf16", _equal(1, 131072), 96, 128,
+                                        "bf16", 20265),
+}
+HEADLINE = "mbs1_128k_h96_d128_bf16"
+
+
+def cu_seqlens_of(lengths, device="cpu") -> torch.Tensor:
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+    return torch.tensor(cu, dtype=torch.int32, device=device)
+
+
+def make_inputs(w: Workload, device="cpu", with_dO: bool = True) -> dict:
+    """Draw the workload's tensors on ``device`` (see the module recipe)."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(w.seed))
+    dt = _DTYPES[w.dtype]
+    S, H, D = w.total_tokens, w.H, w.D
+
+    def normal(shape, mean=0.0, std=1.0):
+        x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        if mean != 0.0:
+            x.add_(mean)
+        return x.to(dt)
+
+    out = {}
+    out["q"] = normal((S, H, D))
+    out["k"] = normal((S, H, D))
+    out["v"] = normal((S, H, D))
+    out["g"] = normal((S, H, D), w.gate_mean, w.gate_std)
+    out["beta"] = normal((S, H))
+    out["dO"] = normal((S, H, D)) if with_dO else None
+    if w.param_std > 0:
+        out["A_log"] = torch.randn((H,), generator=gen, device=dev) * w.param_std
+        out["dt_bias"] = torch.randn((H, D), generator=gen, device=dev) * w.param_std
+    else:
+        out["A_log"] = torch.zeros((H,), device=dev)
+        out["dt_bias"] = torch.zeros((H, D), device=dev)
+    out["cu_seqlens"] = cu_seqlens_of(w.lengths, dev)
+    return out

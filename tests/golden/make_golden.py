@@ -1,0 +1,47 @@
+"""Writes tests/golden/oracle_small.json by calling only the oracle.
+
+The pages print no worked numerical example for KDA, so this fixture is a
+regression record of the pinned oracle on a small seeded problem (two packed
+sequences of 5 and 11 tokens, H=2, D=8, nonzero A_log / dt_bias, scale 0.5).
+Run:  python tests/golden/make_golden.py
+"""
+import json
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+sys.path.insert(0, ROOT)
+import oracle  # noqa: E402
+
+
+def problem():
+    rng = np.random.default_rng(20260)
+    lengths = [5, 11]
+    S, H, D = sum(lengths), 2, 8
+    p = dict(q=rng.standard_normal((S, H, D)), k=rng.standard_normal((S, H, D)),
+             v=rng.standard_normal((S, H, D)), g=rng.standard_normal((S, H, D)),
+             beta=rng.standard_normal((S, H)), A_log=rng.standard_normal(H) * 0.5,
+             dt_bias=rng.standard_normal((H, D)) * 0.5, dO=rng.standard_normal((S, H, D)))
+    # store inputs rounded to float32 so the JSON round-trip is exact
+    p = {k: v.astype(np.float32).astype(np.float64) for k, v in p.items()}
+    p["cu_seqlens"] = [0, 5, 16]
+    return p
+
+
+def main():
+    p = problem()
+    out = oracle.kda_reference(p["q"], p["k"], p["v"], p["g"], p["beta"], p["A_log"],
+                               p["dt_bias"], p["cu_seqlens"], p["dO"], scale=0.5)
+    rec = {"inputs": {k: (v.tolist() if hasattr(v, "tolist") else v) for k, v in p.items()},
+           "scale": 0.5, "lower_bound": -5.0, "eps": 1e-6,
+           "outputs": {k: v.tolist() for k, v in out.items()}}
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "oracle_small.json")
+    with open(path, "w") as f:
+        json.dump(rec, f)
+    print("wrote", path)
+
+
+if __name__ == "__main__":
+    main()
