@@ -1,0 +1,376 @@
+"""KDA forward + backward benchmark (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}]
+                    [--workload NAME] [--e2e-steps E] [--no-cpu-baseline]
+
+A step is one kda_fwd + kda_bwd over the whole workload (every hot-path kernel
+runs once per step). Inputs are seeded synthetic tensors already resident in
+HBM; they total far more than the 129 MB L2, so no flush is needed between
+steps. The value is whole-job tokens/s (all ranks' tokens / max-over-ranks
+time). Under torchrun every rank runs an independent replica of the workload
+on its own GPU (weak scaling, no collective on the data path).
+
+--impl reference times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload per step (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA fwd+bwd tokens/sec at MBS1·128K·H96·D128; % HBM roofline; peak alloc GiB"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes(w):
+    """Bytes the method must move per step (token-head): the forward reads
+    q, k, v, raw gate, raw beta and writes o; the backward re-reads those
+    inputs, reads dO and writes dq, dk, dv, dg, dbeta. Gate parameters,
+    cu_seqlens and checkpoints are negligible / implementation overhead."""
+    e = 2 if w.dtype == "bf16" else 4
+    D = w.D
+    th = w.total_tokens * w.H
+    fwd = th * e * (5 * D + 1)       # q,k,v,g,o (D each) + beta
+    bwd = th * e * (9 * D + 2)       # q,k,v,g,dO + dq,dk,dv,dg (D each) + beta, dbeta
+    return fwd, bwd
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    csrc = os.path.join(ROOT, "recompute_kda_chunkwise_gb300", "csrc")
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json),
+    valid only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(kernel, {}).get(workload)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return float(ent["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = os.environ.get("KDA_BENCH_BACKEND", "nccl")
+    if backend == "nccl":
+        import torch
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, ws, local
+
+
+def max_over_ranks(x: float) -> float:
+    """Max of a host float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def oracle_sample(w, inp_cpu_slices, cores):
+    """Times the fp64 oracle on a bounded sample; returns token-heads/s."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.kda_reference(**inp_cpu_slices, threads=cores)
+    dt = time.perf_counter() - t0
+    th = inp_cpu_slices["q"].shape[0] * inp_cpu_slices["q"].shape[1]
+    return th / dt, dt
+
+
+def make_sample(w, inp, sample_tokens, sample_heads):
+    """First `sample_tokens` tokens of sequence 0 for the first `sample_heads`
+    heads, as CPU tensors, in the oracle's argument names."""
+    T = min(sample_tokens, w.lengths[0])
+    hs = slice(0, sample_heads)
+    cpu = lambda x: x.detach().to("cpu")
+    return dict(q=cpu(inp["q"][:T, hs]), k=cpu(inp["k"][:T, hs]), v=cpu(inp["v"][:T, hs]),
+                g=cpu(inp["g"][:T, hs]), beta=cpu(inp["beta"][:T, hs]), A_log=cpu(inp["A_log"][hs]),
+                dt_bias=cpu(inp["dt_bias"][hs]), cu_seqlens=[0, T], dO=cpu(inp["dO"][:T, hs]),
+                scale=w.scale)
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    import torch
+    from recompute_kda_chunkwise_gb300 import make_inputs
+    cores = os.cpu_count() or 1
+    heads = min(cores, w.H)
+    sample_tokens = args.sample_tokens
+    small = w.with_(lengths=(min(sample_tokens, w.lengths[0]),), H=heads)
+    inp = make_inputs(small, device="cpu")
+    sl = make_sample(small, inp, sample_tokens, heads)
+    for _ in range(args.warmup):
+        oracle_sample(w, sl, cores)
+    rates, times = [], []
+    for _ in range(args.steps):
+        r, dt = oracle_sample(w, sl, cores)
+        rates.append(r)
+        times.append(dt)
+    th_per_s = statistics.median(rates)
+    value = th_per_s / w.H  # tokens/s of the full-H workload
+    desc = (f"first {sl['q'].shape[0]} tokens x {heads} heads of {w.name} per step "
+            f"(fwd+bwd, fp64), scaled to tokens/s over all {w.H} heads")
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "num_seqs": w.num_seqs, "seq_len": w.lengths[0], "heads": w.H,
+                       "head_dim": w.D, "input_dtype": w.dtype},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gb300(args, w, rank, world, local):
+    import torch
+    from recompute_kda_chunkwise_gb300 import make_inputs
+    from recompute_kda_chunkwise_gb300 import kda as K
+
+    os.environ.setdefault("PYTORCH_CUDA_ALLOC_CONF", "expandable_segments:False")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    K.load_library()
+    inp = make_inputs(w, device=dev)
+    q, k, v, g, beta, A_log, dt_bias, cu, dO = (inp[n] for n in
+                                                  ["q", "k", "v", "g", "beta", "A_log", "dt_bias",
+                                                   "cu_seqlens", "dO"])
+    prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale)
+    family = K.kernel_family(prob)
+    torch.cuda.synchronize()
+
+    # peak allocated memory of one fwd+bwd (inputs, dO, o, grads, ctx, workspace)
+    torch.cuda.reset_peak_memory_stats(dev)
+    o, ctx = K.kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu, scale=w.scale)
+    grads = K.kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu, dO, ctx, scale=w.scale)
+    torch.cuda.synchronize()
+    peak_gib = torch.cuda.max_memory_allocated(dev) / 2 ** 30
+    ws = torch.empty(K.workspace_bytes(prob), dtype=torch.uint8, device=dev)
+
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        K.kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu, scale=w.scale, out=o, ctx=ctx)
+        if ev is not None:
+            ev[1].record(stream)
+        K.kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu, dO, ctx, scale=w.scale, workspace=ws, outs=grads)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total)
+    ms_step = ms_total / args.steps
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    status_ok = K.query_device_status(ctx) == 0 and K.query_device_status(ws) == 0
+
+    tokens = w.total_tokens * world
+    value = tokens / (ms_step / 1e3)
+    fwd_b, bwd_b = algorithmic_bytes(w)
+    peak_gbs, peak_kind = measured_peaks()
+    dominant = "kda_bwd" if bwd_ms >= fwd_ms else "kda_fwd"
+    dom_ms, dom_b = (bwd_ms, bwd_b) if dominant == "kda_bwd" else (fwd_ms, fwd_b)
+    achieved = dom_b / (dom_ms / 1e3) / 1e9
+    step_gbs = (fwd_b + bwd_b) / (ms_step / 1e3) / 1e9
+    kname = {0: "simt", 1: "tc"}.get(family, "unknown")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
+                "frac": achieved / peak_gbs, "traffic": ncu_traffic(f"{dominant}_{kname}", w.name),
+                "kernel": f"{dominant} ({kname} kernels)", "peak_kind": f"{peak_kind} hbm_gbs",
+                "algorithmic_bytes_per_launch": dom_b, "ms_per_launch": dom_ms,
+                "step_frac": step_gbs / peak_gbs}
+    launches_per_step = 1 + 2  # forward kernel; backward kernel + gate-parameter reduction
+
+    # end to end through the public API: pinned host inputs -> device -> fwd+bwd -> host outputs
+    e2e = None
+    if args.e2e_steps > 0:
+        names_in = ["q", "k", "v", "g", "beta", "dO"]
+        host_in = {n: torch.empty(inp[n].shape, dtype=inp[n].dtype, pin_memory=True) for n in names_in}
+        for n in names_in:
+            host_in[n].copy_(inp[n])
+        names_out = ["dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias"]
+        host_out = {n: torch.empty(grads[n].shape, dtype=grads[n].dtype, pin_memory=True) for n in names_out}
+        host_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + host_o.numel() * host_o.element_size()
+
+        def e2e_step():
+            for n in names_in:
+                inp[n].copy_(host_in[n], non_blocking=True)
+            step()
+            host_o.copy_(o, non_blocking=True)
+            for n in names_out:
+                host_out[n].copy_(grads[n], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        dt = max_over_ranks(time.perf_counter() - t0) / args.e2e_steps
+        e2e = {"value": tokens / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        heads = min(cores, w.H)
+        sl = make_sample(w, inp, args.sample_tokens, heads)
+        rate, dt = oracle_sample(w, sl, cores)
+        cpu_base = {"value": rate / w.H, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                    "sample": (f"first {sl['q'].shape[0]} tokens x {heads} heads of {w.name} "
+                               f"(fwd+bwd, fp64, {dt:.1f} s wall), scaled to tokens/s over all {w.H} heads")}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+                "config": {"workload": w.name, "num_seqs": w.num_seqs, "seq_len": w.lengths[0],
+                           "heads": w.H, "head_dim": w.D, "scale": w.scale, "gate_lower_bound": -5.0,
+                           "l2_flush": "none needed: inputs (%.1f GB) exceed L2" % (
+                               (fwd_b + bwd_b) / 1e9 / 2),
+                           "parallelism": f"replicas{world}", "kernel_family": kname},
+                "peak_alloc_gib": peak_gib, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                "hbm_roofline_frac": step_gbs / peak_gbs,
+                "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary(),
+                "device_status_ok": status_ok}
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--sample-tokens", type=int, default=4096)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    from recompute_kda_chunkwise_gb300 import HEADLINE, WORKLOADS
+    w = WORKLOADS[args.workload or HEADLINE]
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+    else:
+        run_gb300(args, w, rank, world, local)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,153 @@
+/*
+ * kda.h -- C ABI of the GB300-native chunk-parallel Kimi Delta Attention
+ * (KDA) forward and backward library (libkda_gb300.so).
+ *
+ * The operation (all entry points compute the same operator; see the page
+ * "KDA Memory with Recompute: FLA vs cuDNN Frontend FROST", section
+ * "Sources and measurement configuration", for the operator configuration):
+ *
+ *   per packed sequence n (tokens cu_seqlens[n] .. cu_seqlens[n+1]-1) and
+ *   per head h, with state S (D x D, S_0 = 0, no initial or final state):
+ *     qh_t   = scale * q_t / sqrt(|q_t|^2 + l2_eps)
+ *     kh_t   = k_t / sqrt(|k_t|^2 + l2_eps)
+ *     beta_t = sigmoid(beta_raw_t)
+ *     g_t    = gate_lower_bound * sigmoid(exp(A_log[h]) * (g_raw_t + dt_bias[h,:]))
+ *     S_t    = (I - beta_t kh_t kh_t^T) Diag(exp(g_t)) S_{t-1} + beta_t kh_t v_t^T
+ *     o_t    = S_t^T qh_t
+ *   The gate's closed form is this library's reading of "safe gate with
+ *   lower bound -5" built from the raw gate, A_log and dt_bias; the pages do
+ *   not print it. The chunked evaluation (intra-chunk WY factors, serial
+ *   inter-chunk state scan) follows "KDA at the production shape ...",
+ *   section 2.1 (per-chunk op table) and section 1.1 (state scan).
+ *
+ * Layouts (all row-major, contiguous, no strides):
+ *   q, k, v, g_raw, o, dO, dq, dk, dv, dg_raw : [S, H, D]  (token-major)
+ *   beta_raw, dbeta_raw                        : [S, H]
+ *   A_log, dA_log                              : [H]      fp32
+ *   dt_bias, ddt_bias                          : [H, D]   fp32
+ *   cu_seqlens                                 : [num_seqs + 1] int32, device
+ *   S = cu_seqlens[num_seqs] = total_tokens; K = V = D = head_dim.
+ *   Element type of the [S,H,D] and [S,H] tensors is problem->dtype.
+ *
+ * Ownership: the caller allocates every buffer (inputs, outputs, ctx,
+ * workspace) in device memory. The library never allocates or frees device
+ * memory, never synchronises the stream inside kda_fwd / kda_bwd, and keeps
+ * no pointer after a call returns. Outputs are overwritten (=), never
+ * accumulated. Inputs are read-only. Outputs must not alias inputs.
+ *
+ * Errors: every entry point validates its arguments on the host and returns
+ * a kda_status without launching anything when they are bad. Launch failures
+ * map to KDA_ERR_CUDA. Errors detected inside a kernel (a bounded wait that
+ * ran out, a failed device-side check) are written to a status word inside
+ * ctx (forward) or workspace (backward) and read with
+ * kda_query_device_status. Kernels never trap.
+ *
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ * stream). All device work of a call is enqueued on that stream.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+  KDA_ERR_UNSUPPORTED = 2,   /* head_dim / dtype combination not built */
+  KDA_ERR_WORKSPACE = 3,     /* ctx or workspace smaller than required */
+  KDA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  KDA_ERR_TIMEOUT = 5,       /* device side: a bounded wait ran out */
+  KDA_ERR_DEVICE_CHECK = 6   /* device side: an in-kernel check failed */
+} kda_status;
+
+typedef enum {
+  KDA_DTYPE_BF16 = 0,
+  KDA_DTYPE_F32 = 1
+} kda_dtype;
+
+/* Problem description. cu_seqlens is a DEVICE pointer; the library never
+ * reads it on the host (so no synchronisation), and trusts that it is
+ * non-decreasing, starts at 0 and ends at total_tokens. */
+typedef struct {
+  int64_t total_tokens;       /* S */
+  int32_t num_seqs;           /* N >= 1 */
+  int32_t num_heads;          /* H >= 1 */
+  int32_t head_dim;           /* D = K = V; 64 or 128 */
+  int32_t dtype;              /* kda_dtype of the [S,H,D] / [S,H] tensors */
+  float scale;                /* output scale applied to qh (1.0 = none) */
+  float gate_lower_bound;     /* L < 0, e.g. -5.0 */
+  float l2_eps;               /* epsilon inside the L2-norm square root */
+  int32_t reserved;           /* must be 0 */
+  const int32_t* cu_seqlens;  /* device, num_seqs + 1 entries */
+} kda_problem;
+
+/* Bytes of the forward->backward context: state checkpoints (fp32, one per
+ * 1024 tokens of every sequence and head) plus a 256-byte header holding the
+ * forward's device status word. Returns 0 for an invalid problem. The size
+ * queries ignore cu_seqlens (it may be NULL). */
+size_t kda_ctx_bytes(const kda_problem* p);
+
+/* Bytes of the backward workspace: per-CTA scratch for recomputed chunk
+ * states of one checkpoint segment, gate-parameter partial sums and a
+ * 256-byte header with the backward's device status word. Returns 0 for an
+ * invalid problem. */
+size_t kda_bwd_workspace_bytes(const kda_problem* p);
+
+/* Forward. Writes o [S,H,D]. When ctx is not NULL it must hold
+ * kda_ctx_bytes(p) bytes (16-byte aligned); the forward writes the state
+ * checkpoints there for kda_bwd, and ctx must then stay alive and unmodified
+ * until the matching kda_bwd has been enqueued. ctx == NULL runs the forward
+ * alone (inference), writing no checkpoints.
+ * All tensor pointers must be 16-byte aligned. */
+kda_status kda_fwd(const kda_problem* p,
+                   const void* q, const void* k, const void* v,
+                   const void* g_raw, const void* beta_raw,
+                   const float* A_log, const float* dt_bias,
+                   void* o, void* ctx, void* stream);
+
+/* Backward. Given dO [S,H,D] and the ctx written by kda_fwd on the same
+ * inputs, writes dq, dk, dv, dg_raw [S,H,D], dbeta_raw [S,H] (problem
+ * dtype) and dA_log [H], ddt_bias [H,D] (fp32). It recomputes the chunk
+ * states, the WY factors and the gated q/k chunk by chunk from the inputs and
+ * the checkpoints; no full-sequence intermediate is stored. workspace must
+ * hold kda_bwd_workspace_bytes(p) bytes (16-byte aligned). */
+kda_status kda_bwd(const kda_problem* p,
+                   const void* q, const void* k, const void* v,
+                   const void* g_raw, const void* beta_raw,
+                   const float* A_log, const float* dt_bias,
+                   const void* dO, const void* ctx,
+                   void* dq, void* dk, void* dv, void* dg_raw, void* dbeta_raw,
+                   float* dA_log, float* ddt_bias,
+                   void* workspace, void* stream);
+
+/* Reads the device status word at the head of a ctx or workspace buffer.
+ * Synchronises `stream` first. Returns KDA_OK, KDA_ERR_TIMEOUT or
+ * KDA_ERR_DEVICE_CHECK as recorded by the kernels, or KDA_ERR_CUDA if the
+ * read itself failed. */
+kda_status kda_query_device_status(const void* ctx_or_workspace, void* stream);
+
+/* Static, NUL-terminated name of a status code. */
+const char* kda_status_string(kda_status s);
+
+/* Detail of the last error returned on the calling thread (static storage,
+ * overwritten by the next failing call on that thread). */
+const char* kda_last_error_message(void);
+
+/* Which kernel family a problem dispatches to: 0 = fp32 CUDA-core (SIMT)
+ * kernels, 1 = tcgen05 tensor-core kernels; -1 for an invalid or
+ * unsupported problem. Host only. */
+int kda_kernel_family(const kda_problem* p);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

@@ -1,0 +1,179 @@
+// kda_api.cu -- host side of the C ABI declared in include/kda.h: argument
+// validation, buffer sizing, kernel-family dispatch and launches. No device
+// memory is allocated here and no stream is synchronised inside kda_fwd /
+// kda_bwd.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+kda_status fail(kda_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Largest |lower bound| for which the chunk-factored intra products stay in
+// fp32 range: |L| * 16 tokens * log2(e) must stay below 128 binary orders.
+constexpr float kMaxAbsLower = 5.5f;
+
+kda_status validate(const kda_problem* p, bool need_ptrs = true) {
+  if (!p) return fail(KDA_ERR_INVALID_ARG, "problem is NULL");
+  if (p->num_seqs < 1) return fail(KDA_ERR_INVALID_ARG, "num_seqs must be >= 1 (got %d)", p->num_seqs);
+  if (p->num_heads < 1) return fail(KDA_ERR_INVALID_ARG, "num_heads must be >= 1 (got %d)", p->num_heads);
+  if (p->total_tokens < 0) return fail(KDA_ERR_INVALID_ARG, "total_tokens must be >= 0");
+  if (p->reserved != 0) return fail(KDA_ERR_INVALID_ARG, "reserved field must be 0");
+  if (need_ptrs && !p->cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is NULL");
+  if (p->dtype != KDA_DTYPE_BF16 && p->dtype != KDA_DTYPE_F32)
+    return fail(KDA_ERR_UNSUPPORTED, "dtype %d is not supported", p->dtype);
+  if (p->head_dim != 64 && p->head_dim != 128)
+    return fail(KDA_ERR_UNSUPPORTED, "head_dim %d is not supported (64 or 128)", p->head_dim);
+  if (!isfinite(p->scale)) return fail(KDA_ERR_INVALID_ARG, "scale must be finite");
+  if (!(p->l2_eps >= 0.f) || !isfinite(p->l2_eps)) return fail(KDA_ERR_INVALID_ARG, "l2_eps must be >= 0");
+  if (!(p->gate_lower_bound <= 0.f) || p->gate_lower_bound < -kMaxAbsLower)
+    return fail(KDA_ERR_UNSUPPORTED, "gate_lower_bound must lie in [-%.1f, 0] (got %g)", kMaxAbsLower,
+                p->gate_lower_bound);
+  // element counts must fit comfortably in int64 offsets
+  if (p->total_tokens > ((int64_t)1 << 40) / ((int64_t)p->num_heads * p->head_dim))
+    return fail(KDA_ERR_INVALID_ARG, "problem too large");
+  if ((int64_t)p->num_seqs * p->num_heads > (1 << 30)) return fail(KDA_ERR_INVALID_ARG, "too many sequences x heads");
+  return KDA_OK;
+}
+
+size_t ckpt_slots(const kda_problem* p) {
+  return (size_t)(p->total_tokens / kda::kCkptTokens) + (size_t)p->num_seqs;
+}
+
+size_t ctx_bytes(const kda_problem* p) {
+  const size_t D = (size_t)p->head_dim;
+  return kda::kHeaderBytes + ckpt_slots(p) * (size_t)p->num_heads * D * D * sizeof(float);
+}
+
+size_t partial_bytes(const kda_problem* p) {
+  return round_up((size_t)p->num_seqs * p->num_heads * (p->head_dim + 1) * sizeof(float), 256);
+}
+
+size_t workspace_bytes(const kda_problem* p) {
+  return kda::kHeaderBytes + partial_bytes(p) + kda::bwd_scratch_bytes_simt(p, nullptr);
+}
+
+#define CHECK_PTR(ptr)                                                                   \
+  do {                                                                                   \
+    if (!(ptr)) return fail(KDA_ERR_INVALID_ARG, "%s is NULL", #ptr);                    \
+    if (!aligned16(ptr)) return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #ptr); \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_ctx_bytes(const kda_problem* p) { return validate(p, false) == KDA_OK ? ctx_bytes(p) : 0; }
+
+size_t kda_bwd_workspace_bytes(const kda_problem* p) {
+  return validate(p, false) == KDA_OK ? workspace_bytes(p) : 0;
+}
+
+int kda_kernel_family(const kda_problem* p) { return validate(p, false) == KDA_OK ? 0 : -1; }
+
+int kda_version(void) { return 100; }
+
+const char* kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+    case KDA_ERR_DEVICE_CHECK: return "KDA_ERR_DEVICE_CHECK";
+  }
+  return "KDA_ERR_UNKNOWN";
+}
+
+const char* kda_last_error_message(void) { return g_msg; }
+
+kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
+                   const void* beta_raw, const float* A_log, const float* dt_bias, void* o, void* ctx,
+                   void* stream) {
+  kda_status st = validate(p);
+  if (st != KDA_OK) return st;
+  if (p->total_tokens == 0) return KDA_OK;  // nothing to compute or write
+  CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(g_raw); CHECK_PTR(beta_raw);
+  CHECK_PTR(A_log); CHECK_PTR(dt_bias); CHECK_PTR(o);
+  if (ctx && !aligned16(ctx)) return fail(KDA_ERR_INVALID_ARG, "ctx is not 16-byte aligned");
+  cudaStream_t s = (cudaStream_t)stream;
+  kda::FwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g_raw; a.b = beta_raw; a.A_log = A_log; a.dt_bias = dt_bias;
+  a.o = o;
+  a.ckpt = ctx ? (float*)((char*)ctx + kda::kHeaderBytes) : nullptr;
+  a.status = ctx ? (int*)ctx : nullptr;
+  a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
+  a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
+  if (ctx && cudaMemsetAsync(ctx, 0, sizeof(int), s) != cudaSuccess)
+    return fail(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
+  st = kda::launch_fwd_simt(p, a, s);
+  if (st != KDA_OK) return fail(st, "forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return KDA_OK;
+}
+
+kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
+                   const void* beta_raw, const float* A_log, const float* dt_bias, const void* dO,
+                   const void* ctx, void* dq, void* dk, void* dv, void* dg_raw, void* dbeta_raw,
+                   float* dA_log, float* ddt_bias, void* workspace, void* stream) {
+  kda_status st = validate(p);
+  if (st != KDA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (p->total_tokens == 0) {  // no tokens: the parameter gradients are zero
+    CHECK_PTR(dA_log); CHECK_PTR(ddt_bias);
+    if (cudaMemsetAsync(dA_log, 0, sizeof(float) * p->num_heads, s) != cudaSuccess ||
+        cudaMemsetAsync(ddt_bias, 0, sizeof(float) * p->num_heads * p->head_dim, s) != cudaSuccess)
+      return fail(KDA_ERR_CUDA, "memset failed: %s", cudaGetErrorString(cudaGetLastError()));
+    return KDA_OK;
+  }
+  CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(g_raw); CHECK_PTR(beta_raw);
+  CHECK_PTR(A_log); CHECK_PTR(dt_bias); CHECK_PTR(dO); CHECK_PTR(ctx);
+  CHECK_PTR(dq); CHECK_PTR(dk); CHECK_PTR(dv); CHECK_PTR(dg_raw); CHECK_PTR(dbeta_raw);
+  CHECK_PTR(dA_log); CHECK_PTR(ddt_bias); CHECK_PTR(workspace);
+  kda::BwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g_raw; a.b = beta_raw; a.A_log = A_log; a.dt_bias = dt_bias;
+  a.dO = dO;
+  a.ckpt = (const float*)((const char*)ctx + kda::kHeaderBytes);
+  a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg_raw; a.db = dbeta_raw;
+  a.dA_log = dA_log; a.ddt_bias = ddt_bias;
+  a.status = (int*)workspace;
+  a.partial = (float*)((char*)workspace + kda::kHeaderBytes);
+  a.scratch = (float*)((char*)workspace + kda::kHeaderBytes + partial_bytes(p));
+  a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
+  a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess)
+    return fail(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
+  st = kda::launch_bwd_simt(p, a, s);
+  if (st != KDA_OK) return fail(st, "backward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return KDA_OK;
+}
+
+kda_status kda_query_device_status(const void* buf, void* stream) {
+  if (!buf) return fail(KDA_ERR_INVALID_ARG, "buffer is NULL");
+  cudaStream_t s = (cudaStream_t)stream;
+  int word = 0;
+  if (cudaMemcpyAsync(&word, buf, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return fail(KDA_ERR_CUDA, "status read failed: %s", cudaGetErrorString(cudaGetLastError()));
+  if (word == 0) return KDA_OK;
+  if (word == KDA_ERR_TIMEOUT) return fail(KDA_ERR_TIMEOUT, "a device-side bounded wait ran out");
+  return fail(KDA_ERR_DEVICE_CHECK, "device-side check failed (code %d)", word);
+}
+
+}  // extern "C"

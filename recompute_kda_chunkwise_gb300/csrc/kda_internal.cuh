@@ -1,0 +1,93 @@
+// kda_internal.cuh -- constants, argument blocks and small device helpers
+// shared by the KDA kernels. Not part of the public ABI (include/kda.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Tokens between two state checkpoints stored by the forward in ctx (one
+// fp32 D x D state per checkpoint, sequence and head).
+constexpr int kCkptTokens = 1024;
+// Bytes reserved at the head of ctx / workspace for the device status word.
+constexpr int kHeaderBytes = 256;
+// Upper bound on backward CTAs (persistent grid), which sizes the workspace.
+constexpr int kMaxBwdCtas = 304;
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* g;
+  const void* b;
+  const float* A_log;
+  const float* dt_bias;
+  void* o;
+  float* ckpt;  // NULL: no checkpoints
+  int* status;  // NULL when ckpt is NULL
+  const int32_t* cu;
+  int N, H;
+  float scale, lower, eps;
+};
+
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* g;
+  const void* b;
+  const float* A_log;
+  const float* dt_bias;
+  const void* dO;
+  const float* ckpt;
+  void* dq;
+  void* dk;
+  void* dv;
+  void* dg;
+  void* db;
+  float* dA_log;
+  float* ddt_bias;
+  float* partial;  // [N*H][D+1]
+  float* scratch;  // per-CTA segment states
+  int* status;
+  const int32_t* cu;
+  int N, H;
+  float scale, lower, eps;
+};
+
+// Index of the checkpoint slot of (sequence n, segment j) relative to slot 0:
+// floor(cu[n] / kCkptTokens) + n + j. Sequence n owns ceil(T_n / kCkptTokens)
+// consecutive slots and these ranges never overlap, so the total count is
+// bounded by floor(S / kCkptTokens) + N (see kda_ctx_bytes).
+__host__ __device__ inline int64_t ckpt_slot(int64_t bos, int n, int j) {
+  return bos / kCkptTokens + n + j;
+}
+
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void stf(float* p, float x) { *p = x; }
+__device__ __forceinline__ void stf(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// First error wins; later ones are dropped.
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Host-side launchers (defined in the kernel translation units).
+kda_status launch_fwd_simt(const kda_problem* p, const FwdArgs& a, cudaStream_t s);
+kda_status launch_bwd_simt(const kda_problem* p, const BwdArgs& a, cudaStream_t s);
+size_t bwd_scratch_bytes_simt(const kda_problem* p, int* nctas);
+
+}  // namespace kda

@@ -1,0 +1,695 @@
+// kda_simt.cu -- fp32 CUDA-core (SIMT) kernels for KDA forward and backward.
+//
+// These kernels evaluate the chunked KDA algorithm entirely in fp32 FFMA. They
+// serve every dtype / head size the library accepts and are the path for fp32
+// problems, whose tolerance (1e-4 relative) bf16 tensor-core operands cannot
+// meet. The chunk decomposition follows "KDA at the production shape ...",
+// section 2.1 (per-chunk ops: aqk, akk, w, u, v_new = u - w S, intra, inter,
+// S += (k decay)^T v_new) and section 1.1 (serial state scan, channel-wise
+// decay of the state). With chunk-local inclusive cumulative log-decay G_r
+// (Gamma_r = exp(G_r), gamma = Gamma_{C-1}) and the chunk-start state H:
+//   Abar[r,s] = sum_i kh_ri kh_si exp(G_ri - G_si)     (s < r)
+//   M[r,s]    = sum_i qh_ri kh_si exp(G_ri - G_si)     (s <= r)
+//   T = (I + diag(beta) Abar)^-1   (forward substitution)
+//   W = T diag(beta) (Kh*Gamma),   U = T diag(beta) V
+//   U~ = U - W H,   O = (Qh*Gamma) H + M U~,
+//   H' = diag(gamma) H + Kbar^T U~,  Kbar[s,i] = kh_si exp(G_{C-1,i} - G_si).
+// The factored products (kh*Gamma)(kh/Gamma)^T are safe in fp32 while the
+// chunk's log-decay range stays below ~88 ("KDA at the production shape ...",
+// section 3(a): k/exp(cumsum g) underflows past cumsum < -88, which at the
+// -5 floor limits a chunk to 17 tokens); these kernels use C = 16 (D = 64)
+// and C = 8 (D = 128, to fit the backward's tiles in shared memory).
+//
+// Backward (recompute policy): the forward stores fp32 states every 1024
+// tokens. For each such segment, in reverse order, the backward rebuilds the
+// chunk-start states of the segment into per-CTA scratch with the same code
+// the forward ran, then walks the segment's chunks in reverse: it recomputes
+// the chunk's WY factors and gated q/k, propagates the state gradient dH,
+// and writes dq, dk, dv, dg_raw, dbeta_raw once, in the input dtype.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kNT = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct SimtChunk;
+template <>
+struct SimtChunk<64> {
+  static constexpr int C = 16;
+};
+template <>
+struct SimtChunk<128> {
+  static constexpr int C = 8;
+};
+
+// Shared-memory tiles of one chunk. [C][LD] tiles use row stride LD = D + 1
+// so that column walks by different threads hit different banks.
+template <int D, int C>
+struct Tiles {
+  static constexpr int LD = D + 1, CP = C + 1, TILE = C * LD, SQ = C * CP;
+  float *Qh, *Kh, *Gc, *Vv, *Qg, *Kg, *Ki, *Kb, *Ww, *Uu;
+  float *Abar, *Aqk, *Tm;
+  float *bet, *nq, *nk;
+  float *gam, *dtb;
+  __device__ float* carve(float* p) {
+    Qh = p; p += TILE; Kh = p; p += TILE; Gc = p; p += TILE; Vv = p; p += TILE;
+    Qg = p; p += TILE; Kg = p; p += TILE; Ki = p; p += TILE; Kb = p; p += TILE;
+    Ww = p; p += TILE; Uu = p; p += TILE;
+    Abar = p; p += SQ; Aqk = p; p += SQ; Tm = p; p += SQ;
+    bet = p; p += C; nq = p; p += C; nk = p; p += C;
+    gam = p; p += D; dtb = p; p += D;
+    return p;
+  }
+  static constexpr int floats() { return 10 * TILE + 3 * SQ + 3 * C + 2 * D; }
+};
+
+// Loads rows [t0, t0 + rows) of head h (zeros beyond `rows`, which makes the
+// padded rows inert: k = 0, beta = 0, g = 0) and builds
+//   Qh = q/n_q (unscaled), Kh = k/n_k, Vv = v, bet = sigmoid(b),
+//   Gc = chunk-local inclusive cumsum of g*log2(e), gam = 2^Gc[C-1],
+//   Qg = scale*Qh*2^G, Kg = Kh*2^G, Ki = Kh*2^-G, Kb = Kh*2^(G[C-1]-G).
+// The gate is g = lower * sigmoid(exp(A_log) * (g_raw + dt_bias)).
+template <typename Tin, int D, int C>
+__device__ void chunk_prologue(const Tiles<D, C>& t, const Tin* q, const Tin* k, const Tin* v,
+                               const Tin* g, const Tin* b, int64_t t0, int rows, int h, int H,
+                               float expA, float scale, float lower, float eps) {
+  constexpr int LD = D + 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int x = tid; x < C * D; x += kNT) {
+    const int r = x / D, i = x % D;
+    float qv = 0.f, kv = 0.f, gv = 0.f, vv = 0.f;
+    if (r < rows) {
+      const int64_t off = ((t0 + r) * H + h) * (int64_t)D + i;
+      qv = ldf(q + off);
+      kv = ldf(k + off);
+      vv = ldf(v + off);
+      gv = lower * kLog2e * sigmoidf_(expA * (ldf(g + off) + t.dtb[i]));
+    }
+    t.Qh[r * LD + i] = qv;
+    t.Kh[r * LD + i] = kv;
+    t.Gc[r * LD + i] = gv;
+    t.Vv[r * LD + i] = vv;
+  }
+  if (tid < C) t.bet[tid] = tid < rows ? sigmoidf_(ldf(b + (t0 + tid) * H + h)) : 0.f;
+  __syncthreads();
+  for (int r = warp; r < C; r += kNT / 32) {
+    float sq = 0.f, sk = 0.f;
+    for (int i = lane; i < D; i += 32) {
+      const float a = t.Qh[r * LD + i], c = t.Kh[r * LD + i];
+      sq += a * a;
+      sk += c * c;
+    }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    const float nq = sqrtf(sq + eps), nk = sqrtf(sk + eps);
+    // a zero row (padding, or eps = 0 with q = 0) stays exactly zero
+    const float iq = nq > 0.f ? 1.f / nq : 0.f, ik = nk > 0.f ? 1.f / nk : 0.f;
+    for (int i = lane; i < D; i += 32) {
+      t.Qh[r * LD + i] *= iq;
+      t.Kh[r * LD + i] *= ik;
+    }
+    if (lane == 0) {
+      t.nq[r] = nq;
+      t.nk[r] = nk;
+    }
+  }
+  for (int i = tid; i < D; i += kNT) {
+    float acc = 0.f;
+    for (int r = 0; r < C; ++r) {
+      acc += t.Gc[r * LD + i];
+      t.Gc[r * LD + i] = acc;
+    }
+    t.gam[i] = exp2f(acc);
+  }
+  __syncthreads();
+  for (int x = tid; x < C * D; x += kNT) {
+    const int r = x / D, i = x % D;
+    const float G = t.Gc[r * LD + i], Ge = t.Gc[(C - 1) * LD + i];
+    const float e = exp2f(G), kh = t.Kh[r * LD + i];
+    t.Qg[r * LD + i] = scale * t.Qh[r * LD + i] * e;
+    t.Kg[r * LD + i] = kh * e;
+    t.Ki[r * LD + i] = kh * exp2f(-G);
+    t.Kb[r * LD + i] = kh * exp2f(Ge - G);
+  }
+  __syncthreads();
+}
+
+// Abar (strictly lower), Aqk (lower incl. diagonal), T = (I + diag(beta)Abar)^-1,
+// W = T diag(beta) Kg, U = T diag(beta) V.
+template <int D, int C>
+__device__ void chunk_intra(const Tiles<D, C>& t) {
+  constexpr int LD = D + 1, CP = C + 1;
+  const int tid = threadIdx.x;
+  for (int x = tid; x < C * C; x += kNT) {
+    const int r = x / C, s = x % C;
+    float akk = 0.f, aqk = 0.f;
+    if (s <= r) {
+      for (int i = 0; i < D; ++i) {
+        const float ki = t.Ki[s * LD + i];
+        akk += t.Kg[r * LD + i] * ki;
+        aqk += t.Qg[r * LD + i] * ki;
+      }
+    }
+    t.Abar[r * CP + s] = s < r ? akk : 0.f;
+    t.Aqk[r * CP + s] = s <= r ? aqk : 0.f;
+  }
+  __syncthreads();
+  if (tid < 32) {  // forward substitution, one lane per column of T
+    const int j = tid;
+    for (int r = 0; r < C; ++r) {
+      if (j < C) {
+        float val;
+        if (j == r) {
+          val = 1.f;
+        } else if (j > r) {
+          val = 0.f;
+        } else {
+          val = 0.f;
+          const float br = t.bet[r];
+          for (int s = j; s < r; ++s) val -= br * t.Abar[r * CP + s] * t.Tm[s * CP + j];
+        }
+        t.Tm[r * CP + j] = val;
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  for (int x = tid; x < C * D; x += kNT) {
+    const int r = x / D, i = x % D;
+    float w = 0.f, u = 0.f;
+    for (int s = 0; s <= r; ++s) {
+      const float ts = t.Tm[r * CP + s] * t.bet[s];
+      w += ts * t.Kg[s * LD + i];
+      u += ts * t.Vv[s * LD + i];
+    }
+    t.Ww[r * LD + i] = w;
+    t.Uu[r * LD + i] = u;
+  }
+  __syncthreads();
+}
+
+// U~ = U - W H (in place in Uu). H is D x V with row stride ldh.
+template <int D, int C>
+__device__ void state_residual(const Tiles<D, C>& t, const float* Hs, int ldh) {
+  constexpr int V = D, LD = D + 1, RG = kNT / V, RPT = C / RG;
+  static_assert(C % RG == 0, "rows per thread");
+  const int tid = threadIdx.x, j = tid % V, rg = tid / V;
+  float acc[RPT];
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr) acc[rr] = t.Uu[(rg * RPT + rr) * LD + j];
+  for (int i = 0; i < D; ++i) {
+    const float hv = Hs[i * ldh + j];
+#pragma unroll
+    for (int rr = 0; rr < RPT; ++rr) acc[rr] -= t.Ww[(rg * RPT + rr) * LD + i] * hv;
+  }
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr) t.Uu[(rg * RPT + rr) * LD + j] = acc[rr];
+  __syncthreads();
+}
+
+// H = diag(gam) H + Kb^T U~ (in place).
+template <int D, int C>
+__device__ void state_update(const Tiles<D, C>& t, float* Hs, int ldh) {
+  constexpr int V = D, LD = D + 1, IG = kNT / V, IPT = D / IG;
+  const int tid = threadIdx.x, j = tid % V, ig = tid / V;
+  float u[C];
+#pragma unroll
+  for (int r = 0; r < C; ++r) u[r] = t.Uu[r * LD + j];
+  for (int ii = 0; ii < IPT; ++ii) {
+    const int i = ig * IPT + ii;
+    float acc = t.gam[i] * Hs[i * ldh + j];
+#pragma unroll
+    for (int r = 0; r < C; ++r) acc += t.Kb[r * LD + i] * u[r];
+    Hs[i * ldh + j] = acc;
+  }
+  __syncthreads();
+}
+
+// O = Qg H + Aqk U~, stored for rows < rows.
+template <typename Tin, int D, int C>
+__device__ void chunk_output(const Tiles<D, C>& t, const float* Hs, int ldh, Tin* o, int64_t t0,
+                             int rows, int h, int H) {
+  constexpr int V = D, LD = D + 1, CP = C + 1, RG = kNT / V, RPT = C / RG;
+  const int tid = threadIdx.x, j = tid % V, rg = tid / V;
+  float acc[RPT];
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr) acc[rr] = 0.f;
+  for (int i = 0; i < D; ++i) {
+    const float hv = Hs[i * ldh + j];
+#pragma unroll
+    for (int rr = 0; rr < RPT; ++rr) acc[rr] += t.Qg[(rg * RPT + rr) * LD + i] * hv;
+  }
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr) {
+    const int r = rg * RPT + rr;
+    float a = acc[rr];
+    for (int s = 0; s <= r; ++s) a += t.Aqk[r * CP + s] * t.Uu[s * LD + j];
+    if (r < rows) stf(o + ((t0 + r) * H + h) * (int64_t)V + j, a);
+  }
+  __syncthreads();
+}
+
+template <typename Tin, int D>
+__global__ void __launch_bounds__(kNT, 1) kda_fwd_simt_kernel(const FwdArgs a) {
+  constexpr int C = SimtChunk<D>::C, V = D;
+  extern __shared__ float sm[];
+  Tiles<D, C> t;
+  float* Hs = t.carve(sm);  // [D][V]
+  const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  const int64_t bos = a.cu[n], eos = a.cu[n + 1];
+  const int tid = threadIdx.x;
+  const Tin* q = static_cast<const Tin*>(a.q);
+  const Tin* k = static_cast<const Tin*>(a.k);
+  const Tin* v = static_cast<const Tin*>(a.v);
+  const Tin* g = static_cast<const Tin*>(a.g);
+  const Tin* b = static_cast<const Tin*>(a.b);
+  Tin* o = static_cast<Tin*>(a.o);
+  for (int i = tid; i < D; i += kNT) t.dtb[i] = a.dt_bias[h * D + i];
+  for (int x = tid; x < D * V; x += kNT) Hs[x] = 0.f;
+  const float expA = expf(a.A_log[h]);
+  __syncthreads();
+  for (int64_t t0 = bos; t0 < eos; t0 += C) {
+    const int64_t tt = t0 - bos;
+    if (a.ckpt != nullptr && tt % kCkptTokens == 0) {
+      float* dst = a.ckpt + (ckpt_slot(bos, n, (int)(tt / kCkptTokens)) * a.H + h) * (int64_t)(D * V);
+      for (int x = tid; x < D * V; x += kNT) dst[x] = Hs[x];
+    }
+    const int rows = (int)min((int64_t)C, eos - t0);
+    chunk_prologue<Tin, D, C>(t, q, k, v, g, b, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
+    chunk_intra<D, C>(t);
+    state_residual<D, C>(t, Hs, V);
+    chunk_output<Tin, D, C>(t, Hs, V, o, t0, rows, h, a.H);
+    state_update<D, C>(t, Hs, V);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Backward
+// ---------------------------------------------------------------------------
+template <int D, int C>
+struct BwdTiles {
+  static constexpr int LD = D + 1, CP = C + 1, TILE = C * LD, SQ = C * CP, LDH = D + 1;
+  float *dOt, *dUt, *dQ, *dK, *dGt, *dWt;  // [C][LD]
+  float *dM, *dT, *Yt;                     // [C][CP]
+  float *dbet, *rq, *rk;                   // [C]
+  float *dGe, *part;                       // [D], [kNT]
+  float *Hc, *dH;                          // [D][LDH]
+  float *red;                              // [kNT]
+  __device__ float* carve(float* p) {
+    dOt = p; p += TILE; dUt = p; p += TILE; dQ = p; p += TILE; dK = p; p += TILE;
+    dGt = p; p += TILE; dWt = p; p += TILE;
+    dM = p; p += SQ; dT = p; p += SQ; Yt = p; p += SQ;
+    dbet = p; p += C; rq = p; p += C; rk = p; p += C;
+    dGe = p; p += D; part = p; p += kNT;
+    Hc = p; p += D * LDH; dH = p; p += D * LDH;
+    red = p; p += kNT;
+    return p;
+  }
+  static constexpr int floats() { return 6 * TILE + 3 * SQ + 3 * C + D + 2 * kNT + 2 * D * LDH; }
+};
+
+template <typename Tin, int D>
+__global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
+  constexpr int C = SimtChunk<D>::C, V = D, LD = D + 1, CP = C + 1, LDH = V + 1;
+  constexpr int CPS = kCkptTokens / C;  // chunks per checkpoint segment
+  constexpr int RGD = kNT / D, RPTD = C / RGD;
+  extern __shared__ float sm[];
+  Tiles<D, C> t;
+  BwdTiles<D, C> u;
+  u.carve(t.carve(sm));
+  const int tid = threadIdx.x;
+  const Tin* q = static_cast<const Tin*>(a.q);
+  const Tin* k = static_cast<const Tin*>(a.k);
+  const Tin* v = static_cast<const Tin*>(a.v);
+  const Tin* g = static_cast<const Tin*>(a.g);
+  const Tin* b = static_cast<const Tin*>(a.b);
+  const Tin* dO = static_cast<const Tin*>(a.dO);
+  Tin* dq = static_cast<Tin*>(a.dq);
+  Tin* dk = static_cast<Tin*>(a.dk);
+  Tin* dv = static_cast<Tin*>(a.dv);
+  Tin* dg = static_cast<Tin*>(a.dg);
+  Tin* db = static_cast<Tin*>(a.db);
+  float* scratch = a.scratch + (int64_t)blockIdx.x * CPS * D * LDH;
+  const int nitems = a.N * a.H;
+
+  for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+    const int n = item / a.H, h = item % a.H;
+    const int64_t bos = a.cu[n], eos = a.cu[n + 1];
+    const int64_t T = eos - bos;
+    const int nchunks = (int)((T + C - 1) / C);
+    const int nseg = (int)((T + kCkptTokens - 1) / kCkptTokens);
+    const float expA = expf(a.A_log[h]);
+    for (int i = tid; i < D; i += kNT) t.dtb[i] = a.dt_bias[h * D + i];
+    for (int x = tid; x < D * LDH; x += kNT) u.dH[x] = 0.f;
+    float acc_dtb = 0.f, acc_alog = 0.f;  // thread owns column tid % D
+    __syncthreads();
+
+    for (int seg = nseg - 1; seg >= 0; --seg) {
+      const int c0 = seg * CPS, c1 = min(nchunks, c0 + CPS);
+      {  // checkpoint -> Hc
+        const float* src = a.ckpt + (ckpt_slot(bos, n, seg) * a.H + h) * (int64_t)(D * V);
+        for (int x = tid; x < D * V; x += kNT) u.Hc[(x / V) * LDH + (x % V)] = src[x];
+      }
+      __syncthreads();
+      // rebuild the chunk-start states of this segment
+      for (int c = c0; c < c1; ++c) {
+        float* dst = scratch + (int64_t)(c - c0) * D * LDH;
+        for (int x = tid; x < D * LDH; x += kNT) dst[x] = u.Hc[x];
+        if (c == c1 - 1) break;
+        const int64_t t0 = bos + (int64_t)c * C;
+        const int rows = (int)min((int64_t)C, eos - t0);
+        chunk_prologue<Tin, D, C>(t, q, k, v, g, b, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
+        chunk_intra<D, C>(t);
+        state_residual<D, C>(t, u.Hc, LDH);
+        state_update<D, C>(t, u.Hc, LDH);
+      }
+      __syncthreads();
+
+      for (int c = c1 - 1; c >= c0; --c) {
+        const int64_t t0 = bos + (int64_t)c * C;
+        const int rows = (int)min((int64_t)C, eos - t0);
+        {
+          const float* src = scratch + (int64_t)(c - c0) * D * LDH;
+          for (int x = tid; x < D * LDH; x += kNT) u.Hc[x] = src[x];
+          for (int x = tid; x < C * V; x += kNT) {
+            const int r = x / V, j = x % V;
+            u.dOt[r * LD + j] = r < rows ? ldf(dO + ((t0 + r) * a.H + h) * (int64_t)V + j) : 0.f;
+          }
+        }
+        chunk_prologue<Tin, D, C>(t, q, k, v, g, b, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
+        chunk_intra<D, C>(t);
+        state_residual<D, C>(t, u.Hc, LDH);  // t.Uu = U~, t.Ww = W
+
+        // dU~[r][j] = sum_{r'>=r} Aqk[r'][r] dO[r'][j] + sum_i Kb[r][i] dH[i][j]
+        {
+          constexpr int RG = kNT / V, RPT = C / RG;
+          const int j = tid % V, rg = tid / V;
+          float acc[RPT];
+#pragma unroll
+          for (int rr = 0; rr < RPT; ++rr) {
+            const int r = rg * RPT + rr;
+            float s_ = 0.f;
+            for (int r2 = r; r2 < C; ++r2) s_ += t.Aqk[r2 * CP + r] * u.dOt[r2 * LD + j];
+            acc[rr] = s_;
+          }
+          for (int i = 0; i < D; ++i) {
+            const float dh = u.dH[i * LDH + j];
+#pragma unroll
+            for (int rr = 0; rr < RPT; ++rr) acc[rr] += t.Kb[(rg * RPT + rr) * LD + i] * dh;
+          }
+#pragma unroll
+          for (int rr = 0; rr < RPT; ++rr) u.dUt[(rg * RPT + rr) * LD + j] = acc[rr];
+        }
+        __syncthreads();
+
+        // Terms that contract over the value dimension with H or dH:
+        //   d(Qg) = dO H^T, dW = -dU~ H^T, dKb = U~ dH^T, dgamma = rowsum(H * dH)
+        {
+          const int i = tid % D, rg = tid / D;
+          float aQ[RPTD], aW[RPTD], aK[RPTD], ag = 0.f;
+#pragma unroll
+          for (int rr = 0; rr < RPTD; ++rr) aQ[rr] = aW[rr] = aK[rr] = 0.f;
+          for (int j = 0; j < V; ++j) {
+            const float hv = u.Hc[i * LDH + j], dh = u.dH[i * LDH + j];
+            ag += hv * dh;
+#pragma unroll
+            for (int rr = 0; rr < RPTD; ++rr) {
+              const int r = rg * RPTD + rr;
+              aQ[rr] += u.dOt[r * LD + j] * hv;
+              aW[rr] += u.dUt[r * LD + j] * hv;
+              aK[rr] += t.Uu[r * LD + j] * dh;
+            }
+          }
+          float ge = 0.f;
+#pragma unroll
+          for (int rr = 0; rr < RPTD; ++rr) {
+            const int r = rg * RPTD + rr;
+            const float G = t.Gc[r * LD + i], Ge = t.Gc[(C - 1) * LD + i];
+            u.dQ[r * LD + i] = aQ[rr] * exp2f(G);
+            u.dGt[r * LD + i] = aQ[rr] * t.Qg[r * LD + i] - aK[rr] * t.Kb[r * LD + i];
+            u.dWt[r * LD + i] = -aW[rr];
+            u.dK[r * LD + i] = aK[rr] * exp2f(Ge - G);
+            ge += aK[rr] * t.Kb[r * LD + i];
+          }
+          if (rg == 0) ge += ag * t.gam[i];
+          u.part[tid] = ge;
+        }
+        __syncthreads();
+        for (int i = tid; i < D; i += kNT) {
+          float s_ = 0.f;
+          for (int r = 0; r < RGD; ++r) s_ += u.part[r * D + i];
+          u.dGe[i] = s_;
+        }
+        // dH <- diag(gam) dH + Qg^T dO - W^T dU~  (dH now refers to the chunk start)
+        {
+          constexpr int IG = kNT / V, IPT = D / IG;
+          const int j = tid % V, ig = tid / V;
+          float o_[C], du[C];
+#pragma unroll
+          for (int r = 0; r < C; ++r) {
+            o_[r] = u.dOt[r * LD + j];
+            du[r] = u.dUt[r * LD + j];
+          }
+          for (int ii = 0; ii < IPT; ++ii) {
+            const int i = ig * IPT + ii;
+            float acc = t.gam[i] * u.dH[i * LDH + j];
+#pragma unroll
+            for (int r = 0; r < C; ++r) acc += t.Qg[r * LD + i] * o_[r] - t.Ww[r * LD + i] * du[r];
+            u.dH[i * LDH + j] = acc;
+          }
+        }
+        // dM = tril(dO U~^T);  dT = strictly-lower part of dW Xw^T + dU~ Xu^T
+        for (int x = tid; x < C * C; x += kNT) {
+          const int r = x / C, s = x % C;
+          float dm = 0.f, dt = 0.f;
+          if (s <= r)
+            for (int j = 0; j < V; ++j) dm += u.dOt[r * LD + j] * t.Uu[s * LD + j];
+          if (s < r) {
+            float d1 = 0.f, d2 = 0.f;
+            for (int i = 0; i < D; ++i) d1 += u.dWt[r * LD + i] * t.Kg[s * LD + i];
+            for (int j = 0; j < V; ++j) d2 += u.dUt[r * LD + j] * t.Vv[s * LD + j];
+            dt = t.bet[s] * (d1 + d2);
+          }
+          u.dM[r * CP + s] = dm;
+          u.dT[r * CP + s] = dt;
+        }
+        __syncthreads();
+        // Y = dT T^T
+        for (int x = tid; x < C * C; x += kNT) {
+          const int a_ = x / C, s = x % C;
+          float y = 0.f;
+          const int bmax = min(s, a_ - 1);
+          for (int bb = 0; bb <= bmax; ++bb) y += u.dT[a_ * CP + bb] * t.Tm[s * CP + bb];
+          u.Yt[a_ * CP + s] = y;
+        }
+        __syncthreads();
+        // dA = -(T^T Y) on the strictly lower part (reuse dT for dA)
+        for (int x = tid; x < C * C; x += kNT) {
+          const int r = x / C, s = x % C;
+          float da = 0.f;
+          if (s < r)
+            for (int a_ = r; a_ < C; ++a_) da -= t.Tm[a_ * CP + r] * u.Yt[a_ * CP + s];
+          u.dT[r * CP + s] = da;
+        }
+        // dXw = T^T dW (in place, by column); dXu = T^T dU~ (into dOt, free now)
+        for (int x = tid; x < D + V; x += kNT) {
+          float col[C];
+          float* base = x < D ? (u.dWt + x) : (u.dUt + (x - D));
+#pragma unroll
+          for (int r = 0; r < C; ++r) col[r] = base[r * LD];
+          float* out = x < D ? (u.dWt + x) : (u.dOt + (x - D));
+#pragma unroll
+          for (int r = 0; r < C; ++r) {
+            float s_ = 0.f;
+            for (int r2 = r; r2 < C; ++r2) s_ += t.Tm[r2 * CP + r] * col[r2];
+            out[r * LD] = s_;
+          }
+        }
+        __syncthreads();
+        // dv = beta dXu
+        for (int x = tid; x < C * V; x += kNT) {
+          const int r = x / V, j = x % V;
+          if (r < rows) stf(dv + ((t0 + r) * a.H + h) * (int64_t)V + j, t.bet[r] * u.dOt[r * LD + j]);
+        }
+        // dbeta (before the beta-sigmoid): Xw, Xu and the beta factor of A
+        {
+          const int warp = tid >> 5, lane = tid & 31;
+          for (int r = warp; r < C; r += kNT / 32) {
+            float s_ = 0.f;
+            for (int i = lane; i < D; i += 32)
+              s_ += u.dWt[r * LD + i] * t.Kg[r * LD + i] + u.dOt[r * LD + i] * t.Vv[r * LD + i];
+            for (int s = lane; s < r; s += 32) s_ += u.dT[r * CP + s] * t.Abar[r * CP + s];
+            s_ = warp_sum(s_);
+            if (lane == 0) u.dbet[r] = s_;
+          }
+        }
+        // elementwise contributions of Xw, Abar and Aqk to dq^, dk^, dG
+        for (int x = tid; x < C * D; x += kNT) {
+          const int r = x / D, i = x % D;
+          const float G = t.Gc[r * LD + i], e = exp2f(G), ei = exp2f(-G);
+          const float br = t.bet[r], dxw = u.dWt[r * LD + i];
+          float a1 = 0.f, a2 = 0.f, m1 = 0.f, m2 = 0.f;
+          for (int s = 0; s < r; ++s) a1 += u.dT[r * CP + s] * t.Ki[s * LD + i];
+          a1 *= br;
+          for (int s = r + 1; s < C; ++s) a2 += t.bet[s] * u.dT[s * CP + r] * t.Kg[s * LD + i];
+          for (int s = 0; s <= r; ++s) m1 += u.dM[r * CP + s] * t.Ki[s * LD + i];
+          for (int s = r; s < C; ++s) m2 += u.dM[s * CP + r] * t.Qg[s * LD + i];
+          u.dQ[r * LD + i] += m1 * e;
+          u.dK[r * LD + i] += br * e * dxw + a1 * e + (a2 + m2) * ei;
+          u.dGt[r * LD + i] += br * dxw * t.Kg[r * LD + i] + a1 * t.Kg[r * LD + i] +
+                               m1 * t.Qg[r * LD + i] - (a2 + m2) * t.Ki[r * LD + i];
+        }
+        __syncthreads();
+        // dG of the chunk end, then reverse cumulative sum -> dg (natural log units)
+        for (int i = tid; i < D; i += kNT) {
+          float acc = u.dGe[i];
+          for (int r = C - 1; r >= 0; --r) {
+            acc += u.dGt[r * LD + i];
+            u.dGt[r * LD + i] = acc;
+          }
+        }
+        // row dots for the L2-norm chain rule
+        {
+          const int warp = tid >> 5, lane = tid & 31;
+          for (int r = warp; r < C; r += kNT / 32) {
+            float sq = 0.f, sk = 0.f;
+            for (int i = lane; i < D; i += 32) {
+              sq += t.Qh[r * LD + i] * u.dQ[r * LD + i];
+              sk += t.Kh[r * LD + i] * u.dK[r * LD + i];
+            }
+            sq = warp_sum(sq);
+            sk = warp_sum(sk);
+            if (lane == 0) {
+              u.rq[r] = a.scale * sq;
+              u.rk[r] = sk;
+            }
+          }
+        }
+        __syncthreads();
+        for (int x = tid; x < C * D; x += kNT) {
+          const int r = x / D, i = x % D;
+          if (r < rows) {
+            const int64_t off = ((t0 + r) * a.H + h) * (int64_t)D + i;
+            const float dxq = a.scale * u.dQ[r * LD + i];
+            const float iq = t.nq[r] > 0.f ? 1.f / t.nq[r] : 0.f;
+            const float ik = t.nk[r] > 0.f ? 1.f / t.nk[r] : 0.f;
+            stf(dq + off, (dxq - t.Qh[r * LD + i] * u.rq[r]) * iq);
+            stf(dk + off, (u.dK[r * LD + i] - t.Kh[r * LD + i] * u.rk[r]) * ik);
+            const float z = expA * (ldf(g + off) + t.dtb[i]);
+            const float sg = sigmoidf_(z);
+            const float dz = u.dGt[r * LD + i] * a.lower * sg * (1.f - sg);
+            stf(dg + off, expA * dz);
+            acc_dtb += expA * dz;
+            acc_alog += dz * z;
+          }
+        }
+        if (tid < C && tid < rows) {
+          const float bt = t.bet[tid];
+          stf(db + (t0 + tid) * a.H + h, u.dbet[tid] * bt * (1.f - bt));
+        }
+        __syncthreads();
+      }
+    }
+    // per-(sequence, head) partial sums of the gate-parameter gradients
+    u.red[tid] = acc_dtb;
+    __syncthreads();
+    for (int i = tid; i < D; i += kNT) {
+      float s_ = 0.f;
+      for (int r = 0; r < RGD; ++r) s_ += u.red[r * D + i];
+      a.partial[(int64_t)item * (D + 1) + i] = s_;
+    }
+    __syncthreads();
+    u.red[tid] = acc_alog;
+    __syncthreads();
+    for (int st = kNT / 2; st > 0; st >>= 1) {
+      if (tid < st) u.red[tid] += u.red[tid + st];
+      __syncthreads();
+    }
+    if (tid == 0) a.partial[(int64_t)item * (D + 1) + D] = u.red[0];
+    __syncthreads();
+  }
+}
+
+// dA_log[h] = sum_n partial[n][h][D], ddt_bias[h][i] = sum_n partial[n][h][i],
+// in a fixed order (deterministic).
+__global__ void kda_param_reduce_kernel(const float* partial, int N, int H, int D, float* dA_log,
+                                        float* ddt_bias) {
+  const int h = blockIdx.x;
+  for (int i = threadIdx.x; i <= D; i += blockDim.x) {
+    float s = 0.f;
+    for (int n = 0; n < N; ++n) s += partial[((int64_t)n * H + h) * (D + 1) + i];
+    if (i < D)
+      ddt_bias[h * D + i] = s;
+    else
+      dA_log[h] = s;
+  }
+}
+
+template <typename Tin, int D>
+kda_status launch_fwd_t(const kda_problem* p, const FwdArgs& a, cudaStream_t s) {
+  constexpr int C = SimtChunk<D>::C;
+  const size_t smem = sizeof(float) * (Tiles<D, C>::floats() + D * D);
+  auto kern = kda_fwd_simt_kernel<Tin, D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  const int grid = p->num_seqs * p->num_heads;
+  if (grid > 0) kern<<<grid, kNT, smem, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+template <int D>
+int bwd_ctas(const kda_problem* p) {
+  int items = p->num_seqs * p->num_heads;
+  return items < kMaxBwdCtas ? items : kMaxBwdCtas;
+}
+
+template <typename Tin, int D>
+kda_status launch_bwd_t(const kda_problem* p, const BwdArgs& a, cudaStream_t s) {
+  constexpr int C = SimtChunk<D>::C;
+  const size_t smem = sizeof(float) * (Tiles<D, C>::floats() + BwdTiles<D, C>::floats());
+  auto kern = kda_bwd_simt_kernel<Tin, D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int grid = bwd_ctas<D>(p);
+  if (sms > 0 && grid > sms) grid = sms;  // one resident CTA per SM
+  if (grid > 0) kern<<<grid, kNT, smem, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+  kda_param_reduce_kernel<<<p->num_heads, 128, 0, s>>>(a.partial, p->num_seqs, p->num_heads, D, a.dA_log,
+                                                       a.ddt_bias);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+kda_status launch_fwd_simt(const kda_problem* p, const FwdArgs& a, cudaStream_t s) {
+  const bool bf = p->dtype == KDA_DTYPE_BF16;
+  if (p->head_dim == 64) return bf ? launch_fwd_t<__nv_bfloat16, 64>(p, a, s) : launch_fwd_t<float, 64>(p, a, s);
+  if (p->head_dim == 128) return bf ? launch_fwd_t<__nv_bfloat16, 128>(p, a, s) : launch_fwd_t<float, 128>(p, a, s);
+  return KDA_ERR_UNSUPPORTED;
+}
+
+kda_status launch_bwd_simt(const kda_problem* p, const BwdArgs& a, cudaStream_t s) {
+  const bool bf = p->dtype == KDA_DTYPE_BF16;
+  if (p->head_dim == 64) return bf ? launch_bwd_t<__nv_bfloat16, 64>(p, a, s) : launch_bwd_t<float, 64>(p, a, s);
+  if (p->head_dim == 128) return bf ? launch_bwd_t<__nv_bfloat16, 128>(p, a, s) : launch_bwd_t<float, 128>(p, a, s);
+  return KDA_ERR_UNSUPPORTED;
+}
+
+// Per-CTA scratch of the SIMT backward: the chunk-start states of one
+// checkpoint segment, fp32 with padded rows.
+size_t bwd_scratch_bytes_simt(const kda_problem* p, int* nctas) {
+  const int D = p->head_dim;
+  const int C = D == 64 ? SimtChunk<64>::C : SimtChunk<128>::C;
+  int items = p->num_seqs * p->num_heads;
+  const int ctas = items < kMaxBwdCtas ? items : kMaxBwdCtas;
+  if (nctas) *nctas = ctas;
+  return (size_t)ctas * (kCkptTokens / C) * D * (D + 1) * sizeof(float);
+}
+
+}  // namespace kda

@@ -1,0 +1,204 @@
+"""Thin Python binding of the KDA C ABI (include/kda.h).
+
+Argument marshalling only: every step of the forward and backward runs in
+the CUDA library ``_build/libkda_gb300.so``. PyTorch supplies device memory
+and the current stream. There is no CPU fallback: if the library is missing
+or a call fails, a RuntimeError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkda_gb300.so")
+
+KDA_DTYPE_BF16 = 0
+KDA_DTYPE_F32 = 1
+_DTYPE_CODE = {torch.bfloat16: KDA_DTYPE_BF16, torch.float32: KDA_DTYPE_F32}
+STATUS_NAMES = ["KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_WORKSPACE",
+                "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_ERR_DEVICE_CHECK"]
+
+
+class KdaProblem(ctypes.Structure):
+    """Mirror of ``kda_problem`` in include/kda.h."""
+    _fields_ = [("total_tokens", ctypes.c_int64), ("num_seqs", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("gate_lower_bound", ctypes.c_float), ("l2_eps", ctypes.c_float),
+                ("reserved", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p)]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"{where}: {name}: {detail}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"KDA CUDA library not built: {path} is missing "
+                                   "(run recompute_kda_chunkwise_gb300.build.build())")
+            lib = ctypes.CDLL(path)
+            vp, P = ctypes.c_void_p, ctypes.POINTER(KdaProblem)
+            lib.kda_ctx_bytes.restype = ctypes.c_size_t
+            lib.kda_ctx_bytes.argtypes = [P]
+            lib.kda_bwd_workspace_bytes.restype = ctypes.c_size_t
+            lib.kda_bwd_workspace_bytes.argtypes = [P]
+            lib.kda_fwd.restype = ctypes.c_int
+            lib.kda_fwd.argtypes = [P] + [vp] * 10
+            lib.kda_bwd.restype = ctypes.c_int
+            lib.kda_bwd.argtypes = [P] + [vp] * 18
+            lib.kda_query_device_status.restype = ctypes.c_int
+            lib.kda_query_device_status.argtypes = [vp, vp]
+            lib.kda_status_string.restype = ctypes.c_char_p
+            lib.kda_status_string.argtypes = [ctypes.c_int]
+            lib.kda_last_error_message.restype = ctypes.c_char_p
+            lib.kda_last_error_message.argtypes = []
+            lib.kda_kernel_family.restype = ctypes.c_int
+            lib.kda_kernel_family.argtypes = [P]
+            lib.kda_version.restype = ctypes.c_int
+            lib.kda_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        msg = load_library().kda_last_error_message().decode(errors="replace")
+        raise KdaError(status, where, msg)
+
+
+def make_problem(total_tokens: int, num_seqs: int, num_heads: int, head_dim: int, dtype,
+                 cu_seqlens=None, scale: float = 1.0, lower_bound: float = -5.0,
+                 eps: float = 1e-6) -> KdaProblem:
+    code = _DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    ptr = 0 if cu_seqlens is None else cu_seqlens.data_ptr()
+    return KdaProblem(int(total_tokens), int(num_seqs), int(num_heads), int(head_dim), code,
+                      float(scale), float(lower_bound), float(eps), 0, ptr)
+
+
+def ctx_bytes(p: KdaProblem) -> int:
+    return int(load_library().kda_ctx_bytes(ctypes.byref(p)))
+
+
+def workspace_bytes(p: KdaProblem) -> int:
+    return int(load_library().kda_bwd_workspace_bytes(ctypes.byref(p)))
+
+
+def kernel_family(p: KdaProblem) -> int:
+    return int(load_library().kda_kernel_family(ctypes.byref(p)))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps):
+    if q.dim() != 3:
+        raise ValueError("q must be [S, H, D]")
+    S, H, D = q.shape
+    if q.dtype not in _DTYPE_CODE:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.device != q.device:
+        raise ValueError("cu_seqlens must be int32 on the same device as q")
+    return make_problem(S, cu_seqlens.numel() - 1, H, D, q.dtype, cu_seqlens, scale, lower_bound, eps)
+
+
+def _check_tensors(q, *others, params=()):
+    for t in (q,) + tuple(others):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype or t.device != q.device:
+            raise ValueError("all activations must be contiguous CUDA tensors of one dtype and device")
+    for t in params:
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.float32 or t.device != q.device:
+            raise ValueError("A_log and dt_bias must be contiguous float32 CUDA tensors")
+
+
+def kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
+            lower_bound: float = -5.0, eps: float = 1e-6, save_ctx: bool = True, out=None,
+            ctx=None):
+    """Forward. Returns (o, ctx); ctx is None when save_ctx is False. ``out``
+    and ``ctx`` may be preallocated (ctx of at least ctx_bytes(problem))."""
+    _check_tensors(q, k, v, g, beta, params=(A_log, dt_bias))
+    p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps)
+    o = torch.empty_like(q) if out is None else out
+    if not save_ctx:
+        ctx = None
+    elif ctx is None:
+        ctx = torch.empty(ctx_bytes(p), dtype=torch.uint8, device=q.device)
+    elif ctx.numel() * ctx.element_size() < ctx_bytes(p):
+        raise ValueError("ctx buffer too small")
+    st = load_library().kda_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                _ptr(A_log), _ptr(dt_bias), _ptr(o), _ptr(ctx), _stream_handle(q.device))
+    _check(st, "kda_fwd")
+    return o, ctx
+
+
+def kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO, ctx, *, scale: float = 1.0,
+            lower_bound: float = -5.0, eps: float = 1e-6, workspace=None, outs=None):
+    """Backward. Returns dict dq, dk, dv, dg, dbeta, dA_log, ddt_bias."""
+    _check_tensors(q, k, v, g, beta, dO, params=(A_log, dt_bias))
+    p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps)
+    if outs is None:
+        outs = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                    dg=torch.empty_like(g), dbeta=torch.empty_like(beta),
+                    dA_log=torch.empty_like(A_log), ddt_bias=torch.empty_like(dt_bias))
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(p), dtype=torch.uint8, device=q.device)
+    elif workspace.numel() * workspace.element_size() < workspace_bytes(p):
+        raise ValueError("workspace buffer too small")
+    st = load_library().kda_bwd(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+        _ptr(dO), _ptr(ctx), _ptr(outs["dq"]), _ptr(outs["dk"]), _ptr(outs["dv"]), _ptr(outs["dg"]),
+        _ptr(outs["dbeta"]), _ptr(outs["dA_log"]), _ptr(outs["ddt_bias"]), _ptr(workspace),
+        _stream_handle(q.device))
+    _check(st, "kda_bwd")
+    return outs
+
+
+def query_device_status(buf) -> int:
+    """Status word written by the kernels into a ctx or workspace buffer."""
+    return int(load_library().kda_query_device_status(_ptr(buf), _stream_handle(buf.device)))
+
+
+class KDAFunction(torch.autograd.Function):
+    """Autograd wrapper: forward saves the inputs and the checkpoint ctx only."""
+
+    @staticmethod
+    def forward(actx, q, k, v, g, beta, A_log, dt_bias, cu_seqlens, scale, lower_bound, eps):
+        o, ctx = kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, scale=scale,
+                         lower_bound=lower_bound, eps=eps, save_ctx=True)
+        actx.save_for_backward(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, ctx)
+        actx.args = (scale, lower_bound, eps)
+        return o
+
+    @staticmethod
+    def backward(actx, dO):
+        q, k, v, g, beta, A_log, dt_bias, cu_seqlens, ctx = actx.saved_tensors
+        scale, lower_bound, eps = actx.args
+        r = kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO.contiguous(), ctx,
+                    scale=scale, lower_bound=lower_bound, eps=eps)
+        return (r["dq"], r["dk"], r["dv"], r["dg"], r["dbeta"], r["dA_log"], r["ddt_bias"],
+                None, None, None, None)
+
+
+def kda(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, scale: float = 1.0,
+        lower_bound: float = -5.0, eps: float = 1e-6):
+    """Differentiable KDA over packed sequences (see include/kda.h)."""
+    return KDAFunction.apply(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, scale, lower_bound, eps)

@@ -1,0 +1,81 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function declared in include/kda.h, validates arguments and sizes
+buffers without touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from recompute_kda_chunkwise_gb300 import build as kbuild
+from recompute_kda_chunkwise_gb300 import kda as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return K.load_library()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(kda_\w+)\s*\(", txt))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "kda_fwd" in names and "kda_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_problem_struct_layout_matches_header():
+    assert ctypes.sizeof(K.KdaProblem) == 48
+    assert K.KdaProblem.cu_seqlens.offset == 40
+
+
+def test_size_queries(lib):
+    p = K.make_problem(131072, 1, 96, 128, torch.bfloat16)
+    ckpts = 131072 // 1024 + 1
+    assert K.ctx_bytes(p) == 256 + ckpts * 96 * 128 * 128 * 4
+    assert K.workspace_bytes(p) > 256 + 96 * 129 * 4
+    assert K.kernel_family(p) in (0, 1)
+    bad = K.make_problem(16, 1, 2, 96, torch.bfloat16)
+    assert K.ctx_bytes(bad) == 0 and K.workspace_bytes(bad) == 0 and K.kernel_family(bad) == -1
+    assert b"head_dim" in lib.kda_last_error_message()
+
+
+def test_invalid_arguments_are_rejected_on_host(lib):
+    cu = torch.tensor([0, 16], dtype=torch.int32)  # host tensor: never dereferenced
+    p = K.make_problem(16, 1, 2, 64, torch.bfloat16, cu)
+    nul = ctypes.c_void_p(0)
+    st = lib.kda_fwd(ctypes.byref(p), nul, nul, nul, nul, nul, nul, nul, nul, nul, nul)
+    assert st == 1  # KDA_ERR_INVALID_ARG
+    assert b"NULL" in lib.kda_last_error_message()
+    mis = ctypes.c_void_p(0x1008)  # not 16-byte aligned
+    al = ctypes.c_void_p(0x1000)
+    st = lib.kda_fwd(ctypes.byref(p), mis, al, al, al, al, al, al, al, nul, nul)
+    assert st == 1 and b"aligned" in lib.kda_last_error_message()
+    p.gate_lower_bound = -8.0
+    st = lib.kda_fwd(ctypes.byref(p), al, al, al, al, al, al, al, al, nul, nul)
+    assert st == 2  # KDA_ERR_UNSUPPORTED
+    p.gate_lower_bound = -5.0
+    p.num_seqs = 0
+    assert lib.kda_bwd(ctypes.byref(p), *([al] * 17), nul) == 1
+    p.num_seqs = 1
+    p.dtype = 7
+    assert lib.kda_fwd(ctypes.byref(p), *([al] * 8), nul, nul) == 2
+
+
+def test_status_strings(lib):
+    for i, name in enumerate(K.STATUS_NAMES):
+        assert lib.kda_status_string(i).decode() == name
+    assert lib.kda_version() >= 100

@@ -1,0 +1,58 @@
+"""The benchmark's multi-rank host logic on CPU (gloo, world_size 2): the
+timed value is the max over ranks and the barrier lets all ranks through.
+Each rank runs an independent replica, so there is no data-path collective
+to test."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), KDA_BENCH_BACKEND="gloo")
+    import bench
+    r, ws, local = bench.dist_setup()
+    assert (r, ws, local) == (rank, world, rank)
+    bench.barrier()
+    m = bench.max_over_ranks(10.0 + 5.0 * rank)
+    import torch.distributed as dist
+    dist.destroy_process_group()
+    q.put((rank, m))
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(2))
+    assert got == {0: 15.0, 1: 15.0}
+
+
+def test_single_process_is_identity():
+    import bench
+    assert bench.max_over_ranks(3.25) == 3.25
+
+
+def test_algorithmic_bytes_match_per_token_head_formula():
+    import bench
+    from recompute_kda_chunkwise_gb300 import WORKLOADS
+    w = WORKLOADS["mbs1_128k_h96_d128_bf16"]
+    f, b = bench.algorithmic_bytes(w)
+    # bf16: (10D + 2) forward + (18D + 4) backward bytes per token-head
+    assert f + b == w.total_tokens * w.H * (28 * w.D + 6)
