@@ -125,6 +125,38 @@ kda_status kda_bwd(const kda_problem* p,
                    float* dA_log, float* ddt_bias,
                    void* workspace, void* stream);
 
+/* Size of the fixed scratch buffer that kda_bwd_noalloc uses (64 MiB). */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* Backward without any device allocation. The paper has no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc where they run
+ * the backward (a host that serves all device memory from its own fixed
+ * pool, a plug-in handed device pointers but no allocator, a loop that must
+ * not take an allocation's implicit synchronisation). Same arguments,
+ * layouts and results as kda_bwd, minus the workspace: the backward's scratch
+ * (gate-parameter partials and recomputed chunk-start states) lives in a
+ * KDA_NOALLOC_SCRATCH_BYTES array inside the library, which every GPU that
+ * loads the library holds until the process exits. The caller still passes
+ * all inputs and outputs. It calls no cudaMalloc / cudaFree and no
+ * allocating library routine.
+ * - The first call on a device looks up that device's address of the array
+ *   (cudaGetSymbolAddress, with the device current); make that first call
+ *   before any stream capture.
+ * - Problems whose scratch does not fit (header + partials for N*H
+ *   sequence-heads + one CTA's segment states) return KDA_ERR_WORKSPACE
+ *   with the required size in kda_last_error_message(); use kda_bwd then.
+ * - Fewer CTAs fit than kda_bwd would use, so it is slower.
+ * - Every call shares the array: calls whose GPU work overlaps (other
+ *   streams or threads on the same device) race and give wrong results.
+ * - Device-side status is not readable for this entry point. */
+kda_status kda_bwd_noalloc(const kda_problem* p,
+                           const void* q, const void* k, const void* v,
+                           const void* g_raw, const void* beta_raw,
+                           const float* A_log, const float* dt_bias,
+                           const void* dO, const void* ctx,
+                           void* dq, void* dk, void* dv, void* dg_raw, void* dbeta_raw,
+                           float* dA_log, float* ddt_bias, void* stream);
+
 /* Reads the device status word at the head of a ctx or workspace buffer.
  * Synchronises `stream` first. Returns KDA_OK, KDA_ERR_TIMEOUT or
  * KDA_ERR_DEVICE_CHECK as recorded by the kernels, or KDA_ERR_CUDA if the

@@ -77,6 +77,18 @@ size_t workspace_bytes(const kda_problem* p) {
 
 }  // namespace
 
+namespace kda {
+kda_status validate_problem(const kda_problem* p) { return validate(p); }
+kda_status set_error(kda_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+size_t gate_partial_bytes(const kda_problem* p) { return partial_bytes(p); }
+}  // namespace kda
+
 extern "C" {
 
 size_t kda_ctx_bytes(const kda_problem* p) { return validate(p, false) == KDA_OK ? ctx_bytes(p) : 0; }

@@ -89,5 +89,12 @@ __device__ __forceinline__ void set_status(int* status, int code) {
 kda_status launch_fwd_simt(const kda_problem* p, const FwdArgs& a, cudaStream_t s);
 kda_status launch_bwd_simt(const kda_problem* p, const BwdArgs& a, cudaStream_t s);
 size_t bwd_scratch_bytes_simt(const kda_problem* p, int* nctas);
+kda_status launch_bwd_simt_ctas(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas);
+size_t bwd_scratch_bytes_per_cta_simt(const kda_problem* p);
+
+// Host helpers shared by the entry points (defined in kda_api.cu).
+kda_status validate_problem(const kda_problem* p);
+kda_status set_error(kda_status s, const char* fmt, ...);
+size_t gate_partial_bytes(const kda_problem* p);
 
 }  // namespace kda

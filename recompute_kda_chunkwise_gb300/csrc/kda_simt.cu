@@ -26,6 +26,8 @@
 // the forward ran, then walks the segment's chunks in reverse: it recomputes
 // the chunk's WY factors and gated q/k, propagates the state gradient dH,
 // and writes dq, dk, dv, dg_raw, dbeta_raw once, in the input dtype.
+#include <type_traits>
+
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -679,6 +681,39 @@ kda_status launch_bwd_simt(const kda_problem* p, const BwdArgs& a, cudaStream_t 
   if (p->head_dim == 64) return bf ? launch_bwd_t<__nv_bfloat16, 64>(p, a, s) : launch_bwd_t<float, 64>(p, a, s);
   if (p->head_dim == 128) return bf ? launch_bwd_t<__nv_bfloat16, 128>(p, a, s) : launch_bwd_t<float, 128>(p, a, s);
   return KDA_ERR_UNSUPPORTED;
+}
+
+// Backward launch with a caller-chosen number of persistent CTAs (each CTA
+// owns one per-CTA scratch slot). Used by the no-allocation entry point,
+// whose fixed scratch buffer holds only a few slots.
+kda_status launch_bwd_simt_ctas(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas) {
+  const bool bf = p->dtype == KDA_DTYPE_BF16;
+  if (ctas < 1) return KDA_ERR_WORKSPACE;
+  auto run = [&](auto tin_tag, auto d_tag) -> kda_status {
+    using Tin = decltype(tin_tag);
+    constexpr int D = decltype(d_tag)::value;
+    constexpr int C = SimtChunk<D>::C;
+    const size_t smem = sizeof(float) * (Tiles<D, C>::floats() + BwdTiles<D, C>::floats());
+    auto kern = kda_bwd_simt_kernel<Tin, D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    kern<<<ctas, kNT, smem, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    kda_param_reduce_kernel<<<p->num_heads, 128, 0, s>>>(a.partial, p->num_seqs, p->num_heads, D, a.dA_log,
+                                                         a.ddt_bias);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  };
+  using D64 = std::integral_constant<int, 64>;
+  using D128 = std::integral_constant<int, 128>;
+  if (p->head_dim == 64) return bf ? run(__nv_bfloat16{}, D64{}) : run(float{}, D64{});
+  if (p->head_dim == 128) return bf ? run(__nv_bfloat16{}, D128{}) : run(float{}, D128{});
+  return KDA_ERR_UNSUPPORTED;
+}
+
+size_t bwd_scratch_bytes_per_cta_simt(const kda_problem* p) {
+  const int D = p->head_dim;
+  const int C = D == 64 ? SimtChunk<64>::C : SimtChunk<128>::C;
+  return (size_t)(kCkptTokens / C) * D * (D + 1) * sizeof(float);
 }
 
 // Per-CTA scratch of the SIMT backward: the chunk-start states of one

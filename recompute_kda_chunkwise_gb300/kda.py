@@ -61,6 +61,8 @@ def load_library(path: str = LIB_PATH):
             lib.kda_fwd.argtypes = [P] + [vp] * 10
             lib.kda_bwd.restype = ctypes.c_int
             lib.kda_bwd.argtypes = [P] + [vp] * 18
+            lib.kda_bwd_noalloc.restype = ctypes.c_int
+            lib.kda_bwd_noalloc.argtypes = [P] + [vp] * 17
             lib.kda_query_device_status.restype = ctypes.c_int
             lib.kda_query_device_status.argtypes = [vp, vp]
             lib.kda_status_string.restype = ctypes.c_char_p
@@ -169,6 +171,26 @@ def kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO, ctx, *, scale: flo
         _ptr(outs["dbeta"]), _ptr(outs["dA_log"]), _ptr(outs["ddt_bias"]), _ptr(workspace),
         _stream_handle(q.device))
     _check(st, "kda_bwd")
+    return outs
+
+
+def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO, ctx, *, scale: float = 1.0,
+                    lower_bound: float = -5.0, eps: float = 1e-6, outs=None):
+    """Backward through kda_bwd_noalloc: no workspace, the library's fixed
+    scratch array is used instead (for callers that cannot allocate device
+    memory at this point; calls must not overlap on the GPU). Returns the
+    same dict as kda_bwd."""
+    _check_tensors(q, k, v, g, beta, dO, params=(A_log, dt_bias))
+    p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps)
+    if outs is None:
+        outs = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                    dg=torch.empty_like(g), dbeta=torch.empty_like(beta),
+                    dA_log=torch.empty_like(A_log), ddt_bias=torch.empty_like(dt_bias))
+    st = load_library().kda_bwd_noalloc(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+        _ptr(dO), _ptr(ctx), _ptr(outs["dq"]), _ptr(outs["dk"]), _ptr(outs["dv"]), _ptr(outs["dg"]),
+        _ptr(outs["dbeta"]), _ptr(outs["dA_log"]), _ptr(outs["ddt_bias"]), _stream_handle(q.device))
+    _check(st, "kda_bwd_noalloc")
     return outs
 
 

@@ -1,0 +1,51 @@
+"""kda_bwd_noalloc, the backward for callers that cannot allocate device
+memory where they run it, checked through the C ABI against kda_bwd (the
+entry point with a caller workspace) on two calls in a row.
+
+This file is named so that pytest collects it last. It must pass both on its
+own in a fresh process (the first call then sets up the library's fixed
+scratch array on this device) and after the other tests."""
+import pytest
+import torch
+
+from recompute_kda_chunkwise_gb300 import Workload, make_inputs
+from recompute_kda_chunkwise_gb300 import kda as K
+from tests._parity import TOL, compare, to_dev
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ["dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias"]
+
+
+@pytest.mark.parametrize("D,dtype", [(64, "bf16"), (128, "bf16"), (64, "f32")])
+def test_noalloc_backward_matches_workspace_backward_twice(D, dtype):
+    w = Workload(f"noalloc_d{D}_{dtype}", (1, 700, 0, 2100, 33), 3, D, dtype, seed=7800 + D,
+                 param_std=0.3)
+    inp = to_dev(make_inputs(w))
+    args = (inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["A_log"], inp["dt_bias"],
+            inp["cu_seqlens"])
+    o, ctx = K.kda_fwd(*args)
+    ref = K.kda_bwd(*args, inp["dO"], ctx)
+    torch.cuda.synchronize()
+    ref_np = {n: ref[n].double().cpu().numpy() for n in NAMES}
+    tol = TOL[inp["q"].dtype]
+    for _ in range(2):
+        got = K.kda_bwd_noalloc(*args, inp["dO"], ctx)
+        torch.cuda.synchronize()
+        compare(got, ref_np, tol, names=NAMES)
+
+
+def test_noalloc_rejects_problems_beyond_its_buffer():
+    # 20 million sequence-heads of gate-parameter partials cannot fit in the
+    # fixed buffer: the call must fail on the host with a clear message
+    dev = torch.device("cuda")
+    cu = torch.zeros(2, dtype=torch.int32, device=dev)
+    p = K.make_problem(0, 1, 1, 128, torch.bfloat16, cu)
+    p.num_seqs = 200000
+    p.num_heads = 100
+    import ctypes
+    lib = K.load_library()
+    al = ctypes.c_void_p(1 << 20)
+    st = lib.kda_bwd_noalloc(ctypes.byref(p), *([al] * 16), None)
+    assert st == 3  # KDA_ERR_WORKSPACE
+    assert b"fixed buffer" in lib.kda_last_error_message()
