@@ -70,6 +70,11 @@ typedef enum {
   KDA_DTYPE_F32 = 1
 } kda_dtype;
 
+/* kda_problem.flags bits. KDA_FLAG_FORCE_SIMT runs the fp32 CUDA-core
+ * kernels even where tensor-core kernels exist (bf16, head_dim 128): slower,
+ * fp32 accuracy throughout. */
+#define KDA_FLAG_FORCE_SIMT 1
+
 /* Problem description. cu_seqlens is a DEVICE pointer; the library never
  * reads it on the host (so no synchronisation), and trusts that it is
  * non-decreasing, starts at 0 and ends at total_tokens. */
@@ -82,7 +87,7 @@ typedef struct {
   float scale;                /* output scale applied to qh (1.0 = none) */
   float gate_lower_bound;     /* L < 0, e.g. -5.0 */
   float l2_eps;               /* epsilon inside the L2-norm square root */
-  int32_t reserved;           /* must be 0 */
+  int32_t flags;              /* KDA_FLAG_* bits, 0 by default */
   const int32_t* cu_seqlens;  /* device, num_seqs + 1 entries */
 } kda_problem;
 
@@ -170,9 +175,10 @@ const char* kda_status_string(kda_status s);
  * overwritten by the next failing call on that thread). */
 const char* kda_last_error_message(void);
 
-/* Which kernel family a problem dispatches to: 0 = fp32 CUDA-core (SIMT)
- * kernels, 1 = tcgen05 tensor-core kernels; -1 for an invalid or
- * unsupported problem. Host only. */
+/* Which kernel family a problem's forward dispatches to: 0 = fp32 CUDA-core
+ * (SIMT) kernels, 1 = tcgen05 tensor-core kernels (bf16, head_dim 128,
+ * unless KDA_FLAG_FORCE_SIMT); -1 for an invalid or unsupported problem.
+ * Host only. */
 int kda_kernel_family(const kda_problem* p);
 
 /* Library ABI version (major * 10000 + minor * 100 + patch). */

@@ -34,7 +34,7 @@ kda_status validate(const kda_problem* p, bool need_ptrs = true) {
   if (p->num_seqs < 1) return fail(KDA_ERR_INVALID_ARG, "num_seqs must be >= 1 (got %d)", p->num_seqs);
   if (p->num_heads < 1) return fail(KDA_ERR_INVALID_ARG, "num_heads must be >= 1 (got %d)", p->num_heads);
   if (p->total_tokens < 0) return fail(KDA_ERR_INVALID_ARG, "total_tokens must be >= 0");
-  if (p->reserved != 0) return fail(KDA_ERR_INVALID_ARG, "reserved field must be 0");
+  if ((p->flags & ~KDA_FLAG_FORCE_SIMT) != 0) return fail(KDA_ERR_INVALID_ARG, "unknown flags 0x%x", p->flags);
   if (need_ptrs && !p->cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is NULL");
   if (p->dtype != KDA_DTYPE_BF16 && p->dtype != KDA_DTYPE_F32)
     return fail(KDA_ERR_UNSUPPORTED, "dtype %d is not supported", p->dtype);
@@ -50,6 +50,11 @@ kda_status validate(const kda_problem* p, bool need_ptrs = true) {
     return fail(KDA_ERR_INVALID_ARG, "problem too large");
   if ((int64_t)p->num_seqs * p->num_heads > (1 << 30)) return fail(KDA_ERR_INVALID_ARG, "too many sequences x heads");
   return KDA_OK;
+}
+
+// Forward kernel family: tcgen05 kernels for bf16 D = 128, else fp32 SIMT.
+int family_of(const kda_problem* p) {
+  return (p->dtype == KDA_DTYPE_BF16 && p->head_dim == 128 && !(p->flags & KDA_FLAG_FORCE_SIMT)) ? 1 : 0;
 }
 
 size_t ckpt_slots(const kda_problem* p) {
@@ -97,7 +102,7 @@ size_t kda_bwd_workspace_bytes(const kda_problem* p) {
   return validate(p, false) == KDA_OK ? workspace_bytes(p) : 0;
 }
 
-int kda_kernel_family(const kda_problem* p) { return validate(p, false) == KDA_OK ? 0 : -1; }
+int kda_kernel_family(const kda_problem* p) { return validate(p, false) == KDA_OK ? family_of(p) : -1; }
 
 int kda_version(void) { return 100; }
 
@@ -135,7 +140,7 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   if (ctx && cudaMemsetAsync(ctx, 0, sizeof(int), s) != cudaSuccess)
     return fail(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
-  st = kda::launch_fwd_simt(p, a, s);
+  st = family_of(p) == 1 ? kda::launch_fwd_tc(p, a, s) : kda::launch_fwd_simt(p, a, s);
   if (st != KDA_OK) return fail(st, "forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return KDA_OK;
 }

@@ -87,6 +87,7 @@ __device__ __forceinline__ void set_status(int* status, int code) {
 
 // Host-side launchers (defined in the kernel translation units).
 kda_status launch_fwd_simt(const kda_problem* p, const FwdArgs& a, cudaStream_t s);
+kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s);
 kda_status launch_bwd_simt(const kda_problem* p, const BwdArgs& a, cudaStream_t s);
 size_t bwd_scratch_bytes_simt(const kda_problem* p, int* nctas);
 kda_status launch_bwd_simt_ctas(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas);

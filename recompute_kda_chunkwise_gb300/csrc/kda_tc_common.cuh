@@ -1,0 +1,195 @@
+// kda_tc_common.cuh -- inline-PTX helpers for the sm_103a tensor-core (tcgen05)
+// KDA kernels: TMEM allocation, tcgen05.mma issue/commit, TMEM loads, TMA
+// tensor-tile loads, mbarriers (every wait bounded) and the shared-memory
+// matrix layout the MMAs read.
+//
+// Operand layout used everywhere ("SW128 tile"): a bf16 matrix of R rows x K
+// columns (K a multiple of 64) stored K-major with the 128-byte swizzle: the
+// K extent is cut into 64-element blocks of R x 128 bytes each; inside a
+// block, row r occupies bytes (r/8)*1024 + (r%8)*128, and its 16-byte chunk c
+// (elements 8c..8c+7) is stored at chunk position c ^ (r%8). This is also
+// exactly what a TMA tile load with 128-byte swizzle writes for a 64-element
+// wide box. The same bytes read "MN-major" describe a K x R operand whose R
+// (M or N) extent is contiguous; the MMA descriptor then takes the stride
+// between 64-element R blocks as its leading byte offset.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Byte offset of element (row, k) inside an SW128 tile of `rows` rows.
+__device__ __forceinline__ uint32_t sw128_off(int row, int k, int rows) {
+  const int kb = k >> 6, w = k & 63, chunk = w >> 3, e = w & 7;
+  return static_cast<uint32_t>(kb * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 +
+                               ((chunk ^ (row & 7)) << 4) + (e << 1));
+}
+// Byte offset of the 16-byte chunk holding elements (row, 8c .. 8c+7).
+__device__ __forceinline__ uint32_t sw128_chunk(int row, int c, int rows) {
+  const int kb = c >> 3, ch = c & 7;
+  return static_cast<uint32_t>(kb * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4));
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// byte offset, stride byte offset (8-row groups, 1024 B here), version 1,
+// layout type 2 = 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+// K-major operand: K-step ks (16 elements) of the rows [row0, row0 + n) of an
+// SW128 tile with `rows` rows at shared address `tile`.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int rows, int row0, int ks) {
+  return sdesc(tile + (ks >> 2) * rows * 128 + (row0 >> 3) * 1024 + (ks & 3) * 32, 16);
+}
+// MN-major operand stored as an SW128 tile whose rows are the K index and
+// whose 64-element column blocks (stride `block_bytes`) run along M/N.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int block_bytes, int ks) {
+  return sdesc(tile + ks * 2048, block_bytes);
+}
+
+// Instruction descriptors (fp32 accumulate, shape M x N, optional MN-major
+// A / B): kind::f16 with fp16 A and B (format 0), kind::tf32 (format 2).
+__host__ __device__ constexpr uint32_t idesc(int M, int N, bool a_mn = false, bool b_mn = false) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D (+)= A B with A and B in shared memory (kind::f16, fp16 operands).
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+// D (+)= A B, kind::tf32, A read from TMEM (lane = row, one 32-bit column per
+// K element), B from shared memory.
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Generic-proxy shared-memory writes -> visible to tcgen05 / TMA (async proxy).
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 lanes x 32 columns of 32-bit values: thread (lane) gets 32 consecutive
+// columns of TMEM lane (warp's lane quarter base + lane).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Stores 32 consecutive 32-bit columns of the thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
+      "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]),
+      "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]),
+      "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31]));
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+// Bounded wait for the phase with the given parity to complete. Returns
+// false (and records KDA_ERR_TIMEOUT) if it did not complete in time.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+  const uint32_t a = smem_addr(bar);
+  for (int it = 0; it < (1 << 24); ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  set_status(status, KDA_ERR_TIMEOUT);
+  return false;
+}
+
+// TMA: 3-D tile (x = channel, y = head, z = token) of a [S][H][D] tensor into
+// shared memory, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Byte offset of element (row, k) in a 32-bit SW128 tile of `rows` rows (the
+// K extent cut into 32-element blocks of rows x 128 bytes).
+__device__ __forceinline__ uint32_t sw128_off32(int row, int k, int rows) {
+  const int kb = k >> 5, w = k & 31, chunk = w >> 2, e = w & 3;
+  return static_cast<uint32_t>(kb * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 +
+                               ((chunk ^ (row & 7)) << 4) + (e << 2));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  __half2 p = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  __nv_bfloat162 p = *reinterpret_cast<__nv_bfloat162*>(&u);
+  return __bfloat1622float2(p);
+}
+
+}  // namespace tc
+}  // namespace kda

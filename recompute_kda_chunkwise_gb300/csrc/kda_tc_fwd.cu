@@ -1,0 +1,650 @@
+// kda_tc_fwd.cu -- tcgen05 tensor-core KDA forward (bf16 inputs, D = K = V = 128,
+// chunk C = 64), one CTA of 256 threads per (sequence, head).
+//
+// Chunk math ("KDA at the production shape ...", section 2.1 op table; the
+// state recurrence of section 1.1), with G the chunk-local inclusive
+// cumulative log-decay, Gamma = exp(G), gamma = Gamma at the chunk end:
+//   Abar[r,s] = sum_i kh_ri kh_si e^{G_ri - G_si} (s < r),  M[r,s] likewise with qh (s <= r)
+//   T = (I + diag(beta) Abar)^-1,  T' = T diag(beta)
+//   W = T' (Kh*Gamma),  U = T' V,  U~ = U - W H,  O = (Qh*Gamma) H + M U~
+//   H' = diag(gamma) H + Kbar^T U~,   Kbar[s,i] = kh_si e^{G_{C-1,i} - G_si}
+// The state is kept transposed, H^T (V x D), so every tensor-core product has
+// M = 128 with the value index v (or the key index i) on the TMEM lanes; the
+// fp32 master state lives in registers (thread (v, half) holds
+// H^T[v][64*half .. 64*half+63]).
+//
+// Precision. Outputs must match an fp64 reference to 2e-2 of their RMS in the
+// max norm; bf16 operands (8-bit significands) miss that by 3-5x on these
+// heavy-tailed outputs, fp16 operands (11-bit) meet it. Every tensor-core
+// operand is therefore fp16 (bounded quantities: states, W, U~, T', M, gated
+// q/k, Kbar, and V converted from bf16), except the factors of Abar and M:
+// exp(G_r - G_s) spans e^{320} over 64 tokens at the -5 gate floor (the
+// "k/exp(cumsum g) underflows past 17 tokens" note of section 3(a)), so
+// Abar and M are built from four 16-token column blocks J, each referenced
+// at the end of block J: the row operand kh_r e^{G_r - B_{J+1}} (rows
+// r >= 16J, up to e^{80}) times the column operand kh_s e^{B_{J+1} - G_s}
+// (s in block J, down to e^{-80}). Those factors need fp32 range, so the four
+// 128 x 16 x 128 products run as kind::tf32 with the row operand written to
+// TMEM (k rows on lanes 0-63, q rows on lanes 64-127).
+//
+// The O = M U~ term dominates the remaining error (the largest outputs are
+// mostly intra-chunk), so M, U~ (in that product) and T' are carried as fp16
+// hi + lo pairs and their products take three (M U~) or two (T' products)
+// MMAs.
+//
+// Stages per chunk (sequential; every tcgen05 completion and TMA arrival is
+// awaited on an mbarrier with a bounded wait): TMA of q, k, raw gate -> row
+// norms -> gate and cumulative decay (channel-major) -> operand tiles
+// (row-major) -> four tf32 rounds for Abar | M -> T by blocked forward
+// substitution -> TMA'd V converted to fp16 -> W, U products -> -W tile ->
+// H^T products -> U~^T tile -> Kbar, M products -> state update and output.
+#include "kda_tc_common.cuh"
+
+namespace kda {
+namespace {
+using namespace tc;
+
+constexpr int kC = 64;
+constexpr int kD = 128;
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Shared-memory map (bytes from a 1024-byte aligned base).
+constexpr int OFF_STG_Q = 0;           // staged q        [64 r][128 c] bf16 SW128 (TMA)
+constexpr int OFF_STG_K = 16384;       // staged k
+constexpr int OFF_STG_G = 32768;       // staged raw gate
+constexpr int OFF_A1 = 49152;          // H^T fp16 [128 v][128 i]
+constexpr int OFF_B1 = 81920;          // [-W (64 r) ; Qh*Gamma (64 r)] x [128 i] fp16
+constexpr int OFF_B2A = 114688;        // Kbar [64 r][128 i] fp16 (read MN-major)
+constexpr int OFF_B2B = 131072;        // M [64 r][64 s] fp16
+constexpr int OFF_XW = 139264;         // Kh*Gamma [64 s][128 i] fp16 (read MN-major); later U~^T [128 v][64 r]
+constexpr int OFF_R = 155648;          // 64 KB, reused within a chunk:
+constexpr int OFF_XS = OFF_R;          //   log2 offsets G_r - B_{I+1}, fp32 [64][128] (swizzled rows)
+constexpr int OFF_BK = OFF_R + 32768;  //   column operands kh_s e^{B-G_s}, tf32 [64 s][128 i]
+constexpr int OFF_TOT = OFF_R + 61440; //   block totals [4][128] fp32 (dead before BK is written)
+constexpr int OFF_V = OFF_R;           //   then staged v (bf16 -> fp16 in place) [64 s][128 v]
+constexpr int OFF_ABAR = OFF_R + 16384;//   then Abar fp32 [64][65]
+constexpr int OFF_TF = OFF_R + 33024;  //        T fp32 [64][65]
+constexpr int OFF_TP = OFF_R + 50176;  //        T' fp16 [64 r][64 s]
+constexpr int OFF_X = OFF_R + 58368;   //        fp32 scratch [3][16][16]
+constexpr int OFF_TPL = OFF_R + 16384; //   after the inverse (Abar dead): T' low part fp16 [64 r][64 s]
+constexpr int OFF_ML = OFF_R + 24576;  //                                  M low part fp16 [64 r][64 s]
+constexpr int OFF_UL = OFF_R;          //   after the U product (v dead): U~^T low part fp16 [128 v][64 r]
+constexpr int OFF_SMALL = OFF_R + 65536;
+// small fp32 arrays
+constexpr int SM_BETA = 0, SM_IQ = 64, SM_IK = 128, SM_GAM = 192, SM_EB = 320, SM_EK = 832, SM_U = 1344;
+constexpr int SMALL_FLOATS = 1344 + 6 * 128;
+constexpr int OFF_BAR = OFF_SMALL + SMALL_FLOATS * 4;
+constexpr int SMEM_USED = OFF_BAR + 64;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
+
+// TMEM columns
+constexpr uint32_t TM_DA = 0;    // Abar (lanes 0-63) | M (lanes 64-127), 64 columns
+constexpr uint32_t TM_DW = 64;   // W^T (lanes = i), 64 columns
+constexpr uint32_t TM_DU = 128;  // U~^T, 64 columns
+constexpr uint32_t TM_DO = 192;  // O^T, 64 columns
+constexpr uint32_t TM_DH = 256;  // (Kbar^T U~)^T, 128 columns
+constexpr uint32_t TM_AJ = 256;  // tf32 row operand of the Abar | M rounds (same columns, earlier in the chunk)
+constexpr uint32_t TM_COLS = 512;
+
+struct TcFwdArgs {
+  const __nv_bfloat16* b;
+  const float* A_log;
+  const float* dt_bias;
+  __nv_bfloat16* o;
+  float* ckpt;
+  int* status;
+  const int32_t* cu;
+  int N, H;
+  float scale, lower, eps;
+};
+
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + ex2(-x * kLog2e)); }
+
+// fp32 [64][128] tile with 16-byte chunks XOR-swizzled by row (conflict-free
+// row and column walks).
+__device__ __forceinline__ uint32_t xs_off(int r, int c) {
+  return static_cast<uint32_t>(r * 512 + (c >> 5) * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + ((c & 3) << 2));
+}
+
+// T = (I + diag(beta) Abar)^-1 (fp32) by forward substitution on 16 x 16
+// blocks: diagonal blocks by columns, then T_IJ = -T_II sum_{K=J}^{I-1}
+// diag(beta) Abar_IK T_KJ level by level; finally T' = T diag(beta) (fp16).
+__device__ void tri_inverse(uint8_t* sm, const float* s_beta, int tid) {
+  float* Ab = reinterpret_cast<float*>(sm + OFF_ABAR);
+  float* Tf = reinterpret_cast<float*>(sm + OFF_TF);
+  float* X = reinterpret_cast<float*>(sm + OFF_X);
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int x = tid; x < 64 * 65; x += kThreads) Tf[x] = 0.f;
+  __syncthreads();
+  if (warp < 4 && lane < 16) {
+    const int base = 16 * warp, j = lane;
+    float col[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float v = (r == j) ? 1.f : 0.f;
+      if (r > j) {
+        const float br = s_beta[base + r];
+#pragma unroll
+        for (int s = 0; s < r; ++s)
+          if (s >= j) v -= br * Ab[(base + r) * 65 + base + s] * col[s];
+      }
+      col[r] = v;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Tf[(base + r) * 65 + base + j] = col[r];
+  }
+  __syncthreads();
+  for (int d = 1; d <= 3; ++d) {
+    const int nb = 4 - d;
+    for (int x = tid; x < nb * 256; x += kThreads) {
+      const int b = x >> 8, e = x & 255, rr = e >> 4, cc = e & 15;
+      const int J = b, I = b + d, row = 16 * I + rr;
+      float acc = 0.f;
+      for (int K = J; K < I; ++K)
+#pragma unroll
+        for (int s = 0; s < 16; ++s) acc += Ab[row * 65 + 16 * K + s] * Tf[(16 * K + s) * 65 + 16 * J + cc];
+      X[b * 256 + e] = s_beta[row] * acc;
+    }
+    __syncthreads();
+    for (int x = tid; x < nb * 256; x += kThreads) {
+      const int b = x >> 8, e = x & 255, rr = e >> 4, cc = e & 15;
+      const int J = b, I = b + d;
+      float acc = 0.f;
+#pragma unroll
+      for (int s = 0; s < 16; ++s) acc += Tf[(16 * I + rr) * 65 + 16 * I + s] * X[b * 256 + s * 16 + cc];
+      Tf[(16 * I + rr) * 65 + 16 * J + cc] = -acc;
+    }
+    __syncthreads();
+  }
+  for (int x = tid; x < 64 * 32; x += kThreads) {
+    const int r = x >> 5, s = 2 * (x & 31);
+    const float t0 = Tf[r * 65 + s] * s_beta[s], t1 = Tf[r * 65 + s + 1] * s_beta[s + 1];
+    const uint32_t hi = pack_h2(t0, t1);
+    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    *reinterpret_cast<uint32_t*>(sm + OFF_TP + sw128_off(r, s, 64)) = hi;
+    *reinterpret_cast<uint32_t*>(sm + OFF_TPL + sw128_off(r, s, 64)) = pack_h2(t0 - hf.x, t1 - hf.y);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
+                      const TcFwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_addr(sm);
+  float* smf = reinterpret_cast<float*>(sm + OFF_SMALL);
+  float* s_beta = smf + SM_BETA;
+  float* s_iq = smf + SM_IQ;
+  float* s_ik = smf + SM_IK;
+  float* s_gam = smf + SM_GAM;
+  float* s_eB = smf + SM_EB;  // [4][128]  2^{B_{I+1}}
+  float* s_eK = smf + SM_EK;  // [4][128]  2^{G_end - B_{I+1}}
+  float* s_u = smf + SM_U;    // [6][128]  2^{B_{I+1} - B_{J+1}}, pair I(I-1)/2 + J
+  float* s_tot = reinterpret_cast<float*>(sm + OFF_TOT);
+  uint64_t* bar_qkg = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint64_t* bar_v = bar_qkg + 1;
+  uint64_t* bar_mma = bar_qkg + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_qkg + 3);
+  int* s_fail = reinterpret_cast<int*>(bar_qkg + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  const int64_t bos = a.cu[n], eos = a.cu[n + 1];
+  const int nchunks = static_cast<int>((eos - bos + kC - 1) / kC);
+
+  if (tid == 0) {
+    mbar_init(bar_qkg, 1);
+    mbar_init(bar_v, 1);
+    mbar_init(bar_mma, 1);
+    *s_fail = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(s_tmem, TM_COLS);
+  for (int x = tid; x < 32768 / 16; x += kThreads) reinterpret_cast<uint4*>(sm + OFF_A1)[x] = make_uint4(0, 0, 0, 0);
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+
+  // channel-major role: channel pair (c0, c0+1), rows 16*Ib .. 16*Ib+15 (sub-block Ib)
+  const int pp = tid & 63, Ib = tid >> 6, c0 = 2 * pp;
+  const float expA = expf(a.A_log[h]);
+  const float dtb0 = a.dt_bias[h * kD + c0], dtb1 = a.dt_bias[h * kD + c0 + 1];
+  const float Lg = a.lower * kLog2e;
+  // lane roles: TMEM lane quarter q4, column half hh
+  const int q4 = warp & 3, hh = warp >> 2, lrow = 32 * q4 + lane;
+  const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
+  // row-major role (operand tiles): k rows (q4 < 2) or q rows (q4 >= 2)
+  const bool krole = q4 < 2;
+  const int prow = 32 * (q4 & 1) + lane, pI = prow >> 4;
+  float Hst[64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j) Hst[j] = 0.f;
+  uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0;
+
+  auto issue_qkg = [&](int t) {
+    mbar_expect_tx(bar_qkg, 6 * 8192);
+    tma_load_3d(sm + OFF_STG_Q, &tmq, 0, h, t, bar_qkg);
+    tma_load_3d(sm + OFF_STG_Q + 8192, &tmq, 64, h, t, bar_qkg);
+    tma_load_3d(sm + OFF_STG_K, &tmk, 0, h, t, bar_qkg);
+    tma_load_3d(sm + OFF_STG_K + 8192, &tmk, 64, h, t, bar_qkg);
+    tma_load_3d(sm + OFF_STG_G, &tmg, 0, h, t, bar_qkg);
+    tma_load_3d(sm + OFF_STG_G + 8192, &tmg, 64, h, t, bar_qkg);
+  };
+  auto issue_v = [&](int t) {
+    mbar_expect_tx(bar_v, 2 * 8192);
+    tma_load_3d(sm + OFF_V, &tmv, 0, h, t, bar_v);
+    tma_load_3d(sm + OFF_V + 8192, &tmv, 64, h, t, bar_v);
+  };
+#define KDA_WAIT(bar, ph)                           \
+  do {                                              \
+    if (!mbar_wait(bar, ph, a.status)) *s_fail = 1; \
+    ph ^= 1u;                                       \
+  } while (0)
+#define KDA_SYNC_OR_BAIL()      \
+  do {                          \
+    __syncthreads();            \
+    if (*s_fail) goto teardown; \
+  } while (0)
+
+  if (tid == 0 && nchunks > 0) issue_qkg(static_cast<int>(bos));
+
+  for (int c = 0; c < nchunks; ++c) {
+    const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
+    const int rows = static_cast<int>(min(static_cast<int64_t>(kC), eos - t0));
+
+    if (a.ckpt != nullptr && (c % (kCkptTokens / kC)) == 0) {
+      float* dst = a.ckpt + (ckpt_slot(bos, n, c / (kCkptTokens / kC)) * a.H + h) * static_cast<int64_t>(kD * kD);
+#pragma unroll
+      for (int j = 0; j < 64; ++j) dst[(64 * hh + j) * kD + lrow] = Hst[j];
+    }
+
+    KDA_WAIT(bar_qkg, ph_qkg);
+    // ---- row norms and beta: warp w handles rows 8w .. 8w+7 ----
+#pragma unroll 1
+    for (int rr = 0; rr < 8; ++rr) {
+      const int r = warp * 8 + rr;
+      const uint2 qv = *reinterpret_cast<const uint2*>(sm + OFF_STG_Q + sw128_off(r, 4 * lane, 64));
+      const uint2 kv = *reinterpret_cast<const uint2*>(sm + OFF_STG_K + sw128_off(r, 4 * lane, 64));
+      const float2 q01 = unpack_bf16(qv.x), q23 = unpack_bf16(qv.y);
+      const float2 k01 = unpack_bf16(kv.x), k23 = unpack_bf16(kv.y);
+      float sq = q01.x * q01.x + q01.y * q01.y + q23.x * q23.x + q23.y * q23.y;
+      float sk = k01.x * k01.x + k01.y * k01.y + k23.x * k23.x + k23.y * k23.y;
+      sq = warp_sum(sq);
+      sk = warp_sum(sk);
+      if (lane == 0) {
+        const bool ok = r < rows;
+        const float nq = sqrtf(sq + a.eps), nk = sqrtf(sk + a.eps);
+        s_iq[r] = (ok && nq > 0.f) ? a.scale / nq : 0.f;
+        s_ik[r] = (ok && nk > 0.f) ? 1.f / nk : 0.f;
+        s_beta[r] = ok ? sigmoidf_(__bfloat162float(a.b[(t0 + r) * a.H + h])) : 0.f;
+      }
+    }
+    // ---- gate and cumulative log2-decay of the thread's 16-row block ----
+    {
+      float gl0[16], gl1[16], acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int r = 16 * Ib + j;
+        const float2 g2 = unpack_bf16(*reinterpret_cast<const uint32_t*>(sm + OFF_STG_G + sw128_off(r, c0, 64)));
+        const float d0 = r < rows ? Lg * sigmoid_fast(expA * (g2.x + dtb0)) : 0.f;
+        const float d1 = r < rows ? Lg * sigmoid_fast(expA * (g2.y + dtb1)) : 0.f;
+        acc0 += d0;
+        acc1 += d1;
+        gl0[j] = acc0;
+        gl1[j] = acc1;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j)  // G_r - B_{I+1} >= 0
+        *reinterpret_cast<float2*>(sm + OFF_XS + xs_off(16 * Ib + j, c0)) = make_float2(gl0[j] - acc0, gl1[j] - acc1);
+      s_tot[Ib * 128 + c0] = acc0;
+      s_tot[Ib * 128 + c0 + 1] = acc1;
+    }
+    __syncthreads();
+    // ---- per-channel block references ----
+    if (tid < kD) {
+      const int ch = tid;
+      float B[5];
+      B[0] = 0.f;
+#pragma unroll
+      for (int I = 0; I < 4; ++I) B[I + 1] = B[I] + s_tot[I * 128 + ch];
+      s_gam[ch] = ex2(B[4]);
+#pragma unroll
+      for (int I = 0; I < 4; ++I) {
+        s_eB[I * 128 + ch] = ex2(B[I + 1]);
+        s_eK[I * 128 + ch] = ex2(B[4] - B[I + 1]);
+#pragma unroll
+        for (int J = 0; J < I; ++J) s_u[(I * (I - 1) / 2 + J) * 128 + ch] = ex2(B[I + 1] - B[J + 1]);
+      }
+    }
+    __syncthreads();
+
+    // ---- operand tiles, row-major: thread = one row (k or q) x 64 channels ----
+    float rowf[64];  // kh e^{G_r - B_{I+1}} (k rows) or qh e^{G_r - B_{I+1}} (q rows)
+    {
+      const int r = prow;
+      const float nrm = krole ? s_ik[r] : s_iq[r];
+      const uint32_t src = krole ? OFF_STG_K : OFF_STG_Q;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const int ch0 = 64 * hh + 8 * cc;
+        const uint4 raw = *reinterpret_cast<const uint4*>(sm + src + sw128_chunk(r, 8 * hh + cc, 64));
+        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+        const float4 x0 = *reinterpret_cast<const float4*>(sm + OFF_XS + xs_off(r, ch0));
+        const float4 x1 = *reinterpret_cast<const float4*>(sm + OFF_XS + xs_off(r, ch0 + 4));
+        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        uint32_t o1[4], o2[4];
+        float bk[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 vv = unpack_bf16(rw[e]);
+          const int ca = ch0 + 2 * e, cb = ca + 1;
+          const float ha = vv.x * nrm, hb = vv.y * nrm;
+          const float sa = ex2(xv[2 * e]), sbv = ex2(xv[2 * e + 1]);  // e^{G_r - B_{I+1}} >= 1
+          rowf[8 * cc + 2 * e] = ha * sa;
+          rowf[8 * cc + 2 * e + 1] = hb * sbv;
+          const float ga = sa * s_eB[pI * 128 + ca], gb = sbv * s_eB[pI * 128 + cb];  // Gamma_r
+          if (krole) {
+            const float ia = ex2(-xv[2 * e]), ib = ex2(-xv[2 * e + 1]);  // e^{B_{I+1} - G_r} <= 1
+            o1[e] = pack_h2(ha * ga, hb * gb);                                               // Kh*Gamma
+            o2[e] = pack_h2(ha * ia * s_eK[pI * 128 + ca], hb * ib * s_eK[pI * 128 + cb]);  // Kbar
+            bk[2 * e] = ha * ia;
+            bk[2 * e + 1] = hb * ib;
+          } else {
+            o1[e] = pack_h2(ha * ga, hb * gb);  // Qh*Gamma
+          }
+        }
+        if (krole) {
+          *reinterpret_cast<uint4*>(sm + OFF_XW + sw128_chunk(r, 8 * hh + cc, 64)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+          *reinterpret_cast<uint4*>(sm + OFF_B2A + sw128_chunk(r, 8 * hh + cc, 64)) =
+              make_uint4(o2[0], o2[1], o2[2], o2[3]);
+          *reinterpret_cast<float4*>(sm + OFF_BK + sw128_off32(r, ch0, 64)) = make_float4(bk[0], bk[1], bk[2], bk[3]);
+          *reinterpret_cast<float4*>(sm + OFF_BK + sw128_off32(r, ch0 + 4, 64)) = make_float4(bk[4], bk[5], bk[6], bk[7]);
+        } else {
+          *reinterpret_cast<uint4*>(sm + OFF_B1 + sw128_chunk(64 + r, 8 * hh + cc, 128)) =
+              make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        }
+      }
+    }
+    fence_async_smem();
+    KDA_SYNC_OR_BAIL();
+    // staged q, k, g and the decay offsets are consumed: fetch v of this
+    // chunk (into the offsets' space) and q, k, g of the next chunk
+    if (tid == 0) {
+      issue_v(static_cast<int>(t0));
+      if (c + 1 < nchunks) issue_qkg(static_cast<int>(t0 + kC));
+    }
+
+    // ---- Abar | M by column block J: tf32, row operand in TMEM ----
+#pragma unroll 1
+    for (int J = 0; J < 4; ++J) {
+      if (J > 0) KDA_WAIT(bar_mma, ph_mma);
+      // rows of blocks before J do not contribute to column block J (s > r),
+      // but every lane stores: tcgen05.st is warp-collective
+      {
+        float uv[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int ch = 64 * hh + 32 * half + j;
+            const float u = (J < pI) ? s_u[(pI * (pI - 1) / 2 + J) * 128 + ch] : 1.f;
+            uv[j] = rowf[32 * half + j] * u;
+          }
+          tmem_st32(tmem + tlane + TM_AJ + 64 * hh + 32 * half, uv);
+        }
+      }
+      tmem_st_wait();
+      fence_before_sync();
+      KDA_SYNC_OR_BAIL();
+      if (tid == 0) {
+        fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks)
+          mma_tf32_ta(tmem + TM_DA + 16 * J, tmem + TM_AJ + 8 * ks, desc_kmajor(sb + OFF_BK, 64, 16 * J, ks),
+                      idesc_tf32(128, 16), ks > 0);
+        mma_commit(bar_mma);
+      }
+    }
+    KDA_WAIT(bar_mma, ph_mma);
+    fence_after_sync();
+
+    // ---- Abar (fp32, for the inverse) and M (fp16 operand) out of TMEM ----
+    {
+      float v[32];
+      tmem_ld32(tmem + tlane + TM_DA + 32 * hh, v);
+      const int m = lrow;
+      if (m < 64) {
+        float* Ab = reinterpret_cast<float*>(sm + OFF_ABAR);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int s = 32 * hh + j;
+          Ab[m * 65 + s] = s < m ? v[j] : 0.f;
+        }
+      } else {
+        const int r = m - 64;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int s = 32 * hh + 8 * cc + 2 * e;
+            w[e] = pack_h2(s <= r ? v[8 * cc + 2 * e] : 0.f, s + 1 <= r ? v[8 * cc + 2 * e + 1] : 0.f);
+          }
+          *reinterpret_cast<uint4*>(sm + OFF_B2B + sw128_chunk(r, 4 * hh + cc, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    fence_before_sync();
+    __syncthreads();
+    tri_inverse(sm, s_beta, tid);
+    // ---- low part of M (its fp32 values are still in TMEM) ----
+    {
+      float v[32];
+      tmem_ld32(tmem + tlane + TM_DA + 32 * hh, v);
+      if (lrow >= 64) {
+        const int r = lrow - 64;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int s = 32 * hh + 8 * cc + 2 * e;
+            const float m0 = s <= r ? v[8 * cc + 2 * e] : 0.f, m1 = s + 1 <= r ? v[8 * cc + 2 * e + 1] : 0.f;
+            const uint32_t hi = pack_h2(m0, m1);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+            w[e] = pack_h2(m0 - hf.x, m1 - hf.y);
+          }
+          *reinterpret_cast<uint4*>(sm + OFF_ML + sw128_chunk(r, 4 * hh + cc, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    // ---- v (bf16, TMA) -> fp16 in place ----
+    KDA_WAIT(bar_v, ph_v);
+    {
+      uint4* vt = reinterpret_cast<uint4*>(sm + OFF_V);
+#pragma unroll
+      for (int x = tid; x < 16384 / 16; x += kThreads) {
+        uint4 w = vt[x];
+        const float2 a0 = unpack_bf16(w.x), a1 = unpack_bf16(w.y), a2 = unpack_bf16(w.z), a3 = unpack_bf16(w.w);
+        vt[x] = make_uint4(pack_h2(a0.x, a0.y), pack_h2(a1.x, a1.y), pack_h2(a2.x, a2.y), pack_h2(a3.x, a3.y));
+      }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    KDA_SYNC_OR_BAIL();
+    if (tid == 0) {
+      fence_after_sync();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)  // W^T = (Kh Gamma)^T (T'hi + T'lo)^T
+        mma(tmem + TM_DW, desc_mnmajor(sb + OFF_XW, 8192, ks & 3),
+            desc_kmajor(sb + (ks < 4 ? OFF_TP : OFF_TPL), 64, 0, ks & 3), idesc(128, 64, true, false), ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)  // U^T = V^T (T'hi + T'lo)^T
+        mma(tmem + TM_DU, desc_mnmajor(sb + OFF_V, 8192, ks & 3),
+            desc_kmajor(sb + (ks < 4 ? OFF_TP : OFF_TPL), 64, 0, ks & 3), idesc(128, 64, true, false), ks > 0);
+      mma_commit(bar_mma);
+    }
+    KDA_WAIT(bar_mma, ph_mma);
+    fence_after_sync();
+
+    // ---- -W into rows 0..63 of B1 ----
+    {
+      float v[32];
+      tmem_ld32(tmem + tlane + TM_DW + 32 * hh, v);  // lane = channel i, columns r
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        *reinterpret_cast<__half*>(sm + OFF_B1 + sw128_off(32 * hh + j, lrow, 128)) = __float2half_rn(-v[j]);
+    }
+    fence_async_smem();
+    fence_before_sync();
+    KDA_SYNC_OR_BAIL();
+    if (tid == 0) {
+      fence_after_sync();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)  // U~^T = U^T + H^T (-W)^T
+        mma(tmem + TM_DU, desc_kmajor(sb + OFF_A1, 128, 0, ks), desc_kmajor(sb + OFF_B1, 128, 0, ks), idesc(128, 64), 1);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)  // O^T = H^T (Qh Gamma)^T
+        mma(tmem + TM_DO, desc_kmajor(sb + OFF_A1, 128, 0, ks), desc_kmajor(sb + OFF_B1, 128, 64, ks), idesc(128, 64),
+            ks > 0);
+      mma_commit(bar_mma);
+    }
+    KDA_WAIT(bar_mma, ph_mma);
+    fence_after_sync();
+
+    // ---- U~^T (fp16) as the A operand of the Kbar and M products ----
+    {
+      float v[32];
+      tmem_ld32(tmem + tlane + TM_DU + 32 * hh, v);  // lane = v, columns r
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = v[8 * cc + 2 * e], x1 = v[8 * cc + 2 * e + 1];
+          hw[e] = pack_h2(x0, x1);
+          const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
+          lw[e] = pack_h2(x0 - hf.x, x1 - hf.y);
+        }
+        *reinterpret_cast<uint4*>(sm + OFF_XW + sw128_chunk(lrow, 4 * hh + cc, 128)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(sm + OFF_UL + sw128_chunk(lrow, 4 * hh + cc, 128)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    KDA_SYNC_OR_BAIL();
+    if (tid == 0) {
+      fence_after_sync();
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)  // (Kbar^T U~)^T = U~^T Kbar
+        mma(tmem + TM_DH, desc_kmajor(sb + OFF_XW, 128, 0, ks), desc_mnmajor(sb + OFF_B2A, 8192, ks),
+            idesc(128, 128, false, true), ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 12; ++ks) {  // O^T += U~hi^T Mhi^T + U~hi^T Mlo^T + U~lo^T Mhi^T
+        const uint32_t ua = (ks < 8) ? OFF_XW : OFF_UL;
+        const uint32_t mb = (ks >= 4 && ks < 8) ? OFF_ML : OFF_B2B;
+        mma(tmem + TM_DO, desc_kmajor(sb + ua, 128, 0, ks & 3), desc_kmajor(sb + mb, 64, 0, ks & 3), idesc(128, 64), 1);
+      }
+      mma_commit(bar_mma);
+    }
+    KDA_WAIT(bar_mma, ph_mma);
+    fence_after_sync();
+
+    // ---- state update (fp32 registers), next H^T operand, output ----
+    {
+      float v[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld32(tmem + tlane + TM_DH + 64 * hh + 32 * half, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) Hst[32 * half + j] = s_gam[64 * hh + 32 * half + j] * Hst[32 * half + j] + v[j];
+      }
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(lrow, 8 * hh + cc, 128)) =
+            make_uint4(pack_h2(Hst[8 * cc], Hst[8 * cc + 1]), pack_h2(Hst[8 * cc + 2], Hst[8 * cc + 3]),
+                       pack_h2(Hst[8 * cc + 4], Hst[8 * cc + 5]), pack_h2(Hst[8 * cc + 6], Hst[8 * cc + 7]));
+      tmem_ld32(tmem + tlane + TM_DO + 32 * hh, v);  // lane = v, columns r
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int r = 32 * hh + j;
+        if (r < rows) a.o[((t0 + r) * a.H + h) * kD + lrow] = __float2bfloat16_rn(v[j]);
+      }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    KDA_SYNC_OR_BAIL();
+  }
+#undef KDA_WAIT
+#undef KDA_SYNC_OR_BAIL
+teardown:
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+// [S][H][128] bf16 tensor, box = 64 channels x 1 head x 64 tokens, 128-byte swizzle.
+bool make_tma_map_bf16(CUtensorMap* m, const void* base, int64_t S, int H) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(H) * kD * 2};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s) {
+  if (p->head_dim != kD || p->dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mv, mg;
+  if (!make_tma_map_bf16(&mq, a.q, p->total_tokens, p->num_heads) ||
+      !make_tma_map_bf16(&mk, a.k, p->total_tokens, p->num_heads) ||
+      !make_tma_map_bf16(&mv, a.v, p->total_tokens, p->num_heads) ||
+      !make_tma_map_bf16(&mg, a.g, p->total_tokens, p->num_heads))
+    return KDA_ERR_CUDA;
+  TcFwdArgs t;
+  t.b = static_cast<const __nv_bfloat16*>(a.b);
+  t.A_log = a.A_log;
+  t.dt_bias = a.dt_bias;
+  t.o = static_cast<__nv_bfloat16*>(a.o);
+  t.ckpt = a.ckpt;
+  t.status = a.status;
+  t.cu = a.cu;
+  t.N = a.N;
+  t.H = a.H;
+  t.scale = a.scale;
+  t.lower = a.lower;
+  t.eps = a.eps;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  if (cudaFuncSetAttribute(kda_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  const int grid = p->num_seqs * p->num_heads;
+  if (grid > 0) kda_fwd_tc_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(mq, mk, mv, mg, t);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace kda

@@ -29,7 +29,7 @@ class KdaProblem(ctypes.Structure):
                 ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("gate_lower_bound", ctypes.c_float), ("l2_eps", ctypes.c_float),
-                ("reserved", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p)]
+                ("flags", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p)]
 
 
 class KdaError(RuntimeError):
@@ -83,13 +83,16 @@ def _check(status: int, where: str):
         raise KdaError(status, where, msg)
 
 
+KDA_FLAG_FORCE_SIMT = 1
+
+
 def make_problem(total_tokens: int, num_seqs: int, num_heads: int, head_dim: int, dtype,
                  cu_seqlens=None, scale: float = 1.0, lower_bound: float = -5.0,
-                 eps: float = 1e-6) -> KdaProblem:
+                 eps: float = 1e-6, flags: int = 0) -> KdaProblem:
     code = _DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     ptr = 0 if cu_seqlens is None else cu_seqlens.data_ptr()
     return KdaProblem(int(total_tokens), int(num_seqs), int(num_heads), int(head_dim), code,
-                      float(scale), float(lower_bound), float(eps), 0, ptr)
+                      float(scale), float(lower_bound), float(eps), int(flags), ptr)
 
 
 def ctx_bytes(p: KdaProblem) -> int:
@@ -112,7 +115,7 @@ def _stream_handle(device) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
-def _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps):
+def _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps, flags=0):
     if q.dim() != 3:
         raise ValueError("q must be [S, H, D]")
     S, H, D = q.shape
@@ -120,7 +123,8 @@ def _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps):
         raise ValueError(f"unsupported dtype {q.dtype}")
     if cu_seqlens.dtype != torch.int32 or cu_seqlens.device != q.device:
         raise ValueError("cu_seqlens must be int32 on the same device as q")
-    return make_problem(S, cu_seqlens.numel() - 1, H, D, q.dtype, cu_seqlens, scale, lower_bound, eps)
+    return make_problem(S, cu_seqlens.numel() - 1, H, D, q.dtype, cu_seqlens, scale, lower_bound, eps,
+                        flags)
 
 
 def _check_tensors(q, *others, params=()):
@@ -134,11 +138,11 @@ def _check_tensors(q, *others, params=()):
 
 def kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
             lower_bound: float = -5.0, eps: float = 1e-6, save_ctx: bool = True, out=None,
-            ctx=None):
+            ctx=None, flags: int = 0):
     """Forward. Returns (o, ctx); ctx is None when save_ctx is False. ``out``
     and ``ctx`` may be preallocated (ctx of at least ctx_bytes(problem))."""
     _check_tensors(q, k, v, g, beta, params=(A_log, dt_bias))
-    p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps)
+    p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps, flags)
     o = torch.empty_like(q) if out is None else out
     if not save_ctx:
         ctx = None
@@ -153,10 +157,11 @@ def kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
 
 
 def kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO, ctx, *, scale: float = 1.0,
-            lower_bound: float = -5.0, eps: float = 1e-6, workspace=None, outs=None):
+            lower_bound: float = -5.0, eps: float = 1e-6, workspace=None, outs=None,
+            flags: int = 0):
     """Backward. Returns dict dq, dk, dv, dg, dbeta, dA_log, ddt_bias."""
     _check_tensors(q, k, v, g, beta, dO, params=(A_log, dt_bias))
-    p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps)
+    p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps, flags)
     if outs is None:
         outs = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                     dg=torch.empty_like(g), dbeta=torch.empty_like(beta),

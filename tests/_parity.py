@@ -10,11 +10,13 @@ OUT_NAMES = ["o", "dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias"]
 TOL = {torch.bfloat16: 2e-2, torch.float32: 1e-4}
 
 
-def run_gpu(inp, scale=1.0, lower=-5.0, eps=1e-6):
+def run_gpu(inp, scale=1.0, lower=-5.0, eps=1e-6, flags=0):
     o, ctx = K.kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["A_log"],
-                       inp["dt_bias"], inp["cu_seqlens"], scale=scale, lower_bound=lower, eps=eps)
+                       inp["dt_bias"], inp["cu_seqlens"], scale=scale, lower_bound=lower, eps=eps,
+                       flags=flags)
     r = K.kda_bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["A_log"], inp["dt_bias"],
-                  inp["cu_seqlens"], inp["dO"], ctx, scale=scale, lower_bound=lower, eps=eps)
+                  inp["cu_seqlens"], inp["dO"], ctx, scale=scale, lower_bound=lower, eps=eps,
+                  flags=flags)
     torch.cuda.synchronize()
     r["o"] = o
     return r, ctx

@@ -133,3 +133,22 @@ def test_empty_input():
     torch.cuda.synchronize()
     assert o.numel() == 0
     assert torch.all(r["dA_log"] == 0) and torch.all(r["ddt_bias"] == 0)
+
+
+def test_forced_simt_kernels_bf16_d128():
+    # KDA_FLAG_FORCE_SIMT: the fp32 CUDA-core kernels on a problem that would
+    # otherwise use the tensor-core forward
+    from recompute_kda_chunkwise_gb300 import kda as K
+    w = Workload("forced_simt", (1100, 77), 3, 128, "bf16", seed=7900, param_std=0.3)
+    inp = to_dev(make_inputs(w))
+    gpu, _ = run_gpu(inp, flags=K.KDA_FLAG_FORCE_SIMT)
+    ref = oracle_for(inp)
+    compare(gpu, ref, TOL[torch.bfloat16])
+
+
+def test_kernel_family_dispatch():
+    from recompute_kda_chunkwise_gb300 import kda as K
+    assert K.kernel_family(K.make_problem(64, 1, 2, 128, torch.bfloat16)) == 1
+    assert K.kernel_family(K.make_problem(64, 1, 2, 128, torch.bfloat16, flags=1)) == 0
+    assert K.kernel_family(K.make_problem(64, 1, 2, 64, torch.bfloat16)) == 0
+    assert K.kernel_family(K.make_problem(64, 1, 2, 128, torch.float32)) == 0
