@@ -175,7 +175,7 @@ const char* kda_status_string(kda_status s);
  * overwritten by the next failing call on that thread). */
 const char* kda_last_error_message(void);
 
-/* Which kernel family a problem's forward dispatches to: 0 = fp32 CUDA-core
+/* Which kernel family a problem's forward and backward dispatch to: 0 = fp32 CUDA-core
  * (SIMT) kernels, 1 = tcgen05 tensor-core kernels (bf16, head_dim 128,
  * unless KDA_FLAG_FORCE_SIMT); -1 for an invalid or unsupported problem.
  * Host only. */

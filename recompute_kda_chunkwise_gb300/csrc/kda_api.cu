@@ -52,7 +52,7 @@ kda_status validate(const kda_problem* p, bool need_ptrs = true) {
   return KDA_OK;
 }
 
-// Forward kernel family: tcgen05 kernels for bf16 D = 128, else fp32 SIMT.
+// Kernel family of both passes: tcgen05 kernels for bf16 D = 128, else fp32 SIMT.
 int family_of(const kda_problem* p) {
   return (p->dtype == KDA_DTYPE_BF16 && p->head_dim == 128 && !(p->flags & KDA_FLAG_FORCE_SIMT)) ? 1 : 0;
 }
@@ -70,8 +70,15 @@ size_t partial_bytes(const kda_problem* p) {
   return round_up((size_t)p->num_seqs * p->num_heads * (p->head_dim + 1) * sizeof(float), 256);
 }
 
+int tc_bwd_ctas(const kda_problem* p) {
+  const int64_t items = (int64_t)p->num_seqs * p->num_heads;
+  return (int)(items < kda::kTcBwdCtas ? items : kda::kTcBwdCtas);
+}
+
 size_t workspace_bytes(const kda_problem* p) {
-  return kda::kHeaderBytes + partial_bytes(p) + kda::bwd_scratch_bytes_simt(p, nullptr);
+  const size_t scratch = family_of(p) == 1 ? (size_t)tc_bwd_ctas(p) * kda::bwd_scratch_bytes_per_cta_tc()
+                                           : kda::bwd_scratch_bytes_simt(p, nullptr);
+  return kda::kHeaderBytes + partial_bytes(p) + scratch;
 }
 
 #define CHECK_PTR(ptr)                                                                   \
@@ -176,7 +183,7 @@ kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const voi
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess)
     return fail(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
-  st = kda::launch_bwd_simt(p, a, s);
+  st = family_of(p) == 1 ? kda::launch_bwd_tc(p, a, s, tc_bwd_ctas(p)) : kda::launch_bwd_simt(p, a, s);
   if (st != KDA_OK) return fail(st, "backward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return KDA_OK;
 }

@@ -92,6 +92,10 @@ kda_status launch_bwd_simt(const kda_problem* p, const BwdArgs& a, cudaStream_t 
 size_t bwd_scratch_bytes_simt(const kda_problem* p, int* nctas);
 kda_status launch_bwd_simt_ctas(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas);
 size_t bwd_scratch_bytes_per_cta_simt(const kda_problem* p);
+size_t bwd_scratch_bytes_per_cta_tc();
+kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas);
+// CTAs of the tensor-core backward: one per SM of a 152-SM part (persistent).
+constexpr int kTcBwdCtas = 152;
 
 // Host helpers shared by the entry points (defined in kda_api.cu).
 kda_status validate_problem(const kda_problem* p);

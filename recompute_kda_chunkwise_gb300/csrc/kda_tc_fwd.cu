@@ -84,7 +84,8 @@ constexpr uint32_t TM_DW = 64;   // W^T (lanes = i), 64 columns
 constexpr uint32_t TM_DU = 128;  // U~^T, 64 columns
 constexpr uint32_t TM_DO = 192;  // O^T, 64 columns
 constexpr uint32_t TM_DH = 256;  // (Kbar^T U~)^T, 128 columns
-constexpr uint32_t TM_AJ = 256;  // tf32 row operand of the Abar | M rounds (same columns, earlier in the chunk)
+constexpr uint32_t TM_AJ = 256;  // tf32 row operand of the Abar | M rounds, double-buffered:
+                                 // rounds 0, 2 at 256.. (the DH columns, free then), rounds 1, 3 at 384..
 constexpr uint32_t TM_COLS = 512;
 
 struct TcFwdArgs {
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_mma = bar_qkg + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_qkg + 3);
   int* s_fail = reinterpret_cast<int*>(bar_qkg + 4);
+  uint64_t* bar_odd = bar_qkg + 5;  // completions of the odd Abar | M rounds
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_qkg, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_odd, 1);
     *s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float Hst[64];
 #pragma unroll
   for (int j = 0; j < 64; ++j) Hst[j] = 0.f;
-  uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0;
+  uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0, ph_odd = 0;
 
   auto issue_qkg = [&](int t) {
     mbar_expect_tx(bar_qkg, 6 * 8192);
@@ -262,9 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 64; ++j) dst[(64 * hh + j) * kD + lrow] = Hst[j];
     }
 
+    if (tid < kC) {
+      const int r = tid;
+      s_beta[r] = r < rows ? sigmoidf_(__bfloat162float(a.b[(t0 + r) * a.H + h])) : 0.f;
+    }
     KDA_WAIT(bar_qkg, ph_qkg);
-    // ---- row norms and beta: warp w handles rows 8w .. 8w+7 ----
-#pragma unroll 1
+    // ---- row norms: warp w handles rows 8w .. 8w+7 ----
+#pragma unroll
     for (int rr = 0; rr < 8; ++rr) {
       const int r = warp * 8 + rr;
       const uint2 qv = *reinterpret_cast<const uint2*>(sm + OFF_STG_Q + sw128_off(r, 4 * lane, 64));
@@ -280,7 +287,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float nq = sqrtf(sq + a.eps), nk = sqrtf(sk + a.eps);
         s_iq[r] = (ok && nq > 0.f) ? a.scale / nq : 0.f;
         s_ik[r] = (ok && nk > 0.f) ? 1.f / nk : 0.f;
-        s_beta[r] = ok ? sigmoidf_(__bfloat162float(a.b[(t0 + r) * a.H + h])) : 0.f;
       }
     }
     // ---- gate and cumulative log2-decay of the thread's 16-row block ----
@@ -381,7 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- Abar | M by column block J: tf32, row operand in TMEM ----
 #pragma unroll 1
     for (int J = 0; J < 4; ++J) {
-      if (J > 0) KDA_WAIT(bar_mma, ph_mma);
+      const uint32_t aj = TM_AJ + 128 * (J & 1);
+      // round J-2 read this buffer; even rounds complete on bar_mma, odd ones on
+      // bar_odd, so no barrier ever has two unobserved phases
+      if (J == 2) KDA_WAIT(bar_mma, ph_mma);
+      if (J == 3) KDA_WAIT(bar_odd, ph_odd);
       // rows of blocks before J do not contribute to column block J (s > r),
       // but every lane stores: tcgen05.st is warp-collective
       {
@@ -394,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float u = (J < pI) ? s_u[(pI * (pI - 1) / 2 + J) * 128 + ch] : 1.f;
             uv[j] = rowf[32 * half + j] * u;
           }
-          tmem_st32(tmem + tlane + TM_AJ + 64 * hh + 32 * half, uv);
+          tmem_st32(tmem + tlane + aj + 64 * hh + 32 * half, uv);
         }
       }
       tmem_st_wait();
@@ -404,12 +414,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < 16; ++ks)
-          mma_tf32_ta(tmem + TM_DA + 16 * J, tmem + TM_AJ + 8 * ks, desc_kmajor(sb + OFF_BK, 64, 16 * J, ks),
+          mma_tf32_ta(tmem + TM_DA + 16 * J, tmem + aj + 8 * ks, desc_kmajor(sb + OFF_BK, 64, 16 * J, ks),
                       idesc_tf32(128, 16), ks > 0);
-        mma_commit(bar_mma);
+        mma_commit((J & 1) ? bar_odd : bar_mma);
       }
     }
-    KDA_WAIT(bar_mma, ph_mma);
+    KDA_WAIT(bar_mma, ph_mma);  // round 2
+    KDA_WAIT(bar_odd, ph_odd);  // round 3
     fence_after_sync();
 
     // ---- Abar (fp32, for the inverse) and M (fp16 operand) out of TMEM ----
