@@ -150,7 +150,9 @@ kda_status kda_bwd(const kda_problem* p,
  * - Problems whose scratch does not fit (header + partials for N*H
  *   sequence-heads + one CTA's segment states) return KDA_ERR_WORKSPACE
  *   with the required size in kda_last_error_message(); use kda_bwd then.
- * - Fewer CTAs fit than kda_bwd would use, so it is slower.
+ * - It runs the same kernel family as kda_bwd (kda_kernel_family), so the
+ *   two give bit-identical results; fewer CTAs fit than kda_bwd would use,
+ *   so it is slower.
  * - Every call shares the array: calls whose GPU work overlaps (other
  *   streams or threads on the same device) race and give wrong results.
  * - Device-side status is not readable for this entry point. */

@@ -99,6 +99,7 @@ kda_status set_error(kda_status s, const char* fmt, ...) {
   return s;
 }
 size_t gate_partial_bytes(const kda_problem* p) { return partial_bytes(p); }
+int kernel_family(const kda_problem* p) { return family_of(p); }
 }  // namespace kda
 
 extern "C" {

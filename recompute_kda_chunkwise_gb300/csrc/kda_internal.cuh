@@ -101,5 +101,7 @@ constexpr int kTcBwdCtas = 152;
 kda_status validate_problem(const kda_problem* p);
 kda_status set_error(kda_status s, const char* fmt, ...);
 size_t gate_partial_bytes(const kda_problem* p);
+// 1: tcgen05 kernels (bf16, head_dim 128, no KDA_FLAG_FORCE_SIMT), else 0: fp32 SIMT kernels.
+int kernel_family(const kda_problem* p);
 
 }  // namespace kda

@@ -75,7 +75,9 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
   // Scratch plan inside the fixed array: status header, per-(sequence, head)
   // gate-parameter partials, then as many per-CTA state slots as fit.
   const size_t head = (size_t)kda::kHeaderBytes + kda::gate_partial_bytes(p);
-  const size_t per_cta = kda::bwd_scratch_bytes_per_cta_simt(p);
+  // Same kernel family as kda_bwd, so both entry points give identical results.
+  const bool tc = kda::kernel_family(p) == 1;
+  const size_t per_cta = tc ? kda::bwd_scratch_bytes_per_cta_tc() : kda::bwd_scratch_bytes_per_cta_simt(p);
   const size_t cap = (size_t)KDA_NOALLOC_SCRATCH_BYTES;
   if (head + per_cta > cap)
     return kda::set_error(KDA_ERR_WORKSPACE,
@@ -114,7 +116,7 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   if (cudaMemsetAsync(scratch, 0, sizeof(int), s) != cudaSuccess)
     return kda::set_error(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
-  st = kda::launch_bwd_simt_ctas(p, a, s, (int)ctas);
+  st = tc ? kda::launch_bwd_tc(p, a, s, (int)ctas) : kda::launch_bwd_simt_ctas(p, a, s, (int)ctas);
   if (st != KDA_OK)
     return kda::set_error(st, "no-alloc backward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return KDA_OK;
