@@ -7,12 +7,18 @@
 //
 // Chunk size C = 16: every factor exp(+-(G_r - G_s)) inside a chunk then stays
 // within fp32 range (the "k/exp(cumsum g) underflows past 17 tokens" note of
-// "KDA at the production shape ...", section 3(a)), so the intra-chunk
-// matrices and all their gradients are plain fp32 products on CUDA cores,
-// while every product with a 128-long contraction or a 128 x 128 result
-// (the state terms) runs on tcgen05 with fp16 operands and fp32 accumulators
-// in TMEM (M = 128 with the value index v or the key index i on the lanes).
-// Both fp32 states live in TMEM (H^T during the rebuild, dH^T throughout).
+// "KDA at the production shape ...", section 3(a)). Work split:
+//   * state products (128-long contractions or 128 x 128 results): tcgen05,
+//     fp16 operands, fp32 accumulators in TMEM (lanes = value index v or key
+//     index i); both fp32 states live in TMEM (H^T while rebuilding, dH^T);
+//   * the 16 x 16 intra-chunk matrices, the WY factors and every gradient
+//     product with a 16-long contraction: warp-level tf32 tensor-core tiles
+//     (mma.sync m16n8k8; tcgen05's smallest tile has 64 rows), with operands
+//     split into tf32 hi + lo parts so the products keep fp32 accuracy;
+//   * gate / cumulative-sum / L2-norm elementwise work: CUDA cores.
+// Each chunk's q/k/v/g (and dO) tiles are prefetched one chunk ahead with
+// async copies; the fp16 chunk-start states move to and from scratch with
+// bulk async copies.
 //
 // Per chunk (r, s in 0..15; G chunk-local cumulative log-decay; Gamma = e^G;
 // T' = T diag(beta), T = (I + diag(beta) Abar)^-1):
@@ -32,31 +38,39 @@ constexpr int kD = 128;
 constexpr int kT = 256;
 constexpr int kCPS = kCkptTokens / kC;  // chunks per checkpoint segment (64)
 constexpr int kLd = 132;                // fp32 tile row stride (floats)
-constexpr int kTile = kC * kLd;         // floats per fp32 tile
-constexpr int kSq = 17;                 // 16 x 16 matrices, row stride
+constexpr int kTileF = kC * kLd * 4;    // bytes of one fp32 [16][132] tile
+constexpr int kSq = 20;                 // row stride of the 16 x 16 matrices
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kStateBytes = 32768;  // fp16 128 x 128 state tile
 
-// fp32 tiles [16][132]
-enum { T_GS = 0, T_QG, T_KG, T_KI, T_KB, T_V, T_DO, T_W, T_U, T_DU, T_AQ, T_AK, T_AG, NT32 };
-constexpr int OFF_A1 = 110592;           // H^T fp16 [128 v][128 i] (SW128)
-constexpr int OFF_A1D = OFF_A1 + 32768;  // dH'^T fp16 [128 v][128 i]
-constexpr int OFF_FW = OFF_A1D + 32768;  // -W     fp16 [16 r][128 i]
-constexpr int OFF_FQG = OFF_FW + 4096;   // Qh*Gamma fp16 [16 r][128 i]
-constexpr int OFF_FKB = OFF_FQG + 4096;  // Kbar   fp16 [16 r][128 i]
-constexpr int OFF_FDO = OFF_FKB + 4096;  // dO     fp16 [16 r][128 v]
-constexpr int OFF_FU = OFF_FDO + 4096;   // U~     fp16 [16 r][128 v]
-constexpr int OFF_FDU = OFF_FU + 4096;   // dU~    fp16 [16 r][128 v]
-constexpr int OFF_FM = OFF_FDU + 4096;   // M hi   fp16 [16 r][64 (16 used) s]
-constexpr int OFF_FML = OFF_FM + 2048;   // M lo
-constexpr int OFF_SMALL = OFF_FML + 2048;
-// small fp32 arrays (offsets in floats)
-constexpr int S_AB = 0, S_AQK = 272, S_T = 544, S_TP = 816, S_DM = 1088, S_DTP = 1360, S_DA = 1632, S_Y = 1904;
-constexpr int S_BETA = 2176, S_IQ0 = 2192, S_IK0 = 2208, S_DB = 2224, S_RQ = 2240, S_RK = 2256;
-constexpr int S_GEND = 2272, S_DGE = 2400, S_TOT = 2528, S_RED = 2784, S_PART = 3296;
-constexpr int SMALL_FLOATS = 3584;
+// ---- shared memory map (bytes) ----
+constexpr int OFF_A1 = 0;                  // H^T fp16 [128 v][128 i] (SW128)
+constexpr int OFF_A1D = 32768;             // dH'^T fp16 [128 v][128 i]
+constexpr int OFF_FW = 65536;              // -W     fp16 [16 r][128 i]
+constexpr int OFF_FQG = OFF_FW + 4096;     // Qh*Gamma fp16 [16 r][128 i]
+constexpr int OFF_FKB = OFF_FQG + 4096;    // Kbar   fp16 [16 r][128 i]
+constexpr int OFF_FDO = OFF_FKB + 4096;    // dO     fp16 [16 r][128 v]
+constexpr int OFF_FU = OFF_FDO + 4096;     // U~     fp16 [16 r][128 v]
+constexpr int OFF_FDU = OFF_FU + 4096;     // dU~    fp16 [16 r][128 v]
+constexpr int OFF_FM = OFF_FDU + 4096;     // M hi (K-major B of dU~^T: row s, column r)
+constexpr int OFF_FML = OFF_FM + 2048;     // M lo
+constexpr int OFF_STG = OFF_FML + 2048;    // two buffers of q, k, v, g bf16 [16][128]
+constexpr int kStgBuf = 4 * 4096;
+constexpr int OFF_SDO = OFF_STG + 2 * kStgBuf;  // dO bf16 [16][128]
+constexpr int OFF_F32 = OFF_SDO + 4096;         // fp32 [16][132] tiles
+enum { T_GS = 0, T_QG, T_KG, T_KI, T_U, T_DU, T_W, T_AQ, T_AK, T_AG, NT32 };
+constexpr int OFF_SMALL = OFF_F32 + NT32 * kTileF;
+// small fp32 arrays (offsets in floats); 16 x 16 matrices with row stride kSq
+constexpr int S_AB = 0, S_T = 320, S_TP = 640, S_DM = 960, S_DT1 = 1280, S_DT2 = 1600, S_Y = 1920, S_DAB = 2240;
+constexpr int S_BETA = 2560, S_IQ0 = 2576, S_IK0 = 2592, S_DB = 2608, S_RQ = 2624, S_RK = 2640;
+constexpr int S_GEND = 2656, S_DGE = 2784, S_TOT = 2912, S_PART = 3168;
+constexpr int SMALL_FLOATS = 3424;
 constexpr int OFF_BAR = OFF_SMALL + SMALL_FLOATS * 4;
-constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;
-static_assert(NT32 * kTile * 4 <= OFF_A1, "fp32 tiles");
+constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
+// The dgamma reduce-scatter lands in the M hi / lo tiles (free by then).
+constexpr int OFF_RED = OFF_FM;
+static_assert(OFF_STG % 1024 == 0 && OFF_F32 % 16 == 0, "alignment");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // TMEM columns
 constexpr uint32_t TM_H = 0;     // H^T fp32 state (rebuild pass), 128
@@ -76,19 +90,54 @@ struct TcBwdArgs {
   const float* ckpt;
   __nv_bfloat16 *dq, *dk, *dv, *dg, *db;
   float* partial;
-  uint4* scratch;  // per CTA: kCPS fp16 state tiles of 32 KB
+  uint8_t* scratch;  // per CTA: kCPS fp16 state tiles
   int* status;
   const int32_t* cu;
   int N, H;
   float scale, lower, eps;
 };
 
-__device__ __forceinline__ float bf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float sigm(float x) { return __fdividef(1.f, 1.f + ex2(-x * kLog2e)); }
 __device__ __forceinline__ void st_h(uint8_t* base, uint32_t off, float x) {
   *reinterpret_cast<__half*>(base + off) = __float2half_rn(x);
 }
+__device__ __forceinline__ void st_h2(uint8_t* base, uint32_t off, float x0, float x1) {
+  *reinterpret_cast<uint32_t*>(base + off) = pack_h2(x0, x1);
+}
 __device__ __forceinline__ float lo_part(float x) { return x - __half2float(__float2half_rn(x)); }
+// element (r, c) of a bf16 [16][128] staging tile
+__device__ __forceinline__ float stg(const uint8_t* tile, int r, int c) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + r * 256 + c * 2));
+}
+__device__ __forceinline__ float h16(const uint8_t* base, uint32_t off) {
+  return __half2float(*reinterpret_cast<const __half*>(base + off));
+}
+
+// ---- mma.sync fragment loads from fp32 row-major smem matrices ----
+// A[m][k] = X[m][k]
+__device__ __forceinline__ void ldA(float (&a)[4], const float* X, int ld, int k0, int g, int t) {
+  a[0] = X[g * ld + k0 + t];
+  a[1] = X[(g + 8) * ld + k0 + t];
+  a[2] = X[g * ld + k0 + t + 4];
+  a[3] = X[(g + 8) * ld + k0 + t + 4];
+}
+// A[m][k] = X[k][m]
+__device__ __forceinline__ void ldAT(float (&a)[4], const float* X, int ld, int k0, int g, int t) {
+  a[0] = X[(k0 + t) * ld + g];
+  a[1] = X[(k0 + t) * ld + g + 8];
+  a[2] = X[(k0 + t + 4) * ld + g];
+  a[3] = X[(k0 + t + 4) * ld + g + 8];
+}
+// B[k][n] = Y[n][k]
+__device__ __forceinline__ void ldBc(float (&b)[2], const float* Y, int ld, int n0, int k0, int g, int t) {
+  b[0] = Y[(n0 + g) * ld + k0 + t];
+  b[1] = Y[(n0 + g) * ld + k0 + t + 4];
+}
+// B[k][n] = Z[k][n]
+__device__ __forceinline__ void ldBr(float (&b)[2], const float* Z, int ld, int n0, int k0, int g, int t) {
+  b[0] = Z[(k0 + t) * ld + n0 + g];
+  b[1] = Z[(k0 + t + 4) * ld + n0 + g];
+}
 
 // Sums 64 per-lane values over the 32 lanes of a warp (recursive halving):
 // afterwards lane l holds the totals of indices idx(l, 0) and idx(l, 1) with
@@ -109,38 +158,59 @@ __device__ __forceinline__ void warp_reduce_scatter64(float (&v)[64], int lane) 
   }
 }
 
+// Async copies of the tiles of tokens [t0, t0 + 16) of head h into bf16
+// [16][128] staging tiles (q, k, v, g at dst + 0/4/8/12 KB; dO at dst_dO);
+// rows at or past `rows` are zero-filled. Every thread copies 16 bytes per tile.
+__device__ __forceinline__ void stage_tiles(const TcBwdArgs& a, uint32_t dst, int h, int64_t t0, int rows, int tid,
+                                            bool qkvg, bool dO, uint32_t dst_dO) {
+  const int r = tid >> 4, j = tid & 15;
+  const bool ok = r < rows;
+  const int64_t off = ok ? ((t0 + r) * a.H + h) * kD + 8 * j : 0;
+  const int n = ok ? 16 : 0;
+  const uint32_t so = static_cast<uint32_t>(r * 256 + 16 * j);
+  if (qkvg) {
+    cp_async16(dst + 0 * 4096 + so, a.q + off, n);
+    cp_async16(dst + 1 * 4096 + so, a.k + off, n);
+    cp_async16(dst + 2 * 4096 + so, a.v + off, n);
+    cp_async16(dst + 3 * 4096 + so, a.g + off, n);
+  }
+  if (dO) cp_async16(dst_dO + so, a.dO + off, n);
+}
+
 __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
-  float* F = reinterpret_cast<float*>(sm);
-  float* GS = F + T_GS * kTile;
-  float* QG = F + T_QG * kTile;
-  float* KG = F + T_KG * kTile;
-  float* KI = F + T_KI * kTile;
-  float* KB = F + T_KB * kTile;
-  float* VT = F + T_V * kTile;
-  float* DOT = F + T_DO * kTile;
-  float* WT = F + T_W * kTile;
-  float* UT = F + T_U * kTile;
-  float* DUT = F + T_DU * kTile;
-  float* AQ = F + T_AQ * kTile;
-  float* AK = F + T_AK * kTile;
-  float* AG = F + T_AG * kTile;
+  float* F = reinterpret_cast<float*>(sm + OFF_F32);
+  float* GS = F + T_GS * (kTileF / 4);
+  float* QG = F + T_QG * (kTileF / 4);
+  float* KG = F + T_KG * (kTileF / 4);
+  float* KI = F + T_KI * (kTileF / 4);
+  float* UT = F + T_U * (kTileF / 4);
+  float* DUT = F + T_DU * (kTileF / 4);
+  float* WT = F + T_W * (kTileF / 4);
+  float* AQ = F + T_AQ * (kTileF / 4);
+  float* AK = F + T_AK * (kTileF / 4);
+  float* AG = F + T_AG * (kTileF / 4);
   float* S = reinterpret_cast<float*>(sm + OFF_SMALL);
+  float* RED = reinterpret_cast<float*>(sm + OFF_RED);
+  const uint8_t* SDO = sm + OFF_SDO;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar + 1);
-  int* s_fail = reinterpret_cast<int*>(bar + 2);
+  uint64_t* bar_a1 = bar + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar + 2);
+  int* s_fail = reinterpret_cast<int*>(bar + 3);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ci = tid & 127, rh = tid >> 7;  // channel role: channel ci, rows 8*rh .. 8*rh+7
-  const int q4 = warp & 3, hh = warp >> 2, L = 32 * q4 + lane;  // lane role
+  const int q4 = warp & 3, hh = warp >> 2, L = 32 * q4 + lane;  // TMEM lane role
   const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
-  const int sr = tid >> 4, ss = tid & 15;  // (r, s) role for 16 x 16 matrices
+  const int fg = lane >> 2, ft = lane & 3;  // mma fragment role
+  const int sr = tid >> 4, ss = tid & 15;   // (r, s) role for 16 x 16 matrices
   const float Lg = a.lower * kLog2e;
 
   if (tid == 0) {
     mbar_init(bar, 1);
+    mbar_init(bar_a1, 1);
     *s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -149,13 +219,14 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *s_tmem;
-  uint32_t ph = 0;
-  uint4* scratch = a.scratch + static_cast<size_t>(blockIdx.x) * kCPS * (32768 / 16);
+  uint32_t ph = 0, ph_a1 = 0;
+  bool a1_pending = false;  // a bulk load into A1 is in flight (same value in every thread)
+  uint8_t* scratch = a.scratch + static_cast<size_t>(blockIdx.x) * kCPS * kStateBytes;
 
-#define KDA_WAIT_MMA()                                  \
-  do {                                                  \
-    if (!mbar_wait(bar, ph, a.status)) *s_fail = 1;     \
-    ph ^= 1u;                                           \
+#define KDA_WAIT_MMA()                              \
+  do {                                              \
+    if (!mbar_wait(bar, ph, a.status)) *s_fail = 1; \
+    ph ^= 1u;                                       \
   } while (0)
 #define KDA_SYNC_OR_BAIL()      \
   do {                          \
@@ -202,41 +273,53 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
         }
         tmem_st_wait();
       }
+      fence_async_smem();
       fence_before_sync();
       __syncthreads();
 
-      // Two passes over the segment: pass 0 rebuilds the chunk-start states
-      // (saving each as an fp16 tile), pass 1 walks the chunks in reverse.
+      // Pass 0 rebuilds the chunk-start states c0+1 .. c1-1 (state c is saved
+      // to scratch slot c - c0 before chunk c advances it); pass 1 walks the
+      // chunks c1-1 .. c0 in reverse.
 #pragma unroll 1
       for (int pass = 0; pass < 2; ++pass) {
-#pragma unroll 1
-        for (int step = 0; step < c1 - c0; ++step) {
-          const int c = pass == 0 ? c0 + step : c1 - 1 - step;
-          const bool rev = pass == 1;
-          uint4* slot = scratch + static_cast<size_t>(c - c0) * (32768 / 16);
-          if (!rev) {
-            for (int x = tid; x < 32768 / 16; x += kT) slot[x] = reinterpret_cast<const uint4*>(sm + OFF_A1)[x];
-            if (c == c1 - 1) break;
-          } else {
-            for (int x = tid; x < 32768 / 16; x += kT) reinterpret_cast<uint4*>(sm + OFF_A1)[x] = slot[x];
-          }
+        const bool rev = pass == 1;
+        const int nsteps = rev ? c1 - c0 : c1 - c0 - 1;
+        float braw_next = 0.f;
+        if (nsteps > 0) {  // first chunk of the pass: issue its loads now
+          const int c = rev ? c1 - 1 : c0;
           const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
           const int rows = static_cast<int>(min(static_cast<int64_t>(kC), eos - t0));
+          stage_tiles(a, sb + OFF_STG, h, t0, rows, tid, true, rev, sb + OFF_SDO);
+          cp_async_commit();
+          if (tid < kC && tid < rows) braw_next = __bfloat162float(a.b[(t0 + tid) * a.H + h]);
+        }
+#pragma unroll 1
+        for (int step = 0; step < nsteps; ++step) {
+          const int c = rev ? c1 - 1 - step : c0 + step;
+          const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
+          const int rows = static_cast<int>(min(static_cast<int64_t>(kC), eos - t0));
+          const int buf = step & 1;
+          const uint8_t* SQ = sm + OFF_STG + buf * kStgBuf;
+          const uint8_t* SK = SQ + 4096;
+          const uint8_t* SV = SQ + 2 * 4096;
+          const uint8_t* SG = SQ + 3 * 4096;
+          const bool more = step + 1 < nsteps;
+          const float braw = braw_next;
+          // ---- prefetch the next chunk of this pass; save the start state ----
+          if (more) {
+            const int cn = rev ? c - 1 : c + 1;
+            const int64_t tn = bos + static_cast<int64_t>(cn) * kC;
+            const int rn = static_cast<int>(min(static_cast<int64_t>(kC), eos - tn));
+            stage_tiles(a, sb + OFF_STG + (buf ^ 1) * kStgBuf, h, tn, rn, tid, true, false, 0);
+            if (tid < kC && tid < rn) braw_next = __bfloat162float(a.b[(tn + tid) * a.H + h]);
+          }
+          cp_async_commit();
+          if (!rev && tid == 0) bulk_store(scratch + static_cast<size_t>(c - c0) * kStateBytes, sb + OFF_A1, kStateBytes);
+          cp_async_wait_prev();
+          __syncthreads();
 
           // ================= chunk prologue =================
-          if (tid < kC) S[S_BETA + tid] = tid < rows ? sigm(bf(a.b + (t0 + tid) * a.H + h)) : 0.f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int r = 8 * rh + j;
-            const bool ok = r < rows;
-            const int64_t off = ((t0 + r) * a.H + h) * kD + ci;
-            QG[r * kLd + ci] = ok ? bf(a.q + off) : 0.f;
-            KG[r * kLd + ci] = ok ? bf(a.k + off) : 0.f;
-            VT[r * kLd + ci] = ok ? bf(a.v + off) : 0.f;
-            GS[r * kLd + ci] = ok ? bf(a.g + off) : 0.f;
-            if (rev) DOT[r * kLd + ci] = ok ? bf(a.dO + off) : 0.f;
-          }
-          __syncthreads();
+          if (tid < kC) S[S_BETA + tid] = tid < rows ? sigm(braw) : 0.f;
           {  // row norms: warp w -> rows 2w, 2w+1
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
@@ -244,7 +327,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               float sq = 0.f, sk = 0.f;
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float x = QG[r * kLd + lane + 32 * e], y = KG[r * kLd + lane + 32 * e];
+                const float x = stg(SQ, r, lane + 32 * e), y = stg(SK, r, lane + 32 * e);
                 sq += x * x;
                 sk += y * y;
               }
@@ -262,7 +345,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int r = 8 * rh + j;
-              const float d = r < rows ? Lg * sigm(expA * (GS[r * kLd + ci] + dtb)) : 0.f;
+              const float d = r < rows ? Lg * sigm(expA * (stg(SG, r, ci) + dtb)) : 0.f;
               acc += d;
               GS[r * kLd + ci] = acc;
             }
@@ -279,39 +362,47 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               const float G = GS[r * kLd + ci] + carry;
               GS[r * kLd + ci] = G;
               const float e = ex2(G), ei = ex2(-G);
-              const float qh = QG[r * kLd + ci] * S[S_IQ0 + r] * a.scale;
-              const float kh = KG[r * kLd + ci] * S[S_IK0 + r];
-              const float kb = kh * ex2(gend - G);
-              QG[r * kLd + ci] = qh * e;
+              const float kh = stg(SK, r, ci) * S[S_IK0 + r];
               KG[r * kLd + ci] = kh * e;
               KI[r * kLd + ci] = kh * ei;
-              KB[r * kLd + ci] = kb;
-              st_h(sm + OFF_FKB, sw128_off(r, ci, 16), kb);
+              st_h(sm + OFF_FKB, sw128_off(r, ci, 16), kh * ex2(gend - G));
               if (rev) {
-                st_h(sm + OFF_FQG, sw128_off(r, ci, 16), qh * e);
-                st_h(sm + OFF_FDO, sw128_off(r, ci, 16), DOT[r * kLd + ci]);  // bf16 -> fp16 is exact
+                const float qg = stg(SQ, r, ci) * S[S_IQ0 + r] * a.scale * e;
+                QG[r * kLd + ci] = qg;
+                st_h(sm + OFF_FQG, sw128_off(r, ci, 16), qg);
+                // bf16 -> fp16 is exact for these magnitudes
+                st_h(sm + OFF_FDO, sw128_off(r, ci, 16), stg(SDO, r, ci));
               }
             }
           }
           __syncthreads();
-          // ================= intra-chunk matrices (fp32) =================
-          {
-            const int r = sr, s = ss;
-            float aa = 0.f, am = 0.f;
-            if (s <= r) {
-#pragma unroll 8
-              for (int i = 0; i < kD; ++i) {
-                const float ki = KI[s * kLd + i];
-                aa += KG[r * kLd + i] * ki;
-                am += QG[r * kLd + i] * ki;
-              }
+          if (rev) {  // next chunk's dO (the dO staging tile has been consumed)
+            if (more) stage_tiles(a, 0, h, t0 - kC, kC, tid, false, true, sb + OFF_SDO);
+            cp_async_commit();
+          }
+          // ================= Abar (and M) on tf32 tensor tiles =================
+          if (warp < (rev ? 4 : 2)) {
+            const int nt = warp & 1;
+            const bool is_m = (warp >> 1) != 0;
+            const float* X = is_m ? QG : KG;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int k0 = 0; k0 < kD; k0 += 8) {
+              float fa[4], fb[2];
+              ldA(fa, X, kLd, k0, fg, ft);
+              ldBc(fb, KI, kLd, 8 * nt, k0, fg, ft);
+              mma3(d, fa, fb);
             }
-            S[S_AB + r * kSq + s] = s < r ? aa : 0.f;
-            S[S_AQK + r * kSq + s] = s <= r ? am : 0.f;
-            if (rev) {
-              const float mv = s <= r ? am : 0.f;
-              st_h(sm + OFF_FM, sw128_off(s, r, 16), mv);  // K-major B of dU~^T: row s, column r
-              st_h(sm + OFF_FML, sw128_off(s, r, 16), lo_part(mv));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int r = fg + 8 * (e >> 1), s = 8 * nt + 2 * ft + (e & 1);
+              if (!is_m) {
+                S[S_AB + r * kSq + s] = s < r ? d[e] : 0.f;
+              } else {
+                const float mv = s <= r ? d[e] : 0.f;
+                st_h(sm + OFF_FM, sw128_off(s, r, 16), mv);  // K-major B of dU~^T: row s, column r
+                st_h(sm + OFF_FML, sw128_off(s, r, 16), lo_part(mv));
+              }
             }
           }
           __syncthreads();
@@ -335,28 +426,43 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             }
           }
           __syncthreads();
-          {  // W = T' (Kh Gamma), U = T' V
+          {  // W = T' (Kh Gamma) -> -W fp16;  U = T' V -> fp32  (channels 16w .. 16w+15)
+            float dw[2][4] = {}, du[2][4] = {};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int r = 8 * rh + j;
-              float w = 0.f, u = 0.f;
+            for (int k0 = 0; k0 < kC; k0 += 8) {
+              float fa[4];
+              ldA(fa, S + S_TP, kSq, k0, fg, ft);
 #pragma unroll
-              for (int s = 0; s < 16; ++s) {
-                if (s <= r) {
-                  const float t = S[S_TP + r * kSq + s];
-                  w += t * KG[s * kLd + ci];
-                  u += t * VT[s * kLd + ci];
-                }
+              for (int nt = 0; nt < 2; ++nt) {
+                const int n0 = 16 * warp + 8 * nt;
+                float fb[2], fv[2];
+                ldBr(fb, KG, kLd, n0, k0, fg, ft);
+                mma3(dw[nt], fa, fb);
+                fv[0] = stg(SV, k0 + ft, n0 + fg);
+                fv[1] = stg(SV, k0 + ft + 4, n0 + fg);
+                mma2_bexact(du[nt], fa, fv);
               }
-              WT[r * kLd + ci] = w;
-              UT[r * kLd + ci] = u;
-              st_h(sm + OFF_FW, sw128_off(r, ci, 16), -w);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              const int i = 16 * warp + 8 * nt + 2 * ft;
+#pragma unroll
+              for (int hr = 0; hr < 2; ++hr) {
+                const int r = fg + 8 * hr;
+                st_h2(sm + OFF_FW, sw128_off(r, i, 16), -dw[nt][2 * hr], -dw[nt][2 * hr + 1]);
+                *reinterpret_cast<float2*>(UT + r * kLd + i) = make_float2(du[nt][2 * hr], du[nt][2 * hr + 1]);
+              }
             }
           }
           fence_async_smem();
           fence_before_sync();
           KDA_SYNC_OR_BAIL();
-          // ================= U~ = U - W H (tensor cores) =================
+          // ================= U~ = U - W H (tcgen05) =================
+          if (a1_pending) {  // this chunk's start state, loaded during the prologue
+            if (!mbar_wait(bar_a1, ph_a1, a.status)) *s_fail = 1;
+            ph_a1 ^= 1u;
+            a1_pending = false;
+          }
           if (tid == 0) {
             fence_after_sync();
 #pragma unroll
@@ -385,6 +491,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           if (!rev) {
             // ============ rebuild pass: H <- diag(gamma) H + Kbar^T U~ ============
             if (tid == 0) {
+              bulk_wait_read();  // the scratch copy of A1 has been read out
               fence_after_sync();
               mma(tmem + TM_D2, desc_mnmajor(sb + OFF_FU, 2048, 0), desc_mnmajor(sb + OFF_FKB, 2048, 0),
                   idesc(128, 128, true, true), 0);
@@ -466,7 +573,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           }
           KDA_WAIT_MMA();
           fence_after_sync();
-          // ---- dH update, dgamma (lane = v); dQG, dW, dKbar (lane = i) ----
+          // ---- [E] dH update, dgamma (lane = v); dQG, dW, dKbar (lane = i) ----
           {
             float p[64];
 #pragma unroll
@@ -503,82 +610,95 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             {
               const int base = 32 * ((lane >> 4) & 1) + 16 * ((lane >> 3) & 1) + 8 * ((lane >> 2) & 1) +
                                4 * ((lane >> 1) & 1) + 2 * (lane & 1);
-              S[S_RED + q4 * 128 + 64 * hh + base] = p[0];
-              S[S_RED + q4 * 128 + 64 * hh + base + 1] = p[1];
+              RED[q4 * 128 + 64 * hh + base] = p[0];
+              RED[q4 * 128 + 64 * hh + base + 1] = p[1];
             }
             float xq[8], xw[8], xk[8];
             tmem_ld8(tmem + tlane + TM_DQ + 8 * hh, xq);  // lane = i, columns r
             tmem_ld8(tmem + tlane + TM_DW + 8 * hh, xw);
             tmem_ld8(tmem + tlane + TM_DK + 8 * hh, xk);
             const int i = L;
-            const float gend = S[S_GEND + i];
+            const float gend = S[S_GEND + i], gam = ex2(gend);
             float part = 0.f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int r = 8 * hh + j;
               const float G = GS[r * kLd + i];
-              const float kbv = KB[r * kLd + i];
+              const float kbv = KI[r * kLd + i] * gam;
               AQ[r * kLd + i] = xq[j] * ex2(G);
               AG[r * kLd + i] = xq[j] * QG[r * kLd + i] - xk[j] * kbv;
               AK[r * kLd + i] = xk[j] * ex2(gend - G);
-              WT[r * kLd + i] = -xw[j];  // dW (W itself is no longer needed)
+              WT[r * kLd + i] = -xw[j];  // dW
               part += xk[j] * kbv;
             }
             S[S_PART + hh * 128 + i] = part;
           }
+          fence_async_smem();
           __syncthreads();
-          if (tid < kD) {  // d(chunk-end log decay) of channel tid
+          // the next chunk's start state into A1 (its last reader was [E])
+          if (more) {
+            if (tid == 0) {
+              mbar_expect_tx(bar_a1, kStateBytes);
+              bulk_load(sb + OFF_A1, scratch + static_cast<size_t>(c - 1 - c0) * kStateBytes, kStateBytes, bar_a1);
+            }
+            a1_pending = true;
+          }
+          // ---- [D1] d(chunk-end log decay); dM, dT' parts on tf32 tiles ----
+          if (tid < kD) {
             const int i = tid;
-            const float dgam = S[S_RED + i] + S[S_RED + 128 + i] + S[S_RED + 256 + i] + S[S_RED + 384 + i];
+            const float dgam = RED[i] + RED[128 + i] + RED[256 + i] + RED[384 + i];
             S[S_DGE + i] = S[S_PART + i] + S[S_PART + 128 + i] + dgam * ex2(S[S_GEND + i]);
           }
-          {  // dM = tril(dO U~^T), dT' = dW (Kh Gamma)^T + dU~ V^T
-            const int r = sr, s = ss;
-            float dm = 0.f, dt = 0.f;
-#pragma unroll 8
-            for (int i = 0; i < kD; ++i) {
-              dm += DOT[r * kLd + i] * UT[s * kLd + i];
-              dt += WT[r * kLd + i] * KG[s * kLd + i] + DUT[r * kLd + i] * VT[s * kLd + i];
+          if (warp < 6) {
+            const int nt = warp & 1, kind = warp >> 1;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int k0 = 0; k0 < kD; k0 += 8) {
+              float fa[4], fb[2];
+              if (kind == 0) {  // dM = dO U~^T   (dO exact in tf32)
+                fa[0] = h16(sm + OFF_FDO, sw128_off(fg, k0 + ft, 16));
+                fa[1] = h16(sm + OFF_FDO, sw128_off(fg + 8, k0 + ft, 16));
+                fa[2] = h16(sm + OFF_FDO, sw128_off(fg, k0 + ft + 4, 16));
+                fa[3] = h16(sm + OFF_FDO, sw128_off(fg + 8, k0 + ft + 4, 16));
+                ldBc(fb, UT, kLd, 8 * nt, k0, fg, ft);
+                mma2_aexact(d, fa, fb);
+              } else if (kind == 1) {  // dW (Kh Gamma)^T
+                ldA(fa, WT, kLd, k0, fg, ft);
+                ldBc(fb, KG, kLd, 8 * nt, k0, fg, ft);
+                mma3(d, fa, fb);
+              } else {  // dU~ V^T   (V exact in tf32)
+                ldA(fa, DUT, kLd, k0, fg, ft);
+                fb[0] = stg(SV, 8 * nt + fg, k0 + ft);
+                fb[1] = stg(SV, 8 * nt + fg, k0 + ft + 4);
+                mma2_bexact(d, fa, fb);
+              }
             }
-            S[S_DM + r * kSq + s] = s <= r ? dm : 0.f;
-            S[S_DTP + r * kSq + s] = dt;
+            const int dst = kind == 0 ? S_DM : (kind == 1 ? S_DT1 : S_DT2);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int r = fg + 8 * (e >> 1), s = 8 * nt + 2 * ft + (e & 1);
+              S[dst + r * kSq + s] = (kind == 0 && s > r) ? 0.f : d[e];
+            }
           }
           __syncthreads();
-          {  // dV = T'^T dU~ (output), d(Kh Gamma) += T'^T dW
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int r = 8 * rh + j;
-              float dvv = 0.f, dkg = 0.f;
-#pragma unroll
-              for (int s = 0; s < 16; ++s) {
-                if (s >= r) {
-                  const float t = S[S_TP + s * kSq + r];
-                  dvv += t * DUT[s * kLd + ci];
-                  dkg += t * WT[s * kLd + ci];
-                }
-              }
-              if (r < rows) a.dv[((t0 + r) * a.H + h) * kD + ci] = __float2bfloat16_rn(dvv);
-              const float G = GS[r * kLd + ci];
-              AK[r * kLd + ci] += dkg * ex2(G);
-              AG[r * kLd + ci] += dkg * KG[r * kLd + ci];
-            }
-          }
-          {  // dbeta from T' = T diag(beta); Y = (dT' diag(beta)) T^T
+          {  // [D2] dbeta from T' = T diag(beta); Y = (dT' diag(beta)) T^T
             const int r = sr, s = ss;
             if (tid < kC) {
               float db = 0.f;
 #pragma unroll
-              for (int r2 = 0; r2 < 16; ++r2) db += S[S_T + r2 * kSq + tid] * S[S_DTP + r2 * kSq + tid];
+              for (int r2 = 0; r2 < 16; ++r2)
+                db += S[S_T + r2 * kSq + tid] * (S[S_DT1 + r2 * kSq + tid] + S[S_DT2 + r2 * kSq + tid]);
               S[S_DB + tid] = db;
             }
             float y = 0.f;
 #pragma unroll
             for (int b2 = 0; b2 < 16; ++b2)
-              if (b2 < r && b2 <= s) y += S[S_DTP + r * kSq + b2] * S[S_BETA + b2] * S[S_T + s * kSq + b2];
+              if (b2 < r && b2 <= s)
+                y += (S[S_DT1 + r * kSq + b2] + S[S_DT2 + r * kSq + b2]) * S[S_BETA + b2] * S[S_T + s * kSq + b2];
             S[S_Y + r * kSq + s] = y;
           }
           __syncthreads();
-          {  // dA = -(T^T Y) strictly lower; dAbar = diag(beta) dA
+          {  // [D3] dA = -(T^T Y) strictly lower; DAB = diag(beta) dA; dA .* Abar
             const int r = sr, s = ss;
             float da = 0.f;
             if (s < r) {
@@ -586,36 +706,62 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               for (int a2 = 0; a2 < 16; ++a2)
                 if (a2 >= r) da -= S[S_T + a2 * kSq + r] * S[S_Y + a2 * kSq + s];
             }
-            S[S_DA + r * kSq + s] = da;
+            S[S_DAB + r * kSq + s] = S[S_BETA + r] * da;
+            S[S_DT2 + r * kSq + s] = da * S[S_AB + r * kSq + s];
           }
           __syncthreads();
           if (tid < kC) {  // dbeta of rows: A = diag(beta) Abar
-            const int r = tid;
-            float db = S[S_DB + r];
+            float db = S[S_DB + tid];
 #pragma unroll
-            for (int s = 0; s < 16; ++s)
-              if (s < r) db += S[S_DA + r * kSq + s] * S[S_AB + r * kSq + s];
-            S[S_DB + r] = db;
+            for (int s = 0; s < 16; ++s) db += S[S_DT2 + tid * kSq + s];
+            S[S_DB + tid] = db;
           }
-          {  // Abar and M gradients back to kh, qh, G
+          {  // ---- [F] 16 x 128 gradient products (channels 16w .. 16w+15) ----
+            float dvv[2][4] = {}, dkg[2][4] = {}, a1[2][4] = {}, m1[2][4] = {}, a2[2][4] = {};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int r = 8 * rh + j;
-              const float br = S[S_BETA + r];
-              float a1 = 0.f, a2 = 0.f, m1 = 0.f, m2 = 0.f;
+            for (int k0 = 0; k0 < kC; k0 += 8) {
+              float tpt[4], dab[4], dabt[4], dm[4], dmt[4];
+              ldAT(tpt, S + S_TP, kSq, k0, fg, ft);
+              ldA(dab, S + S_DAB, kSq, k0, fg, ft);
+              ldAT(dabt, S + S_DAB, kSq, k0, fg, ft);
+              ldA(dm, S + S_DM, kSq, k0, fg, ft);
+              ldAT(dmt, S + S_DM, kSq, k0, fg, ft);
 #pragma unroll
-              for (int s = 0; s < 16; ++s) {
-                const float kis = KI[s * kLd + ci];
-                if (s < r) a1 += S[S_DA + r * kSq + s] * kis;
-                if (s > r) a2 += S[S_BETA + s] * S[S_DA + s * kSq + r] * KG[s * kLd + ci];
-                if (s <= r) m1 += S[S_DM + r * kSq + s] * kis;
-                if (s >= r) m2 += S[S_DM + s * kSq + r] * QG[s * kLd + ci];
+              for (int nt = 0; nt < 2; ++nt) {
+                const int n0 = 16 * warp + 8 * nt;
+                float fb[2];
+                ldBr(fb, DUT, kLd, n0, k0, fg, ft);
+                mma3(dvv[nt], tpt, fb);  // dV = T'^T dU~
+                ldBr(fb, WT, kLd, n0, k0, fg, ft);
+                mma3(dkg[nt], tpt, fb);  // d(Kh Gamma) += T'^T dW
+                ldBr(fb, KI, kLd, n0, k0, fg, ft);
+                mma3(a1[nt], dab, fb);  // (diag(beta) dA) (Kh / Gamma)
+                mma3(m1[nt], dm, fb);   // dM (Kh / Gamma)
+                ldBr(fb, KG, kLd, n0, k0, fg, ft);
+                mma3(a2[nt], dabt, fb);  // (diag(beta) dA)^T (Kh Gamma)
+                ldBr(fb, QG, kLd, n0, k0, fg, ft);
+                mma3(a2[nt], dmt, fb);  // + dM^T (Qh Gamma)
               }
-              a1 *= br;
-              const float G = GS[r * kLd + ci], e = ex2(G), ei = ex2(-G);
-              AQ[r * kLd + ci] += m1 * e;
-              AK[r * kLd + ci] += a1 * e + (a2 + m2) * ei;
-              AG[r * kLd + ci] += a1 * KG[r * kLd + ci] + m1 * QG[r * kLd + ci] - (a2 + m2) * KI[r * kLd + ci];
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+              for (int hr = 0; hr < 2; ++hr) {
+                const int r = fg + 8 * hr;
+                const int i0 = 16 * warp + 8 * nt + 2 * ft;
+                if (r < rows)
+                  *reinterpret_cast<uint32_t*>(a.dv + ((t0 + r) * a.H + h) * kD + i0) =
+                      pack_bf16(dvv[nt][2 * hr], dvv[nt][2 * hr + 1]);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int x = r * kLd + i0 + e, f = 2 * hr + e;
+                  const float G = GS[x], eg = ex2(G), egi = ex2(-G);
+                  const float kgp = dkg[nt][f] + a1[nt][f];
+                  AQ[x] += m1[nt][f] * eg;
+                  AK[x] += kgp * eg + a2[nt][f] * egi;
+                  AG[x] += kgp * KG[x] + m1[nt][f] * QG[x] - a2[nt][f] * KI[x];
+                }
+              }
             }
           }
           __syncthreads();
@@ -640,20 +786,17 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             for (int rr = 0; rr < 2; ++rr) {
               const int r = 2 * warp + rr;
               float sq = 0.f, sk = 0.f;
-              if (r < rows) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int i = lane + 32 * e;
-                  const int64_t off = ((t0 + r) * a.H + h) * kD + i;
-                  sq += bf(a.q + off) * S[S_IQ0 + r] * AQ[r * kLd + i];
-                  sk += bf(a.k + off) * S[S_IK0 + r] * AK[r * kLd + i];
-                }
+              for (int e = 0; e < 4; ++e) {
+                const int i = lane + 32 * e;
+                sq += stg(SQ, r, i) * AQ[r * kLd + i];
+                sk += stg(SK, r, i) * AK[r * kLd + i];
               }
               sq = warp_sum(sq);
               sk = warp_sum(sk);
               if (lane == 0) {
-                S[S_RQ + r] = a.scale * sq;
-                S[S_RK + r] = sk;
+                S[S_RQ + r] = a.scale * sq * S[S_IQ0 + r];
+                S[S_RK + r] = sk * S[S_IK0 + r];
               }
             }
           }
@@ -665,10 +808,10 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               if (r < rows) {
                 const int64_t off = ((t0 + r) * a.H + h) * kD + ci;
                 const float iq0 = S[S_IQ0 + r], ik0 = S[S_IK0 + r];
-                const float xq = bf(a.q + off) * iq0, xk = bf(a.k + off) * ik0;
+                const float xq = stg(SQ, r, ci) * iq0, xk = stg(SK, r, ci) * ik0;
                 a.dq[off] = __float2bfloat16_rn((a.scale * AQ[r * kLd + ci] - xq * S[S_RQ + r]) * iq0);
                 a.dk[off] = __float2bfloat16_rn((AK[r * kLd + ci] - xk * S[S_RK + r]) * ik0);
-                const float z = expA * (bf(a.g + off) + dtb);
+                const float z = expA * (stg(SG, r, ci) + dtb);
                 const float sg = sigm(z);
                 const float dz = AG[r * kLd + ci] * a.lower * sg * (1.f - sg);
                 a.dg[off] = __float2bfloat16_rn(expA * dz);
@@ -685,26 +828,32 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           fence_before_sync();
           KDA_SYNC_OR_BAIL();
         }
+        if (!rev && tid == 0) bulk_wait_all();  // scratch states written before pass 1 reads them
         __syncthreads();
       }
     }
     // ---- per-(sequence, head) partial sums of the gate-parameter gradients ----
-    S[S_RED + tid] = acc_dtb;
+    float* R = S + S_TOT;  // 256 floats
+    R[tid] = acc_dtb;
     __syncthreads();
-    if (tid < kD) a.partial[static_cast<int64_t>(item) * (kD + 1) + tid] = S[S_RED + tid] + S[S_RED + 128 + tid];
+    if (tid < kD) a.partial[static_cast<int64_t>(item) * (kD + 1) + tid] = R[tid] + R[128 + tid];
     __syncthreads();
-    S[S_RED + tid] = acc_alog;
+    R[tid] = acc_alog;
     __syncthreads();
     for (int st = kT / 2; st > 0; st >>= 1) {
-      if (tid < st) S[S_RED + tid] += S[S_RED + tid + st];
+      if (tid < st) R[tid] += R[tid + st];
       __syncthreads();
     }
-    if (tid == 0) a.partial[static_cast<int64_t>(item) * (kD + 1) + kD] = S[S_RED];
+    if (tid == 0) a.partial[static_cast<int64_t>(item) * (kD + 1) + kD] = R[0];
     __syncthreads();
   }
 #undef KDA_WAIT_MMA
 #undef KDA_SYNC_OR_BAIL
 teardown:
+  // no async copy may still target this CTA's shared memory when it exits
+  if (a1_pending) mbar_wait(bar_a1, ph_a1, a.status);
+  if (tid == 0) bulk_wait_all();
+  asm volatile("cp.async.wait_all;" ::: "memory");
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, TM_COLS);
@@ -724,7 +873,7 @@ __global__ void kda_param_reduce_tc_kernel(const float* partial, int N, int H, i
 
 }  // namespace
 
-size_t bwd_scratch_bytes_per_cta_tc() { return static_cast<size_t>(kCPS) * 32768; }
+size_t bwd_scratch_bytes_per_cta_tc() { return static_cast<size_t>(kCPS) * kStateBytes; }
 
 kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas) {
   if (p->head_dim != kD || p->dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
@@ -744,7 +893,7 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   t.dg = static_cast<__nv_bfloat16*>(a.dg);
   t.db = static_cast<__nv_bfloat16*>(a.db);
   t.partial = a.partial;
-  t.scratch = reinterpret_cast<uint4*>(a.scratch);
+  t.scratch = reinterpret_cast<uint8_t*>(a.scratch);
   t.status = a.status;
   t.cu = a.cu;
   t.N = a.N;
@@ -752,7 +901,6 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   t.scale = a.scale;
   t.lower = a.lower;
   t.eps = a.eps;
-  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   if (cudaFuncSetAttribute(kda_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
     return KDA_ERR_CUDA;
   if (ctas > 0) kda_bwd_tc_kernel<<<ctas, kT, SMEM_BYTES, s>>>(t);

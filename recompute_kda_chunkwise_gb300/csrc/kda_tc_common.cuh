@@ -188,6 +188,81 @@ __device__ __forceinline__ uint32_t sw128_off32(int row, int k, int rows) {
                                ((chunk ^ (row & 7)) << 4) + (e << 2));
 }
 
+// ---- per-thread async copies (16 bytes; src_bytes = 0 writes zeros) ----
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most the newest group of this thread's copies is pending.
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// ---- bulk (non-tensor) async copies between shared and global memory ----
+// Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The source shared memory of every committed bulk store may be reused.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Every committed bulk store has completed (its writes are visible).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sdst),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// ---- warp-level tf32 tensor-core tiles (mma.sync m16n8k8) for 16-row work ----
+// Fragment layout (g = lane / 4, t = lane % 4): A[16 x 8] rows g, g + 8 and
+// columns t, t + 4 in a0..a3 = (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4);
+// B[8 x 8] b0 = (k = t, n = g), b1 = (k = t + 4, n = g); C[16 x 8]
+// c0..c3 = (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  lo = __float_as_uint(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_tf32_16x8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// d += A B with both operands split into tf32 hi + lo parts (hi*hi + hi*lo +
+// lo*hi): about fp32 accuracy.
+__device__ __forceinline__ void mma3(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
+  uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split_tf32(a[i], ah[i], al[i]);
+  split_tf32(b[0], bh[0], bl[0]);
+  split_tf32(b[1], bh[1], bl[1]);
+  mma_tf32_16x8(d, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+  mma_tf32_16x8(d, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+  mma_tf32_16x8(d, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
+}
+// d += A B where B is exact in tf32 (bf16 / fp16 values): A split only.
+__device__ __forceinline__ void mma2_bexact(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
+  uint32_t ah[4], al[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split_tf32(a[i], ah[i], al[i]);
+  const uint32_t b0 = __float_as_uint(b[0]), b1 = __float_as_uint(b[1]);
+  mma_tf32_16x8(d, al[0], al[1], al[2], al[3], b0, b1);
+  mma_tf32_16x8(d, ah[0], ah[1], ah[2], ah[3], b0, b1);
+}
+// d += A B where A is exact in tf32: B split only.
+__device__ __forceinline__ void mma2_aexact(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
+  uint32_t bh[2], bl[2];
+  split_tf32(b[0], bh[0], bl[0]);
+  split_tf32(b[1], bh[1], bl[1]);
+  const uint32_t a0 = __float_as_uint(a[0]), a1 = __float_as_uint(a[1]), a2 = __float_as_uint(a[2]),
+                 a3 = __float_as_uint(a[3]);
+  mma_tf32_16x8(d, a0, a1, a2, a3, bl[0], bl[1]);
+  mma_tf32_16x8(d, a0, a1, a2, a3, bh[0], bh[1]);
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 p = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
