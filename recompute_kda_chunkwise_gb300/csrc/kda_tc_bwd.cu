@@ -63,8 +63,8 @@ constexpr int OFF_SMALL = OFF_F32 + NT32 * kTileF;
 // small fp32 arrays (offsets in floats); 16 x 16 matrices with row stride kSq
 constexpr int S_AB = 0, S_T = 320, S_TP = 640, S_DM = 960, S_DT1 = 1280, S_DT2 = 1600, S_Y = 1920, S_DAB = 2240;
 constexpr int S_BETA = 2560, S_IQ0 = 2576, S_IK0 = 2592, S_DB = 2608, S_RQ = 2624, S_RK = 2640;
-constexpr int S_GEND = 2656, S_DGE = 2784, S_TOT = 2912, S_PART = 3168;
-constexpr int SMALL_FLOATS = 3424;
+constexpr int S_GEND = 2656, S_DGE = 2784, S_TOT = 2912, S_PART = 3168, S_GAM = 3424;
+constexpr int SMALL_FLOATS = 3552;
 constexpr int OFF_BAR = OFF_SMALL + SMALL_FLOATS * 4;
 constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
 // The dgamma reduce-scatter lands in the M hi / lo tiles (free by then).
@@ -113,32 +113,6 @@ __device__ __forceinline__ float h16(const uint8_t* base, uint32_t off) {
   return __half2float(*reinterpret_cast<const __half*>(base + off));
 }
 
-// ---- mma.sync fragment loads from fp32 row-major smem matrices ----
-// A[m][k] = X[m][k]
-__device__ __forceinline__ void ldA(float (&a)[4], const float* X, int ld, int k0, int g, int t) {
-  a[0] = X[g * ld + k0 + t];
-  a[1] = X[(g + 8) * ld + k0 + t];
-  a[2] = X[g * ld + k0 + t + 4];
-  a[3] = X[(g + 8) * ld + k0 + t + 4];
-}
-// A[m][k] = X[k][m]
-__device__ __forceinline__ void ldAT(float (&a)[4], const float* X, int ld, int k0, int g, int t) {
-  a[0] = X[(k0 + t) * ld + g];
-  a[1] = X[(k0 + t) * ld + g + 8];
-  a[2] = X[(k0 + t + 4) * ld + g];
-  a[3] = X[(k0 + t + 4) * ld + g + 8];
-}
-// B[k][n] = Y[n][k]
-__device__ __forceinline__ void ldBc(float (&b)[2], const float* Y, int ld, int n0, int k0, int g, int t) {
-  b[0] = Y[(n0 + g) * ld + k0 + t];
-  b[1] = Y[(n0 + g) * ld + k0 + t + 4];
-}
-// B[k][n] = Z[k][n]
-__device__ __forceinline__ void ldBr(float (&b)[2], const float* Z, int ld, int n0, int k0, int g, int t) {
-  b[0] = Z[(k0 + t) * ld + n0 + g];
-  b[1] = Z[(k0 + t + 4) * ld + n0 + g];
-}
-
 // Sums 64 per-lane values over the 32 lanes of a warp (recursive halving):
 // afterwards lane l holds the totals of indices idx(l, 0) and idx(l, 1) with
 // idx(l, e) = 32*b4 + 16*b3 + 8*b2 + 4*b1 + 2*b0 + e (b = bits of l).
@@ -162,14 +136,14 @@ __device__ __forceinline__ void warp_reduce_scatter64(float (&v)[64], int lane) 
 // [16][128] staging tiles (q, k, v, g at dst + 0/4/8/12 KB; dO at dst_dO);
 // rows at or past `rows` are zero-filled. Every thread copies 16 bytes per tile.
 __device__ __forceinline__ void stage_tiles(const TcBwdArgs& a, uint32_t dst, int h, int64_t t0, int rows, int tid,
-                                            bool qkvg, bool dO, uint32_t dst_dO) {
+                                            bool qkvg, bool dO, uint32_t dst_dO, bool with_q = true) {
   const int r = tid >> 4, j = tid & 15;
   const bool ok = r < rows;
   const int64_t off = ok ? ((t0 + r) * a.H + h) * kD + 8 * j : 0;
   const int n = ok ? 16 : 0;
   const uint32_t so = static_cast<uint32_t>(r * 256 + 16 * j);
   if (qkvg) {
-    cp_async16(dst + 0 * 4096 + so, a.q + off, n);
+    if (with_q) cp_async16(dst + 0 * 4096 + so, a.q + off, n);
     cp_async16(dst + 1 * 4096 + so, a.k + off, n);
     cp_async16(dst + 2 * 4096 + so, a.v + off, n);
     cp_async16(dst + 3 * 4096 + so, a.g + off, n);
@@ -289,7 +263,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           const int c = rev ? c1 - 1 : c0;
           const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
           const int rows = static_cast<int>(min(static_cast<int64_t>(kC), eos - t0));
-          stage_tiles(a, sb + OFF_STG, h, t0, rows, tid, true, rev, sb + OFF_SDO);
+          stage_tiles(a, sb + OFF_STG, h, t0, rows, tid, true, rev, sb + OFF_SDO, rev);
           cp_async_commit();
           if (tid < kC && tid < rows) braw_next = __bfloat162float(a.b[(t0 + tid) * a.H + h]);
         }
@@ -310,7 +284,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             const int cn = rev ? c - 1 : c + 1;
             const int64_t tn = bos + static_cast<int64_t>(cn) * kC;
             const int rn = static_cast<int>(min(static_cast<int64_t>(kC), eos - tn));
-            stage_tiles(a, sb + OFF_STG + (buf ^ 1) * kStgBuf, h, tn, rn, tid, true, false, 0);
+            stage_tiles(a, sb + OFF_STG + (buf ^ 1) * kStgBuf, h, tn, rn, tid, true, false, 0, rev);
             if (tid < kC && tid < rn) braw_next = __bfloat162float(a.b[(tn + tid) * a.H + h]);
           }
           cp_async_commit();
@@ -327,12 +301,15 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               float sq = 0.f, sk = 0.f;
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float x = stg(SQ, r, lane + 32 * e), y = stg(SK, r, lane + 32 * e);
-                sq += x * x;
+                const float y = stg(SK, r, lane + 32 * e);
                 sk += y * y;
+                if (rev) {  // the rebuild pass does not use q
+                  const float x = stg(SQ, r, lane + 32 * e);
+                  sq += x * x;
+                }
               }
-              sq = warp_sum(sq);
               sk = warp_sum(sk);
+              if (rev) sq = warp_sum(sq);
               if (lane == 0) {
                 const float nq = sqrtf(sq + a.eps), nk = sqrtf(sk + a.eps);
                 S[S_IQ0 + r] = nq > 0.f ? 1.f / nq : 0.f;
@@ -341,30 +318,43 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             }
           }
           {  // gate, per-half cumulative log2 decay
+            float gv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) gv[j] = stg(SG, 8 * rh + j, ci);
             float acc = 0.f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const int r = 8 * rh + j;
-              const float d = r < rows ? Lg * sigm(expA * (stg(SG, r, ci) + dtb)) : 0.f;
+              const float d = 8 * rh + j < rows ? Lg * sigm(expA * (gv[j] + dtb)) : 0.f;
               acc += d;
-              GS[r * kLd + ci] = acc;
+              gv[j] = acc;
             }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) GS[(8 * rh + j) * kLd + ci] = gv[j];
             S[S_TOT + rh * 128 + ci] = acc;
           }
           __syncthreads();
           {  // full cumsum, gated operands
             const float carry = rh ? S[S_TOT + ci] : 0.f;
             const float gend = S[S_TOT + ci] + S[S_TOT + 128 + ci];
-            if (rh == 0) S[S_GEND + ci] = gend;
+            if (rh == 0) {
+              S[S_GEND + ci] = gend;
+              S[S_GAM + ci] = ex2(gend);
+            }
+            float Gv[8], kv[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int r = 8 * rh + j;
-              const float G = GS[r * kLd + ci] + carry;
+              Gv[j] = GS[r * kLd + ci] + carry;
+              kv[j] = stg(SK, r, ci) * S[S_IK0 + r];
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int r = 8 * rh + j;
+              const float G = Gv[j], kh = kv[j];
+              const float e = ex2(G);
               GS[r * kLd + ci] = G;
-              const float e = ex2(G), ei = ex2(-G);
-              const float kh = stg(SK, r, ci) * S[S_IK0 + r];
               KG[r * kLd + ci] = kh * e;
-              KI[r * kLd + ci] = kh * ei;
+              KI[r * kLd + ci] = kh * ex2(-G);
               st_h(sm + OFF_FKB, sw128_off(r, ci, 16), kh * ex2(gend - G));
               if (rev) {
                 const float qg = stg(SQ, r, ci) * S[S_IQ0 + r] * a.scale * e;
@@ -385,14 +375,19 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             const int nt = warp & 1;
             const bool is_m = (warp >> 1) != 0;
             const float* X = is_m ? QG : KG;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-            for (int k0 = 0; k0 < kD; k0 += 8) {
+            for (int k0 = 0; k0 < kD; k0 += 16) {  // two independent accumulator chains
               float fa[4], fb[2];
               ldA(fa, X, kLd, k0, fg, ft);
               ldBc(fb, KI, kLd, 8 * nt, k0, fg, ft);
               mma3(d, fa, fb);
+              ldA(fa, X, kLd, k0 + 8, fg, ft);
+              ldBc(fb, KI, kLd, 8 * nt, k0 + 8, fg, ft);
+              mma3(d2, fa, fb);
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[e] += d2[e];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int r = fg + 8 * (e >> 1), s = 8 * nt + 2 * ft + (e & 1);
@@ -406,22 +401,23 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             }
           }
           __syncthreads();
-          if (warp == 0) {  // T = (I + diag(beta) Abar)^-1, lane j: column j
-            const int j = lane;
-            float col[16];
+          if (warp == 0) {  // T = (I + diag(beta) Abar)^-1 by forward substitution, lane j: column j
+            const int j = lane & 15;
+            float x[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-              float v = (r == j) ? 1.f : 0.f;
-              if (r > j && j < 16) {
-                const float br = S[S_BETA + r];
+            for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
+            // right-looking: once x[s] is final, eliminate it from every later row
 #pragma unroll
-                for (int s = 0; s < r; ++s)
-                  if (s >= j) v -= br * S[S_AB + r * kSq + s] * col[s];
-              }
-              col[r] = v;
-              if (j < 16) {
-                S[S_T + r * kSq + j] = v;
-                S[S_TP + r * kSq + j] = v * S[S_BETA + j];
+            for (int s2 = 0; s2 < 15; ++s2) {
+#pragma unroll
+              for (int r = s2 + 1; r < 16; ++r) x[r] -= S[S_BETA + r] * S[S_AB + r * kSq + s2] * x[s2];
+            }
+            if (lane < 16) {
+              const float bj = S[S_BETA + j];
+#pragma unroll
+              for (int r = 0; r < 16; ++r) {
+                S[S_T + r * kSq + j] = x[r];
+                S[S_TP + r * kSq + j] = x[r] * bj;
               }
             }
           }
@@ -507,7 +503,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 const int i = 64 * hh + 32 * half + j;
-                hv[j] = ex2(S[S_GEND + i]) * hv[j] + dv[j];
+                hv[j] = S[S_GAM + i] * hv[j] + dv[j];
               }
               tmem_st32(tmem + tlane + TM_H + 64 * hh + 32 * half, hv);
 #pragma unroll
@@ -571,6 +567,61 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             }
             mma_commit(bar);
           }
+          // ---- work that needs only dU~ and U~ runs while the state MMAs do ----
+          if (warp < 4) {  // dM = dO U~^T (warps 0, 1), dU~ V^T (warps 2, 3)
+            const int nt = warp & 1;
+            const bool is_dm = warp < 2;
+            float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int kk = 0; kk < kD; kk += 8) {
+              float fa[4], fb[2];
+              float(&acc)[4] = (kk & 8) ? d2 : d;  // two independent accumulator chains
+              if (is_dm) {  // dO exact in tf32
+                fa[0] = h16(sm + OFF_FDO, sw128_off(fg, kk + ft, 16));
+                fa[1] = h16(sm + OFF_FDO, sw128_off(fg + 8, kk + ft, 16));
+                fa[2] = h16(sm + OFF_FDO, sw128_off(fg, kk + ft + 4, 16));
+                fa[3] = h16(sm + OFF_FDO, sw128_off(fg + 8, kk + ft + 4, 16));
+                ldBc(fb, UT, kLd, 8 * nt, kk, fg, ft);
+                mma2_aexact(acc, fa, fb);
+              } else {  // V exact in tf32
+                ldA(fa, DUT, kLd, kk, fg, ft);
+                fb[0] = stg(SV, 8 * nt + fg, kk + ft);
+                fb[1] = stg(SV, 8 * nt + fg, kk + ft + 4);
+                mma2_bexact(acc, fa, fb);
+              }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int r = fg + 8 * (e >> 1), s = 8 * nt + 2 * ft + (e & 1);
+              if (is_dm)
+                S[S_DM + r * kSq + s] = s > r ? 0.f : d[e] + d2[e];
+              else
+                S[S_DT2 + r * kSq + s] = d[e] + d2[e];
+            }
+          } else {  // dV = T'^T dU~ for channels 32 (w - 4) .. +31
+            float dvv[4][4] = {};
+#pragma unroll
+            for (int k0 = 0; k0 < kC; k0 += 8) {
+              float tpt[4];
+              ldAT(tpt, S + S_TP, kSq, k0, fg, ft);
+#pragma unroll
+              for (int nt = 0; nt < 4; ++nt) {
+                float fb[2];
+                ldBr(fb, DUT, kLd, 32 * (warp - 4) + 8 * nt, k0, fg, ft);
+                mma3(dvv[nt], tpt, fb);
+              }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+              for (int hr = 0; hr < 2; ++hr) {
+                const int r = fg + 8 * hr;
+                if (r < rows)
+                  *reinterpret_cast<uint32_t*>(a.dv + ((t0 + r) * a.H + h) * kD + 32 * (warp - 4) + 8 * nt + 2 * ft) =
+                      pack_bf16(dvv[nt][2 * hr], dvv[nt][2 * hr + 1]);
+              }
+            }
+          }
           KDA_WAIT_MMA();
           fence_after_sync();
           // ---- [E] dH update, dgamma (lane = v); dQG, dW, dKbar (lane = i) ----
@@ -595,7 +646,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 const int i = 64 * hh + 32 * half + j;
-                dh[j] = ex2(S[S_GEND + i]) * dh[j] + inc[j];
+                dh[j] = S[S_GAM + i] * dh[j] + inc[j];
               }
               tmem_st32(tmem + tlane + TM_DH + 64 * hh + 32 * half, dh);
 #pragma unroll
@@ -618,7 +669,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             tmem_ld8(tmem + tlane + TM_DW + 8 * hh, xw);
             tmem_ld8(tmem + tlane + TM_DK + 8 * hh, xk);
             const int i = L;
-            const float gend = S[S_GEND + i], gam = ex2(gend);
+            const float gend = S[S_GEND + i], gam = S[S_GAM + i];
             float part = 0.f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -643,41 +694,28 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             }
             a1_pending = true;
           }
-          // ---- [D1] d(chunk-end log decay); dM, dT' parts on tf32 tiles ----
-          if (tid < kD) {
-            const int i = tid;
+          // ---- [D1] d(chunk-end log decay); dW (Kh Gamma)^T on tf32 tiles ----
+          if (tid >= kD) {
+            const int i = tid - kD;
             const float dgam = RED[i] + RED[128 + i] + RED[256 + i] + RED[384 + i];
-            S[S_DGE + i] = S[S_PART + i] + S[S_PART + 128 + i] + dgam * ex2(S[S_GEND + i]);
-          }
-          if (warp < 6) {
-            const int nt = warp & 1, kind = warp >> 1;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int k0 = 0; k0 < kD; k0 += 8) {
+            S[S_DGE + i] = S[S_PART + i] + S[S_PART + 128 + i] + dgam * S[S_GAM + i];
+          } else {  // warps 0..3: column block nt, contraction half kh (partial sums in DT1 / DAB)
+            const int nt = warp & 1, kh = warp >> 1;
+            float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 64 * kh; kk < 64 * kh + 64; kk += 16) {
               float fa[4], fb[2];
-              if (kind == 0) {  // dM = dO U~^T   (dO exact in tf32)
-                fa[0] = h16(sm + OFF_FDO, sw128_off(fg, k0 + ft, 16));
-                fa[1] = h16(sm + OFF_FDO, sw128_off(fg + 8, k0 + ft, 16));
-                fa[2] = h16(sm + OFF_FDO, sw128_off(fg, k0 + ft + 4, 16));
-                fa[3] = h16(sm + OFF_FDO, sw128_off(fg + 8, k0 + ft + 4, 16));
-                ldBc(fb, UT, kLd, 8 * nt, k0, fg, ft);
-                mma2_aexact(d, fa, fb);
-              } else if (kind == 1) {  // dW (Kh Gamma)^T
-                ldA(fa, WT, kLd, k0, fg, ft);
-                ldBc(fb, KG, kLd, 8 * nt, k0, fg, ft);
-                mma3(d, fa, fb);
-              } else {  // dU~ V^T   (V exact in tf32)
-                ldA(fa, DUT, kLd, k0, fg, ft);
-                fb[0] = stg(SV, 8 * nt + fg, k0 + ft);
-                fb[1] = stg(SV, 8 * nt + fg, k0 + ft + 4);
-                mma2_bexact(d, fa, fb);
-              }
+              ldA(fa, WT, kLd, kk, fg, ft);
+              ldBc(fb, KG, kLd, 8 * nt, kk, fg, ft);
+              mma3(d, fa, fb);
+              ldA(fa, WT, kLd, kk + 8, fg, ft);
+              ldBc(fb, KG, kLd, 8 * nt, kk + 8, fg, ft);
+              mma3(d2, fa, fb);
             }
-            const int dst = kind == 0 ? S_DM : (kind == 1 ? S_DT1 : S_DT2);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int r = fg + 8 * (e >> 1), s = 8 * nt + 2 * ft + (e & 1);
-              S[dst + r * kSq + s] = (kind == 0 && s > r) ? 0.f : d[e];
+              S[(kh ? S_DAB : S_DT1) + r * kSq + s] = d[e] + d2[e];
             }
           }
           __syncthreads();
@@ -687,14 +725,16 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               float db = 0.f;
 #pragma unroll
               for (int r2 = 0; r2 < 16; ++r2)
-                db += S[S_T + r2 * kSq + tid] * (S[S_DT1 + r2 * kSq + tid] + S[S_DT2 + r2 * kSq + tid]);
+                db += S[S_T + r2 * kSq + tid] *
+                      (S[S_DT1 + r2 * kSq + tid] + S[S_DAB + r2 * kSq + tid] + S[S_DT2 + r2 * kSq + tid]);
               S[S_DB + tid] = db;
             }
             float y = 0.f;
 #pragma unroll
             for (int b2 = 0; b2 < 16; ++b2)
               if (b2 < r && b2 <= s)
-                y += (S[S_DT1 + r * kSq + b2] + S[S_DT2 + r * kSq + b2]) * S[S_BETA + b2] * S[S_T + s * kSq + b2];
+                y += (S[S_DT1 + r * kSq + b2] + S[S_DAB + r * kSq + b2] + S[S_DT2 + r * kSq + b2]) * S[S_BETA + b2] *
+                     S[S_T + s * kSq + b2];
             S[S_Y + r * kSq + s] = y;
           }
           __syncthreads();
@@ -717,7 +757,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             S[S_DB + tid] = db;
           }
           {  // ---- [F] 16 x 128 gradient products (channels 16w .. 16w+15) ----
-            float dvv[2][4] = {}, dkg[2][4] = {}, a1[2][4] = {}, m1[2][4] = {}, a2[2][4] = {};
+            float dkg[2][4] = {}, a1[2][4] = {}, m1[2][4] = {}, a2[2][4] = {};
 #pragma unroll
             for (int k0 = 0; k0 < kC; k0 += 8) {
               float tpt[4], dab[4], dabt[4], dm[4], dmt[4];
@@ -730,8 +770,6 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               for (int nt = 0; nt < 2; ++nt) {
                 const int n0 = 16 * warp + 8 * nt;
                 float fb[2];
-                ldBr(fb, DUT, kLd, n0, k0, fg, ft);
-                mma3(dvv[nt], tpt, fb);  // dV = T'^T dU~
                 ldBr(fb, WT, kLd, n0, k0, fg, ft);
                 mma3(dkg[nt], tpt, fb);  // d(Kh Gamma) += T'^T dW
                 ldBr(fb, KI, kLd, n0, k0, fg, ft);
@@ -749,9 +787,6 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               for (int hr = 0; hr < 2; ++hr) {
                 const int r = fg + 8 * hr;
                 const int i0 = 16 * warp + 8 * nt + 2 * ft;
-                if (r < rows)
-                  *reinterpret_cast<uint32_t*>(a.dv + ((t0 + r) * a.H + h) * kD + i0) =
-                      pack_bf16(dvv[nt][2 * hr], dvv[nt][2 * hr + 1]);
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                   const int x = r * kLd + i0 + e, f = 2 * hr + e;

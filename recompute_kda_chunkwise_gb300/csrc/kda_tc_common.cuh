@@ -263,6 +263,33 @@ __device__ __forceinline__ void mma2_aexact(float (&d)[4], const float (&a)[4], 
   mma_tf32_16x8(d, a0, a1, a2, a3, bh[0], bh[1]);
 }
 
+// mma.sync fragment loads from fp32 row-major shared-memory matrices (g = lane / 4,
+// t = lane % 4; ld = row stride in floats)
+// A[m][k] = X[m][k]
+__device__ __forceinline__ void ldA(float (&a)[4], const float* X, int ld, int k0, int g, int t) {
+  a[0] = X[g * ld + k0 + t];
+  a[1] = X[(g + 8) * ld + k0 + t];
+  a[2] = X[g * ld + k0 + t + 4];
+  a[3] = X[(g + 8) * ld + k0 + t + 4];
+}
+// A[m][k] = X[k][m]
+__device__ __forceinline__ void ldAT(float (&a)[4], const float* X, int ld, int k0, int g, int t) {
+  a[0] = X[(k0 + t) * ld + g];
+  a[1] = X[(k0 + t) * ld + g + 8];
+  a[2] = X[(k0 + t + 4) * ld + g];
+  a[3] = X[(k0 + t + 4) * ld + g + 8];
+}
+// B[k][n] = Y[n][k]
+__device__ __forceinline__ void ldBc(float (&b)[2], const float* Y, int ld, int n0, int k0, int g, int t) {
+  b[0] = Y[(n0 + g) * ld + k0 + t];
+  b[1] = Y[(n0 + g) * ld + k0 + t + 4];
+}
+// B[k][n] = Z[k][n]
+__device__ __forceinline__ void ldBr(float (&b)[2], const float* Z, int ld, int n0, int k0, int g, int t) {
+  b[0] = Z[(k0 + t) * ld + n0 + g];
+  b[1] = Z[(k0 + t + 4) * ld + n0 + g];
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 p = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);

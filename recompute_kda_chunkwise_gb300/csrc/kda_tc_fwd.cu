@@ -66,7 +66,7 @@ constexpr int OFF_V = OFF_R;           //   then staged v (bf16 -> fp16 in place
 constexpr int OFF_ABAR = OFF_R + 16384;//   then Abar fp32 [64][65]
 constexpr int OFF_TF = OFF_R + 33024;  //        T fp32 [64][65]
 constexpr int OFF_TP = OFF_R + 50176;  //        T' fp16 [64 r][64 s]
-constexpr int OFF_X = OFF_R + 58368;   //        fp32 scratch [3][16][16]
+constexpr int OFF_X = OFF_R + 58368;   //        fp32 scratch [6][16][9]
 constexpr int OFF_TPL = OFF_R + 16384; //   after the inverse (Abar dead): T' low part fp16 [64 r][64 s]
 constexpr int OFF_ML = OFF_R + 24576;  //                                  M low part fp16 [64 r][64 s]
 constexpr int OFF_UL = OFF_R;          //   after the U product (v dead): U~^T low part fp16 [128 v][64 r]
@@ -108,53 +108,70 @@ __device__ __forceinline__ uint32_t xs_off(int r, int c) {
   return static_cast<uint32_t>(r * 512 + (c >> 5) * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + ((c & 3) << 2));
 }
 
-// T = (I + diag(beta) Abar)^-1 (fp32) by forward substitution on 16 x 16
-// blocks: diagonal blocks by columns, then T_IJ = -T_II sum_{K=J}^{I-1}
-// diag(beta) Abar_IK T_KJ level by level; finally T' = T diag(beta) (fp16).
-__device__ void tri_inverse(uint8_t* sm, const float* s_beta, int tid) {
+// T = (I + diag(beta) Abar)^-1 (fp32) on 16 x 16 blocks: the diagonal blocks
+// by right-looking forward substitution (one warp per block, one lane per
+// column), then level by level T_IJ = -T_II diag(beta_I) sum_{K=J}^{I-1}
+// Abar_IK T_KJ on warp-level tf32 tiles split into hi + lo parts (about fp32
+// accuracy); finally T' = T diag(beta) as fp16 hi + lo parts.
+__device__ __forceinline__ void tri_inverse(uint8_t* sm, const float* s_beta, int tid) {
   float* Ab = reinterpret_cast<float*>(sm + OFF_ABAR);
   float* Tf = reinterpret_cast<float*>(sm + OFF_TF);
   float* X = reinterpret_cast<float*>(sm + OFF_X);
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int x = tid; x < 64 * 65; x += kThreads) Tf[x] = 0.f;
-  __syncthreads();
-  if (warp < 4 && lane < 16) {
-    const int base = 16 * warp, j = lane;
-    float col[16];
+  const int warp = tid >> 5, lane = tid & 31, fg = lane >> 2, ft = lane & 3;
+  if (warp < 4) {
+    const int base = 16 * warp, j = lane & 15;
+    float x[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float v = (r == j) ? 1.f : 0.f;
-      if (r > j) {
-        const float br = s_beta[base + r];
+    for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
-        for (int s = 0; s < r; ++s)
-          if (s >= j) v -= br * Ab[(base + r) * 65 + base + s] * col[s];
-      }
-      col[r] = v;
+    for (int s2 = 0; s2 < 15; ++s2) {
+#pragma unroll
+      for (int r = s2 + 1; r < 16; ++r) x[r] -= s_beta[base + r] * Ab[(base + r) * 65 + base + s2] * x[s2];
     }
+    if (lane < 16) {
 #pragma unroll
-    for (int r = 0; r < 16; ++r) Tf[(base + r) * 65 + base + j] = col[r];
+      for (int r = 0; r < 16; ++r) Tf[(base + r) * 65 + base + j] = x[r];
+    }
+  } else {  // blocks above the diagonal are zero
+    for (int x = tid - 128; x < 64 * 64; x += 128) {
+      const int r = x >> 6, c = x & 63;
+      if ((c >> 4) > (r >> 4)) Tf[r * 65 + c] = 0.f;
+    }
   }
   __syncthreads();
+#pragma unroll 1
   for (int d = 1; d <= 3; ++d) {
-    const int nb = 4 - d;
-    for (int x = tid; x < nb * 256; x += kThreads) {
-      const int b = x >> 8, e = x & 255, rr = e >> 4, cc = e & 15;
-      const int J = b, I = b + d, row = 16 * I + rr;
-      float acc = 0.f;
-      for (int K = J; K < I; ++K)
+    if (warp < 2 * (4 - d)) {  // two warps (8-column halves) per block (I, J = I - d)
+      const int J = warp >> 1, nt = warp & 1, I = J + d;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int K = J; K < I; ++K) {
 #pragma unroll
-        for (int s = 0; s < 16; ++s) acc += Ab[row * 65 + 16 * K + s] * Tf[(16 * K + s) * 65 + 16 * J + cc];
-      X[b * 256 + e] = s_beta[row] * acc;
-    }
-    __syncthreads();
-    for (int x = tid; x < nb * 256; x += kThreads) {
-      const int b = x >> 8, e = x & 255, rr = e >> 4, cc = e & 15;
-      const int J = b, I = b + d;
-      float acc = 0.f;
+        for (int k0 = 0; k0 < 16; k0 += 8) {
+          float fa[4], fb[2];
+          ldA(fa, Ab + (16 * I) * 65 + 16 * K, 65, k0, fg, ft);
+          ldBr(fb, Tf + (16 * K) * 65 + 16 * J, 65, 8 * nt, k0, fg, ft);
+          mma3(acc, fa, fb);
+        }
+      }
+      float* Xw = X + warp * (16 * 9);  // diag(beta_I) sum_K Abar_IK T_KJ, this warp's 8 columns
+      Xw[fg * 9 + 2 * ft] = s_beta[16 * I + fg] * acc[0];
+      Xw[fg * 9 + 2 * ft + 1] = s_beta[16 * I + fg] * acc[1];
+      Xw[(fg + 8) * 9 + 2 * ft] = s_beta[16 * I + fg + 8] * acc[2];
+      Xw[(fg + 8) * 9 + 2 * ft + 1] = s_beta[16 * I + fg + 8] * acc[3];
+      __syncwarp();
+      float t2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int s = 0; s < 16; ++s) acc += Tf[(16 * I + rr) * 65 + 16 * I + s] * X[b * 256 + s * 16 + cc];
-      Tf[(16 * I + rr) * 65 + 16 * J + cc] = -acc;
+      for (int k0 = 0; k0 < 16; k0 += 8) {
+        float fa[4], fb[2];
+        ldA(fa, Tf + (16 * I) * 65 + 16 * I, 65, k0, fg, ft);
+        ldBr(fb, Xw, 9, 0, k0, fg, ft);
+        mma3(t2, fa, fb);
+      }
+      float* dst = Tf + (16 * I) * 65 + 16 * J + 8 * nt + 2 * ft;
+      dst[fg * 65] = -t2[0];
+      dst[fg * 65 + 1] = -t2[1];
+      dst[(fg + 8) * 65] = -t2[2];
+      dst[(fg + 8) * 65 + 1] = -t2[3];
     }
     __syncthreads();
   }
@@ -270,23 +287,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_beta[r] = r < rows ? sigmoidf_(__bfloat162float(a.b[(t0 + r) * a.H + h])) : 0.f;
     }
     KDA_WAIT(bar_qkg, ph_qkg);
-    // ---- row norms: warp w handles rows 8w .. 8w+7 ----
+    // ---- row norms: warp w handles rows 8w .. 8w+7, four at a time (sums
+    // interleaved; lanes 0-3 finish the q rows, lanes 8-11 the k rows) ----
 #pragma unroll
-    for (int rr = 0; rr < 8; ++rr) {
-      const int r = warp * 8 + rr;
-      const uint2 qv = *reinterpret_cast<const uint2*>(sm + OFF_STG_Q + sw128_off(r, 4 * lane, 64));
-      const uint2 kv = *reinterpret_cast<const uint2*>(sm + OFF_STG_K + sw128_off(r, 4 * lane, 64));
-      const float2 q01 = unpack_bf16(qv.x), q23 = unpack_bf16(qv.y);
-      const float2 k01 = unpack_bf16(kv.x), k23 = unpack_bf16(kv.y);
-      float sq = q01.x * q01.x + q01.y * q01.y + q23.x * q23.x + q23.y * q23.y;
-      float sk = k01.x * k01.x + k01.y * k01.y + k23.x * k23.x + k23.y * k23.y;
-      sq = warp_sum(sq);
-      sk = warp_sum(sk);
-      if (lane == 0) {
+    for (int b4 = 0; b4 < 2; ++b4) {
+      float sq[4], sk[4];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = warp * 8 + 4 * b4 + rr;
+        const uint2 qv = *reinterpret_cast<const uint2*>(sm + OFF_STG_Q + sw128_off(r, 4 * lane, 64));
+        const uint2 kv = *reinterpret_cast<const uint2*>(sm + OFF_STG_K + sw128_off(r, 4 * lane, 64));
+        const float2 q01 = unpack_bf16(qv.x), q23 = unpack_bf16(qv.y);
+        const float2 k01 = unpack_bf16(kv.x), k23 = unpack_bf16(kv.y);
+        sq[rr] = q01.x * q01.x + q01.y * q01.y + q23.x * q23.x + q23.y * q23.y;
+        sk[rr] = k01.x * k01.x + k01.y * k01.y + k23.x * k23.x + k23.y * k23.y;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          sq[rr] += __shfl_xor_sync(0xffffffffu, sq[rr], o);
+          sk[rr] += __shfl_xor_sync(0xffffffffu, sk[rr], o);
+        }
+      }
+      float mine = sq[0];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        if ((lane & 3) == rr) mine = (lane & 8) ? sk[rr] : sq[rr];
+      }
+      if ((lane & 4) == 0 && lane < 16) {
+        const int r = warp * 8 + 4 * b4 + (lane & 3);
         const bool ok = r < rows;
-        const float nq = sqrtf(sq + a.eps), nk = sqrtf(sk + a.eps);
-        s_iq[r] = (ok && nq > 0.f) ? a.scale / nq : 0.f;
-        s_ik[r] = (ok && nk > 0.f) ? 1.f / nk : 0.f;
+        const float nrm = sqrtf(mine + a.eps);
+        if (lane & 8)
+          s_ik[r] = (ok && nrm > 0.f) ? 1.f / nrm : 0.f;
+        else
+          s_iq[r] = (ok && nrm > 0.f) ? a.scale / nrm : 0.f;
       }
     }
     // ---- gate and cumulative log2-decay of the thread's 16-row block ----
