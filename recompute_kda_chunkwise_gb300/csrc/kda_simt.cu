@@ -16,8 +16,9 @@
 //   H' = diag(gamma) H + Kbar^T U~,  Kbar[s,i] = kh_si exp(G_{C-1,i} - G_si).
 // The factored products (kh*Gamma)(kh/Gamma)^T are safe in fp32 while the
 // chunk's log-decay range stays below ~88 ("KDA at the production shape ...",
-// section 3(a): k/exp(cumsum g) underflows past cumsum < -88, which at the
-// -5 floor limits a chunk to 17 tokens); these kernels use C = 16 (D = 64)
+// section 3(a): the inverse-decay factor of k leaves fp32 range once the
+// cumulative log-decay passes -88, which at the -5 floor limits a chunk to
+// 17 tokens); these kernels use C = 16 (D = 64)
 // and C = 8 (D = 128, to fit the backward's tiles in shared memory).
 //
 // Backward (recompute policy): the forward stores fp32 states every 1024

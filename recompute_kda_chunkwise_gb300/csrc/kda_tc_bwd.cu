@@ -6,8 +6,9 @@
 // q/k from the inputs and propagating the state gradient dH.
 //
 // Chunk size C = 16: every factor exp(+-(G_r - G_s)) inside a chunk then stays
-// within fp32 range (the "k/exp(cumsum g) underflows past 17 tokens" note of
-// "KDA at the production shape ...", section 3(a)). Work split:
+// within fp32 range ("KDA at the production shape ...", section 3(a): the
+// inverse-decay factor of k leaves fp32 range once the cumulative log-decay
+// passes -88, i.e. beyond 17 tokens at the -5 floor). Work split:
 //   * state products (128-long contractions or 128 x 128 results): tcgen05,
 //     fp16 operands, fp32 accumulators in TMEM (lanes = value index v or key
 //     index i); both fp32 states live in TMEM (H^T while rebuilding, dH^T);

@@ -18,8 +18,9 @@
 // heavy-tailed outputs, fp16 operands (11-bit) meet it. Every tensor-core
 // operand is therefore fp16 (bounded quantities: states, W, U~, T', M, gated
 // q/k, Kbar, and V converted from bf16), except the factors of Abar and M:
-// exp(G_r - G_s) spans e^{320} over 64 tokens at the -5 gate floor (the
-// "k/exp(cumsum g) underflows past 17 tokens" note of section 3(a)), so
+// exp(G_r - G_s) spans e^{320} over 64 tokens at the -5 gate floor (section
+// 3(a) of the same page: the inverse-decay factor of k leaves fp32 range once
+// the cumulative log-decay passes -88, i.e. beyond 17 tokens at that floor), so
 // Abar and M are built from four 16-token column blocks J, each referenced
 // at the end of block J: the row operand kh_r e^{G_r - B_{J+1}} (rows
 // r >= 16J, up to e^{80}) times the column operand kh_s e^{B_{J+1} - G_s}
