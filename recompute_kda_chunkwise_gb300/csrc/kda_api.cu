@@ -75,10 +75,23 @@ int tc_bwd_ctas(const kda_problem* p) {
   return (int)(items < kda::kTcBwdCtas ? items : kda::kTcBwdCtas);
 }
 
+// Tensor-core backward: per-item hand-off counters for helper CTAs (only
+// problems with fewer items than the 152-CTA grid can use them).
+size_t flag_bytes(const kda_problem* p) {
+  if (family_of(p) != 1) return 0;
+  return round_up((size_t)tc_bwd_ctas(p) * 2 * sizeof(uint32_t), 256);
+}
+
 size_t workspace_bytes(const kda_problem* p) {
-  const size_t scratch = family_of(p) == 1 ? (size_t)tc_bwd_ctas(p) * kda::bwd_scratch_bytes_per_cta_tc()
-                                           : kda::bwd_scratch_bytes_simt(p, nullptr);
-  return kda::kHeaderBytes + partial_bytes(p) + scratch;
+  size_t scratch = kda::bwd_scratch_bytes_simt(p, nullptr);
+  if (family_of(p) == 1) {
+    // inline mode: one segment's states per CTA; split mode (items < 152):
+    // two segment buffers per item
+    const int64_t items = (int64_t)p->num_seqs * p->num_heads;
+    const size_t per = kda::bwd_scratch_bytes_per_cta_tc();
+    scratch = items < kda::kTcBwdCtas ? (size_t)items * 2 * per : (size_t)kda::kTcBwdCtas * per;
+  }
+  return kda::kHeaderBytes + partial_bytes(p) + flag_bytes(p) + scratch;
 }
 
 #define CHECK_PTR(ptr)                                                                   \
@@ -179,7 +192,8 @@ kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const voi
   a.dA_log = dA_log; a.ddt_bias = ddt_bias;
   a.status = (int*)workspace;
   a.partial = (float*)((char*)workspace + kda::kHeaderBytes);
-  a.scratch = (float*)((char*)workspace + kda::kHeaderBytes + partial_bytes(p));
+  a.flags = flag_bytes(p) ? (uint32_t*)((char*)workspace + kda::kHeaderBytes + partial_bytes(p)) : nullptr;
+  a.scratch = (float*)((char*)workspace + kda::kHeaderBytes + partial_bytes(p) + flag_bytes(p));
   a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess)

@@ -53,6 +53,7 @@ struct BwdArgs {
   float* ddt_bias;
   float* partial;  // [N*H][D+1]
   float* scratch;  // per-CTA segment states
+  uint32_t* flags;  // tensor-core backward: per-item hand-off counters (NULL: no helper CTAs)
   int* status;
   const int32_t* cu;
   int N, H;

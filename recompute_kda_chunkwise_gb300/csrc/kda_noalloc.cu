@@ -112,6 +112,7 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
   a.status = (int*)scratch;
   a.partial = (float*)((char*)scratch + kda::kHeaderBytes);
   a.scratch = (float*)((char*)scratch + head);
+  a.flags = nullptr;  // no helper CTAs here: few CTAs fit the fixed buffer
   a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   if (cudaMemsetAsync(scratch, 0, sizeof(int), s) != cudaSuccess)

@@ -91,12 +91,32 @@ struct TcBwdArgs {
   const float* ckpt;
   __nv_bfloat16 *dq, *dk, *dv, *dg, *db;
   float* partial;
-  uint8_t* scratch;  // per CTA: kCPS fp16 state tiles
+  uint8_t* scratch;  // fp16 chunk-start state tiles (per CTA, or per item and level parity)
+  uint32_t* flags;   // per item: segments rebuilt, segments consumed (split mode)
   int* status;
   const int32_t* cu;
   int N, H;
+  int helpers;  // > 0: CTAs N*H .. N*H+helpers-1 rebuild segment states for the others
   float scale, lower, eps;
 };
+
+// ---- cross-CTA hand-off of rebuilt segment states (co-resident CTAs of one
+// cooperative launch; every wait bounded) ----
+__device__ __forceinline__ bool wait_flag_geq(const uint32_t* f, uint32_t target, int* status) {
+  for (int it = 0; it < (1 << 24); ++it) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v >= target) return true;
+    __nanosleep(64);
+  }
+  set_status(status, KDA_ERR_TIMEOUT);
+  return false;
+}
+__device__ __forceinline__ void st_release(uint32_t* f, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+// orders this thread's generic-proxy accesses with its async-proxy accesses of global memory
+__device__ __forceinline__ void fence_proxy_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 __device__ __forceinline__ float sigm(float x) { return __fdividef(1.f, 1.f + ex2(-x * kLog2e)); }
 __device__ __forceinline__ void st_h(uint8_t* base, uint32_t off, float x) {
@@ -196,7 +216,6 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   const uint32_t tmem = *s_tmem;
   uint32_t ph = 0, ph_a1 = 0;
   bool a1_pending = false;  // a bulk load into A1 is in flight (same value in every thread)
-  uint8_t* scratch = a.scratch + static_cast<size_t>(blockIdx.x) * kCPS * kStateBytes;
 
 #define KDA_WAIT_MMA()                              \
   do {                                              \
@@ -209,30 +228,94 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
     if (*s_fail) goto teardown; \
   } while (0)
 
-  for (int item = blockIdx.x; item < a.N * a.H; item += gridDim.x) {
-    const int n = item / a.H, h = item % a.H;
-    const int64_t bos = a.cu[n], eos = a.cu[n + 1];
-    const int nchunks = static_cast<int>((eos - bos + kC - 1) / kC);
-    const int nseg = static_cast<int>((eos - bos + kCkptTokens - 1) / kCkptTokens);
-    const float expA = expf(a.A_log[h]);
-    const float dtb = a.dt_bias[h * kD + ci];
-    float acc_dtb = 0.f, acc_alog = 0.f;
+  // Work iteration. A reverse CTA walks its items (blockIdx.x, + gridDim.x,
+  // ...) and each item's segments from the last. In split mode (helpers > 0,
+  // one reverse CTA per item) the helper CTAs rebuild the segment states:
+  // helper j walks levels L = 0, 1, ... (segment nseg-1-L) over the items
+  // j, j + helpers, ..., one level ahead of the reverse CTAs, through two
+  // scratch buffers per item.
+  const int items = a.N * a.H;
+  const bool split = a.helpers > 0;
+  const bool helper = split && static_cast<int>(blockIdx.x) >= items;
+  int item = helper ? static_cast<int>(blockIdx.x) - items : static_cast<int>(blockIdx.x);
+  int seg = -1, lvl = 0;
+  bool open = false, lvl_any = false;
+  int n = 0, h = 0, nchunks = 0, nseg = 0;
+  int64_t bos = 0, eos = 0;
+  float expA = 0.f, dtb = 0.f, acc_dtb = 0.f, acc_alog = 0.f;
 
-    // dH' = 0 (TMEM state and its fp16 operand copy)
-    {
-      float z[32];
+  while (true) {
+    if (!helper) {
+      if (!open) {
+        if (item >= items) break;
+        n = item / a.H;
+        h = item % a.H;
+        bos = a.cu[n];
+        eos = a.cu[n + 1];
+        nchunks = static_cast<int>((eos - bos + kC - 1) / kC);
+        nseg = static_cast<int>((eos - bos + kCkptTokens - 1) / kCkptTokens);
+        expA = expf(a.A_log[h]);
+        dtb = a.dt_bias[h * kD + ci];
+        acc_dtb = 0.f;
+        acc_alog = 0.f;
+        open = true;
+        seg = nseg - 1;
+        // dH' = 0 (TMEM state and its fp16 operand copy)
+        float z[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) z[j] = 0.f;
-      tmem_st32(tmem + tlane + TM_DH + 64 * hh, z);
-      tmem_st32(tmem + tlane + TM_DH + 64 * hh + 32, z);
-      tmem_st_wait();
-      for (int x = tid; x < 32768 / 16; x += kT) reinterpret_cast<uint4*>(sm + OFF_A1D)[x] = make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < 32; ++j) z[j] = 0.f;
+        tmem_st32(tmem + tlane + TM_DH + 64 * hh, z);
+        tmem_st32(tmem + tlane + TM_DH + 64 * hh + 32, z);
+        tmem_st_wait();
+        for (int x = tid; x < 32768 / 16; x += kT) reinterpret_cast<uint4*>(sm + OFF_A1D)[x] = make_uint4(0, 0, 0, 0);
+      }
+    } else {
+      bool found = false;
+      while (true) {
+        if (item >= items) {
+          if (!lvl_any) break;
+          ++lvl;
+          lvl_any = false;
+          item = static_cast<int>(blockIdx.x) - items;
+        }
+        n = item / a.H;
+        h = item % a.H;
+        bos = a.cu[n];
+        eos = a.cu[n + 1];
+        nchunks = static_cast<int>((eos - bos + kC - 1) / kC);
+        nseg = static_cast<int>((eos - bos + kCkptTokens - 1) / kCkptTokens);
+        if (lvl < nseg) {
+          found = true;
+          lvl_any = true;
+          break;
+        }
+        item += a.helpers;
+      }
+      if (!found) break;
+      seg = nseg - 1 - lvl;
+      expA = expf(a.A_log[h]);
+      dtb = a.dt_bias[h * kD + ci];
     }
 
-    for (int seg = nseg - 1; seg >= 0; --seg) {
+    if (seg >= 0) {
+      const int lv = nseg - 1 - seg;  // level: segments counted from the end
       const int c0 = seg * kCPS, c1 = min(nchunks, c0 + kCPS);
-      // ---- segment start state: checkpoint (fp32 [i][v]) -> TMEM H^T and fp16 A1 ----
-      {
+      const bool rebuild = !split || helper;
+      uint8_t* segbuf = split ? a.scratch + (static_cast<size_t>(item) * 2 + (lv & 1)) * kCPS * kStateBytes
+                              : a.scratch + static_cast<size_t>(blockIdx.x) * kCPS * kStateBytes;
+      if (split) {  // hand-off: the helper waits until level lv-2's buffer is consumed,
+                    // the reverse CTA until level lv has been rebuilt
+        if (tid == 0) {
+          bool ok = true;
+          if (helper && lv >= 2) ok = wait_flag_geq(a.flags + 2 * item + 1, static_cast<uint32_t>(lv - 1), a.status);
+          if (!helper) ok = wait_flag_geq(a.flags + 2 * item, static_cast<uint32_t>(lv + 1), a.status);
+          if (!ok) *s_fail = 1;
+          fence_proxy_global();
+        }
+        KDA_SYNC_OR_BAIL();
+      }
+      if (rebuild) {
+        // ---- segment start state: checkpoint (fp32 [i][v]) -> TMEM H^T and fp16 A1 ----
         const float* src = a.ckpt + (ckpt_slot(bos, n, seg) * a.H + h) * static_cast<int64_t>(kD * kD);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -247,18 +330,25 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                            pack_h2(x[8 * cc + 4], x[8 * cc + 5]), pack_h2(x[8 * cc + 6], x[8 * cc + 7]));
         }
         tmem_st_wait();
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
       }
-      fence_async_smem();
-      fence_before_sync();
-      __syncthreads();
 
       // Pass 0 rebuilds the chunk-start states c0+1 .. c1-1 (state c is saved
       // to scratch slot c - c0 before chunk c advances it); pass 1 walks the
       // chunks c1-1 .. c0 in reverse.
 #pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
+      for (int pass = rebuild ? 0 : 1; pass < (helper ? 1 : 2); ++pass) {
         const bool rev = pass == 1;
         const int nsteps = rev ? c1 - c0 : c1 - c0 - 1;
+        if (rev && !rebuild) {  // split mode: the last chunk's start state comes from scratch too
+          if (tid == 0) {
+            mbar_expect_tx(bar_a1, kStateBytes);
+            bulk_load(sb + OFF_A1, segbuf + static_cast<size_t>(c1 - 1 - c0) * kStateBytes, kStateBytes, bar_a1);
+          }
+          a1_pending = true;
+        }
         float braw_next = 0.f;
         if (nsteps > 0) {  // first chunk of the pass: issue its loads now
           const int c = rev ? c1 - 1 : c0;
@@ -289,7 +379,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             if (tid < kC && tid < rn) braw_next = __bfloat162float(a.b[(tn + tid) * a.H + h]);
           }
           cp_async_commit();
-          if (!rev && tid == 0) bulk_store(scratch + static_cast<size_t>(c - c0) * kStateBytes, sb + OFF_A1, kStateBytes);
+          if (!rev && tid == 0) bulk_store(segbuf + static_cast<size_t>(c - c0) * kStateBytes, sb + OFF_A1, kStateBytes);
           cp_async_wait_prev();
           __syncthreads();
 
@@ -691,7 +781,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           if (more) {
             if (tid == 0) {
               mbar_expect_tx(bar_a1, kStateBytes);
-              bulk_load(sb + OFF_A1, scratch + static_cast<size_t>(c - 1 - c0) * kStateBytes, kStateBytes, bar_a1);
+              bulk_load(sb + OFF_A1, segbuf + static_cast<size_t>(c - 1 - c0) * kStateBytes, kStateBytes, bar_a1);
             }
             a1_pending = true;
           }
@@ -864,11 +954,29 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           fence_before_sync();
           KDA_SYNC_OR_BAIL();
         }
-        if (!rev && tid == 0) bulk_wait_all();  // scratch states written before pass 1 reads them
+        if (!rev && tid == 0) {
+          // the helper also saves the segment's last chunk-start state
+          if (helper) bulk_store(segbuf + static_cast<size_t>(c1 - 1 - c0) * kStateBytes, sb + OFF_A1, kStateBytes);
+          bulk_wait_all();  // scratch states written before pass 1 reads them
+          if (helper) {
+            fence_proxy_global();
+            st_release(a.flags + 2 * item, static_cast<uint32_t>(lv + 1));
+          }
+        }
+        if (rev && split && tid == 0) st_release(a.flags + 2 * item + 1, static_cast<uint32_t>(lv + 1));
         __syncthreads();
       }
     }
-    // ---- per-(sequence, head) partial sums of the gate-parameter gradients ----
+
+    if (helper) {
+      item += a.helpers;
+      continue;
+    }
+    if (seg > 0) {
+      --seg;
+      continue;
+    }
+    // ---- item done: per-(sequence, head) partial sums of the gate-parameter gradients ----
     float* R = S + S_TOT;  // 256 floats
     R[tid] = acc_dtb;
     __syncthreads();
@@ -882,6 +990,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
     }
     if (tid == 0) a.partial[static_cast<int64_t>(item) * (kD + 1) + kD] = R[0];
     __syncthreads();
+    open = false;
+    item += gridDim.x;
   }
 #undef KDA_WAIT_MMA
 #undef KDA_SYNC_OR_BAIL
@@ -930,16 +1040,44 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   t.db = static_cast<__nv_bfloat16*>(a.db);
   t.partial = a.partial;
   t.scratch = reinterpret_cast<uint8_t*>(a.scratch);
+  t.flags = a.flags;
   t.status = a.status;
   t.cu = a.cu;
   t.N = a.N;
   t.H = a.H;
+  t.helpers = 0;
   t.scale = a.scale;
   t.lower = a.lower;
   t.eps = a.eps;
   if (cudaFuncSetAttribute(kda_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
     return KDA_ERR_CUDA;
-  if (ctas > 0) kda_bwd_tc_kernel<<<ctas, kT, SMEM_BYTES, s>>>(t);
+  // Split mode: with fewer (sequence, head) items than SMs, the spare SMs
+  // rebuild segment states for the reverse CTAs. Their hand-off waits need
+  // every CTA resident at once, which a cooperative launch guarantees (or
+  // refuses, and the inline mode runs instead).
+  const int items = p->num_seqs * p->num_heads;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_bwd_tc_kernel, kT, SMEM_BYTES);
+  int helpers = 0;
+  if (a.flags != nullptr && items < kTcBwdCtas && items < sms) {
+    const int spare = sms * per_sm - items;
+    if (spare * 5 >= items * 2) helpers = spare < items ? spare : items;
+  }
+  bool launched = false;
+  if (helpers > 0) {
+    t.helpers = helpers;
+    if (cudaMemsetAsync(a.flags, 0, sizeof(uint32_t) * 2 * items, s) != cudaSuccess) return KDA_ERR_CUDA;
+    void* kargs[] = {&t};
+    launched = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kda_bwd_tc_kernel), dim3(items + helpers),
+                                           dim3(kT), kargs, SMEM_BYTES, s) == cudaSuccess;
+    if (!launched) {
+      cudaGetLastError();  // clear the refusal; run inline instead
+      t.helpers = 0;
+    }
+  }
+  if (!launched && ctas > 0) kda_bwd_tc_kernel<<<ctas, kT, SMEM_BYTES, s>>>(t);
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   kda_param_reduce_tc_kernel<<<p->num_heads, 128, 0, s>>>(a.partial, p->num_seqs, p->num_heads, kD, a.dA_log,
                                                           a.ddt_bias);
