@@ -64,8 +64,8 @@ constexpr int OFF_SMALL = OFF_F32 + NT32 * kTileF;
 // small fp32 arrays (offsets in floats); 16 x 16 matrices with row stride kSq
 constexpr int S_AB = 0, S_T = 320, S_TP = 640, S_DM = 960, S_DT1 = 1280, S_DT2 = 1600, S_Y = 1920, S_DAB = 2240;
 constexpr int S_BETA = 2560, S_IQ0 = 2576, S_IK0 = 2592, S_DB = 2608, S_RQ = 2624, S_RK = 2640;
-constexpr int S_GEND = 2656, S_DGE = 2784, S_TOT = 2912, S_PART = 3168, S_GAM = 3424;
-constexpr int SMALL_FLOATS = 3552;
+constexpr int S_GEND = 2656, S_DGE = 2784, S_TOT = 2912, S_PART = 3168, S_GAM = 3424, S_PR = 3552;
+constexpr int SMALL_FLOATS = 3872;
 constexpr int OFF_BAR = OFF_SMALL + SMALL_FLOATS * 4;
 constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
 // The dgamma reduce-scatter lands in the M hi / lo tiles (free by then).
@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
+  const uint64_t D0 = sdesc(sb, 0);  // base of every tcgen05 shared-memory descriptor
   float* F = reinterpret_cast<float*>(sm + OFF_F32);
   float* GS = F + T_GS * (kTileF / 4);
   float* QG = F + T_QG * (kTileF / 4);
@@ -385,27 +386,31 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
 
           // ================= chunk prologue =================
           if (tid < kC) S[S_BETA + tid] = tid < rows ? sigm(braw) : 0.f;
-          {  // row norms: warp w -> rows 2w, 2w+1
+          {  // row norms: warp w -> rows 2w, 2w+1 (sums interleaved; lanes 0-3 finish them)
+            float sk0 = 0.f, sk1 = 0.f, sq0 = 0.f, sq1 = 0.f;
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-              const int r = 2 * warp + rr;
-              float sq = 0.f, sk = 0.f;
+            for (int e = 0; e < 4; ++e) {
+              const float y0 = stg(SK, 2 * warp, lane + 32 * e), y1 = stg(SK, 2 * warp + 1, lane + 32 * e);
+              sk0 += y0 * y0;
+              sk1 += y1 * y1;
+              if (rev) {  // the rebuild does not use q
+                const float x0 = stg(SQ, 2 * warp, lane + 32 * e), x1 = stg(SQ, 2 * warp + 1, lane + 32 * e);
+                sq0 += x0 * x0;
+                sq1 += x1 * x1;
+              }
+            }
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float y = stg(SK, r, lane + 32 * e);
-                sk += y * y;
-                if (rev) {  // the rebuild pass does not use q
-                  const float x = stg(SQ, r, lane + 32 * e);
-                  sq += x * x;
-                }
-              }
-              sk = warp_sum(sk);
-              if (rev) sq = warp_sum(sq);
-              if (lane == 0) {
-                const float nq = sqrtf(sq + a.eps), nk = sqrtf(sk + a.eps);
-                S[S_IQ0 + r] = nq > 0.f ? 1.f / nq : 0.f;
-                S[S_IK0 + r] = nk > 0.f ? 1.f / nk : 0.f;
-              }
+            for (int o = 16; o > 0; o >>= 1) {
+              sk0 += __shfl_xor_sync(0xffffffffu, sk0, o);
+              sk1 += __shfl_xor_sync(0xffffffffu, sk1, o);
+              sq0 += __shfl_xor_sync(0xffffffffu, sq0, o);
+              sq1 += __shfl_xor_sync(0xffffffffu, sq1, o);
+            }
+            if (lane < 4) {  // lane 0/1: k rows, lane 2/3: q rows
+              const float v = lane == 0 ? sk0 : (lane == 1 ? sk1 : (lane == 2 ? sq0 : sq1));
+              const float nrm = sqrtf(v + a.eps);
+              const float inv = nrm > 0.f ? 1.f / nrm : 0.f;
+              S[(lane < 2 ? S_IK0 : S_IQ0) + 2 * warp + (lane & 1)] = inv;
             }
           }
           {  // gate, per-half cumulative log2 decay
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             fence_after_sync();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-              mma(tmem + TM_D1, desc_kmajor(sb + OFF_A1, 128, 0, ks), desc_kmajor(sb + OFF_FW, 16, 0, ks),
+              mma(tmem + TM_D1, desc_k(D0, OFF_A1, 128, 0, ks), desc_k(D0, OFF_FW, 16, 0, ks),
                   idesc(128, 16), ks > 0);
             mma_commit(bar);
           }
@@ -580,7 +585,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             if (tid == 0) {
               bulk_wait_read();  // the scratch copy of A1 has been read out
               fence_after_sync();
-              mma(tmem + TM_D2, desc_mnmajor(sb + OFF_FU, 2048, 0), desc_mnmajor(sb + OFF_FKB, 2048, 0),
+              mma(tmem + TM_D2, desc_mn(D0, OFF_FU, 2048, 0), desc_mn(D0, OFF_FKB, 2048, 0),
                   idesc(128, 128, true, true), 0);
               mma_commit(bar);
             }
@@ -591,10 +596,14 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               float hv[32], dv[32];
               tmem_ld32(tmem + tlane + TM_H + 64 * hh + 32 * half, hv);
               tmem_ld32(tmem + tlane + TM_D2 + 64 * hh + 32 * half, dv);
+              const float4* g4 = reinterpret_cast<const float4*>(S + S_GAM + 64 * hh + 32 * half);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int i = 64 * hh + 32 * half + j;
-                hv[j] = S[S_GAM + i] * hv[j] + dv[j];
+              for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 gm = g4[j4];
+                hv[4 * j4] = gm.x * hv[4 * j4] + dv[4 * j4];
+                hv[4 * j4 + 1] = gm.y * hv[4 * j4 + 1] + dv[4 * j4 + 1];
+                hv[4 * j4 + 2] = gm.z * hv[4 * j4 + 2] + dv[4 * j4 + 2];
+                hv[4 * j4 + 3] = gm.w * hv[4 * j4 + 3] + dv[4 * j4 + 3];
               }
               tmem_st32(tmem + tlane + TM_H + 64 * hh + 32 * half, hv);
 #pragma unroll
@@ -614,13 +623,13 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           // dU~^T = dO^T (Mhi + Mlo) + dH'^T Kbar^T
           if (tid == 0) {
             fence_after_sync();
-            mma(tmem + TM_DU, desc_mnmajor(sb + OFF_FDO, 2048, 0), desc_kmajor(sb + OFF_FM, 16, 0, 0),
+            mma(tmem + TM_DU, desc_mn(D0, OFF_FDO, 2048, 0), desc_k(D0, OFF_FM, 16, 0, 0),
                 idesc(128, 16, true, false), 0);
-            mma(tmem + TM_DU, desc_mnmajor(sb + OFF_FDO, 2048, 0), desc_kmajor(sb + OFF_FML, 16, 0, 0),
+            mma(tmem + TM_DU, desc_mn(D0, OFF_FDO, 2048, 0), desc_k(D0, OFF_FML, 16, 0, 0),
                 idesc(128, 16, true, false), 1);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-              mma(tmem + TM_DU, desc_kmajor(sb + OFF_A1D, 128, 0, ks), desc_kmajor(sb + OFF_FKB, 16, 0, ks),
+              mma(tmem + TM_DU, desc_k(D0, OFF_A1D, 128, 0, ks), desc_k(D0, OFF_FKB, 16, 0, ks),
                   idesc(128, 16), 1);
             mma_commit(bar);
           }
@@ -642,29 +651,32 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           if (tid == 0) {
             fence_after_sync();
             // state increment (Qh Gamma)^T dO - W^T dU~, transposed: dO^T QG + dU~^T (-W)
-            mma(tmem + TM_D2, desc_mnmajor(sb + OFF_FDO, 2048, 0), desc_mnmajor(sb + OFF_FQG, 2048, 0),
+            mma(tmem + TM_D2, desc_mn(D0, OFF_FDO, 2048, 0), desc_mn(D0, OFF_FQG, 2048, 0),
                 idesc(128, 128, true, true), 0);
-            mma(tmem + TM_D2, desc_mnmajor(sb + OFF_FDU, 2048, 0), desc_mnmajor(sb + OFF_FW, 2048, 0),
+            mma(tmem + TM_D2, desc_mn(D0, OFF_FDU, 2048, 0), desc_mn(D0, OFF_FW, 2048, 0),
                 idesc(128, 128, true, true), 1);
             // (H dO^T), (H dU~^T), (dH' U~^T): lanes = key index i
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-              mma(tmem + TM_DQ, desc_mnmajor(sb + OFF_A1, 16384, ks), desc_kmajor(sb + OFF_FDO, 16, 0, ks),
+              mma(tmem + TM_DQ, desc_mn(D0, OFF_A1, 16384, ks), desc_k(D0, OFF_FDO, 16, 0, ks),
                   idesc(128, 16, true, false), ks > 0);
-              mma(tmem + TM_DW, desc_mnmajor(sb + OFF_A1, 16384, ks), desc_kmajor(sb + OFF_FDU, 16, 0, ks),
+              mma(tmem + TM_DW, desc_mn(D0, OFF_A1, 16384, ks), desc_k(D0, OFF_FDU, 16, 0, ks),
                   idesc(128, 16, true, false), ks > 0);
-              mma(tmem + TM_DK, desc_mnmajor(sb + OFF_A1D, 16384, ks), desc_kmajor(sb + OFF_FU, 16, 0, ks),
+              mma(tmem + TM_DK, desc_mn(D0, OFF_A1D, 16384, ks), desc_k(D0, OFF_FU, 16, 0, ks),
                   idesc(128, 16, true, false), ks > 0);
             }
             mma_commit(bar);
           }
-          // ---- work that needs only dU~ and U~ runs while the state MMAs do ----
-          if (warp < 4) {  // dM = dO U~^T (warps 0, 1), dU~ V^T (warps 2, 3)
-            const int nt = warp & 1;
-            const bool is_dm = warp < 2;
+          // ---- work that needs only dU~ and U~ runs while the state MMAs do:
+          // dM = dO U~^T (warps 0-3) and dU~ V^T (warps 4-7), warp w: column
+          // block w & 1, contraction half (w >> 1) & 1; the second halves land
+          // in the PR / DAB scratch matrices and are folded in [D1] ----
+          {
+            const int nt = warp & 1, kh = (warp >> 1) & 1;
+            const bool is_dm = warp < 4;
             float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int kk = 0; kk < kD; kk += 8) {
+#pragma unroll
+            for (int kk = 64 * kh; kk < 64 * kh + 64; kk += 8) {
               float fa[4], fb[2];
               float(&acc)[4] = (kk & 8) ? d2 : d;  // two independent accumulator chains
               if (is_dm) {  // dO exact in tf32
@@ -681,36 +693,11 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                 mma2_bexact(acc, fa, fb);
               }
             }
+            const int dst = is_dm ? (kh ? S_PR : S_DM) : (kh ? S_DAB : S_DT2);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int r = fg + 8 * (e >> 1), s = 8 * nt + 2 * ft + (e & 1);
-              if (is_dm)
-                S[S_DM + r * kSq + s] = s > r ? 0.f : d[e] + d2[e];
-              else
-                S[S_DT2 + r * kSq + s] = d[e] + d2[e];
-            }
-          } else {  // dV = T'^T dU~ for channels 32 (w - 4) .. +31
-            float dvv[4][4] = {};
-#pragma unroll
-            for (int k0 = 0; k0 < kC; k0 += 8) {
-              float tpt[4];
-              ldAT(tpt, S + S_TP, kSq, k0, fg, ft);
-#pragma unroll
-              for (int nt = 0; nt < 4; ++nt) {
-                float fb[2];
-                ldBr(fb, DUT, kLd, 32 * (warp - 4) + 8 * nt, k0, fg, ft);
-                mma3(dvv[nt], tpt, fb);
-              }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-              for (int hr = 0; hr < 2; ++hr) {
-                const int r = fg + 8 * hr;
-                if (r < rows)
-                  *reinterpret_cast<uint32_t*>(a.dv + ((t0 + r) * a.H + h) * kD + 32 * (warp - 4) + 8 * nt + 2 * ft) =
-                      pack_bf16(dvv[nt][2 * hr], dvv[nt][2 * hr + 1]);
-              }
+              const int r = fg + 8 * (e >> 1), sc = 8 * nt + 2 * ft + (e & 1);
+              S[dst + r * kSq + sc] = d[e] + d2[e];
             }
           }
           KDA_WAIT_MMA();
@@ -734,10 +721,14 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                   p[32 * half + 8 * cc + 2 * e + 1] = hf.y * dh[8 * cc + 2 * e + 1];
                 }
               }
+              const float4* g4 = reinterpret_cast<const float4*>(S + S_GAM + 64 * hh + 32 * half);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int i = 64 * hh + 32 * half + j;
-                dh[j] = S[S_GAM + i] * dh[j] + inc[j];
+              for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 gm = g4[j4];
+                dh[4 * j4] = gm.x * dh[4 * j4] + inc[4 * j4];
+                dh[4 * j4 + 1] = gm.y * dh[4 * j4 + 1] + inc[4 * j4 + 1];
+                dh[4 * j4 + 2] = gm.z * dh[4 * j4 + 2] + inc[4 * j4 + 2];
+                dh[4 * j4 + 3] = gm.w * dh[4 * j4 + 3] + inc[4 * j4 + 3];
               }
               tmem_st32(tmem + tlane + TM_DH + 64 * hh + 32 * half, dh);
 #pragma unroll
@@ -790,7 +781,13 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             const int i = tid - kD;
             const float dgam = RED[i] + RED[128 + i] + RED[256 + i] + RED[384 + i];
             S[S_DGE + i] = S[S_PART + i] + S[S_PART + 128 + i] + dgam * S[S_GAM + i];
-          } else {  // warps 0..3: column block nt, contraction half kh (partial sums in DT1 / DAB)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {  // fold the second contraction halves of dM and dU~ V^T
+              const int x = 2 * i + e, r = x >> 4, sc = x & 15, o = r * kSq + sc;
+              S[S_DM + o] = sc > r ? 0.f : S[S_DM + o] + S[S_PR + o];
+              S[S_DT2 + o] += S[S_DAB + o];
+            }
+          } else {  // warps 0..3: column block nt, contraction half kh (partial sums in DT1 / Y)
             const int nt = warp & 1, kh = warp >> 1;
             float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -806,49 +803,67 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int r = fg + 8 * (e >> 1), s = 8 * nt + 2 * ft + (e & 1);
-              S[(kh ? S_DAB : S_DT1) + r * kSq + s] = d[e] + d2[e];
+              S[(kh ? S_Y : S_DT1) + r * kSq + s] = d[e] + d2[e];
             }
           }
           __syncthreads();
-          {  // [D2] dbeta from T' = T diag(beta); Y = (dT' diag(beta)) T^T
-            const int r = sr, s = ss;
-            if (tid < kC) {
-              float db = 0.f;
+          // ---- [D2] dT = dT' diag(beta) (strictly lower; dT' = DT1 + Y + DT2 partials),
+          // Y = dT T^T and dA = -T^T Y on tf32 tiles, warp nt: columns 8nt .. 8nt+7 ----
+          if (warp < 2) {
+            const int nt = warp;
+            float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-              for (int r2 = 0; r2 < 16; ++r2)
-                db += S[S_T + r2 * kSq + tid] *
-                      (S[S_DT1 + r2 * kSq + tid] + S[S_DAB + r2 * kSq + tid] + S[S_DT2 + r2 * kSq + tid]);
-              S[S_DB + tid] = db;
+            for (int k0 = 0; k0 < kC; k0 += 8) {
+              float fa[4], fb[2];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int r = fg + 8 * (e & 1), b2 = k0 + ft + 4 * (e >> 1);
+                const int x = r * kSq + b2;
+                fa[e] = b2 < r ? (S[S_DT1 + x] + S[S_Y + x] + S[S_DT2 + x]) * S[S_BETA + b2] : 0.f;
+              }
+              ldBc(fb, S + S_T, kSq, 8 * nt, k0, fg, ft);  // B[b][s] = T[s][b]
+              mma3(y, fa, fb);
             }
-            float y = 0.f;
+            float* Yw = S + S_DAB;  // this warp's columns of Y, then of diag(beta) dA
+            Yw[fg * kSq + 8 * nt + 2 * ft] = y[0];
+            Yw[fg * kSq + 8 * nt + 2 * ft + 1] = y[1];
+            Yw[(fg + 8) * kSq + 8 * nt + 2 * ft] = y[2];
+            Yw[(fg + 8) * kSq + 8 * nt + 2 * ft + 1] = y[3];
+            __syncwarp();
+            float da[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int b2 = 0; b2 < 16; ++b2)
-              if (b2 < r && b2 <= s)
-                y += (S[S_DT1 + r * kSq + b2] + S[S_DAB + r * kSq + b2] + S[S_DT2 + r * kSq + b2]) * S[S_BETA + b2] *
-                     S[S_T + s * kSq + b2];
-            S[S_Y + r * kSq + s] = y;
-          }
-          __syncthreads();
-          {  // [D3] dA = -(T^T Y) strictly lower; DAB = diag(beta) dA; dA .* Abar
-            const int r = sr, s = ss;
-            float da = 0.f;
-            if (s < r) {
-#pragma unroll
-              for (int a2 = 0; a2 < 16; ++a2)
-                if (a2 >= r) da -= S[S_T + a2 * kSq + r] * S[S_Y + a2 * kSq + s];
+            for (int k0 = 0; k0 < kC; k0 += 8) {
+              float fa[4], fb[2];
+              ldAT(fa, S + S_T, kSq, k0, fg, ft);              // A[r][a] = T[a][r]
+              ldBr(fb, Yw, kSq, 8 * nt, k0, fg, ft);           // B[a][s] = Y[a][s]
+              mma3(da, fa, fb);
             }
-            S[S_DAB + r * kSq + s] = S[S_BETA + r] * da;
-            S[S_DT2 + r * kSq + s] = da * S[S_AB + r * kSq + s];
+            __syncwarp();
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int r = fg + 8 * (e >> 1), sc = 8 * nt + 2 * ft + (e & 1);
+              const float d = sc < r ? -da[e] : 0.f;
+              Yw[r * kSq + sc] = S[S_BETA + r] * d;
+              S[S_PR + r * kSq + sc] = d * S[S_AB + r * kSq + sc];
+            }
+          } else if (warp == 2 && lane < kC) {  // dbeta from T' = T diag(beta)
+            float db = 0.f;
+#pragma unroll
+            for (int r2 = 0; r2 < 16; ++r2) {
+              const int x = r2 * kSq + lane;
+              db += S[S_T + x] * (S[S_DT1 + x] + S[S_Y + x] + S[S_DT2 + x]);
+            }
+            S[S_DB + lane] = db;
           }
           __syncthreads();
           if (tid < kC) {  // dbeta of rows: A = diag(beta) Abar
             float db = S[S_DB + tid];
 #pragma unroll
-            for (int s = 0; s < 16; ++s) db += S[S_DT2 + tid * kSq + s];
+            for (int s = 0; s < 16; ++s) db += S[S_PR + tid * kSq + s];
             S[S_DB + tid] = db;
           }
           {  // ---- [F] 16 x 128 gradient products (channels 16w .. 16w+15) ----
-            float dkg[2][4] = {}, a1[2][4] = {}, m1[2][4] = {}, a2[2][4] = {};
+            float dvv[2][4] = {}, dkg[2][4] = {}, a1[2][4] = {}, m1[2][4] = {}, a2[2][4] = {};
 #pragma unroll
             for (int k0 = 0; k0 < kC; k0 += 8) {
               float tpt[4], dab[4], dabt[4], dm[4], dmt[4];
@@ -861,6 +876,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               for (int nt = 0; nt < 2; ++nt) {
                 const int n0 = 16 * warp + 8 * nt;
                 float fb[2];
+                ldBr(fb, DUT, kLd, n0, k0, fg, ft);
+                mma3(dvv[nt], tpt, fb);  // dV = T'^T dU~
                 ldBr(fb, WT, kLd, n0, k0, fg, ft);
                 mma3(dkg[nt], tpt, fb);  // d(Kh Gamma) += T'^T dW
                 ldBr(fb, KI, kLd, n0, k0, fg, ft);
@@ -878,6 +895,9 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               for (int hr = 0; hr < 2; ++hr) {
                 const int r = fg + 8 * hr;
                 const int i0 = 16 * warp + 8 * nt + 2 * ft;
+                if (r < rows)
+                  *reinterpret_cast<uint32_t*>(a.dv + ((t0 + r) * a.H + h) * kD + i0) =
+                      pack_bf16(dvv[nt][2 * hr], dvv[nt][2 * hr + 1]);
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                   const int x = r * kLd + i0 + e, f = 2 * hr + e;

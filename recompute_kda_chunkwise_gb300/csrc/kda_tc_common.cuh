@@ -57,6 +57,19 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int block_bytes,
   return sdesc(tile + ks * 2048, block_bytes);
 }
 
+// The same descriptors as offsets from a base descriptor D0 = sdesc(smem
+// base, 0) of a 1024-byte aligned shared-memory base: the start field
+// (address / 16, 14 bits) and the leading-byte-offset field are plain sums
+// that never carry, so with a constant `off` each descriptor is D0 plus a
+// compile-time constant (one add at issue time).
+__device__ __forceinline__ uint64_t desc_k(uint64_t D0, uint32_t off, int rows, int row0, int ks) {
+  return D0 + ((static_cast<uint64_t>((off + (ks >> 2) * rows * 128 + (row0 >> 3) * 1024 + (ks & 3) * 32) >> 4)) |
+               (static_cast<uint64_t>(16 >> 4) << 16));
+}
+__device__ __forceinline__ uint64_t desc_mn(uint64_t D0, uint32_t off, int block_bytes, int ks) {
+  return D0 + ((static_cast<uint64_t>((off + ks * 2048) >> 4)) | (static_cast<uint64_t>(block_bytes >> 4) << 16));
+}
+
 // Instruction descriptors (fp32 accumulate, shape M x N, optional MN-major
 // A / B): kind::f16 with fp16 A and B (format 0), kind::tf32 (format 2).
 __host__ __device__ constexpr uint32_t idesc(int M, int N, bool a_mn = false, bool b_mn = false) {

@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
+  const uint64_t D0 = sdesc(sb, 0);  // base of every tcgen05 shared-memory descriptor
   float* smf = reinterpret_cast<float*>(sm + OFF_SMALL);
   float* s_beta = smf + SM_BETA;
   float* s_iq = smf + SM_IQ;
@@ -451,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < 16; ++ks)
-          mma_tf32_ta(tmem + TM_DA + 16 * J, tmem + aj + 8 * ks, desc_kmajor(sb + OFF_BK, 64, 16 * J, ks),
+          mma_tf32_ta(tmem + TM_DA + 16 * J, tmem + aj + 8 * ks, desc_k(D0, OFF_BK, 64, 16 * J, ks),
                       idesc_tf32(128, 16), ks > 0);
         mma_commit((J & 1) ? bar_odd : bar_mma);
       }
@@ -528,12 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after_sync();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)  // W^T = (Kh Gamma)^T (T'hi + T'lo)^T
-        mma(tmem + TM_DW, desc_mnmajor(sb + OFF_XW, 8192, ks & 3),
-            desc_kmajor(sb + (ks < 4 ? OFF_TP : OFF_TPL), 64, 0, ks & 3), idesc(128, 64, true, false), ks > 0);
+        mma(tmem + TM_DW, desc_mn(D0, OFF_XW, 8192, ks & 3),
+            desc_k(D0, (ks < 4 ? OFF_TP : OFF_TPL), 64, 0, ks & 3), idesc(128, 64, true, false), ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)  // U^T = V^T (T'hi + T'lo)^T
-        mma(tmem + TM_DU, desc_mnmajor(sb + OFF_V, 8192, ks & 3),
-            desc_kmajor(sb + (ks < 4 ? OFF_TP : OFF_TPL), 64, 0, ks & 3), idesc(128, 64, true, false), ks > 0);
+        mma(tmem + TM_DU, desc_mn(D0, OFF_V, 8192, ks & 3),
+            desc_k(D0, (ks < 4 ? OFF_TP : OFF_TPL), 64, 0, ks & 3), idesc(128, 64, true, false), ks > 0);
       mma_commit(bar_mma);
     }
     KDA_WAIT(bar_mma, ph_mma);
@@ -554,10 +555,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after_sync();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)  // U~^T = U^T + H^T (-W)^T
-        mma(tmem + TM_DU, desc_kmajor(sb + OFF_A1, 128, 0, ks), desc_kmajor(sb + OFF_B1, 128, 0, ks), idesc(128, 64), 1);
+        mma(tmem + TM_DU, desc_k(D0, OFF_A1, 128, 0, ks), desc_k(D0, OFF_B1, 128, 0, ks), idesc(128, 64), 1);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)  // O^T = H^T (Qh Gamma)^T
-        mma(tmem + TM_DO, desc_kmajor(sb + OFF_A1, 128, 0, ks), desc_kmajor(sb + OFF_B1, 128, 64, ks), idesc(128, 64),
+        mma(tmem + TM_DO, desc_k(D0, OFF_A1, 128, 0, ks), desc_k(D0, OFF_B1, 128, 64, ks), idesc(128, 64),
             ks > 0);
       mma_commit(bar_mma);
     }
@@ -589,13 +590,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after_sync();
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)  // (Kbar^T U~)^T = U~^T Kbar
-        mma(tmem + TM_DH, desc_kmajor(sb + OFF_XW, 128, 0, ks), desc_mnmajor(sb + OFF_B2A, 8192, ks),
+        mma(tmem + TM_DH, desc_k(D0, OFF_XW, 128, 0, ks), desc_mn(D0, OFF_B2A, 8192, ks),
             idesc(128, 128, false, true), ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 12; ++ks) {  // O^T += U~hi^T Mhi^T + U~hi^T Mlo^T + U~lo^T Mhi^T
         const uint32_t ua = (ks < 8) ? OFF_XW : OFF_UL;
         const uint32_t mb = (ks >= 4 && ks < 8) ? OFF_ML : OFF_B2B;
-        mma(tmem + TM_DO, desc_kmajor(sb + ua, 128, 0, ks & 3), desc_kmajor(sb + mb, 64, 0, ks & 3), idesc(128, 64), 1);
+        mma(tmem + TM_DO, desc_k(D0, ua, 128, 0, ks & 3), desc_k(D0, mb, 64, 0, ks & 3), idesc(128, 64), 1);
       }
       mma_commit(bar_mma);
     }
