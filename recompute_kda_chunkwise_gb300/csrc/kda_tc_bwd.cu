@@ -201,7 +201,6 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   const int q4 = warp & 3, hh = warp >> 2, L = 32 * q4 + lane;  // TMEM lane role
   const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
   const int fg = lane >> 2, ft = lane & 3;  // mma fragment role
-  const int sr = tid >> 4, ss = tid & 15;   // (r, s) role for 16 x 16 matrices
   const float Lg = a.lower * kLog2e;
 
   if (tid == 0) {

@@ -67,6 +67,9 @@ WORKLOADS = {
                                              "bf16", 202642, gate_std=2.0),
     "mbs1_128k_h96_d128_bf16": Workload("mbs1_128k_h96_d128_bf16", _equal(1, 131072), 96, 128,
                                         "bf16", 20265),
+    # The long-context shape cut to 8192 tokens: the same launch configuration
+    # (96 sequence-heads) for profiler captures that must stay small.
+    "mbs1_8k_h96_d128_bf16": Workload("mbs1_8k_h96_d128_bf16", _equal(1, 8192), 96, 128, "bf16", 20266),
 }
 HEADLINE = "mbs1_128k_h96_d128_bf16"
 

@@ -34,6 +34,7 @@ def _check_workload(w: Workload, heads=None, device_inputs=False, scale=None):
     "mbs2_8k_h96_d128_bf16_gate2",
     "mbs1_8k_h64_d128_bf16_gate2",
     "mbs1_8k_h128_d128_bf16_gate2",
+    "mbs1_8k_h96_d128_bf16",
 ])
 def test_workload_parity_all_heads(name):
     _check_workload(WORKLOADS[name])
