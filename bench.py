@@ -357,7 +357,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default=None)
     ap.add_argument("--e2e-steps", type=int, default=2)
-    ap.add_argument("--sample-tokens", type=int, default=4096)
+    ap.add_argument("--sample-tokens", type=int, default=65536)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     from recompute_kda_chunkwise_gb300 import HEADLINE, WORKLOADS
