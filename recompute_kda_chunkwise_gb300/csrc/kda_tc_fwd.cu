@@ -113,7 +113,8 @@ __device__ __forceinline__ uint32_t xs_off(int r, int c) {
 // by right-looking forward substitution (one warp per block, one lane per
 // column), then level by level T_IJ = -T_II diag(beta_I) sum_{K=J}^{I-1}
 // Abar_IK T_KJ on warp-level tf32 tiles split into hi + lo parts (about fp32
-// accuracy); finally T' = T diag(beta) as fp16 hi + lo parts.
+// accuracy); finally T' = T diag(beta) as fp16 hi + lo parts. The Abar tile
+// already holds diag(beta) Abar (rows scaled when it is written).
 __device__ __forceinline__ void tri_inverse(uint8_t* sm, const float* s_beta, int tid) {
   float* Ab = reinterpret_cast<float*>(sm + OFF_ABAR);
   float* Tf = reinterpret_cast<float*>(sm + OFF_TF);
@@ -127,16 +128,17 @@ __device__ __forceinline__ void tri_inverse(uint8_t* sm, const float* s_beta, in
 #pragma unroll
     for (int s2 = 0; s2 < 15; ++s2) {
 #pragma unroll
-      for (int r = s2 + 1; r < 16; ++r) x[r] -= s_beta[base + r] * Ab[(base + r) * 65 + base + s2] * x[s2];
+      for (int r = s2 + 1; r < 16; ++r) x[r] -= Ab[(base + r) * 65 + base + s2] * x[s2];
     }
     if (lane < 16) {
 #pragma unroll
       for (int r = 0; r < 16; ++r) Tf[(base + r) * 65 + base + j] = x[r];
     }
-  } else {  // blocks above the diagonal are zero
-    for (int x = tid - 128; x < 64 * 64; x += 128) {
-      const int r = x >> 6, c = x & 63;
-      if ((c >> 4) > (r >> 4)) Tf[r * 65 + c] = 0.f;
+  } else {  // the six blocks above the diagonal are zero
+    for (int x = tid - 128; x < 6 * 256; x += 128) {
+      const int b = x >> 8, e = x & 255;
+      const int I = b < 3 ? 0 : (b < 5 ? 1 : 2), J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+      Tf[(16 * I + (e >> 4)) * 65 + 16 * J + (e & 15)] = 0.f;
     }
   }
   __syncthreads();
@@ -155,10 +157,10 @@ __device__ __forceinline__ void tri_inverse(uint8_t* sm, const float* s_beta, in
         }
       }
       float* Xw = X + warp * (16 * 9);  // diag(beta_I) sum_K Abar_IK T_KJ, this warp's 8 columns
-      Xw[fg * 9 + 2 * ft] = s_beta[16 * I + fg] * acc[0];
-      Xw[fg * 9 + 2 * ft + 1] = s_beta[16 * I + fg] * acc[1];
-      Xw[(fg + 8) * 9 + 2 * ft] = s_beta[16 * I + fg + 8] * acc[2];
-      Xw[(fg + 8) * 9 + 2 * ft + 1] = s_beta[16 * I + fg + 8] * acc[3];
+      Xw[fg * 9 + 2 * ft] = acc[0];
+      Xw[fg * 9 + 2 * ft + 1] = acc[1];
+      Xw[(fg + 8) * 9 + 2 * ft] = acc[2];
+      Xw[(fg + 8) * 9 + 2 * ft + 1] = acc[3];
       __syncwarp();
       float t2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -467,11 +469,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + tlane + TM_DA + 32 * hh, v);
       const int m = lrow;
       if (m < 64) {
-        float* Ab = reinterpret_cast<float*>(sm + OFF_ABAR);
+        float* Ab = reinterpret_cast<float*>(sm + OFF_ABAR);  // diag(beta) Abar
+        const float bm = s_beta[m];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int s = 32 * hh + j;
-          Ab[m * 65 + s] = s < m ? v[j] : 0.f;
+          Ab[m * 65 + s] = s < m ? bm * v[j] : 0.f;
         }
       } else {
         const int r = m - 64;
@@ -609,8 +612,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         tmem_ld32(tmem + tlane + TM_DH + 64 * hh + 32 * half, v);
+        const float4* g4 = reinterpret_cast<const float4*>(s_gam + 64 * hh + 32 * half);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) Hst[32 * half + j] = s_gam[64 * hh + 32 * half + j] * Hst[32 * half + j] + v[j];
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 gm = g4[j4];
+          const int j = 32 * half + 4 * j4;
+          Hst[j] = gm.x * Hst[j] + v[4 * j4];
+          Hst[j + 1] = gm.y * Hst[j + 1] + v[4 * j4 + 1];
+          Hst[j + 2] = gm.z * Hst[j + 2] + v[4 * j4 + 2];
+          Hst[j + 3] = gm.w * Hst[j + 3] + v[4 * j4 + 3];
+        }
       }
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc)
