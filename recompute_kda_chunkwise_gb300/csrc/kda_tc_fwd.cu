@@ -85,8 +85,9 @@ constexpr uint32_t TM_DW = 64;   // W^T (lanes = i), 64 columns
 constexpr uint32_t TM_DU = 128;  // U~^T, 64 columns
 constexpr uint32_t TM_DO = 192;  // O^T, 64 columns
 constexpr uint32_t TM_DH = 256;  // (Kbar^T U~)^T, 128 columns
-constexpr uint32_t TM_AJ = 256;  // tf32 row operand of the Abar | M rounds, double-buffered:
-                                 // rounds 0, 2 at 256.. (the DH columns, free then), rounds 1, 3 at 384..
+constexpr uint32_t TM_AJ = 64;   // tf32 row operands of the Abar | M rounds: rounds 0..2 at
+                                 // 64 + 128 J (columns free until the W/U products), round 3
+                                 // reuses round 0's columns
 constexpr uint32_t TM_COLS = 512;
 
 struct TcFwdArgs {
@@ -210,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_mma = bar_qkg + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_qkg + 3);
   int* s_fail = reinterpret_cast<int*>(bar_qkg + 4);
-  uint64_t* bar_odd = bar_qkg + 5;  // completions of the odd Abar | M rounds
+  uint64_t* bar_odd = bar_qkg + 5;  // completion of Abar | M round 1
+  uint64_t* bar_r2 = bar_qkg + 6;   // completion of Abar | M round 2
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
@@ -222,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
     mbar_init(bar_odd, 1);
+    mbar_init(bar_r2, 1);
     *s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float Hst[64];
 #pragma unroll
   for (int j = 0; j < 64; ++j) Hst[j] = 0.f;
-  uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0, ph_odd = 0;
+  uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0, ph_odd = 0, ph_r2 = 0;
 
   auto issue_qkg = [&](int t) {
     mbar_expect_tx(bar_qkg, 6 * 8192);
@@ -424,43 +427,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (c + 1 < nchunks) issue_qkg(static_cast<int>(t0 + kC));
     }
 
-    // ---- Abar | M by column block J: tf32, row operand in TMEM ----
-#pragma unroll 1
-    for (int J = 0; J < 4; ++J) {
-      const uint32_t aj = TM_AJ + 128 * (J & 1);
-      // round J-2 read this buffer; even rounds complete on bar_mma, odd ones on
-      // bar_odd, so no barrier ever has two unobserved phases
-      if (J == 2) KDA_WAIT(bar_mma, ph_mma);
-      if (J == 3) KDA_WAIT(bar_odd, ph_odd);
-      // rows of blocks before J do not contribute to column block J (s > r),
-      // but every lane stores: tcgen05.st is warp-collective
-      {
-        float uv[32];
+    // ---- Abar | M by column block J: tf32, row operand in TMEM. Rounds 0-2
+    // are written at once and issued in parallel by lane 0 of warps 0-2 (each
+    // commits to its own mbarrier); round 3 reuses round 0's columns. Rows of
+    // blocks before J do not contribute to column block J (s > r), but every
+    // lane stores: tcgen05.st is warp-collective. ----
+    auto store_round = [&](int J, uint32_t aj) {
+      float uv[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < 2; ++half) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int ch = 64 * hh + 32 * half + j;
-            const float u = (J < pI) ? s_u[(pI * (pI - 1) / 2 + J) * 128 + ch] : 1.f;
-            uv[j] = rowf[32 * half + j] * u;
-          }
-          tmem_st32(tmem + tlane + aj + 64 * hh + 32 * half, uv);
+        for (int j = 0; j < 32; ++j) {
+          const int ch = 64 * hh + 32 * half + j;
+          const float u = (J < pI) ? s_u[(pI * (pI - 1) / 2 + J) * 128 + ch] : 1.f;
+          uv[j] = rowf[32 * half + j] * u;
         }
+        tmem_st32(tmem + tlane + aj + 64 * hh + 32 * half, uv);
       }
-      tmem_st_wait();
-      fence_before_sync();
-      KDA_SYNC_OR_BAIL();
-      if (tid == 0) {
-        fence_after_sync();
+    };
+    auto issue_round = [&](int J, uint32_t aj, uint64_t* done) {
+      fence_after_sync();
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks)
-          mma_tf32_ta(tmem + TM_DA + 16 * J, tmem + aj + 8 * ks, desc_k(D0, OFF_BK, 64, 16 * J, ks),
-                      idesc_tf32(128, 16), ks > 0);
-        mma_commit((J & 1) ? bar_odd : bar_mma);
-      }
-    }
-    KDA_WAIT(bar_mma, ph_mma);  // round 2
-    KDA_WAIT(bar_odd, ph_odd);  // round 3
+      for (int ks = 0; ks < 16; ++ks)
+        mma_tf32_ta(tmem + TM_DA + 16 * J, tmem + aj + 8 * ks, desc_k(D0, OFF_BK, 64, 16 * J, ks),
+                    idesc_tf32(128, 16), ks > 0);
+      mma_commit(done);
+    };
+#pragma unroll 1
+    for (int J = 0; J < 3; ++J) store_round(J, TM_AJ + 128 * J);
+    tmem_st_wait();
+    fence_before_sync();
+    KDA_SYNC_OR_BAIL();
+    if (lane == 0 && warp < 3) issue_round(warp, TM_AJ + 128 * warp, warp == 0 ? bar_mma : (warp == 1 ? bar_odd : bar_r2));
+    KDA_WAIT(bar_mma, ph_mma);  // round 0 has read its columns
+    fence_after_sync();
+    store_round(3, TM_AJ);
+    tmem_st_wait();
+    fence_before_sync();
+    KDA_SYNC_OR_BAIL();
+    if (tid == 0) issue_round(3, TM_AJ, bar_mma);
+    KDA_WAIT(bar_odd, ph_odd);  // round 1
+    KDA_WAIT(bar_r2, ph_r2);    // round 2
+    KDA_WAIT(bar_mma, ph_mma);  // round 3
     fence_after_sync();
 
     // ---- Abar (fp32, for the inverse) and M (fp16 operand) out of TMEM ----
