@@ -79,7 +79,7 @@ int tc_bwd_ctas(const kda_problem* p) {
 // problems with fewer items than the 152-CTA grid can use them).
 size_t flag_bytes(const kda_problem* p) {
   if (family_of(p) != 1) return 0;
-  return round_up((size_t)tc_bwd_ctas(p) * 2 * sizeof(uint32_t), 256);
+  return round_up((size_t)tc_bwd_ctas(p) * 3 * sizeof(uint32_t), 256);
 }
 
 size_t workspace_bytes(const kda_problem* p) {

@@ -92,7 +92,7 @@ struct TcBwdArgs {
   __nv_bfloat16 *dq, *dk, *dv, *dg, *db;
   float* partial;
   uint8_t* scratch;  // fp16 chunk-start state tiles (per CTA, or per item and level parity)
-  uint32_t* flags;   // per item: segments rebuilt, segments consumed (split mode)
+  uint32_t* flags;   // per item: last level + 1 rebuilt into buffer 0 / buffer 1, levels consumed (split mode)
   int* status;
   const int32_t* cu;
   int N, H;
@@ -195,6 +195,9 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   uint64_t* bar_a1 = bar + 1;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar + 2);
   int* s_fail = reinterpret_cast<int*>(bar + 3);
+  uint64_t* bar_du = bar + 4;  // dU~ products (issued early, reverse pass)
+  uint64_t* bar_g1 = bar + 5;  // (H dU~^T) products
+  uint64_t* bar_g2 = bar + 6;  // (dH' U~^T) products
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ci = tid & 127, rh = tid >> 7;  // channel role: channel ci, rows 8*rh .. 8*rh+7
@@ -206,6 +209,9 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   if (tid == 0) {
     mbar_init(bar, 1);
     mbar_init(bar_a1, 1);
+    mbar_init(bar_du, 1);
+    mbar_init(bar_g1, 1);
+    mbar_init(bar_g2, 1);
     *s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *s_tmem;
-  uint32_t ph = 0, ph_a1 = 0;
+  uint32_t ph = 0, ph_a1 = 0, ph_du = 0, ph_g1 = 0, ph_g2 = 0;
   bool a1_pending = false;  // a bulk load into A1 is in flight (same value in every thread)
 
 #define KDA_WAIT_MMA()                              \
@@ -231,15 +237,23 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   // Work iteration. A reverse CTA walks its items (blockIdx.x, + gridDim.x,
   // ...) and each item's segments from the last. In split mode (helpers > 0,
   // one reverse CTA per item) the helper CTAs rebuild the segment states:
-  // helper j walks levels L = 0, 1, ... (segment nseg-1-L) over the items
-  // j, j + helpers, ..., one level ahead of the reverse CTAs, through two
-  // scratch buffers per item.
+  // the jobs (level L = segment nseg-1-L, item) are numbered level-major,
+  // job = L * items + item, and helper j takes jobs j, j + helpers, ... in
+  // order, so every helper carries the same load and the levels complete in
+  // order, ahead of the reverse CTAs; each item has two scratch buffers.
   const int items = a.N * a.H;
   const bool split = a.helpers > 0;
   const bool helper = split && static_cast<int>(blockIdx.x) >= items;
-  int item = helper ? static_cast<int>(blockIdx.x) - items : static_cast<int>(blockIdx.x);
+  int item = helper ? 0 : static_cast<int>(blockIdx.x);
   int seg = -1, lvl = 0;
-  bool open = false, lvl_any = false;
+  bool open = false;
+  int job = static_cast<int>(blockIdx.x) - items, max_jobs = 0;
+  if (helper) {  // jobs run up to the longest sequence's segment count
+    int max_seg = 0;
+    for (int s2 = 0; s2 < a.N; ++s2)
+      max_seg = max(max_seg, static_cast<int>((a.cu[s2 + 1] - a.cu[s2] + kCkptTokens - 1) / kCkptTokens));
+    max_jobs = max_seg * items;
+  }
   int n = 0, h = 0, nchunks = 0, nseg = 0;
   int64_t bos = 0, eos = 0;
   float expA = 0.f, dtb = 0.f, acc_dtb = 0.f, acc_alog = 0.f;
@@ -271,13 +285,10 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
       }
     } else {
       bool found = false;
-      while (true) {
-        if (item >= items) {
-          if (!lvl_any) break;
-          ++lvl;
-          lvl_any = false;
-          item = static_cast<int>(blockIdx.x) - items;
-        }
+      while (job < max_jobs) {
+        lvl = job / items;
+        item = job % items;
+        job += a.helpers;
         n = item / a.H;
         h = item % a.H;
         bos = a.cu[n];
@@ -286,10 +297,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
         nseg = static_cast<int>((eos - bos + kCkptTokens - 1) / kCkptTokens);
         if (lvl < nseg) {
           found = true;
-          lvl_any = true;
           break;
         }
-        item += a.helpers;
       }
       if (!found) break;
       seg = nseg - 1 - lvl;
@@ -307,8 +316,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                     // the reverse CTA until level lv has been rebuilt
         if (tid == 0) {
           bool ok = true;
-          if (helper && lv >= 2) ok = wait_flag_geq(a.flags + 2 * item + 1, static_cast<uint32_t>(lv - 1), a.status);
-          if (!helper) ok = wait_flag_geq(a.flags + 2 * item, static_cast<uint32_t>(lv + 1), a.status);
+          if (helper && lv >= 2) ok = wait_flag_geq(a.flags + 3 * item + 2, static_cast<uint32_t>(lv - 1), a.status);
+          if (!helper) ok = wait_flag_geq(a.flags + 3 * item + (lv & 1), static_cast<uint32_t>(lv + 1), a.status);
           if (!ok) *s_fail = 1;
           fence_proxy_global();
         }
@@ -495,7 +504,23 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               }
             }
           }
+          fence_async_smem();
+          fence_before_sync();
           __syncthreads();
+          // dU~^T = dO^T (Mhi + Mlo) + dH'^T Kbar^T needs no U~: issue it now (warp 4 is idle
+          // during the inverse) so it runs under the inverse and the W/U stage
+          if (rev && warp == 4 && lane == 0) {
+            fence_after_sync();
+            mma(tmem + TM_DU, desc_mn(D0, OFF_FDO, 2048, 0), desc_k(D0, OFF_FM, 16, 0, 0),
+                idesc(128, 16, true, false), 0);
+            mma(tmem + TM_DU, desc_mn(D0, OFF_FDO, 2048, 0), desc_k(D0, OFF_FML, 16, 0, 0),
+                idesc(128, 16, true, false), 1);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              mma(tmem + TM_DU, desc_k(D0, OFF_A1D, 128, 0, ks), desc_k(D0, OFF_FKB, 16, 0, ks),
+                  idesc(128, 16), 1);
+            mma_commit(bar_du);
+          }
           if (warp == 0) {  // T = (I + diag(beta) Abar)^-1 by forward substitution, lane j: column j
             const int j = lane & 15;
             float x[16];
@@ -563,6 +588,10 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             mma_commit(bar);
           }
           KDA_WAIT_MMA();
+          if (rev) {
+            if (!mbar_wait(bar_du, ph_du, a.status)) *s_fail = 1;
+            ph_du ^= 1u;
+          }
           fence_after_sync();
           {
             float x[8];
@@ -573,6 +602,15 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               const float u = UT[r * kLd + L] + x[j];
               UT[r * kLd + L] = u;
               st_h(sm + OFF_FU, sw128_off(r, L, 16), u);
+            }
+            if (rev) {
+              tmem_ld8(tmem + tlane + TM_DU + 8 * hh, x);  // dU~^T: lane = v, columns r
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int r = 8 * hh + j;
+                DUT[r * kLd + L] = x[j];
+                st_h(sm + OFF_FDU, sw128_off(r, L, 16), x[j]);
+              }
             }
           }
           fence_async_smem();
@@ -619,52 +657,34 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           }
 
           // ================= reverse pass: backward of chunk c =================
-          // dU~^T = dO^T (Mhi + Mlo) + dH'^T Kbar^T
-          if (tid == 0) {
+          // Three issuers (lane 0 of warps 0-2), one mbarrier each:
+          // state increment (Qh Gamma)^T dO - W^T dU~, transposed: dO^T QG + dU~^T (-W),
+          // and (H dO^T); (H dU~^T); (dH' U~^T) -- lanes = key index i
+          if (lane == 0 && warp < 3) {
             fence_after_sync();
-            mma(tmem + TM_DU, desc_mn(D0, OFF_FDO, 2048, 0), desc_k(D0, OFF_FM, 16, 0, 0),
-                idesc(128, 16, true, false), 0);
-            mma(tmem + TM_DU, desc_mn(D0, OFF_FDO, 2048, 0), desc_k(D0, OFF_FML, 16, 0, 0),
-                idesc(128, 16, true, false), 1);
+            if (warp == 0) {
+              mma(tmem + TM_D2, desc_mn(D0, OFF_FDO, 2048, 0), desc_mn(D0, OFF_FQG, 2048, 0),
+                  idesc(128, 128, true, true), 0);
+              mma(tmem + TM_D2, desc_mn(D0, OFF_FDU, 2048, 0), desc_mn(D0, OFF_FW, 2048, 0),
+                  idesc(128, 128, true, true), 1);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              mma(tmem + TM_DU, desc_k(D0, OFF_A1D, 128, 0, ks), desc_k(D0, OFF_FKB, 16, 0, ks),
-                  idesc(128, 16), 1);
-            mma_commit(bar);
-          }
-          KDA_WAIT_MMA();
-          fence_after_sync();
-          {
-            float x[8];
-            tmem_ld8(tmem + tlane + TM_DU + 8 * hh, x);  // lane = v, columns r
+              for (int ks = 0; ks < 8; ++ks)
+                mma(tmem + TM_DQ, desc_mn(D0, OFF_A1, 16384, ks), desc_k(D0, OFF_FDO, 16, 0, ks),
+                    idesc(128, 16, true, false), ks > 0);
+              mma_commit(bar);
+            } else if (warp == 1) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int r = 8 * hh + j;
-              DUT[r * kLd + L] = x[j];
-              st_h(sm + OFF_FDU, sw128_off(r, L, 16), x[j]);
+              for (int ks = 0; ks < 8; ++ks)
+                mma(tmem + TM_DW, desc_mn(D0, OFF_A1, 16384, ks), desc_k(D0, OFF_FDU, 16, 0, ks),
+                    idesc(128, 16, true, false), ks > 0);
+              mma_commit(bar_g1);
+            } else {
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks)
+                mma(tmem + TM_DK, desc_mn(D0, OFF_A1D, 16384, ks), desc_k(D0, OFF_FU, 16, 0, ks),
+                    idesc(128, 16, true, false), ks > 0);
+              mma_commit(bar_g2);
             }
-          }
-          fence_async_smem();
-          fence_before_sync();
-          KDA_SYNC_OR_BAIL();
-          if (tid == 0) {
-            fence_after_sync();
-            // state increment (Qh Gamma)^T dO - W^T dU~, transposed: dO^T QG + dU~^T (-W)
-            mma(tmem + TM_D2, desc_mn(D0, OFF_FDO, 2048, 0), desc_mn(D0, OFF_FQG, 2048, 0),
-                idesc(128, 128, true, true), 0);
-            mma(tmem + TM_D2, desc_mn(D0, OFF_FDU, 2048, 0), desc_mn(D0, OFF_FW, 2048, 0),
-                idesc(128, 128, true, true), 1);
-            // (H dO^T), (H dU~^T), (dH' U~^T): lanes = key index i
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              mma(tmem + TM_DQ, desc_mn(D0, OFF_A1, 16384, ks), desc_k(D0, OFF_FDO, 16, 0, ks),
-                  idesc(128, 16, true, false), ks > 0);
-              mma(tmem + TM_DW, desc_mn(D0, OFF_A1, 16384, ks), desc_k(D0, OFF_FDU, 16, 0, ks),
-                  idesc(128, 16, true, false), ks > 0);
-              mma(tmem + TM_DK, desc_mn(D0, OFF_A1D, 16384, ks), desc_k(D0, OFF_FU, 16, 0, ks),
-                  idesc(128, 16, true, false), ks > 0);
-            }
-            mma_commit(bar);
           }
           // ---- work that needs only dU~ and U~ runs while the state MMAs do:
           // dM = dO U~^T (warps 0-3) and dU~ V^T (warps 4-7), warp w: column
@@ -700,6 +720,10 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             }
           }
           KDA_WAIT_MMA();
+          if (!mbar_wait(bar_g1, ph_g1, a.status)) *s_fail = 1;
+          ph_g1 ^= 1u;
+          if (!mbar_wait(bar_g2, ph_g2, a.status)) *s_fail = 1;
+          ph_g2 ^= 1u;
           fence_after_sync();
           // ---- [E] dH update, dgamma (lane = v); dQG, dW, dKbar (lane = i) ----
           {
@@ -979,18 +1003,15 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           bulk_wait_all();  // scratch states written before pass 1 reads them
           if (helper) {
             fence_proxy_global();
-            st_release(a.flags + 2 * item, static_cast<uint32_t>(lv + 1));
+            st_release(a.flags + 3 * item + (lv & 1), static_cast<uint32_t>(lv + 1));
           }
         }
-        if (rev && split && tid == 0) st_release(a.flags + 2 * item + 1, static_cast<uint32_t>(lv + 1));
+        if (rev && split && tid == 0) st_release(a.flags + 3 * item + 2, static_cast<uint32_t>(lv + 1));
         __syncthreads();
       }
     }
 
-    if (helper) {
-      item += a.helpers;
-      continue;
-    }
+    if (helper) continue;
     if (seg > 0) {
       --seg;
       continue;
@@ -1087,7 +1108,7 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   bool launched = false;
   if (helpers > 0) {
     t.helpers = helpers;
-    if (cudaMemsetAsync(a.flags, 0, sizeof(uint32_t) * 2 * items, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaMemsetAsync(a.flags, 0, sizeof(uint32_t) * 3 * items, s) != cudaSuccess) return KDA_ERR_CUDA;
     void* kargs[] = {&t};
     launched = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kda_bwd_tc_kernel), dim3(items + helpers),
                                            dim3(kT), kargs, SMEM_BYTES, s) == cudaSuccess;
