@@ -43,6 +43,12 @@ constexpr int kTileF = kC * kLd * 4;    // bytes of one fp32 [16][132] tile
 constexpr int kSq = 20;                 // row stride of the 16 x 16 matrices
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kStateBytes = 32768;  // fp16 128 x 128 state tile
+// One scratch slot per chunk: the chunk-start state, then (split mode) the
+// chunk's Abar, T, T' (the 16 x kSq small matrices at S_AB .. S_TP) and the
+// M hi / lo tiles, written by a helper CTA for the reverse CTA.
+constexpr uint32_t kPrepSBytes = 3 * 320 * 4;  // S_AB, S_T, S_TP
+constexpr uint32_t kPrepMBytes = 4096;         // M hi + lo tiles
+constexpr uint32_t kSlotBytes = kStateBytes + 8192;
 
 // ---- shared memory map (bytes) ----
 constexpr int OFF_A1 = 0;                  // H^T fp16 [128 v][128 i] (SW128)
@@ -198,6 +204,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   uint64_t* bar_du = bar + 4;  // dU~ products (issued early, reverse pass)
   uint64_t* bar_g1 = bar + 5;  // (H dU~^T) products
   uint64_t* bar_g2 = bar + 6;  // (dH' U~^T) products
+  uint64_t* bar_sm = bar + 7;  // split mode: a chunk's Abar, T, T', M loaded from scratch
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ci = tid & 127, rh = tid >> 7;  // channel role: channel ci, rows 8*rh .. 8*rh+7
@@ -212,6 +219,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
     mbar_init(bar_du, 1);
     mbar_init(bar_g1, 1);
     mbar_init(bar_g2, 1);
+    mbar_init(bar_sm, 1);
     *s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -220,7 +228,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *s_tmem;
-  uint32_t ph = 0, ph_a1 = 0, ph_du = 0, ph_g1 = 0, ph_g2 = 0;
+  uint32_t ph = 0, ph_a1 = 0, ph_du = 0, ph_g1 = 0, ph_g2 = 0, ph_sm = 0;
+  bool sm_pending = false;  // a bulk load of a chunk's small matrices is in flight
   bool a1_pending = false;  // a bulk load into A1 is in flight (same value in every thread)
 
 #define KDA_WAIT_MMA()                              \
@@ -310,8 +319,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
       const int lv = nseg - 1 - seg;  // level: segments counted from the end
       const int c0 = seg * kCPS, c1 = min(nchunks, c0 + kCPS);
       const bool rebuild = !split || helper;
-      uint8_t* segbuf = split ? a.scratch + (static_cast<size_t>(item) * 2 + (lv & 1)) * kCPS * kStateBytes
-                              : a.scratch + static_cast<size_t>(blockIdx.x) * kCPS * kStateBytes;
+      uint8_t* segbuf = split ? a.scratch + (static_cast<size_t>(item) * 2 + (lv & 1)) * kCPS * kSlotBytes
+                              : a.scratch + static_cast<size_t>(blockIdx.x) * kCPS * kSlotBytes;
       if (split) {  // hand-off: the helper waits until level lv-2's buffer is consumed,
                     // the reverse CTA until level lv has been rebuilt
         if (tid == 0) {
@@ -350,20 +359,28 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
 #pragma unroll 1
       for (int pass = rebuild ? 0 : 1; pass < (helper ? 1 : 2); ++pass) {
         const bool rev = pass == 1;
-        const int nsteps = rev ? c1 - c0 : c1 - c0 - 1;
+        // a helper also walks the segment's last chunk (its Abar, T, T', M only)
+        const int nsteps = (rev || helper) ? c1 - c0 : c1 - c0 - 1;
+        const bool prep = !(rev && split);  // this CTA builds Abar / M / T itself
+        const bool need_m = rev || helper;   // M is needed (reverse pass, or for it)
         if (rev && !rebuild) {  // split mode: the last chunk's start state comes from scratch too
           if (tid == 0) {
             mbar_expect_tx(bar_a1, kStateBytes);
-            bulk_load(sb + OFF_A1, segbuf + static_cast<size_t>(c1 - 1 - c0) * kStateBytes, kStateBytes, bar_a1);
+            bulk_load(sb + OFF_A1, segbuf + static_cast<size_t>(c1 - 1 - c0) * kSlotBytes, kStateBytes, bar_a1);
+            uint8_t* slot = segbuf + static_cast<size_t>(c1 - 1 - c0) * kSlotBytes;
+            mbar_expect_tx(bar_sm, kPrepSBytes + kPrepMBytes);
+            bulk_load(sb + OFF_SMALL, slot + kStateBytes, kPrepSBytes, bar_sm);
+            bulk_load(sb + OFF_FM, slot + kStateBytes + kPrepSBytes, kPrepMBytes, bar_sm);
           }
           a1_pending = true;
+          sm_pending = true;
         }
         float braw_next = 0.f;
         if (nsteps > 0) {  // first chunk of the pass: issue its loads now
           const int c = rev ? c1 - 1 : c0;
           const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
           const int rows = static_cast<int>(min(static_cast<int64_t>(kC), eos - t0));
-          stage_tiles(a, sb + OFF_STG, h, t0, rows, tid, true, rev, sb + OFF_SDO, rev);
+          stage_tiles(a, sb + OFF_STG, h, t0, rows, tid, true, rev, sb + OFF_SDO, need_m);
           cp_async_commit();
           if (tid < kC && tid < rows) braw_next = __bfloat162float(a.b[(t0 + tid) * a.H + h]);
         }
@@ -384,11 +401,11 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             const int cn = rev ? c - 1 : c + 1;
             const int64_t tn = bos + static_cast<int64_t>(cn) * kC;
             const int rn = static_cast<int>(min(static_cast<int64_t>(kC), eos - tn));
-            stage_tiles(a, sb + OFF_STG + (buf ^ 1) * kStgBuf, h, tn, rn, tid, true, false, 0, rev);
+            stage_tiles(a, sb + OFF_STG + (buf ^ 1) * kStgBuf, h, tn, rn, tid, true, false, 0, need_m);
             if (tid < kC && tid < rn) braw_next = __bfloat162float(a.b[(tn + tid) * a.H + h]);
           }
           cp_async_commit();
-          if (!rev && tid == 0) bulk_store(segbuf + static_cast<size_t>(c - c0) * kStateBytes, sb + OFF_A1, kStateBytes);
+          if (!rev && tid == 0) bulk_store(segbuf + static_cast<size_t>(c - c0) * kSlotBytes, sb + OFF_A1, kStateBytes);
           cp_async_wait_prev();
           __syncthreads();
 
@@ -401,7 +418,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               const float y0 = stg(SK, 2 * warp, lane + 32 * e), y1 = stg(SK, 2 * warp + 1, lane + 32 * e);
               sk0 += y0 * y0;
               sk1 += y1 * y1;
-              if (rev) {  // the rebuild does not use q
+              if (need_m) {  // the rebuild alone does not use q
                 const float x0 = stg(SQ, 2 * warp, lane + 32 * e), x1 = stg(SQ, 2 * warp + 1, lane + 32 * e);
                 sq0 += x0 * x0;
                 sq1 += x1 * x1;
@@ -460,22 +477,29 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               KG[r * kLd + ci] = kh * e;
               KI[r * kLd + ci] = kh * ex2(-G);
               st_h(sm + OFF_FKB, sw128_off(r, ci, 16), kh * ex2(gend - G));
-              if (rev) {
+              if (need_m) {
                 const float qg = stg(SQ, r, ci) * S[S_IQ0 + r] * a.scale * e;
                 QG[r * kLd + ci] = qg;
-                st_h(sm + OFF_FQG, sw128_off(r, ci, 16), qg);
-                // bf16 -> fp16 is exact for these magnitudes
-                st_h(sm + OFF_FDO, sw128_off(r, ci, 16), stg(SDO, r, ci));
+                if (rev) {
+                  st_h(sm + OFF_FQG, sw128_off(r, ci, 16), qg);
+                  // bf16 -> fp16 is exact for these magnitudes
+                  st_h(sm + OFF_FDO, sw128_off(r, ci, 16), stg(SDO, r, ci));
+                }
               }
             }
           }
           __syncthreads();
+          if (!prep) {  // split mode: this chunk's Abar, T, T', M come from the helper
+            if (!mbar_wait(bar_sm, ph_sm, a.status)) *s_fail = 1;
+            ph_sm ^= 1u;
+            sm_pending = false;
+          }
           if (rev) {  // next chunk's dO (the dO staging tile has been consumed)
             if (more) stage_tiles(a, 0, h, t0 - kC, kC, tid, false, true, sb + OFF_SDO);
             cp_async_commit();
           }
           // ================= Abar (and M) on tf32 tensor tiles =================
-          if (warp < (rev ? 4 : 2)) {
+          if (prep && warp < (need_m ? 4 : 2)) {
             const int nt = warp & 1;
             const bool is_m = (warp >> 1) != 0;
             const float* X = is_m ? QG : KG;
@@ -521,7 +545,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                   idesc(128, 16), 1);
             mma_commit(bar_du);
           }
-          if (warp == 0) {  // T = (I + diag(beta) Abar)^-1 by forward substitution, lane j: column j
+          if (prep && warp == 0) {  // T = (I + diag(beta) Abar)^-1 by forward substitution, lane j: column j
             const int j = lane & 15;
             float x[16];
 #pragma unroll
@@ -541,7 +565,16 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               }
             }
           }
+          fence_async_smem();
           __syncthreads();
+          if (helper) {  // hand this chunk's Abar, T, T' and M hi / lo to the reverse CTA
+            if (tid == 0) {
+              uint8_t* slot = segbuf + static_cast<size_t>(c - c0) * kSlotBytes;
+              bulk_store(slot + kStateBytes, sb + OFF_SMALL, kPrepSBytes);
+              bulk_store(slot + kStateBytes + kPrepSBytes, sb + OFF_FM, kPrepMBytes);
+            }
+            if (c == c1 - 1) continue;  // the segment's last chunk advances no state
+          }
           {  // W = T' (Kh Gamma) -> -W fp16;  U = T' V -> fp32  (channels 16w .. 16w+15)
             float dw[2][4] = {}, du[2][4] = {};
 #pragma unroll
@@ -795,7 +828,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           if (more) {
             if (tid == 0) {
               mbar_expect_tx(bar_a1, kStateBytes);
-              bulk_load(sb + OFF_A1, segbuf + static_cast<size_t>(c - 1 - c0) * kStateBytes, kStateBytes, bar_a1);
+              bulk_load(sb + OFF_A1, segbuf + static_cast<size_t>(c - 1 - c0) * kSlotBytes, kStateBytes, bar_a1);
             }
             a1_pending = true;
           }
@@ -933,7 +966,17 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               }
             }
           }
+          fence_async_smem();
           __syncthreads();
+          if (!prep && more) {  // the next chunk's Abar, T, T', M (last read in [D2] and [F])
+            if (tid == 0) {
+              uint8_t* slot = segbuf + static_cast<size_t>(c - 1 - c0) * kSlotBytes;
+              mbar_expect_tx(bar_sm, kPrepSBytes + kPrepMBytes);
+              bulk_load(sb + OFF_SMALL, slot + kStateBytes, kPrepSBytes, bar_sm);
+              bulk_load(sb + OFF_FM, slot + kStateBytes + kPrepSBytes, kPrepMBytes, bar_sm);
+            }
+            sm_pending = true;
+          }
           {  // dG of the chunk end, reverse cumulative sum (natural-log units)
             float sum = 0.f;
 #pragma unroll
@@ -998,8 +1041,6 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           KDA_SYNC_OR_BAIL();
         }
         if (!rev && tid == 0) {
-          // the helper also saves the segment's last chunk-start state
-          if (helper) bulk_store(segbuf + static_cast<size_t>(c1 - 1 - c0) * kStateBytes, sb + OFF_A1, kStateBytes);
           bulk_wait_all();  // scratch states written before pass 1 reads them
           if (helper) {
             fence_proxy_global();
@@ -1038,6 +1079,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
 teardown:
   // no async copy may still target this CTA's shared memory when it exits
   if (a1_pending) mbar_wait(bar_a1, ph_a1, a.status);
+  if (sm_pending) mbar_wait(bar_sm, ph_sm, a.status);
   if (tid == 0) bulk_wait_all();
   asm volatile("cp.async.wait_all;" ::: "memory");
   fence_before_sync();
@@ -1059,7 +1101,7 @@ __global__ void kda_param_reduce_tc_kernel(const float* partial, int N, int H, i
 
 }  // namespace
 
-size_t bwd_scratch_bytes_per_cta_tc() { return static_cast<size_t>(kCPS) * kStateBytes; }
+size_t bwd_scratch_bytes_per_cta_tc() { return static_cast<size_t>(kCPS) * kSlotBytes; }
 
 kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas) {
   if (p->head_dim != kD || p->dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
