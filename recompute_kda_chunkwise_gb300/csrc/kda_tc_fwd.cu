@@ -374,14 +374,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- operand tiles, row-major: thread = one row (k or q) x 64 channels ----
     float rowf[64];  // kh e^{G_r - B_{I+1}} (k rows) or qh e^{G_r - B_{I+1}} (q rows)
     {
+      // k rows build Kh*Gamma and Kbar, q rows build Qh*Gamma and the tf32 column
+      // operand of the same token's k row (two exponentials each, balanced)
       const int r = prow;
       const float nrm = krole ? s_ik[r] : s_iq[r];
+      const float nrmk = s_ik[r];
       const uint32_t src = krole ? OFF_STG_K : OFF_STG_Q;
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
         const int ch0 = 64 * hh + 8 * cc;
         const uint4 raw = *reinterpret_cast<const uint4*>(sm + src + sw128_chunk(r, 8 * hh + cc, 64));
         const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint4 rawk = raw;
+        if (!krole) rawk = *reinterpret_cast<const uint4*>(sm + OFF_STG_K + sw128_chunk(r, 8 * hh + cc, 64));
+        const uint32_t rk[4] = {rawk.x, rawk.y, rawk.z, rawk.w};
         const float4 x0 = *reinterpret_cast<const float4*>(sm + OFF_XS + xs_off(r, ch0));
         const float4 x1 = *reinterpret_cast<const float4*>(sm + OFF_XS + xs_off(r, ch0 + 4));
         const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -393,28 +399,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ca = ch0 + 2 * e, cb = ca + 1;
           const float ha = vv.x * nrm, hb = vv.y * nrm;
           const float sa = ex2(xv[2 * e]), sbv = ex2(xv[2 * e + 1]);  // e^{G_r - B_{I+1}} >= 1
+          const float ia = ex2(-xv[2 * e]), ib = ex2(-xv[2 * e + 1]);  // e^{B_{I+1} - G_r} <= 1
           rowf[8 * cc + 2 * e] = ha * sa;
           rowf[8 * cc + 2 * e + 1] = hb * sbv;
           const float ga = sa * s_eB[pI * 128 + ca], gb = sbv * s_eB[pI * 128 + cb];  // Gamma_r
+          o1[e] = pack_h2(ha * ga, hb * gb);  // Kh*Gamma (k rows) or Qh*Gamma (q rows)
           if (krole) {
-            const float ia = ex2(-xv[2 * e]), ib = ex2(-xv[2 * e + 1]);  // e^{B_{I+1} - G_r} <= 1
-            o1[e] = pack_h2(ha * ga, hb * gb);                                               // Kh*Gamma
             o2[e] = pack_h2(ha * ia * s_eK[pI * 128 + ca], hb * ib * s_eK[pI * 128 + cb]);  // Kbar
-            bk[2 * e] = ha * ia;
-            bk[2 * e + 1] = hb * ib;
           } else {
-            o1[e] = pack_h2(ha * ga, hb * gb);  // Qh*Gamma
+            const float2 kk = unpack_bf16(rk[e]);
+            bk[2 * e] = kk.x * nrmk * ia;  // kh_r e^{B_{I+1} - G_r}
+            bk[2 * e + 1] = kk.y * nrmk * ib;
           }
         }
         if (krole) {
           *reinterpret_cast<uint4*>(sm + OFF_XW + sw128_chunk(r, 8 * hh + cc, 64)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
           *reinterpret_cast<uint4*>(sm + OFF_B2A + sw128_chunk(r, 8 * hh + cc, 64)) =
               make_uint4(o2[0], o2[1], o2[2], o2[3]);
-          *reinterpret_cast<float4*>(sm + OFF_BK + sw128_off32(r, ch0, 64)) = make_float4(bk[0], bk[1], bk[2], bk[3]);
-          *reinterpret_cast<float4*>(sm + OFF_BK + sw128_off32(r, ch0 + 4, 64)) = make_float4(bk[4], bk[5], bk[6], bk[7]);
         } else {
           *reinterpret_cast<uint4*>(sm + OFF_B1 + sw128_chunk(64 + r, 8 * hh + cc, 128)) =
               make_uint4(o1[0], o1[1], o1[2], o1[3]);
+          *reinterpret_cast<float4*>(sm + OFF_BK + sw128_off32(r, ch0, 64)) = make_float4(bk[0], bk[1], bk[2], bk[3]);
+          *reinterpret_cast<float4*>(sm + OFF_BK + sw128_off32(r, ch0 + 4, 64)) = make_float4(bk[4], bk[5], bk[6], bk[7]);
         }
       }
     }
