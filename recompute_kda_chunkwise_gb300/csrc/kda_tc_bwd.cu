@@ -457,9 +457,10 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           {  // full cumsum, gated operands
             const float carry = rh ? S[S_TOT + ci] : 0.f;
             const float gend = S[S_TOT + ci] + S[S_TOT + 128 + ci];
+            const float gam = ex2(gend);
             if (rh == 0) {
               S[S_GEND + ci] = gend;
-              S[S_GAM + ci] = ex2(gend);
+              S[S_GAM + ci] = gam;
             }
             float Gv[8], kv[8];
 #pragma unroll
@@ -475,8 +476,9 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               const float e = ex2(G);
               GS[r * kLd + ci] = G;
               KG[r * kLd + ci] = kh * e;
-              KI[r * kLd + ci] = kh * ex2(-G);
-              st_h(sm + OFF_FKB, sw128_off(r, ci, 16), kh * ex2(gend - G));
+              const float ki = kh * ex2(-G);
+              KI[r * kLd + ci] = ki;
+              st_h(sm + OFF_FKB, sw128_off(r, ci, 16), ki * gam);  // Kbar = kh e^{G_end - G}
               if (need_m) {
                 const float qg = stg(SQ, r, ci) * S[S_IQ0 + r] * a.scale * e;
                 QG[r * kLd + ci] = qg;
