@@ -74,6 +74,13 @@ typedef enum {
  * kernels even where tensor-core kernels exist (bf16, head_dim 128): slower,
  * fp32 accuracy throughout. */
 #define KDA_FLAG_FORCE_SIMT 1
+/* Test only: exercises the device-side failure path without faulting the GPU.
+ * The tensor-core forward skips the first q/k/gate tile load, so its bounded
+ * wait for that load runs out (after a short spin); the kernel records
+ * KDA_ERR_TIMEOUT in ctx's status word, frees its tensor memory and returns.
+ * o is not written. kda_query_device_status(ctx) then reports the timeout and
+ * the context stays usable. Ignored by the CUDA-core kernels. */
+#define KDA_FLAG_TEST_TIMEOUT 2
 
 /* Problem description. cu_seqlens is a DEVICE pointer; the library never
  * reads it on the host (so no synchronisation), and trusts that it is

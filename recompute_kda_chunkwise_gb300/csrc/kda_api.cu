@@ -34,7 +34,8 @@ kda_status validate(const kda_problem* p, bool need_ptrs = true) {
   if (p->num_seqs < 1) return fail(KDA_ERR_INVALID_ARG, "num_seqs must be >= 1 (got %d)", p->num_seqs);
   if (p->num_heads < 1) return fail(KDA_ERR_INVALID_ARG, "num_heads must be >= 1 (got %d)", p->num_heads);
   if (p->total_tokens < 0) return fail(KDA_ERR_INVALID_ARG, "total_tokens must be >= 0");
-  if ((p->flags & ~KDA_FLAG_FORCE_SIMT) != 0) return fail(KDA_ERR_INVALID_ARG, "unknown flags 0x%x", p->flags);
+  if ((p->flags & ~(KDA_FLAG_FORCE_SIMT | KDA_FLAG_TEST_TIMEOUT)) != 0)
+    return fail(KDA_ERR_INVALID_ARG, "unknown flags 0x%x", p->flags);
   if (need_ptrs && !p->cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is NULL");
   if (p->dtype != KDA_DTYPE_BF16 && p->dtype != KDA_DTYPE_F32)
     return fail(KDA_ERR_UNSUPPORTED, "dtype %d is not supported", p->dtype);
@@ -159,6 +160,7 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
   a.status = ctx ? (int*)ctx : nullptr;
   a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
+  a.test_timeout = (p->flags & KDA_FLAG_TEST_TIMEOUT) ? 1 : 0;
   if (ctx && cudaMemsetAsync(ctx, 0, sizeof(int), s) != cudaSuccess)
     return fail(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
   st = family_of(p) == 1 ? kda::launch_fwd_tc(p, a, s) : kda::launch_fwd_simt(p, a, s);

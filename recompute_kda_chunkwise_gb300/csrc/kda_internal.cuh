@@ -32,6 +32,7 @@ struct FwdArgs {
   const int32_t* cu;
   int N, H;
   float scale, lower, eps;
+  int test_timeout;  // KDA_FLAG_TEST_TIMEOUT (tensor-core forward only)
 };
 
 struct BwdArgs {

@@ -161,10 +161,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 // Bounded wait for the phase with the given parity to complete. Returns
-// false (and records KDA_ERR_TIMEOUT) if it did not complete in time.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+// false (and records KDA_ERR_TIMEOUT) if it did not complete within `limit`
+// polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int limit = 1 << 24) {
   const uint32_t a = smem_addr(bar);
-  for (int it = 0; it < (1 << 24); ++it) {
+  for (int it = 0; it < limit; ++it) {
     uint32_t ok;
     asm volatile(
         "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"

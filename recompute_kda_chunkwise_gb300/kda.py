@@ -84,6 +84,7 @@ def _check(status: int, where: str):
 
 
 KDA_FLAG_FORCE_SIMT = 1
+KDA_FLAG_TEST_TIMEOUT = 2  # test only: the forward's bounded wait runs out (see include/kda.h)
 
 
 def make_problem(total_tokens: int, num_seqs: int, num_heads: int, head_dim: int, dtype,

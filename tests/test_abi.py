@@ -73,6 +73,12 @@ def test_invalid_arguments_are_rejected_on_host(lib):
     p.num_seqs = 1
     p.dtype = 7
     assert lib.kda_fwd(ctypes.byref(p), *([al] * 8), nul, nul) == 2
+    p.dtype = 0
+    p.flags = 4  # no such flag
+    assert lib.kda_fwd(ctypes.byref(p), *([al] * 8), nul, nul) == 1
+    assert b"unknown flags" in lib.kda_last_error_message()
+    p.flags = K.KDA_FLAG_FORCE_SIMT | K.KDA_FLAG_TEST_TIMEOUT  # both known: sizes still answer
+    assert lib.kda_ctx_bytes(ctypes.byref(p)) > 0
 
 
 def test_status_strings(lib):
