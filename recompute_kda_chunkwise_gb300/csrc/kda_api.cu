@@ -62,10 +62,21 @@ size_t ckpt_slots(const kda_problem* p) {
   return (size_t)(p->total_tokens / kda::kCkptTokens) + (size_t)p->num_seqs;
 }
 
-size_t ctx_bytes(const kda_problem* p) {
+size_t ckpt_bytes(const kda_problem* p) {
   const size_t D = (size_t)p->head_dim;
-  return kda::kHeaderBytes + ckpt_slots(p) * (size_t)p->num_heads * D * D * sizeof(float);
+  return ckpt_slots(p) * (size_t)p->num_heads * D * D * sizeof(float);
 }
+
+// Tensor-core forward with fewer (sequence, head) items than the 152-CTA
+// grid: the spare SMs prepare every other chunk; the hand-off area follows
+// the checkpoints in ctx.
+size_t fwd_handoff(const kda_problem* p) {
+  const int64_t items = (int64_t)p->num_seqs * p->num_heads;
+  if (family_of(p) != 1 || items <= 0 || items >= kda::kTcBwdCtas) return 0;
+  return kda::fwd_handoff_bytes((int)items);
+}
+
+size_t ctx_bytes(const kda_problem* p) { return kda::kHeaderBytes + ckpt_bytes(p) + fwd_handoff(p); }
 
 size_t partial_bytes(const kda_problem* p) {
   return round_up((size_t)p->num_seqs * p->num_heads * (p->head_dim + 1) * sizeof(float), 256);
@@ -161,6 +172,12 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
   a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   a.test_timeout = (p->flags & KDA_FLAG_TEST_TIMEOUT) ? 1 : 0;
+  a.xflags = nullptr;
+  a.xbuf = nullptr;
+  if (ctx && fwd_handoff(p)) {
+    a.xflags = (uint32_t*)((char*)ctx + kda::kHeaderBytes + ckpt_bytes(p));
+    a.xbuf = (uint8_t*)a.xflags + round_up((size_t)p->num_seqs * p->num_heads * 5 * sizeof(uint32_t), 256);
+  }
   if (ctx && cudaMemsetAsync(ctx, 0, sizeof(int), s) != cudaSuccess)
     return fail(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
   st = family_of(p) == 1 ? kda::launch_fwd_tc(p, a, s) : kda::launch_fwd_simt(p, a, s);

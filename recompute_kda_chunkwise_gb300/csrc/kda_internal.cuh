@@ -33,6 +33,10 @@ struct FwdArgs {
   int N, H;
   float scale, lower, eps;
   int test_timeout;  // KDA_FLAG_TEST_TIMEOUT (tensor-core forward only)
+  // tensor-core forward, split mode: per-item hand-off counters and slots in
+  // ctx (NULL: no helper CTAs)
+  uint32_t* xflags;
+  uint8_t* xbuf;
 };
 
 struct BwdArgs {
@@ -95,6 +99,9 @@ size_t bwd_scratch_bytes_simt(const kda_problem* p, int* nctas);
 kda_status launch_bwd_simt_ctas(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas);
 size_t bwd_scratch_bytes_per_cta_simt(const kda_problem* p);
 size_t bwd_scratch_bytes_per_cta_tc();
+// Bytes of the tensor-core forward's hand-off area (counters + slots) for
+// `items` (sequence, head) items.
+size_t fwd_handoff_bytes(int items);
 kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas);
 // CTAs of the tensor-core backward: one per SM of a 152-SM part (persistent).
 constexpr int kTcBwdCtas = 152;

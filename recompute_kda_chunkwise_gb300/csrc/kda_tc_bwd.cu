@@ -106,24 +106,6 @@ struct TcBwdArgs {
   float scale, lower, eps;
 };
 
-// ---- cross-CTA hand-off of rebuilt segment states (co-resident CTAs of one
-// cooperative launch; every wait bounded) ----
-__device__ __forceinline__ bool wait_flag_geq(const uint32_t* f, uint32_t target, int* status) {
-  for (int it = 0; it < (1 << 24); ++it) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-    if (v >= target) return true;
-    __nanosleep(64);
-  }
-  set_status(status, KDA_ERR_TIMEOUT);
-  return false;
-}
-__device__ __forceinline__ void st_release(uint32_t* f, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
-}
-// orders this thread's generic-proxy accesses with its async-proxy accesses of global memory
-__device__ __forceinline__ void fence_proxy_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
 __device__ __forceinline__ float sigm(float x) { return __fdividef(1.f, 1.f + ex2(-x * kLog2e)); }
 __device__ __forceinline__ void st_h(uint8_t* base, uint32_t off, float x) {
   *reinterpret_cast<__half*>(base + off) = __float2half_rn(x);

@@ -304,6 +304,24 @@ __device__ __forceinline__ void ldBr(float (&b)[2], const float* Z, int ld, int 
   b[1] = Z[(k0 + t + 4) * ld + n0 + g];
 }
 
+// ---- cross-CTA hand-off between co-resident CTAs of one cooperative launch
+// (every wait bounded) ----
+__device__ __forceinline__ bool wait_flag_geq(const uint32_t* f, uint32_t target, int* status) {
+  for (int it = 0; it < (1 << 24); ++it) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v >= target) return true;
+    __nanosleep(64);
+  }
+  set_status(status, KDA_ERR_TIMEOUT);
+  return false;
+}
+__device__ __forceinline__ void st_release(uint32_t* f, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+// orders this thread's generic-proxy accesses with its async-proxy accesses of global memory
+__device__ __forceinline__ void fence_proxy_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 p = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);

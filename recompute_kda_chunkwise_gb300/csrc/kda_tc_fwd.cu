@@ -71,13 +71,26 @@ constexpr int OFF_X = OFF_R + 58368;   //        fp32 scratch [6][16][9]
 constexpr int OFF_TPL = OFF_R + 16384; //   after the inverse (Abar dead): T' low part fp16 [64 r][64 s]
 constexpr int OFF_ML = OFF_R + 24576;  //                                  M low part fp16 [64 r][64 s]
 constexpr int OFF_UL = OFF_R;          //   after the U product (v dead): U~^T low part fp16 [128 v][64 r]
+constexpr int OFF_XU = OFF_R + 32768;  //   split mode: U^T fp32 [128 v][64 r] of a handed-over chunk (BK dead)
 constexpr int OFF_SMALL = OFF_R + 65536;
 // small fp32 arrays
 constexpr int SM_BETA = 0, SM_IQ = 64, SM_IK = 128, SM_GAM = 192, SM_EB = 320, SM_EK = 832, SM_U = 1344;
-constexpr int SMALL_FLOATS = 1344 + 6 * 128;
+constexpr int SM_GAM2 = 1344 + 6 * 128;  // gamma of a handed-over chunk (split mode)
+constexpr int SMALL_FLOATS = SM_GAM2 + 128;
 constexpr int OFF_BAR = OFF_SMALL + SMALL_FLOATS * 4;
 constexpr int SMEM_USED = OFF_BAR + 64;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
+
+// Split-mode hand-off slot (bytes, all 16-byte multiples): the prepared
+// operand tiles of one odd chunk as the main CTA's shared memory holds them.
+constexpr uint32_t kXB1 = 0;                      // [-W ; Qh*Gamma] fp16, 32 KB (OFF_B1)
+constexpr uint32_t kXB2A = kXB1 + 32768;          // Kbar fp16, 16 KB (OFF_B2A)
+constexpr uint32_t kXB2B = kXB2A + 16384;         // M hi fp16, 8 KB (OFF_B2B)
+constexpr uint32_t kXML = kXB2B + 8192;           // M lo fp16, 8 KB (OFF_ML)
+constexpr uint32_t kXU = kXML + 8192;             // U^T fp32 [128 v][64 r], 32 KB (into TMEM)
+constexpr uint32_t kXGAM = kXU + 32768;           // gamma [128] fp32
+constexpr uint32_t kXSlotBytes = kXGAM + 512;
+constexpr int kXSlots = 4;                        // ring depth per item
 
 // TMEM columns
 constexpr uint32_t TM_DA = 0;    // Abar (lanes 0-63) | M (lanes 64-127), 64 columns
@@ -101,6 +114,11 @@ struct TcFwdArgs {
   int N, H;
   float scale, lower, eps;
   int test_timeout;
+  // split mode (helpers > 0): CTAs N*H .. N*H+helpers-1 prepare the odd
+  // chunks of every item and hand them over through xbuf / xflags
+  int helpers;
+  uint32_t* xflags;  // per item: [4] last odd-chunk index + 1 written into slot q, [4] consumed count
+  uint8_t* xbuf;     // per item: kXSlots slots of kXSlotBytes
 };
 
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + ex2(-x * kLog2e)); }
@@ -214,11 +232,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_fail = reinterpret_cast<int*>(bar_qkg + 4);
   uint64_t* bar_odd = bar_qkg + 5;  // completion of Abar | M round 1
   uint64_t* bar_r2 = bar_qkg + 6;   // completion of Abar | M round 2
+  uint64_t* bar_x = bar_qkg + 7;    // split mode: a handed-over odd chunk has landed
+  float* s_gam2 = smf + SM_GAM2;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
-  const int64_t bos = a.cu[n], eos = a.cu[n + 1];
-  const int nchunks = static_cast<int>((eos - bos + kC - 1) / kC);
+  // Roles. Without helpers, CTA b walks every chunk of item b. In split mode
+  // the main CTA b < items prepares its even chunks itself and takes the odd
+  // ones prepared by the helper CTAs, which walk jobs t * items + item (odd
+  // chunk 2t + 1 of item) in order, helper j taking jobs j, j + helpers, ...
+  const int items = a.N * a.H;
+  const bool split = a.helpers > 0;
+  const bool helper = split && static_cast<int>(blockIdx.x) >= items;
+  int item = helper ? 0 : static_cast<int>(blockIdx.x);
+  int n = item / a.H, h = item % a.H;
+  int64_t bos = a.cu[n], eos = a.cu[n + 1];
+  int nchunks = helper ? 0 : static_cast<int>((eos - bos + kC - 1) / kC);
+  int job = static_cast<int>(blockIdx.x) - items, max_jobs = 0;
+  if (helper) {
+    int max_odd = 0;
+    for (int s2 = 0; s2 < a.N; ++s2)
+      max_odd = max(max_odd, static_cast<int>((a.cu[s2 + 1] - a.cu[s2] + kC - 1) / kC) / 2);
+    max_jobs = max_odd * items;
+  }
 
   if (tid == 0) {
     mbar_init(bar_qkg, 1);
@@ -226,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_mma, 1);
     mbar_init(bar_odd, 1);
     mbar_init(bar_r2, 1);
+    mbar_init(bar_x, 1);
     *s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -239,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // channel-major role: channel pair (c0, c0+1), rows 16*Ib .. 16*Ib+15 (sub-block Ib)
   const int pp = tid & 63, Ib = tid >> 6, c0 = 2 * pp;
-  const float expA = expf(a.A_log[h]);
-  const float dtb0 = a.dt_bias[h * kD + c0], dtb1 = a.dt_bias[h * kD + c0 + 1];
+  float expA = expf(a.A_log[h]);
+  float dtb0 = a.dt_bias[h * kD + c0], dtb1 = a.dt_bias[h * kD + c0 + 1];
   const float Lg = a.lower * kLog2e;
   // lane roles: TMEM lane quarter q4, column half hh
   const int q4 = warp & 3, hh = warp >> 2, lrow = 32 * q4 + lane;
@@ -251,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float Hst[64];
 #pragma unroll
   for (int j = 0; j < 64; ++j) Hst[j] = 0.f;
-  uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0, ph_odd = 0, ph_r2 = 0;
+  uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0, ph_odd = 0, ph_r2 = 0, ph_x = 0;
+  bool x_pending = false;  // a hand-over load into shared memory is in flight
 
   auto issue_qkg = [&](int t) {
     mbar_expect_tx(bar_qkg, 6 * 8192);
@@ -282,16 +319,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int wait_limit = a.test_timeout ? (1 << 12) : (1 << 24);
   if (tid == 0 && nchunks > 0 && !a.test_timeout) issue_qkg(static_cast<int>(bos));
 
-  for (int c = 0; c < nchunks; ++c) {
+  int c = -1;
+  while (true) {
+    if (!helper) {
+      if (++c >= nchunks) break;
+    } else {  // the next job with an odd chunk
+      bool found = false;
+      while (job < max_jobs) {
+        const int tt = job / items;
+        item = job % items;
+        job += a.helpers;
+        n = item / a.H;
+        h = item % a.H;
+        bos = a.cu[n];
+        eos = a.cu[n + 1];
+        nchunks = static_cast<int>((eos - bos + kC - 1) / kC);
+        if (2 * tt + 1 < nchunks) {
+          c = 2 * tt + 1;
+          found = true;
+          break;
+        }
+      }
+      if (!found) break;
+      expA = expf(a.A_log[h]);
+      dtb0 = a.dt_bias[h * kD + c0];
+      dtb1 = a.dt_bias[h * kD + c0 + 1];
+      if (tid == 0) {  // the slot is free once the main CTA consumed odd chunk t - kXSlots
+        const int tt = c >> 1;
+        if (tt >= kXSlots && !wait_flag_geq(a.xflags + 5 * item + 4, static_cast<uint32_t>(tt - kXSlots + 1), a.status))
+          *s_fail = 1;
+        fence_proxy_global();
+        issue_qkg(static_cast<int>(bos + static_cast<int64_t>(c) * kC));
+      }
+    }
+    const bool handed = split && !helper && (c & 1);  // prepared by a helper
     const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
     const int rows = static_cast<int>(min(static_cast<int64_t>(kC), eos - t0));
 
-    if (a.ckpt != nullptr && (c % (kCkptTokens / kC)) == 0) {
+    if (!helper && a.ckpt != nullptr && (c % (kCkptTokens / kC)) == 0) {
       float* dst = a.ckpt + (ckpt_slot(bos, n, c / (kCkptTokens / kC)) * a.H + h) * static_cast<int64_t>(kD * kD);
 #pragma unroll
       for (int j = 0; j < 64; ++j) dst[(64 * hh + j) * kD + lrow] = Hst[j];
     }
 
+    if (!handed) {
     if (tid < kC) {
       const int r = tid;
       s_beta[r] = r < rows ? sigmoidf_(__bfloat162float(a.b[(t0 + r) * a.H + h])) : 0.f;
@@ -433,7 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk (into the offsets' space) and q, k, g of the next chunk
     if (tid == 0) {
       issue_v(static_cast<int>(t0));
-      if (c + 1 < nchunks) issue_qkg(static_cast<int>(t0 + kC));
+      // the next chunk this CTA prepares itself (a helper fetches per job)
+      const int cn = split ? c + 2 : c + 1;
+      if (!helper && cn < nchunks) issue_qkg(static_cast<int>(bos + static_cast<int64_t>(cn) * kC));
     }
 
     // ---- Abar | M by column block J: tf32, row operand in TMEM. Rounds 0-2
@@ -571,6 +644,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_async_smem();
     fence_before_sync();
     KDA_SYNC_OR_BAIL();
+    }  // prepared here
+    if (helper) {
+      // ---- hand the prepared odd chunk over: U^T (TMEM) to fp32 staging, then
+      // the operand tiles and gamma to the item's slot, then publish it ----
+      {
+        float v[32];
+        tmem_ld32(tmem + tlane + TM_DU + 32 * hh, v);  // lane = v, columns r
+        float4* dst = reinterpret_cast<float4*>(sm + OFF_XU + lrow * 256 + 128 * hh);
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) dst[j4] = make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+      }
+      fence_async_smem();
+      KDA_SYNC_OR_BAIL();
+      if (tid == 0) {
+        const int tt = c >> 1;
+        uint8_t* slot = a.xbuf + (static_cast<size_t>(item) * kXSlots + tt % kXSlots) * kXSlotBytes;
+        bulk_store(slot + kXB1, sb + OFF_B1, 32768);
+        bulk_store(slot + kXB2A, sb + OFF_B2A, 16384);
+        bulk_store(slot + kXB2B, sb + OFF_B2B, 8192);
+        bulk_store(slot + kXML, sb + OFF_ML, 8192);
+        bulk_store(slot + kXU, sb + OFF_XU, 32768);
+        bulk_store(slot + kXGAM, smem_addr(s_gam), 512);
+        bulk_wait_all();
+        fence_proxy_global();
+        st_release(a.xflags + 5 * item + tt % kXSlots, static_cast<uint32_t>(tt + 1));
+      }
+      __syncthreads();  // the shared tiles are read out before the next job rewrites them
+      continue;
+    }
+    if (handed) {
+      // ---- a helper prepared this chunk: its tiles landed during the previous
+      // chunk; U^T goes into TMEM, where the U~ product accumulates onto it ----
+      if (!mbar_wait(bar_x, ph_x, a.status, wait_limit)) *s_fail = 1;
+      ph_x ^= 1u;
+      x_pending = false;
+      {
+        float v[32];
+        const float4* src = reinterpret_cast<const float4*>(sm + OFF_XU + lrow * 256 + 128 * hh);
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 x = src[j4];
+          v[4 * j4] = x.x;
+          v[4 * j4 + 1] = x.y;
+          v[4 * j4 + 2] = x.z;
+          v[4 * j4 + 3] = x.w;
+        }
+        tmem_st32(tmem + tlane + TM_DU + 32 * hh, v);
+      }
+      tmem_st_wait();
+      if (tid == 0) st_release(a.xflags + 5 * item + 4, static_cast<uint32_t>((c >> 1) + 1));  // slot consumed
+      fence_before_sync();
+      KDA_SYNC_OR_BAIL();
+    }
     if (tid == 0) {
       fence_after_sync();
 #pragma unroll
@@ -622,6 +748,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     KDA_WAIT(bar_mma, ph_mma);
     fence_after_sync();
+    if (split && !(c & 1) && c + 1 < nchunks) {
+      // fetch the helper-prepared next (odd) chunk into the tiles this chunk
+      // has finished with (its last product above has completed)
+      if (tid == 0) {
+        const int tt = (c + 1) >> 1;
+        if (!wait_flag_geq(a.xflags + 5 * item + tt % kXSlots, static_cast<uint32_t>(tt + 1), a.status)) *s_fail = 1;
+        fence_proxy_global();
+        const uint8_t* slot = a.xbuf + (static_cast<size_t>(item) * kXSlots + tt % kXSlots) * kXSlotBytes;
+        mbar_expect_tx(bar_x, kXSlotBytes);
+        bulk_load(sb + OFF_B1, slot + kXB1, 32768, bar_x);
+        bulk_load(sb + OFF_B2A, slot + kXB2A, 16384, bar_x);
+        bulk_load(sb + OFF_B2B, slot + kXB2B, 8192, bar_x);
+        bulk_load(sb + OFF_ML, slot + kXML, 8192, bar_x);
+        bulk_load(sb + OFF_XU, slot + kXU, 32768, bar_x);
+        bulk_load(smem_addr(s_gam2), slot + kXGAM, 512, bar_x);
+      }
+      x_pending = true;
+    }
 
     // ---- state update (fp32 registers), next H^T operand, output ----
     {
@@ -629,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         tmem_ld32(tmem + tlane + TM_DH + 64 * hh + 32 * half, v);
-        const float4* g4 = reinterpret_cast<const float4*>(s_gam + 64 * hh + 32 * half);
+        const float4* g4 = reinterpret_cast<const float4*>((handed ? s_gam2 : s_gam) + 64 * hh + 32 * half);
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
           const float4 gm = g4[j4];
@@ -659,6 +803,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #undef KDA_WAIT
 #undef KDA_SYNC_OR_BAIL
 teardown:
+  // no async copy may still target this CTA's shared memory when it exits
+  if (x_pending) mbar_wait(bar_x, ph_x, a.status, wait_limit);
+  if (tid == 0) bulk_wait_all();
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, TM_COLS);
@@ -695,6 +842,11 @@ bool make_tma_map_bf16(CUtensorMap* m, const void* base, int64_t S, int H) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+size_t fwd_handoff_bytes(int items) {
+  const size_t flags = (static_cast<size_t>(items) * 5 * sizeof(uint32_t) + 255) / 256 * 256;
+  return flags + static_cast<size_t>(items) * kXSlots * kXSlotBytes;
+}
+
 kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s) {
   if (p->head_dim != kD || p->dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
   CUtensorMap mq, mk, mv, mg;
@@ -717,11 +869,38 @@ kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s)
   t.lower = a.lower;
   t.eps = a.eps;
   t.test_timeout = a.test_timeout;
+  t.helpers = 0;
+  t.xflags = a.xflags;
+  t.xbuf = a.xbuf;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   if (cudaFuncSetAttribute(kda_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
     return KDA_ERR_CUDA;
-  const int grid = p->num_seqs * p->num_heads;
-  if (grid > 0) kda_fwd_tc_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(mq, mk, mv, mg, t);
+  const int items = p->num_seqs * p->num_heads;
+  // Split mode: with at least half as many spare SMs as items, helper CTAs
+  // prepare every other chunk. Their hand-off waits need every CTA resident
+  // at once, which a cooperative launch guarantees (or refuses, and the
+  // plain launch runs instead).
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_fwd_tc_kernel, kThreads, SMEM_BYTES);
+  bool launched = false;
+  if (a.xflags != nullptr && !a.test_timeout && items > 0 && items < sms * per_sm) {
+    const int spare = sms * per_sm - items;
+    if (2 * spare >= items) {
+      t.helpers = spare < items ? spare : items;
+      if (cudaMemsetAsync(a.xflags, 0, sizeof(uint32_t) * 5 * items, s) != cudaSuccess) return KDA_ERR_CUDA;
+      void* kargs[] = {&mq, &mk, &mv, &mg, &t};
+      launched = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kda_fwd_tc_kernel),
+                                             dim3(items + t.helpers), dim3(kThreads), kargs, SMEM_BYTES,
+                                             s) == cudaSuccess;
+      if (!launched) {
+        cudaGetLastError();  // clear the refusal; run without helpers
+        t.helpers = 0;
+      }
+    }
+  }
+  if (!launched && items > 0) kda_fwd_tc_kernel<<<items, kThreads, SMEM_BYTES, s>>>(mq, mk, mv, mg, t);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

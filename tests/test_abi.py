@@ -45,7 +45,15 @@ def test_problem_struct_layout_matches_header():
 def test_size_queries(lib):
     p = K.make_problem(131072, 1, 96, 128, torch.bfloat16)
     ckpts = 131072 // 1024 + 1
-    assert K.ctx_bytes(p) == 256 + ckpts * 96 * 128 * 128 * 4
+    states = 256 + ckpts * 96 * 128 * 128 * 4
+    # tensor-core family with fewer items than the 152-CTA grid: the forward's
+    # hand-off area (5 counters per item, 4 slots of 98816 bytes) follows
+    handoff = (96 * 5 * 4 + 255) // 256 * 256 + 96 * 4 * 98816
+    assert K.ctx_bytes(p) == states + handoff
+    simt = K.make_problem(131072, 1, 96, 128, torch.bfloat16, flags=K.KDA_FLAG_FORCE_SIMT)
+    assert K.ctx_bytes(simt) == states
+    many = K.make_problem(131072, 2, 96, 128, torch.bfloat16)  # 192 items: no helpers
+    assert K.ctx_bytes(many) == 256 + (131072 // 1024 + 2) * 96 * 128 * 128 * 4
     assert K.workspace_bytes(p) > 256 + 96 * 129 * 4
     assert K.kernel_family(p) in (0, 1)
     bad = K.make_problem(16, 1, 2, 96, torch.bfloat16)
