@@ -71,7 +71,6 @@ constexpr int OFF_X = OFF_R + 58368;   //        fp32 scratch [6][16][9]
 constexpr int OFF_TPL = OFF_R + 16384; //   after the inverse (Abar dead): T' low part fp16 [64 r][64 s]
 constexpr int OFF_ML = OFF_R + 24576;  //                                  M low part fp16 [64 r][64 s]
 constexpr int OFF_UL = OFF_R;          //   after the U product (v dead): U~^T low part fp16 [128 v][64 r]
-constexpr int OFF_XU = OFF_R + 32768;  //   split mode: U^T fp32 [128 v][64 r] of a handed-over chunk (BK dead)
 constexpr int OFF_SMALL = OFF_R + 65536;
 // small fp32 arrays
 constexpr int SM_BETA = 0, SM_IQ = 64, SM_IK = 128, SM_GAM = 192, SM_EB = 320, SM_EK = 832, SM_U = 1344;
@@ -82,14 +81,18 @@ constexpr int SMEM_USED = OFF_BAR + 64;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
 
 // Split-mode hand-off slot (bytes, all 16-byte multiples): the prepared
-// operand tiles of one odd chunk as the main CTA's shared memory holds them.
-constexpr uint32_t kXB1 = 0;                      // [-W ; Qh*Gamma] fp16, 32 KB (OFF_B1)
-constexpr uint32_t kXB2A = kXB1 + 32768;          // Kbar fp16, 16 KB (OFF_B2A)
-constexpr uint32_t kXB2B = kXB2A + 16384;         // M hi fp16, 8 KB (OFF_B2B)
-constexpr uint32_t kXML = kXB2B + 8192;           // M lo fp16, 8 KB (OFF_ML)
-constexpr uint32_t kXU = kXML + 8192;             // U^T fp32 [128 v][64 r], 32 KB (into TMEM)
-constexpr uint32_t kXGAM = kXU + 32768;           // gamma [128] fp32
+// operands of one odd chunk as the main CTA's shared memory holds them, in
+// two contiguous runs of that memory plus T' hi and gamma. The main CTA forms
+// U^T = V^T T'^T itself, in the product that also accumulates H^T (-W)^T.
+constexpr uint32_t kXB = 0;                       // OFF_B1..OFF_XW: [-W ; Qh*Gamma] | Kbar | M hi, 56 KB
+constexpr uint32_t kXBBytes = OFF_XW - OFF_B1;
+constexpr uint32_t kXR = kXB + kXBBytes;          // OFF_V..: v fp16 | T' lo | M lo, 32 KB
+constexpr uint32_t kXRBytes = OFF_ML + 8192 - OFF_V;
+constexpr uint32_t kXTP = kXR + kXRBytes;         // T' hi fp16, 8 KB (OFF_TP)
+constexpr uint32_t kXGAM = kXTP + 8192;           // gamma [128] fp32
 constexpr uint32_t kXSlotBytes = kXGAM + 512;
+static_assert(OFF_B2A == OFF_B1 + 32768 && OFF_B2B == OFF_B2A + 16384 && OFF_XW == OFF_B2B + 8192, "slot run B");
+static_assert(OFF_TPL == OFF_V + 16384 && OFF_ML == OFF_TPL + 8192, "slot run R");
 constexpr int kXSlots = 4;                        // ring depth per item
 
 // TMEM columns
@@ -290,19 +293,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0, ph_odd = 0, ph_r2 = 0, ph_x = 0;
   bool x_pending = false;  // a hand-over load into shared memory is in flight
 
-  auto issue_qkg = [&](int t) {
+  auto issue_qkg = [&](int hd, int t) {
     mbar_expect_tx(bar_qkg, 6 * 8192);
-    tma_load_3d(sm + OFF_STG_Q, &tmq, 0, h, t, bar_qkg);
-    tma_load_3d(sm + OFF_STG_Q + 8192, &tmq, 64, h, t, bar_qkg);
-    tma_load_3d(sm + OFF_STG_K, &tmk, 0, h, t, bar_qkg);
-    tma_load_3d(sm + OFF_STG_K + 8192, &tmk, 64, h, t, bar_qkg);
-    tma_load_3d(sm + OFF_STG_G, &tmg, 0, h, t, bar_qkg);
-    tma_load_3d(sm + OFF_STG_G + 8192, &tmg, 64, h, t, bar_qkg);
+    tma_load_3d(sm + OFF_STG_Q, &tmq, 0, hd, t, bar_qkg);
+    tma_load_3d(sm + OFF_STG_Q + 8192, &tmq, 64, hd, t, bar_qkg);
+    tma_load_3d(sm + OFF_STG_K, &tmk, 0, hd, t, bar_qkg);
+    tma_load_3d(sm + OFF_STG_K + 8192, &tmk, 64, hd, t, bar_qkg);
+    tma_load_3d(sm + OFF_STG_G, &tmg, 0, hd, t, bar_qkg);
+    tma_load_3d(sm + OFF_STG_G + 8192, &tmg, 64, hd, t, bar_qkg);
   };
   auto issue_v = [&](int t) {
     mbar_expect_tx(bar_v, 2 * 8192);
     tma_load_3d(sm + OFF_V, &tmv, 0, h, t, bar_v);
     tma_load_3d(sm + OFF_V + 8192, &tmv, 64, h, t, bar_v);
+  };
+  auto issue_u = [&]() {  // U^T = V^T (T'hi + T'lo)^T
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      mma(tmem + TM_DU, desc_mn(D0, OFF_V, 8192, ks & 3), desc_k(D0, (ks < 4 ? OFF_TP : OFF_TPL), 64, 0, ks & 3),
+          idesc(128, 64, true, false), ks > 0);
   };
 #define KDA_WAIT(bar, ph)                                         \
   do {                                                            \
@@ -317,40 +326,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // (KDA_FLAG_TEST_TIMEOUT: the first load is skipped, so its short wait runs out)
   const int wait_limit = a.test_timeout ? (1 << 12) : (1 << 24);
-  if (tid == 0 && nchunks > 0 && !a.test_timeout) issue_qkg(static_cast<int>(bos));
+  // a helper looks one job ahead, so that the next job's loads overlap this one
+  int nx_item = 0, nx_c = -1;
+  auto find_job = [&]() {
+    nx_c = -1;
+    while (job < max_jobs) {
+      const int tt = job / items, it = job % items, s2 = it / a.H;
+      job += a.helpers;
+      if (2 * tt + 1 < static_cast<int>((a.cu[s2 + 1] - a.cu[s2] + kC - 1) / kC)) {
+        nx_item = it;
+        nx_c = 2 * tt + 1;
+        return;
+      }
+    }
+  };
+  auto issue_next_job = [&]() {
+    issue_qkg(nx_item % a.H, static_cast<int>(a.cu[nx_item / a.H] + static_cast<int64_t>(nx_c) * kC));
+  };
+  bool pub_pending = false;  // helper: a hand-off whose stores are in flight, not yet published
+  int pub_item = 0, pub_tt = 0;
+  auto publish = [&]() {  // thread 0 of a helper
+    bulk_wait_all();
+    fence_proxy_global();
+    st_release(a.xflags + 5 * pub_item + pub_tt % kXSlots, static_cast<uint32_t>(pub_tt + 1));
+  };
+  if (helper) {
+    find_job();
+    if (tid == 0 && nx_c >= 0) issue_next_job();
+  } else if (tid == 0 && nchunks > 0 && !a.test_timeout) {
+    issue_qkg(h, static_cast<int>(bos));
+  }
 
   int c = -1;
   while (true) {
     if (!helper) {
       if (++c >= nchunks) break;
-    } else {  // the next job with an odd chunk
-      bool found = false;
-      while (job < max_jobs) {
-        const int tt = job / items;
-        item = job % items;
-        job += a.helpers;
-        n = item / a.H;
-        h = item % a.H;
-        bos = a.cu[n];
-        eos = a.cu[n + 1];
-        nchunks = static_cast<int>((eos - bos + kC - 1) / kC);
-        if (2 * tt + 1 < nchunks) {
-          c = 2 * tt + 1;
-          found = true;
-          break;
-        }
-      }
-      if (!found) break;
+    } else {  // the job found ahead, whose q, k, g are in flight
+      if (nx_c < 0) break;
+      item = nx_item;
+      c = nx_c;
+      n = item / a.H;
+      h = item % a.H;
+      bos = a.cu[n];
+      eos = a.cu[n + 1];
+      nchunks = static_cast<int>((eos - bos + kC - 1) / kC);
       expA = expf(a.A_log[h]);
       dtb0 = a.dt_bias[h * kD + c0];
       dtb1 = a.dt_bias[h * kD + c0 + 1];
-      if (tid == 0) {  // the slot is free once the main CTA consumed odd chunk t - kXSlots
-        const int tt = c >> 1;
-        if (tt >= kXSlots && !wait_flag_geq(a.xflags + 5 * item + 4, static_cast<uint32_t>(tt - kXSlots + 1), a.status))
-          *s_fail = 1;
-        fence_proxy_global();
-        issue_qkg(static_cast<int>(bos + static_cast<int64_t>(c) * kC));
-      }
+      find_job();
     }
     const bool handed = split && !helper && (c & 1);  // prepared by a helper
     const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
@@ -405,6 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           s_iq[r] = (ok && nrm > 0.f) ? a.scale / nrm : 0.f;
       }
+    }
+    if (pub_pending) {  // the previous job's stores still read the region the offsets go to
+      if (tid == 0) bulk_wait_read();
+      __syncthreads();
     }
     // ---- gate and cumulative log2-decay of the thread's 16-row block ----
     {
@@ -504,10 +531,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk (into the offsets' space) and q, k, g of the next chunk
     if (tid == 0) {
       issue_v(static_cast<int>(t0));
-      // the next chunk this CTA prepares itself (a helper fetches per job)
-      const int cn = split ? c + 2 : c + 1;
-      if (!helper && cn < nchunks) issue_qkg(static_cast<int>(bos + static_cast<int64_t>(cn) * kC));
+      const int cn = split ? c + 2 : c + 1;  // the next chunk this CTA prepares itself
+      if (helper) {
+        if (nx_c >= 0) issue_next_job();
+        if (pub_pending) publish();  // the previous job's stores have long completed
+      } else if (cn < nchunks) {
+        issue_qkg(h, static_cast<int>(bos + static_cast<int64_t>(cn) * kC));
+      }
     }
+    pub_pending = false;
 
     // ---- Abar | M by column block J: tf32, row operand in TMEM. Rounds 0-2
     // are written at once and issued in parallel by lane 0 of warps 0-2 (each
@@ -624,10 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = 0; ks < 8; ++ks)  // W^T = (Kh Gamma)^T (T'hi + T'lo)^T
         mma(tmem + TM_DW, desc_mn(D0, OFF_XW, 8192, ks & 3),
             desc_k(D0, (ks < 4 ? OFF_TP : OFF_TPL), 64, 0, ks & 3), idesc(128, 64, true, false), ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)  // U^T = V^T (T'hi + T'lo)^T
-        mma(tmem + TM_DU, desc_mn(D0, OFF_V, 8192, ks & 3),
-            desc_k(D0, (ks < 4 ? OFF_TP : OFF_TPL), 64, 0, ks & 3), idesc(128, 64, true, false), ks > 0);
+      if (!helper) issue_u();  // a helper hands v and T' over instead
       mma_commit(bar_mma);
     }
     KDA_WAIT(bar_mma, ph_mma);
@@ -646,59 +675,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     KDA_SYNC_OR_BAIL();
     }  // prepared here
     if (helper) {
-      // ---- hand the prepared odd chunk over: U^T (TMEM) to fp32 staging, then
-      // the operand tiles and gamma to the item's slot, then publish it ----
-      {
-        float v[32];
-        tmem_ld32(tmem + tlane + TM_DU + 32 * hh, v);  // lane = v, columns r
-        float4* dst = reinterpret_cast<float4*>(sm + OFF_XU + lrow * 256 + 128 * hh);
-#pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) dst[j4] = make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
-      }
-      fence_async_smem();
-      KDA_SYNC_OR_BAIL();
+      // ---- hand the prepared odd chunk over: the operand runs, T' hi and
+      // gamma to the item's slot once the main CTA has drained it; the stores
+      // complete, and are published, during the next job ----
       if (tid == 0) {
         const int tt = c >> 1;
-        uint8_t* slot = a.xbuf + (static_cast<size_t>(item) * kXSlots + tt % kXSlots) * kXSlotBytes;
-        bulk_store(slot + kXB1, sb + OFF_B1, 32768);
-        bulk_store(slot + kXB2A, sb + OFF_B2A, 16384);
-        bulk_store(slot + kXB2B, sb + OFF_B2B, 8192);
-        bulk_store(slot + kXML, sb + OFF_ML, 8192);
-        bulk_store(slot + kXU, sb + OFF_XU, 32768);
-        bulk_store(slot + kXGAM, smem_addr(s_gam), 512);
-        bulk_wait_all();
+        if (tt >= kXSlots && !wait_flag_geq(a.xflags + 5 * item + 4, static_cast<uint32_t>(tt - kXSlots + 1), a.status))
+          *s_fail = 1;
         fence_proxy_global();
-        st_release(a.xflags + 5 * item + tt % kXSlots, static_cast<uint32_t>(tt + 1));
+        uint8_t* slot = a.xbuf + (static_cast<size_t>(item) * kXSlots + tt % kXSlots) * kXSlotBytes;
+        bulk_store(slot + kXB, sb + OFF_B1, kXBBytes);
+        bulk_store(slot + kXR, sb + OFF_V, kXRBytes);
+        bulk_store(slot + kXTP, sb + OFF_TP, 8192);
+        bulk_store(slot + kXGAM, smem_addr(s_gam), 512);
+        pub_item = item;
+        pub_tt = tt;
       }
-      __syncthreads();  // the shared tiles are read out before the next job rewrites them
+      pub_pending = true;
       continue;
     }
     if (handed) {
-      // ---- a helper prepared this chunk: its tiles landed during the previous
-      // chunk; U^T goes into TMEM, where the U~ product accumulates onto it ----
-      if (!mbar_wait(bar_x, ph_x, a.status, wait_limit)) *s_fail = 1;
+      // ---- a helper prepared this chunk; its operands landed during the
+      // previous chunk, and the slot is free again ----
+      if (mbar_wait(bar_x, ph_x, a.status, wait_limit))
+        x_pending = false;
+      else
+        *s_fail = 1;
       ph_x ^= 1u;
-      x_pending = false;
-      {
-        float v[32];
-        const float4* src = reinterpret_cast<const float4*>(sm + OFF_XU + lrow * 256 + 128 * hh);
-#pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 x = src[j4];
-          v[4 * j4] = x.x;
-          v[4 * j4 + 1] = x.y;
-          v[4 * j4 + 2] = x.z;
-          v[4 * j4 + 3] = x.w;
-        }
-        tmem_st32(tmem + tlane + TM_DU + 32 * hh, v);
-      }
-      tmem_st_wait();
-      if (tid == 0) st_release(a.xflags + 5 * item + 4, static_cast<uint32_t>((c >> 1) + 1));  // slot consumed
-      fence_before_sync();
-      KDA_SYNC_OR_BAIL();
+      if (tid == 0) st_release(a.xflags + 5 * item + 4, static_cast<uint32_t>((c >> 1) + 1));
     }
     if (tid == 0) {
       fence_after_sync();
+      if (handed) issue_u();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)  // U~^T = U^T + H^T (-W)^T
         mma(tmem + TM_DU, desc_k(D0, OFF_A1, 128, 0, ks), desc_k(D0, OFF_B1, 128, 0, ks), idesc(128, 64), 1);
@@ -757,11 +765,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_global();
         const uint8_t* slot = a.xbuf + (static_cast<size_t>(item) * kXSlots + tt % kXSlots) * kXSlotBytes;
         mbar_expect_tx(bar_x, kXSlotBytes);
-        bulk_load(sb + OFF_B1, slot + kXB1, 32768, bar_x);
-        bulk_load(sb + OFF_B2A, slot + kXB2A, 16384, bar_x);
-        bulk_load(sb + OFF_B2B, slot + kXB2B, 8192, bar_x);
-        bulk_load(sb + OFF_ML, slot + kXML, 8192, bar_x);
-        bulk_load(sb + OFF_XU, slot + kXU, 32768, bar_x);
+        bulk_load(sb + OFF_B1, slot + kXB, kXBBytes, bar_x);
+        bulk_load(sb + OFF_V, slot + kXR, kXRBytes, bar_x);
+        bulk_load(sb + OFF_TP, slot + kXTP, 8192, bar_x);
         bulk_load(smem_addr(s_gam2), slot + kXGAM, 512, bar_x);
       }
       x_pending = true;
@@ -805,7 +811,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 teardown:
   // no async copy may still target this CTA's shared memory when it exits
   if (x_pending) mbar_wait(bar_x, ph_x, a.status, wait_limit);
-  if (tid == 0) bulk_wait_all();
+  if (tid == 0) {
+    if (pub_pending)
+      publish();
+    else
+      bulk_wait_all();
+  }
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, TM_COLS);
