@@ -386,10 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (!handed) {
-    if (tid < kC) {
-      const int r = tid;
-      s_beta[r] = r < rows ? sigmoidf_(__bfloat162float(a.b[(t0 + r) * a.H + h])) : 0.f;
-    }
+    // raw beta: loaded now, stored once the norms are done (its latency hidden)
+    const float braw = (tid < rows) ? __bfloat162float(a.b[(t0 + tid) * a.H + h]) : 0.f;
     KDA_WAIT(bar_qkg, ph_qkg);
     // ---- row norms: warp w handles rows 8w .. 8w+7, four at a time (sums
     // interleaved; lanes 0-3 finish the q rows, lanes 8-11 the k rows) ----
@@ -429,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_iq[r] = (ok && nrm > 0.f) ? a.scale / nrm : 0.f;
       }
     }
+    if (tid < kC) s_beta[tid] = tid < rows ? sigmoidf_(braw) : 0.f;
     if (pub_pending) {  // the previous job's stores still read the region the offsets go to
       if (tid == 0) bulk_wait_read();
       __syncthreads();
@@ -534,12 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cn = split ? c + 2 : c + 1;  // the next chunk this CTA prepares itself
       if (helper) {
         if (nx_c >= 0) issue_next_job();
-        if (pub_pending) publish();  // the previous job's stores have long completed
       } else if (cn < nchunks) {
         issue_qkg(h, static_cast<int>(bos + static_cast<int64_t>(cn) * kC));
       }
     }
-    pub_pending = false;
 
     // ---- Abar | M by column block J: tf32, row operand in TMEM. Rounds 0-2
     // are written at once and issued in parallel by lane 0 of warps 0-2 (each
@@ -579,7 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_st_wait();
     fence_before_sync();
     KDA_SYNC_OR_BAIL();
-    if (tid == 0) issue_round(3, TM_AJ, bar_mma);
+    if (tid == 0) {
+      issue_round(3, TM_AJ, bar_mma);
+      if (pub_pending) publish();  // the previous job's stores have long completed
+    }
+    pub_pending = false;
     KDA_WAIT(bar_odd, ph_odd);  // round 1
     KDA_WAIT(bar_r2, ph_r2);    // round 2
     KDA_WAIT(bar_mma, ph_mma);  // round 3
