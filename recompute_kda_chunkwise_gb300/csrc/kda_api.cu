@@ -87,21 +87,21 @@ int tc_bwd_ctas(const kda_problem* p) {
   return (int)(items < kda::kTcBwdCtas ? items : kda::kTcBwdCtas);
 }
 
-// Tensor-core backward: per-item hand-off counters for helper CTAs (only
-// problems with fewer items than the 152-CTA grid can use them).
+// Tensor-core backward: per-item hand-off counters for helper CTAs and their
+// job counter (only problems with fewer items than the 152-CTA grid use them).
 size_t flag_bytes(const kda_problem* p) {
   if (family_of(p) != 1) return 0;
-  return round_up((size_t)tc_bwd_ctas(p) * 3 * sizeof(uint32_t), 256);
+  return round_up(((size_t)tc_bwd_ctas(p) * kda::kTcBwdFlags + 1) * sizeof(uint32_t), 256);
 }
 
 size_t workspace_bytes(const kda_problem* p) {
   size_t scratch = kda::bwd_scratch_bytes_simt(p, nullptr);
   if (family_of(p) == 1) {
     // inline mode: one segment's states per CTA; split mode (items < 152):
-    // two segment buffers per item
+    // kTcBwdBufs segment buffers per item
     const int64_t items = (int64_t)p->num_seqs * p->num_heads;
-    const size_t per = kda::bwd_scratch_bytes_per_cta_tc();
-    scratch = items < kda::kTcBwdCtas ? (size_t)items * 2 * per : (size_t)kda::kTcBwdCtas * per;
+    scratch = items < kda::kTcBwdCtas ? (size_t)items * kda::kTcBwdBufs * kda::bwd_scratch_bytes_per_buf_split_tc()
+                                      : (size_t)kda::kTcBwdCtas * kda::bwd_scratch_bytes_per_cta_tc();
   }
   return kda::kHeaderBytes + partial_bytes(p) + flag_bytes(p) + scratch;
 }

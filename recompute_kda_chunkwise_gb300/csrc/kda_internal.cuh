@@ -99,12 +99,18 @@ size_t bwd_scratch_bytes_simt(const kda_problem* p, int* nctas);
 kda_status launch_bwd_simt_ctas(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas);
 size_t bwd_scratch_bytes_per_cta_simt(const kda_problem* p);
 size_t bwd_scratch_bytes_per_cta_tc();
+size_t bwd_scratch_bytes_per_buf_split_tc();
 // Bytes of the tensor-core forward's hand-off area (counters + slots) for
 // `items` (sequence, head) items.
 size_t fwd_handoff_bytes(int items);
 kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas);
 // CTAs of the tensor-core backward: one per SM of a 152-SM part (persistent).
 constexpr int kTcBwdCtas = 152;
+// Split-mode backward: segment buffers per item (helpers rebuild up to
+// kTcBwdBufs - 1 levels ahead of the reverse CTA) and hand-off counters per
+// item (one "rebuilt" counter per buffer, then one "consumed" counter).
+constexpr int kTcBwdBufs = 3;
+constexpr int kTcBwdFlags = kTcBwdBufs + 1;
 
 // Host helpers shared by the entry points (defined in kda_api.cu).
 kda_status validate_problem(const kda_problem* p);

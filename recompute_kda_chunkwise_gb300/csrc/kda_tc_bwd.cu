@@ -43,12 +43,17 @@ constexpr int kTileF = kC * kLd * 4;    // bytes of one fp32 [16][132] tile
 constexpr int kSq = 20;                 // row stride of the 16 x 16 matrices
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kStateBytes = 32768;  // fp16 128 x 128 state tile
-// One scratch slot per chunk: the chunk-start state, then (split mode) the
-// chunk's Abar, T, T' (the 16 x kSq small matrices at S_AB .. S_TP) and the
-// M hi / lo tiles, written by a helper CTA for the reverse CTA.
+// One scratch slot per chunk: the chunk-start state and, in split mode, what
+// a helper CTA prepares for the reverse CTA: the chunk's Abar, T, T' (the
+// 16 x kSq small matrices at S_AB .. S_TP), the M hi / lo tiles, -W and U~
+// (fp16 operand tiles) and U~ (fp32 tile).
 constexpr uint32_t kPrepSBytes = 3 * 320 * 4;  // S_AB, S_T, S_TP
 constexpr uint32_t kPrepMBytes = 4096;         // M hi + lo tiles
-constexpr uint32_t kSlotBytes = kStateBytes + 8192;
+constexpr uint32_t kPrepWOff = kStateBytes + 8192;  // -W fp16 [16][128]
+constexpr uint32_t kPrepUOff = kPrepWOff + 4096;    // U~ fp16 [16][128]
+constexpr uint32_t kPrepUTOff = kPrepUOff + 4096;   // U~ fp32 [16][kLd]
+constexpr uint32_t kSlotBytesSplit = kPrepUTOff + kC * kLd * 4;
+constexpr uint32_t kSlotBytesInline = kStateBytes;  // the state alone
 
 // ---- shared memory map (bytes) ----
 constexpr int OFF_A1 = 0;                  // H^T fp16 [128 v][128 i] (SW128)
@@ -98,7 +103,7 @@ struct TcBwdArgs {
   __nv_bfloat16 *dq, *dk, *dv, *dg, *db;
   float* partial;
   uint8_t* scratch;  // fp16 chunk-start state tiles (per CTA, or per item and level parity)
-  uint32_t* flags;   // per item: last level + 1 rebuilt into buffer 0 / buffer 1, levels consumed (split mode)
+  uint32_t* flags;   // per item: last level + 1 rebuilt into each buffer, levels consumed (split mode)
   int* status;
   const int32_t* cu;
   int N, H;
@@ -183,6 +188,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   uint64_t* bar_a1 = bar + 1;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar + 2);
   int* s_fail = reinterpret_cast<int*>(bar + 3);
+  int* s_job = s_fail + 1;     // split mode: a helper's claimed job
   uint64_t* bar_du = bar + 4;  // dU~ products (issued early, reverse pass)
   uint64_t* bar_g1 = bar + 5;  // (H dU~^T) products
   uint64_t* bar_g2 = bar + 6;  // (dH' U~^T) products
@@ -213,6 +219,20 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   uint32_t ph = 0, ph_a1 = 0, ph_du = 0, ph_g1 = 0, ph_g2 = 0, ph_sm = 0;
   bool sm_pending = false;  // a bulk load of a chunk's small matrices is in flight
   bool a1_pending = false;  // a bulk load into A1 is in flight (same value in every thread)
+  // split mode, thread 0: a chunk's helper-prepared operands, scratch slot <-> shared memory
+  auto load_prep = [&](const uint8_t* slot) {
+    mbar_expect_tx(bar_sm, kPrepSBytes + kPrepMBytes + 8192 + kTileF);
+    bulk_load(sb + OFF_SMALL, slot + kStateBytes, kPrepSBytes, bar_sm);
+    bulk_load(sb + OFF_FM, slot + kStateBytes + kPrepSBytes, kPrepMBytes, bar_sm);
+    bulk_load(sb + OFF_FW, slot + kPrepWOff, 4096, bar_sm);
+    bulk_load(sb + OFF_FU, slot + kPrepUOff, 4096, bar_sm);
+    bulk_load(sb + OFF_F32 + T_U * kTileF, slot + kPrepUTOff, kTileF, bar_sm);
+  };
+  auto ship_wu = [&](uint8_t* slot) {
+    bulk_store(slot + kPrepWOff, sb + OFF_FW, 4096);
+    bulk_store(slot + kPrepUOff, sb + OFF_FU, 4096);
+    bulk_store(slot + kPrepUTOff, sb + OFF_F32 + T_U * kTileF, kTileF);
+  };
 
 #define KDA_WAIT_MMA()                              \
   do {                                              \
@@ -229,16 +249,16 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   // ...) and each item's segments from the last. In split mode (helpers > 0,
   // one reverse CTA per item) the helper CTAs rebuild the segment states:
   // the jobs (level L = segment nseg-1-L, item) are numbered level-major,
-  // job = L * items + item, and helper j takes jobs j, j + helpers, ... in
-  // order, so every helper carries the same load and the levels complete in
-  // order, ahead of the reverse CTAs; each item has two scratch buffers.
+  // job = L * items + item, and a free helper claims the next one from a
+  // global counter, so the levels complete in order, ahead of the reverse
+  // CTAs; each item has kTcBwdBufs scratch buffers.
   const int items = a.N * a.H;
   const bool split = a.helpers > 0;
   const bool helper = split && static_cast<int>(blockIdx.x) >= items;
   int item = helper ? 0 : static_cast<int>(blockIdx.x);
   int seg = -1, lvl = 0;
   bool open = false;
-  int job = static_cast<int>(blockIdx.x) - items, max_jobs = 0;
+  int max_jobs = 0;
   if (helper) {  // jobs run up to the longest sequence's segment count
     int max_seg = 0;
     for (int s2 = 0; s2 < a.N; ++s2)
@@ -275,11 +295,17 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
         for (int x = tid; x < 32768 / 16; x += kT) reinterpret_cast<uint4*>(sm + OFF_A1D)[x] = make_uint4(0, 0, 0, 0);
       }
     } else {
+      // claim the next job (a counter after the items' hand-off counters): a
+      // helper blocked on one item's buffer holds back no other item's job
       bool found = false;
-      while (job < max_jobs) {
-        lvl = job / items;
-        item = job % items;
-        job += a.helpers;
+      while (true) {
+        if (tid == 0) *s_job = static_cast<int>(atomicAdd(a.flags + kTcBwdFlags * items, 1u));
+        __syncthreads();
+        const int jb = *s_job;
+        __syncthreads();
+        if (jb >= max_jobs) break;
+        lvl = jb / items;
+        item = jb % items;
         n = item / a.H;
         h = item % a.H;
         bos = a.cu[n];
@@ -301,14 +327,17 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
       const int lv = nseg - 1 - seg;  // level: segments counted from the end
       const int c0 = seg * kCPS, c1 = min(nchunks, c0 + kCPS);
       const bool rebuild = !split || helper;
-      uint8_t* segbuf = split ? a.scratch + (static_cast<size_t>(item) * 2 + (lv & 1)) * kCPS * kSlotBytes
-                              : a.scratch + static_cast<size_t>(blockIdx.x) * kCPS * kSlotBytes;
-      if (split) {  // hand-off: the helper waits until level lv-2's buffer is consumed,
-                    // the reverse CTA until level lv has been rebuilt
+      const uint32_t sbytes = split ? kSlotBytesSplit : kSlotBytesInline;
+      uint8_t* segbuf = split ? a.scratch + (static_cast<size_t>(item) * kTcBwdBufs + lv % kTcBwdBufs) * kCPS * sbytes
+                              : a.scratch + static_cast<size_t>(blockIdx.x) * kCPS * sbytes;
+      if (split) {  // hand-off: the helper waits until the level that last used this
+                    // buffer (lv - kTcBwdBufs) is consumed, the reverse CTA until level lv is rebuilt
         if (tid == 0) {
           bool ok = true;
-          if (helper && lv >= 2) ok = wait_flag_geq(a.flags + 3 * item + 2, static_cast<uint32_t>(lv - 1), a.status);
-          if (!helper) ok = wait_flag_geq(a.flags + 3 * item + (lv & 1), static_cast<uint32_t>(lv + 1), a.status);
+          uint32_t* f = a.flags + kTcBwdFlags * item;
+          if (helper && lv >= kTcBwdBufs)
+            ok = wait_flag_geq(f + kTcBwdBufs, static_cast<uint32_t>(lv - kTcBwdBufs + 1), a.status);
+          if (!helper) ok = wait_flag_geq(f + lv % kTcBwdBufs, static_cast<uint32_t>(lv + 1), a.status);
           if (!ok) *s_fail = 1;
           fence_proxy_global();
         }
@@ -347,24 +376,23 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
         const bool need_m = rev || helper;   // M is needed (reverse pass, or for it)
         if (rev && !rebuild) {  // split mode: the last chunk's start state comes from scratch too
           if (tid == 0) {
+            const uint8_t* slot = segbuf + static_cast<size_t>(c1 - 1 - c0) * sbytes;
             mbar_expect_tx(bar_a1, kStateBytes);
-            bulk_load(sb + OFF_A1, segbuf + static_cast<size_t>(c1 - 1 - c0) * kSlotBytes, kStateBytes, bar_a1);
-            uint8_t* slot = segbuf + static_cast<size_t>(c1 - 1 - c0) * kSlotBytes;
-            mbar_expect_tx(bar_sm, kPrepSBytes + kPrepMBytes);
-            bulk_load(sb + OFF_SMALL, slot + kStateBytes, kPrepSBytes, bar_sm);
-            bulk_load(sb + OFF_FM, slot + kStateBytes + kPrepSBytes, kPrepMBytes, bar_sm);
+            bulk_load(sb + OFF_A1, slot, kStateBytes, bar_a1);
+            load_prep(slot);
           }
           a1_pending = true;
           sm_pending = true;
         }
-        float braw_next = 0.f;
+        // raw bf16 bits of beta: converted where used, so no thread waits on the load early
+        unsigned short braw_next = 0;
         if (nsteps > 0) {  // first chunk of the pass: issue its loads now
           const int c = rev ? c1 - 1 : c0;
           const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
           const int rows = static_cast<int>(min(static_cast<int64_t>(kC), eos - t0));
           stage_tiles(a, sb + OFF_STG, h, t0, rows, tid, true, rev, sb + OFF_SDO, need_m);
           cp_async_commit();
-          if (tid < kC && tid < rows) braw_next = __bfloat162float(a.b[(t0 + tid) * a.H + h]);
+          if (tid < kC && tid < rows) braw_next = beta_bits(a.b, (t0 + tid) * a.H + h);
         }
 #pragma unroll 1
         for (int step = 0; step < nsteps; ++step) {
@@ -377,22 +405,22 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           const uint8_t* SV = SQ + 2 * 4096;
           const uint8_t* SG = SQ + 3 * 4096;
           const bool more = step + 1 < nsteps;
-          const float braw = braw_next;
+          const unsigned short braw = braw_next;
           // ---- prefetch the next chunk of this pass; save the start state ----
           if (more) {
             const int cn = rev ? c - 1 : c + 1;
             const int64_t tn = bos + static_cast<int64_t>(cn) * kC;
             const int rn = static_cast<int>(min(static_cast<int64_t>(kC), eos - tn));
             stage_tiles(a, sb + OFF_STG + (buf ^ 1) * kStgBuf, h, tn, rn, tid, true, false, 0, need_m);
-            if (tid < kC && tid < rn) braw_next = __bfloat162float(a.b[(tn + tid) * a.H + h]);
+            if (tid < kC && tid < rn) braw_next = beta_bits(a.b, (tn + tid) * a.H + h);
           }
           cp_async_commit();
-          if (!rev && tid == 0) bulk_store(segbuf + static_cast<size_t>(c - c0) * kSlotBytes, sb + OFF_A1, kStateBytes);
+          if (!rev && tid == 0) bulk_store(segbuf + static_cast<size_t>(c - c0) * sbytes, sb + OFF_A1, kStateBytes);
           cp_async_wait_prev();
           __syncthreads();
 
           // ================= chunk prologue =================
-          if (tid < kC) S[S_BETA + tid] = tid < rows ? sigm(braw) : 0.f;
+          if (tid < kC) S[S_BETA + tid] = tid < rows ? sigm(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
           {  // row norms: warp w -> rows 2w, 2w+1 (sums interleaved; lanes 0-3 finish them)
             float sk0 = 0.f, sk1 = 0.f, sq0 = 0.f, sq1 = 0.f;
 #pragma unroll
@@ -549,17 +577,19 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               }
             }
           }
+          // -W and U~ are rewritten next: the previous step's copies of them (all
+          // but this step's state copy) have been read out
+          if (helper && tid == 0) bulk_wait_read_but<1>();
           fence_async_smem();
           __syncthreads();
           if (helper) {  // hand this chunk's Abar, T, T' and M hi / lo to the reverse CTA
             if (tid == 0) {
-              uint8_t* slot = segbuf + static_cast<size_t>(c - c0) * kSlotBytes;
+              uint8_t* slot = segbuf + static_cast<size_t>(c - c0) * sbytes;
               bulk_store(slot + kStateBytes, sb + OFF_SMALL, kPrepSBytes);
               bulk_store(slot + kStateBytes + kPrepSBytes, sb + OFF_FM, kPrepMBytes);
             }
-            if (c == c1 - 1) continue;  // the segment's last chunk advances no state
           }
-          {  // W = T' (Kh Gamma) -> -W fp16;  U = T' V -> fp32  (channels 16w .. 16w+15)
+          if (prep) {  // W = T' (Kh Gamma) -> -W fp16;  U = T' V -> fp32  (channels 16w .. 16w+15)
             float dw[2][4] = {}, du[2][4] = {};
 #pragma unroll
             for (int k0 = 0; k0 < kC; k0 += 8) {
@@ -596,15 +626,17 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             ph_a1 ^= 1u;
             a1_pending = false;
           }
-          if (tid == 0) {
-            fence_after_sync();
+          if (prep) {  // (split mode: the helper shipped -W and U~ with the chunk's matrices)
+            if (tid == 0) {
+              fence_after_sync();
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              mma(tmem + TM_D1, desc_k(D0, OFF_A1, 128, 0, ks), desc_k(D0, OFF_FW, 16, 0, ks),
-                  idesc(128, 16), ks > 0);
-            mma_commit(bar);
+              for (int ks = 0; ks < 8; ++ks)
+                mma(tmem + TM_D1, desc_k(D0, OFF_A1, 128, 0, ks), desc_k(D0, OFF_FW, 16, 0, ks),
+                    idesc(128, 16), ks > 0);
+              mma_commit(bar);
+            }
+            KDA_WAIT_MMA();
           }
-          KDA_WAIT_MMA();
           if (rev) {
             if (!mbar_wait(bar_du, ph_du, a.status)) *s_fail = 1;
             ph_du ^= 1u;
@@ -612,13 +644,15 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           fence_after_sync();
           {
             float x[8];
-            tmem_ld8(tmem + tlane + TM_D1 + 8 * hh, x);  // lane = v, columns r
+            if (prep) {
+              tmem_ld8(tmem + tlane + TM_D1 + 8 * hh, x);  // lane = v, columns r
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int r = 8 * hh + j;
-              const float u = UT[r * kLd + L] + x[j];
-              UT[r * kLd + L] = u;
-              st_h(sm + OFF_FU, sw128_off(r, L, 16), u);
+              for (int j = 0; j < 8; ++j) {
+                const int r = 8 * hh + j;
+                const float u = UT[r * kLd + L] + x[j];
+                UT[r * kLd + L] = u;
+                st_h(sm + OFF_FU, sw128_off(r, L, 16), u);
+              }
             }
             if (rev) {
               tmem_ld8(tmem + tlane + TM_DU + 8 * hh, x);  // dU~^T: lane = v, columns r
@@ -635,12 +669,21 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           KDA_SYNC_OR_BAIL();
 
           if (!rev) {
+            if (helper) {  // hand -W and U~ over; the segment's last chunk advances no state
+              if (tid == 0) ship_wu(segbuf + static_cast<size_t>(c - c0) * sbytes);
+              if (c == c1 - 1) continue;
+            }
             // ============ rebuild pass: H <- diag(gamma) H + Kbar^T U~ ============
             if (tid == 0) {
-              bulk_wait_read();  // the scratch copy of A1 has been read out
               fence_after_sync();
               mma(tmem + TM_D2, desc_mn(D0, OFF_FU, 2048, 0), desc_mn(D0, OFF_FKB, 2048, 0),
                   idesc(128, 128, true, true), 0);
+              // the scratch copy of A1 has been read out (a helper's three -W / U~
+              // copies may still be in flight: the next step waits for those)
+              if (helper)
+                bulk_wait_read_but<3>();
+              else
+                bulk_wait_read();
               mma_commit(bar);
             }
             KDA_WAIT_MMA();
@@ -812,7 +855,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           if (more) {
             if (tid == 0) {
               mbar_expect_tx(bar_a1, kStateBytes);
-              bulk_load(sb + OFF_A1, segbuf + static_cast<size_t>(c - 1 - c0) * kSlotBytes, kStateBytes, bar_a1);
+              bulk_load(sb + OFF_A1, segbuf + static_cast<size_t>(c - 1 - c0) * sbytes, kStateBytes, bar_a1);
             }
             a1_pending = true;
           }
@@ -953,12 +996,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           fence_async_smem();
           __syncthreads();
           if (!prep && more) {  // the next chunk's Abar, T, T', M (last read in [D2] and [F])
-            if (tid == 0) {
-              uint8_t* slot = segbuf + static_cast<size_t>(c - 1 - c0) * kSlotBytes;
-              mbar_expect_tx(bar_sm, kPrepSBytes + kPrepMBytes);
-              bulk_load(sb + OFF_SMALL, slot + kStateBytes, kPrepSBytes, bar_sm);
-              bulk_load(sb + OFF_FM, slot + kStateBytes + kPrepSBytes, kPrepMBytes, bar_sm);
-            }
+            if (tid == 0) load_prep(segbuf + static_cast<size_t>(c - 1 - c0) * sbytes);
             sm_pending = true;
           }
           {  // dG of the chunk end, reverse cumulative sum (natural-log units)
@@ -1028,10 +1066,10 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           bulk_wait_all();  // scratch states written before pass 1 reads them
           if (helper) {
             fence_proxy_global();
-            st_release(a.flags + 3 * item + (lv & 1), static_cast<uint32_t>(lv + 1));
+            st_release(a.flags + kTcBwdFlags * item + lv % kTcBwdBufs, static_cast<uint32_t>(lv + 1));
           }
         }
-        if (rev && split && tid == 0) st_release(a.flags + 3 * item + 2, static_cast<uint32_t>(lv + 1));
+        if (rev && split && tid == 0) st_release(a.flags + kTcBwdFlags * item + kTcBwdBufs, static_cast<uint32_t>(lv + 1));
         __syncthreads();
       }
     }
@@ -1085,7 +1123,8 @@ __global__ void kda_param_reduce_tc_kernel(const float* partial, int N, int H, i
 
 }  // namespace
 
-size_t bwd_scratch_bytes_per_cta_tc() { return static_cast<size_t>(kCPS) * kSlotBytes; }
+size_t bwd_scratch_bytes_per_cta_tc() { return static_cast<size_t>(kCPS) * kSlotBytesInline; }
+size_t bwd_scratch_bytes_per_buf_split_tc() { return static_cast<size_t>(kCPS) * kSlotBytesSplit; }
 
 kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas) {
   if (p->head_dim != kD || p->dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
@@ -1134,7 +1173,8 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   bool launched = false;
   if (helpers > 0) {
     t.helpers = helpers;
-    if (cudaMemsetAsync(a.flags, 0, sizeof(uint32_t) * 3 * items, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaMemsetAsync(a.flags, 0, sizeof(uint32_t) * (kTcBwdFlags * items + 1), s) != cudaSuccess)
+      return KDA_ERR_CUDA;
     void* kargs[] = {&t};
     launched = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kda_bwd_tc_kernel), dim3(items + helpers),
                                            dim3(kT), kargs, SMEM_BYTES, s) == cudaSuccess;

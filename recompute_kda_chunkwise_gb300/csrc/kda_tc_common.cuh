@@ -219,6 +219,11 @@ __device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t b
 }
 // The source shared memory of every committed bulk store may be reused.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// The source shared memory of all but the N most recent bulk stores may be reused.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_but() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 // Every committed bulk store has completed (its writes are visible).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
@@ -321,6 +326,12 @@ __device__ __forceinline__ void st_release(uint32_t* f, uint32_t v) {
 }
 // orders this thread's generic-proxy accesses with its async-proxy accesses of global memory
 __device__ __forceinline__ void fence_proxy_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Raw bits of one bf16 element (the caller converts where it uses the value,
+// so that nothing waits on the load before then).
+__device__ __forceinline__ unsigned short beta_bits(const __nv_bfloat16* p, int64_t i) {
+  return reinterpret_cast<const unsigned short*>(p)[i];
+}
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 p = __floats2half2_rn(lo, hi);

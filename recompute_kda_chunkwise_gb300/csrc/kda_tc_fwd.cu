@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (!handed) {
     // raw beta: loaded now, stored once the norms are done (its latency hidden)
-    const float braw = (tid < rows) ? __bfloat162float(a.b[(t0 + tid) * a.H + h]) : 0.f;
+    const unsigned short braw = (tid < rows) ? beta_bits(a.b, (t0 + tid) * a.H + h) : 0;
     KDA_WAIT(bar_qkg, ph_qkg);
     // ---- row norms: warp w handles rows 8w .. 8w+7, four at a time (sums
     // interleaved; lanes 0-3 finish the q rows, lanes 8-11 the k rows) ----
@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_iq[r] = (ok && nrm > 0.f) ? a.scale / nrm : 0.f;
       }
     }
-    if (tid < kC) s_beta[tid] = tid < rows ? sigmoidf_(braw) : 0.f;
+    if (tid < kC) s_beta[tid] = tid < rows ? sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
     if (pub_pending) {  // the previous job's stores still read the region the offsets go to
       if (tid == 0) bulk_wait_read();
       __syncthreads();
