@@ -500,6 +500,9 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               }
             }
           }
+          // split mode: the tiles above feed the early dU~ product directly (the
+          // Abar / M, inverse and W/U stages and their barriers are the helper's)
+          if (!prep) fence_async_smem();
           __syncthreads();
           if (!prep) {  // split mode: this chunk's Abar, T, T', M come from the helper
             if (!mbar_wait(bar_sm, ph_sm, a.status)) *s_fail = 1;
@@ -540,9 +543,11 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               }
             }
           }
-          fence_async_smem();
-          fence_before_sync();
-          __syncthreads();
+          if (prep) {
+            fence_async_smem();
+            fence_before_sync();
+            __syncthreads();
+          }
           // dU~^T = dO^T (Mhi + Mlo) + dH'^T Kbar^T needs no U~: issue it now (warp 4 is idle
           // during the inverse) so it runs under the inverse and the W/U stage
           if (rev && warp == 4 && lane == 0) {
@@ -580,8 +585,10 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           // -W and U~ are rewritten next: the previous step's copies of them (all
           // but this step's state copy) have been read out
           if (helper && tid == 0) bulk_wait_read_but<1>();
-          fence_async_smem();
-          __syncthreads();
+          if (prep) {
+            fence_async_smem();
+            __syncthreads();
+          }
           if (helper) {  // hand this chunk's Abar, T, T' and M hi / lo to the reverse CTA
             if (tid == 0) {
               uint8_t* slot = segbuf + static_cast<size_t>(c - c0) * sbytes;
@@ -617,9 +624,11 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               }
             }
           }
-          fence_async_smem();
-          fence_before_sync();
-          KDA_SYNC_OR_BAIL();
+          if (prep) {
+            fence_async_smem();
+            fence_before_sync();
+            KDA_SYNC_OR_BAIL();
+          }
           // ================= U~ = U - W H (tcgen05) =================
           if (a1_pending) {  // this chunk's start state, loaded during the prologue
             if (!mbar_wait(bar_a1, ph_a1, a.status)) *s_fail = 1;
