@@ -514,13 +514,15 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             cp_async_commit();
           }
           // ================= Abar (and M) on tf32 tensor tiles =================
-          if (prep && warp < (need_m ? 4 : 2)) {
-            const int nt = warp & 1;
-            const bool is_m = (warp >> 1) != 0;
+          // warp w: column block nt = w & 1, contraction half kh = (w >> 1) & 1, Abar (w < 4) or
+          // M (w >= 4); the kh = 1 warps hand their partial sums over in S_DT1 / S_DT2 (free here)
+          if (prep && warp < (need_m ? 8 : 4)) {
+            const int nt = warp & 1, kh = (warp >> 1) & 1;
+            const bool is_m = (warp >> 2) != 0;
             const float* X = is_m ? QG : KG;
             float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int k0 = 0; k0 < kD; k0 += 16) {  // two independent accumulator chains
+#pragma unroll
+            for (int k0 = 64 * kh; k0 < 64 * kh + 64; k0 += 16) {  // two independent accumulator chains
               float fa[4], fb[2];
               ldA(fa, X, kLd, k0, fg, ft);
               ldBc(fb, KI, kLd, 8 * nt, k0, fg, ft);
@@ -529,8 +531,16 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               ldBc(fb, KI, kLd, 8 * nt, k0 + 8, fg, ft);
               mma3(d2, fa, fb);
             }
+            float* part = S + (is_m ? S_DT2 : S_DT1);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) d[e] += d2[e];
+            for (int e = 0; e < 4; ++e) {
+              d[e] += d2[e];
+              if (kh) part[(fg + 8 * (e >> 1)) * kSq + 8 * nt + 2 * ft + (e & 1)] = d[e];
+            }
+            named_bar_sync(1, need_m ? 256 : 128);
+            if (kh == 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[e] += part[(fg + 8 * (e >> 1)) * kSq + 8 * nt + 2 * ft + (e & 1)];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int r = fg + 8 * (e >> 1), s = 8 * nt + 2 * ft + (e & 1);
@@ -541,6 +551,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                 st_h(sm + OFF_FM, sw128_off(s, r, 16), mv);  // K-major B of dU~^T: row s, column r
                 st_h(sm + OFF_FML, sw128_off(s, r, 16), lo_part(mv));
               }
+            }
             }
           }
           if (prep) {

@@ -324,6 +324,10 @@ __device__ __forceinline__ bool wait_flag_geq(const uint32_t* f, uint32_t target
 __device__ __forceinline__ void st_release(uint32_t* f, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
 }
+// barrier `id` (1..15) over the first `n` threads of the CTA (n a multiple of 32)
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 // orders this thread's generic-proxy accesses with its async-proxy accesses of global memory
 __device__ __forceinline__ void fence_proxy_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
