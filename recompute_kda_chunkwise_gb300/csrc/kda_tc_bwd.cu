@@ -573,23 +573,52 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                   idesc(128, 16), 1);
             mma_commit(bar_du);
           }
-          if (prep && warp == 0) {  // T = (I + diag(beta) Abar)^-1 by forward substitution, lane j: column j
-            const int j = lane & 15;
-            float x[16];
+          if (prep && warp == 0) {
+            // T = (I + N)^-1 with N = diag(beta) Abar strictly lower, in 8 x 8 blocks: lane j < 16
+            // solves column j of its diagonal block (T11 or T22) by forward substitution, then lane
+            // j < 8 forms column j of T21 = -T22 N21 T11 (lanes 16-31 repeat lanes 0-15, unused)
+            const int j = lane & 15, b8 = 8 * (j >> 3);
+            float x[8];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
-            // right-looking: once x[s] is final, eliminate it from every later row
+            for (int k = 0; k < 8; ++k) x[k] = (b8 + k == j) ? 1.f : 0.f;
 #pragma unroll
-            for (int s2 = 0; s2 < 15; ++s2) {
+            for (int s2 = 0; s2 < 7; ++s2) {  // right-looking: x[s2] is final, eliminate it below
 #pragma unroll
-              for (int r = s2 + 1; r < 16; ++r) x[r] -= S[S_BETA + r] * S[S_AB + r * kSq + s2] * x[s2];
+              for (int k = s2 + 1; k < 8; ++k)
+                x[k] -= S[S_BETA + b8 + k] * S[S_AB + (b8 + k) * kSq + b8 + s2] * x[s2];
+            }
+            if (lane < 16) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) S[S_T + (b8 + k) * kSq + j] = x[k];
+            }
+            __syncwarp();
+            float z[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) z[k] = 0.f;
+            if (lane < 8) {
+              float y[8];  // (N21 T11)[., j]
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                float acc = 0.f;
+#pragma unroll
+                for (int s3 = 0; s3 < 8; ++s3) acc += S[S_AB + (8 + k) * kSq + s3] * x[s3];
+                y[k] = S[S_BETA + 8 + k] * acc;
+              }
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m <= k; ++m) acc += S[S_T + (8 + k) * kSq + 8 + m] * y[m];
+                z[k] = -acc;
+              }
             }
             if (lane < 16) {
               const float bj = S[S_BETA + j];
 #pragma unroll
               for (int r = 0; r < 16; ++r) {
-                S[S_T + r * kSq + j] = x[r];
-                S[S_TP + r * kSq + j] = x[r] * bj;
+                const float t = ((r >> 3) == (j >> 3)) ? x[r & 7] : ((r >= 8) ? z[r - 8] : 0.f);
+                S[S_T + r * kSq + j] = t;
+                S[S_TP + r * kSq + j] = t * bj;
               }
             }
           }
