@@ -7,10 +7,11 @@ token-by-token recurrence plus its hand-derived reverse-time adjoint) built
 with gcc into ``oracle/_build/libkda_oracle.so`` and called through ctypes.
 
 Parity status of each part (what pins it is listed in the tests):
-  * recurrence and output -- pinned (explicit transition-matrix product form,
-    closed-form special cases, invariants);
-  * backward -- pinned (central finite differences, fp64 autograd of an
-    independent explicit-matrix forward);
+  * recurrence, output and final state -- pinned (explicit transition-matrix
+    product form, closed-form special cases, invariants, chaining of a
+    sequence split in two through its state);
+  * backward, with the initial-state gradient -- pinned (central finite
+    differences, fp64 autograd of an independent explicit-matrix forward);
   * gate formula g = L*sigmoid(exp(A_log)*(a + dt_bias)) and the shapes
     A_log[H], dt_bias[H,D] -- parity unpinned: the pages name only a
     "safe gate with lower bound -5" built from these three inputs.
@@ -58,7 +59,7 @@ def _load():
             f.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
                           ctypes.c_int, dp, dp, dp, dp, dp, dp, dp,
                           ctypes.c_double, ctypes.c_double, ctypes.c_double, dp,
-                          dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
+                          dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -78,14 +79,18 @@ def _ptr(a, ctype):
 
 def kda_reference(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO=None, *,
                   scale: float = 1.0, lower_bound: float = -5.0, eps: float = 1e-6,
-                  threads: int | None = None, want_o: bool = True) -> dict:
+                  threads: int | None = None, want_o: bool = True, h0=None, dht=None,
+                  want_state: bool = False) -> dict:
     """Run the oracle.
 
     Arrays are numpy arrays or torch tensors; they are widened to float64
     (exact for bf16 and fp32 values). q,k,v,g,dO: [S,H,D]; beta: [S,H]; A_log: [H];
-    dt_bias: [H,D]; cu_seqlens: [N+1] int. Returns float64 arrays: 'o'
-    (when want_o) and, when dO is given, 'dq','dk','dv','dg','dbeta',
-    'dA_log','ddt_bias'.
+    dt_bias: [H,D]; cu_seqlens: [N+1] int; h0 (initial states) and dht
+    (gradient of the final states): [N,H,D,D] (rows: key index), zero when
+    None. Returns float64 arrays: 'o' (when want_o) and, when dO is given,
+    'dq','dk','dv','dg','dbeta','dA_log','ddt_bias'. With want_state (or h0 /
+    dht given) it also returns the final states 'hT' and, when dO is given,
+    the initial-state gradient 'dh0', both [N,H,D,D].
     """
     q = _f64(q)
     if q.ndim != 3:
@@ -99,7 +104,15 @@ def kda_reference(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO=None, *,
     if cu.ndim != 1 or cu.size < 1 or cu[0] != 0 or cu[-1] != S:
         raise ValueError("cu_seqlens must start at 0 and end at S")
     N = cu.size - 1
+    want_state = want_state or h0 is not None or dht is not None
+    h0 = None if h0 is None else _f64(h0, (N, H, D, D))
+    dht = None if dht is None else _f64(dht, (N, H, D, D))
     out = {}
+    hT = dh0 = None
+    if want_state:
+        hT = out["hT"] = np.zeros((N, H, D, D))
+        if dO is not None:
+            dh0 = out["dh0"] = np.zeros((N, H, D, D))
     o = np.zeros((S, H, D), np.float64) if want_o else None
     if want_o:
         out["o"] = o
@@ -121,7 +134,8 @@ def kda_reference(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO=None, *,
         _ptr(A_log, fp), _ptr(dt_bias, fp), float(scale), float(lower_bound), float(eps),
         _ptr(dO, fp), _ptr(o, dpt), _ptr(G.get("dq"), dpt), _ptr(G.get("dk"), dpt),
         _ptr(G.get("dv"), dpt), _ptr(G.get("dg"), dpt), _ptr(G.get("dbeta"), dpt),
-        _ptr(G.get("dA_log"), dpt), _ptr(G.get("ddt_bias"), dpt), int(threads))
+        _ptr(G.get("dA_log"), dpt), _ptr(G.get("ddt_bias"), dpt), _ptr(h0, fp), _ptr(hT, dpt),
+        _ptr(dht, fp), _ptr(dh0, dpt), int(threads))
     if rc != 0:
         raise RuntimeError(f"kda_oracle_run failed with code {rc}")
     return out

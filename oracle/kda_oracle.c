@@ -23,7 +23,8 @@
  *   A_log and dt_bias; the closed form above is this project's reading (the
  *   smooth bounded map). Parity of that mapping is unpinned by the pages.
  *
- *   recurrence (the KDA gated delta rule, state S is D x V, S_0 = 0):
+ *   recurrence (the KDA gated delta rule, state S is D x V; S_0 = h0, the
+ *   initial state, zero unless given):
  *     S_t = (I - beta_t kh_t kh_t^T) Diag(alpha_t) S_{t-1} + beta_t kh_t v_t^T
  *     o_t = S_t^T qh_t
  *   written out with the obvious associativity so each step is O(D*V):
@@ -33,13 +34,15 @@
  *   channel-wise decay of the state, "b_h1 *= exp2(b_gk_last1)", and the
  *   section 2.1 table lists the chunked form of exactly this recurrence.)
  *
- *   backward: the exact reverse-time adjoint of the loop above, derived by
- *   hand. With Gb the adjoint of S_t (Gb = 0 after the last token):
+ *   final state hT = S_T. backward: the exact reverse-time adjoint of the loop
+ *   above, derived by hand. With Gb the adjoint of S_t (Gb = dhT, the
+ *   gradient of the final state, after the last token; zero unless given):
  *     Gb    += qh_t dO_t^T ;   dqh_t = S_t dO_t
  *     dbeta_t = kh_t^T Gb r_t ;  dr = beta_t Gb^T kh_t ;  dv_t = dr
  *     dkh_t = beta_t Gb r_t - P_t dr
  *     dP    = Gb - kh_t dr^T ;  dalpha_t[i] = sum_j dP[i][j] S_{t-1}[i][j]
  *     Gb    = Diag(alpha_t) dP          (adjoint of S_{t-1})
+ *   and after the first token dh0 = Gb, the gradient of the initial state;
  *   then the elementwise chain rule through the prologue. States S_{t-1}
  *   for the reverse loop are rebuilt segment by segment from states stored
  *   every SEG tokens (same recurrence, same order, so bit-identical).
@@ -59,6 +62,8 @@ typedef struct {
   int num_seqs, H, D;
   const int64_t* cu;
   const double *q, *k, *v, *g, *b, *A_log, *dt_bias, *dO;
+  const double *h0, *dhT; /* [num_seqs][H][D][V] or NULL (zero) */
+  double *hT, *dh0;       /* [num_seqs][H][D][V] or NULL (not written) */
   double scale, lower, eps;
   double *o, *dq, *dk, *dv, *dg, *db;
   double* partial; /* [num_seqs][H][D+1]: ddt_bias[D], dA_log */
@@ -131,8 +136,15 @@ static int run_one(job_t* J, int n, int h) {
   const int D = J->D, V = J->D, H = J->H;
   const int64_t bos = J->cu[n], eos = J->cu[n + 1];
   const int64_t T = eos - bos;
-  if (T <= 0) return 0;
   const int64_t DV = (int64_t)D * V;
+  const int64_t soff = ((int64_t)n * H + h) * DV; /* this (sequence, head)'s state */
+  if (T <= 0) { /* no tokens: hT = h0 and dh0 = dhT */
+    for (int64_t x = 0; x < DV; ++x) {
+      if (J->hT) J->hT[soff + x] = J->h0 ? J->h0[soff + x] : 0.0;
+      if (J->dh0) J->dh0[soff + x] = J->dhT ? J->dhT[soff + x] : 0.0;
+    }
+    return 0;
+  }
   const int64_t nseg = (T + SEG - 1) / SEG;
   const int want_bwd = J->dO != NULL;
 
@@ -158,6 +170,9 @@ static int run_one(job_t* J, int n, int h) {
   double* dkh = work + 13 * D;
   double* dalpha = work + 14 * D;
 
+  if (J->h0) memcpy(S, J->h0 + soff, sizeof(double) * DV);
+  if (want_bwd && J->dhT) memcpy(Gb, J->dhT + soff, sizeof(double) * DV);
+
   /* ---------------- forward ---------------- */
   for (int64_t tt = 0; tt < T; ++tt) {
     if (want_bwd && tt % SEG == 0) memcpy(ckpt + (tt / SEG) * DV, S, sizeof(double) * DV);
@@ -174,6 +189,8 @@ static int run_one(job_t* J, int n, int h) {
       }
     }
   }
+
+  if (J->hT) memcpy(J->hT + soff, S, sizeof(double) * DV);
 
   /* ---------------- backward ---------------- */
   if (want_bwd) {
@@ -269,6 +286,7 @@ static int run_one(job_t* J, int n, int h) {
       }
     }
     ddtb[D] = dAlog;
+    if (J->dh0) memcpy(J->dh0 + soff, Gb, sizeof(double) * DV);
   }
   free(S); free(ckpt); free(segS); free(Gb); free(dP); free(work);
   return 0;
@@ -294,15 +312,19 @@ static void* worker(void* arg) {
  * Entry point. Layouts: q,k,v,g,dO,o,dq,dk,dv,dg are [S,H,D] (token-major),
  * b and db are [S,H], A_log and dA_log are [H], dt_bias and ddt_bias are
  * [H,D]. S = cu_seqlens[num_seqs]. dO == NULL runs the forward only. o may
- * be NULL when only gradients are wanted. Returns 0 on success, -1 on a bad
- * argument, -2 when memory could not be allocated.
+ * be NULL when only gradients are wanted. h0 (initial states), hT (final
+ * states), dhT (gradient of the final states) and dh0 (gradient of the
+ * initial states) are [num_seqs][H][D][V] with rows the key index; each may
+ * be NULL (h0 / dhT: zero; hT / dh0: not written). Returns 0 on success, -1
+ * on a bad argument, -2 when memory could not be allocated.
  */
 int kda_oracle_run(int num_seqs, const int64_t* cu_seqlens, int H, int D,
                    const double* q, const double* k, const double* v, const double* g,
                    const double* b, const double* A_log, const double* dt_bias,
                    double scale, double lower_bound, double eps, const double* dO,
                    double* o, double* dq, double* dk, double* dv, double* dg, double* db,
-                   double* dA_log, double* ddt_bias, int num_threads) {
+                   double* dA_log, double* ddt_bias, const double* h0, double* hT,
+                   const double* dhT, double* dh0, int num_threads) {
   if (num_seqs < 0 || H <= 0 || D <= 0 || !cu_seqlens) return -1;
   for (int n = 0; n < num_seqs; ++n)
     if (cu_seqlens[n + 1] < cu_seqlens[n]) return -1;
@@ -313,6 +335,7 @@ int kda_oracle_run(int num_seqs, const int64_t* cu_seqlens, int H, int D,
   J.q = q; J.k = k; J.v = v; J.g = g; J.b = b; J.A_log = A_log; J.dt_bias = dt_bias;
   J.dO = dO; J.scale = scale; J.lower = lower_bound; J.eps = eps;
   J.o = o; J.dq = dq; J.dk = dk; J.dv = dv; J.dg = dg; J.db = db;
+  J.h0 = h0; J.hT = hT; J.dhT = dO ? dhT : NULL; J.dh0 = dO ? dh0 : NULL;
   J.njobs = num_seqs * H;
   if (dO) {
     J.partial = calloc((size_t)num_seqs * H * (D + 1) + 1, sizeof(double));

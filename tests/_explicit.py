@@ -19,16 +19,22 @@ def prologue(q, k, g, b, A_log, dt_bias, scale, lower, eps):
     return qh, kh, alpha, beta
 
 
-def explicit_forward(q, k, v, g, b, A_log, dt_bias, cu, scale=1.0, lower=-5.0, eps=1e-6):
+def explicit_forward(q, k, v, g, b, A_log, dt_bias, cu, scale=1.0, lower=-5.0, eps=1e-6,
+                     h0=None, final_states=None):
+    """o [S,H,D]. h0 [N,H,D,D] (rows: key index) starts each recurrence
+    (zero when None); when ``final_states`` is a list, the final states are
+    appended to it as one [N,H,D,D] tensor."""
     S_, H, D = q.shape
     qh, kh, alpha, beta = prologue(q, k, g, b, A_log, dt_bias, scale, lower, eps)
     eye = torch.eye(D, dtype=q.dtype)
     outs = []
+    finals = []
     cu = [int(x) for x in cu]
     for n in range(len(cu) - 1):
         for_heads = []
+        fin_heads = []
         for h in range(H):
-            S = torch.zeros(D, D, dtype=q.dtype)
+            S = torch.zeros(D, D, dtype=q.dtype) if h0 is None else h0[n, h]
             os_ = []
             for t in range(cu[n], cu[n + 1]):
                 kk = kh[t, h][:, None]
@@ -36,5 +42,9 @@ def explicit_forward(q, k, v, g, b, A_log, dt_bias, cu, scale=1.0, lower=-5.0, e
                 S = B @ S + beta[t, h] * kk @ v[t, h][None, :]
                 os_.append(S.T @ qh[t, h])
             for_heads.append(torch.stack(os_) if os_ else torch.zeros(0, D, dtype=q.dtype))
+            fin_heads.append(S)
         outs.append(torch.stack(for_heads, 1))
+        finals.append(torch.stack(fin_heads, 0))
+    if final_states is not None:
+        final_states.append(torch.stack(finals, 0))
     return torch.cat(outs, 0)

@@ -260,3 +260,94 @@ def test_backward_across_stored_state_segments():
     for gname, iname in pairs.items():
         np.testing.assert_allclose(out[gname], t[iname].grad.numpy(), rtol=1e-8, atol=1e-10,
                                    err_msg=gname)
+
+
+# ---- initial state h0, final state hT and their gradients ----
+
+def rand_states(p, seed, scale=0.5):
+    rng = np.random.default_rng(seed)
+    N = len(p["cu_seqlens"]) - 1
+    H, D = p["q"].shape[1], p["q"].shape[2]
+    return rng.standard_normal((N, H, D, D)) * scale, rng.standard_normal((N, H, D, D))
+
+
+def test_final_state_and_state_gradients_match_autograd_of_explicit_form():
+    p = rand_problem([4, 0, 6], H=2, D=5, seed=21)
+    h0, dht = rand_states(p, 22)
+    t = torch_inputs(p)
+    th0 = torch.tensor(h0, requires_grad=True)
+    names = ["q", "k", "v", "g", "beta", "A_log", "dt_bias"]
+    for n in names:
+        t[n].requires_grad_(True)
+    fin = []
+    o = explicit_forward(t["q"], t["k"], t["v"], t["g"], t["beta"], t["A_log"], t["dt_bias"],
+                         p["cu_seqlens"], scale=0.7, h0=th0, final_states=fin)
+    ((o * t["dO"]).sum() + (fin[0] * torch.tensor(dht)).sum()).backward()
+    out = run(p, scale=0.7, h0=h0, dht=dht)
+    np.testing.assert_allclose(out["o"], o.detach().numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(out["hT"], fin[0].detach().numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(out["dh0"], th0.grad.numpy(), rtol=1e-9, atol=1e-11)
+    pairs = dict(dq="q", dk="k", dv="v", dg="g", dbeta="beta", dA_log="A_log", ddt_bias="dt_bias")
+    for gname, iname in pairs.items():
+        np.testing.assert_allclose(out[gname], t[iname].grad.numpy(), rtol=1e-9, atol=1e-11,
+                                   err_msg=gname)
+    # the empty sequence passes its state through, and its gradient back
+    np.testing.assert_array_equal(out["hT"][1], h0[1])
+    np.testing.assert_array_equal(out["dh0"][1], dht[1])
+
+
+def test_splitting_a_sequence_through_its_state_changes_nothing():
+    # running [0, T) equals running [0, T1) and then [T1, T) from the first
+    # part's final state; in the backward the second part's dh0 is the first
+    # part's dhT (the recurrence is a composition of per-token maps)
+    T, T1 = 11, 4
+    p = rand_problem([T], H=2, D=4, seed=23)
+    h0, dht = rand_states(p, 24)
+    full = run(p, h0=h0, dht=dht)
+
+    def part(a, b):
+        q = {k: (v[a:b] if k not in ("A_log", "dt_bias", "cu_seqlens") else v) for k, v in p.items()}
+        q["cu_seqlens"] = np.array([0, b - a], np.int64)
+        return q
+
+    second_h0 = run(part(0, T1), dO=False, h0=h0)["hT"]
+    second = run(part(T1, T), h0=second_h0, dht=dht)
+    first = run(part(0, T1), h0=h0, dht=second["dh0"])
+    np.testing.assert_allclose(second["hT"], full["hT"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(np.concatenate([first["o"], second["o"]]), full["o"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(first["dh0"], full["dh0"], rtol=1e-11, atol=1e-12)
+    for g in ("dq", "dk", "dv", "dg", "dbeta"):
+        np.testing.assert_allclose(np.concatenate([first[g], second[g]]), full[g], rtol=1e-11,
+                                   atol=1e-12, err_msg=g)
+    for g in ("dA_log", "ddt_bias"):
+        np.testing.assert_allclose(first[g] + second[g], full[g], rtol=1e-11, atol=1e-12, err_msg=g)
+
+
+def test_beta_zero_decays_the_initial_state_channel_by_channel():
+    # beta = 0 (raw beta -> -inf): S_t = Diag(alpha_t) S_{t-1}, so
+    # hT = Diag(prod_t alpha_t) h0, o_t = S_t^T qh_t, dh0 = Diag(prod alpha) dhT
+    p = rand_problem([5], H=1, D=3, seed=25)
+    p["beta"][:] = -1e4
+    h0, dht = rand_states(p, 26)
+    out = run(p, h0=h0, dht=dht, dO=False)
+    z = np.exp(p["A_log"])[None, :, None] * (p["g"] + p["dt_bias"][None])
+    alpha = np.exp(-5.0 * expit(z))  # [T,H,D]
+    decay = alpha[:, 0].prod(0)
+    np.testing.assert_allclose(out["hT"][0, 0], decay[:, None] * h0[0, 0], rtol=1e-12, atol=1e-14)
+    qh = p["q"] / np.sqrt((p["q"] ** 2).sum(-1, keepdims=True) + 1e-6)
+    St = h0[0, 0].copy()
+    for t in range(5):
+        St = alpha[t, 0][:, None] * St
+        np.testing.assert_allclose(out["o"][t, 0], St.T @ qh[t, 0], rtol=1e-11, atol=1e-13)
+    p["dO"][:] = 0.0
+    g = run(p, h0=h0, dht=dht)
+    np.testing.assert_allclose(g["dh0"][0, 0], decay[:, None] * dht[0, 0], rtol=1e-12, atol=1e-14)
+
+
+def test_zero_state_arguments_match_the_stateless_run():
+    p = rand_problem([3, 7], H=2, D=4, seed=27)
+    N, H, D = 2, 2, 4
+    z = np.zeros((N, H, D, D))
+    a, b = run(p), run(p, h0=z, dht=z)
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
