@@ -7,7 +7,8 @@
  * "Sources and measurement configuration", for the operator configuration):
  *
  *   per packed sequence n (tokens cu_seqlens[n] .. cu_seqlens[n+1]-1) and
- *   per head h, with state S (D x D, S_0 = 0, no initial or final state):
+ *   per head h, with state S (D x D; S_0 = h0[n][h], zero unless given; the
+ *   final state S_T is returned as hT[n][h] when asked for):
  *     qh_t   = scale * q_t / sqrt(|q_t|^2 + l2_eps)
  *     kh_t   = k_t / sqrt(|k_t|^2 + l2_eps)
  *     beta_t = sigmoid(beta_raw_t)
@@ -26,6 +27,7 @@
  *   A_log, dA_log                              : [H]      fp32
  *   dt_bias, ddt_bias                          : [H, D]   fp32
  *   cu_seqlens                                 : [num_seqs + 1] int32, device
+ *   h0, hT, dhT, dh0 (optional states)         : [num_seqs, H, D, D] fp32
  *   S = cu_seqlens[num_seqs] = total_tokens; K = V = D = head_dim.
  *   Element type of the [S,H,D] and [S,H] tensors is problem->dtype.
  *
@@ -110,31 +112,41 @@ size_t kda_ctx_bytes(const kda_problem* p);
  * invalid problem. */
 size_t kda_bwd_workspace_bytes(const kda_problem* p);
 
-/* Forward. Writes o [S,H,D]. When ctx is not NULL it must hold
- * kda_ctx_bytes(p) bytes (16-byte aligned); the forward writes the state
- * checkpoints there for kda_bwd, and ctx must then stay alive and unmodified
- * until the matching kda_bwd has been enqueued. ctx == NULL runs the forward
- * alone (inference), writing no checkpoints.
- * All tensor pointers must be 16-byte aligned. */
+/* Recurrent states at the ABI (initial state h0, final state hT and their
+ * gradients dh0, dhT): fp32 [N][H][D][D], contiguous, row index = key
+ * channel i, column index = value channel j, so that one sequence's state is
+ * the D x V matrix S of the recurrence. Every state pointer is optional:
+ * NULL h0 / dhT mean zero, NULL hT / dh0 are not written. */
+
+/* Forward. Writes o [S,H,D] and, when hT is not NULL, the final states;
+ * the recurrence of sequence n, head h starts from h0[n][h] (zero when h0 is
+ * NULL). When ctx is not NULL it must hold kda_ctx_bytes(p) bytes (16-byte
+ * aligned); the forward writes the state checkpoints there for kda_bwd, and
+ * ctx must then stay alive and unmodified until the matching kda_bwd has been
+ * enqueued. ctx == NULL runs the forward alone (inference), writing no
+ * checkpoints. All tensor pointers must be 16-byte aligned. */
 kda_status kda_fwd(const kda_problem* p,
                    const void* q, const void* k, const void* v,
                    const void* g_raw, const void* beta_raw,
                    const float* A_log, const float* dt_bias,
-                   void* o, void* ctx, void* stream);
+                   const float* h0,
+                   void* o, float* hT, void* ctx, void* stream);
 
-/* Backward. Given dO [S,H,D] and the ctx written by kda_fwd on the same
- * inputs, writes dq, dk, dv, dg_raw [S,H,D], dbeta_raw [S,H] (problem
- * dtype) and dA_log [H], ddt_bias [H,D] (fp32). It recomputes the chunk
- * states, the WY factors and the gated q/k chunk by chunk from the inputs and
- * the checkpoints; no full-sequence intermediate is stored. workspace must
- * hold kda_bwd_workspace_bytes(p) bytes (16-byte aligned). */
+/* Backward. Given dO [S,H,D], the gradient of the final states dhT (zero
+ * when NULL) and the ctx written by kda_fwd on the same inputs (and the same
+ * h0: the checkpoints carry it), writes dq, dk, dv, dg_raw [S,H,D],
+ * dbeta_raw [S,H] (problem dtype), dA_log [H], ddt_bias [H,D] (fp32) and,
+ * when dh0 is not NULL, the gradient of the initial states. It recomputes
+ * the chunk states, the WY factors and the gated q/k chunk by chunk from the
+ * inputs and the checkpoints; no full-sequence intermediate is stored.
+ * workspace must hold kda_bwd_workspace_bytes(p) bytes (16-byte aligned). */
 kda_status kda_bwd(const kda_problem* p,
                    const void* q, const void* k, const void* v,
                    const void* g_raw, const void* beta_raw,
                    const float* A_log, const float* dt_bias,
-                   const void* dO, const void* ctx,
+                   const void* dO, const float* dhT, const void* ctx,
                    void* dq, void* dk, void* dv, void* dg_raw, void* dbeta_raw,
-                   float* dA_log, float* ddt_bias,
+                   float* dA_log, float* ddt_bias, float* dh0,
                    void* workspace, void* stream);
 
 /* Size of the fixed scratch buffer that kda_bwd_noalloc uses (64 MiB). */
@@ -167,9 +179,9 @@ kda_status kda_bwd_noalloc(const kda_problem* p,
                            const void* q, const void* k, const void* v,
                            const void* g_raw, const void* beta_raw,
                            const float* A_log, const float* dt_bias,
-                           const void* dO, const void* ctx,
+                           const void* dO, const float* dhT, const void* ctx,
                            void* dq, void* dk, void* dv, void* dg_raw, void* dbeta_raw,
-                           float* dA_log, float* ddt_bias, void* stream);
+                           float* dA_log, float* ddt_bias, float* dh0, void* stream);
 
 /* Reads the device status word at the head of a ctx or workspace buffer.
  * Synchronises `stream` first. Returns KDA_OK, KDA_ERR_TIMEOUT or

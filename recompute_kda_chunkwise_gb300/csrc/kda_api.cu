@@ -111,6 +111,24 @@ size_t workspace_bytes(const kda_problem* p) {
     if (!(ptr)) return fail(KDA_ERR_INVALID_ARG, "%s is NULL", #ptr);                    \
     if (!aligned16(ptr)) return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #ptr); \
   } while (0)
+#define CHECK_OPT(ptr)                                                                             \
+  do {                                                                                             \
+    if ((ptr) && !aligned16(ptr)) return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #ptr); \
+  } while (0)
+
+// Bytes of one [N][H][D][D] fp32 state tensor.
+size_t state_bytes(const kda_problem* p) {
+  return (size_t)p->num_seqs * p->num_heads * p->head_dim * p->head_dim * sizeof(float);
+}
+
+// dst = src (or zero when src is NULL): the state of a sequence without tokens.
+kda_status pass_state(float* dst, const float* src, const kda_problem* p, cudaStream_t s) {
+  if (!dst) return KDA_OK;
+  const cudaError_t e = src ? cudaMemcpyAsync(dst, src, state_bytes(p), cudaMemcpyDeviceToDevice, s)
+                            : cudaMemsetAsync(dst, 0, state_bytes(p), s);
+  return e == cudaSuccess ? KDA_OK
+                          : fail(KDA_ERR_CUDA, "state copy failed: %s", cudaGetErrorString(cudaGetLastError()));
+}
 
 }  // namespace
 
@@ -137,7 +155,7 @@ size_t kda_bwd_workspace_bytes(const kda_problem* p) {
 
 int kda_kernel_family(const kda_problem* p) { return validate(p, false) == KDA_OK ? family_of(p) : -1; }
 
-int kda_version(void) { return 100; }
+int kda_version(void) { return 200; }
 
 const char* kda_status_string(kda_status s) {
   switch (s) {
@@ -155,11 +173,12 @@ const char* kda_status_string(kda_status s) {
 const char* kda_last_error_message(void) { return g_msg; }
 
 kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
-                   const void* beta_raw, const float* A_log, const float* dt_bias, void* o, void* ctx,
-                   void* stream) {
+                   const void* beta_raw, const float* A_log, const float* dt_bias, const float* h0, void* o,
+                   float* hT, void* ctx, void* stream) {
   kda_status st = validate(p);
   if (st != KDA_OK) return st;
-  if (p->total_tokens == 0) return KDA_OK;  // nothing to compute or write
+  CHECK_OPT(h0); CHECK_OPT(hT);
+  if (p->total_tokens == 0) return pass_state(hT, h0, p, (cudaStream_t)stream);  // hT = h0
   CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(g_raw); CHECK_PTR(beta_raw);
   CHECK_PTR(A_log); CHECK_PTR(dt_bias); CHECK_PTR(o);
   if (ctx && !aligned16(ctx)) return fail(KDA_ERR_INVALID_ARG, "ctx is not 16-byte aligned");
@@ -167,6 +186,8 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
   kda::FwdArgs a;
   a.q = q; a.k = k; a.v = v; a.g = g_raw; a.b = beta_raw; a.A_log = A_log; a.dt_bias = dt_bias;
   a.o = o;
+  a.h0 = h0;
+  a.hT = hT;
   a.ckpt = ctx ? (float*)((char*)ctx + kda::kHeaderBytes) : nullptr;
   a.status = ctx ? (int*)ctx : nullptr;
   a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
@@ -187,17 +208,19 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
 
 kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
                    const void* beta_raw, const float* A_log, const float* dt_bias, const void* dO,
-                   const void* ctx, void* dq, void* dk, void* dv, void* dg_raw, void* dbeta_raw,
-                   float* dA_log, float* ddt_bias, void* workspace, void* stream) {
+                   const float* dhT, const void* ctx, void* dq, void* dk, void* dv, void* dg_raw,
+                   void* dbeta_raw, float* dA_log, float* ddt_bias, float* dh0, void* workspace,
+                   void* stream) {
   kda_status st = validate(p);
   if (st != KDA_OK) return st;
+  CHECK_OPT(dhT); CHECK_OPT(dh0);
   cudaStream_t s = (cudaStream_t)stream;
-  if (p->total_tokens == 0) {  // no tokens: the parameter gradients are zero
+  if (p->total_tokens == 0) {  // no tokens: zero parameter gradients, dh0 = dhT
     CHECK_PTR(dA_log); CHECK_PTR(ddt_bias);
     if (cudaMemsetAsync(dA_log, 0, sizeof(float) * p->num_heads, s) != cudaSuccess ||
         cudaMemsetAsync(ddt_bias, 0, sizeof(float) * p->num_heads * p->head_dim, s) != cudaSuccess)
       return fail(KDA_ERR_CUDA, "memset failed: %s", cudaGetErrorString(cudaGetLastError()));
-    return KDA_OK;
+    return pass_state(dh0, dhT, p, s);
   }
   CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(g_raw); CHECK_PTR(beta_raw);
   CHECK_PTR(A_log); CHECK_PTR(dt_bias); CHECK_PTR(dO); CHECK_PTR(ctx);
@@ -206,6 +229,8 @@ kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const voi
   kda::BwdArgs a;
   a.q = q; a.k = k; a.v = v; a.g = g_raw; a.b = beta_raw; a.A_log = A_log; a.dt_bias = dt_bias;
   a.dO = dO;
+  a.dhT = dhT;
+  a.dh0 = dh0;
   a.ckpt = (const float*)((const char*)ctx + kda::kHeaderBytes);
   a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg_raw; a.db = dbeta_raw;
   a.dA_log = dA_log; a.ddt_bias = ddt_bias;

@@ -27,6 +27,8 @@ struct FwdArgs {
   const float* A_log;
   const float* dt_bias;
   void* o;
+  const float* h0;  // initial states [N][H][D][D] (NULL: zero)
+  float* hT;        // final states (NULL: not written)
   float* ckpt;  // NULL: no checkpoints
   int* status;  // NULL when ckpt is NULL
   const int32_t* cu;
@@ -48,6 +50,8 @@ struct BwdArgs {
   const float* A_log;
   const float* dt_bias;
   const void* dO;
+  const float* dhT;  // gradient of the final states [N][H][D][D] (NULL: zero)
+  float* dh0;        // gradient of the initial states (NULL: not written)
   const float* ckpt;
   void* dq;
   void* dk;

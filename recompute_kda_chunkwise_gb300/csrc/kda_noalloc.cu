@@ -59,11 +59,13 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const void* k, const void* v,
                                       const void* g_raw, const void* beta_raw, const float* A_log,
-                                      const float* dt_bias, const void* dO, const void* ctx, void* dq, void* dk,
-                                      void* dv, void* dg_raw, void* dbeta_raw, float* dA_log, float* ddt_bias,
-                                      void* stream) {
+                                      const float* dt_bias, const void* dO, const float* dhT, const void* ctx,
+                                      void* dq, void* dk, void* dv, void* dg_raw, void* dbeta_raw,
+                                      float* dA_log, float* ddt_bias, float* dh0, void* stream) {
   kda_status st = kda::validate_problem(p);
   if (st != KDA_OK) return st;
+  if ((dhT && !aligned16(dhT)) || (dh0 && !aligned16(dh0)))
+    return kda::set_error(KDA_ERR_INVALID_ARG, "dhT / dh0 is not 16-byte aligned");
   const void* ptrs[] = {q, k, v, g_raw, beta_raw, A_log, dt_bias, dO, ctx, dq, dk, dv, dg_raw, dbeta_raw,
                         dA_log, ddt_bias};
   const char* names[] = {"q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias", "dO", "ctx", "dq", "dk", "dv",
@@ -89,6 +91,13 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
     if (cudaMemsetAsync(dA_log, 0, sizeof(float) * p->num_heads, s) != cudaSuccess ||
         cudaMemsetAsync(ddt_bias, 0, sizeof(float) * p->num_heads * p->head_dim, s) != cudaSuccess)
       return kda::set_error(KDA_ERR_CUDA, "memset failed: %s", cudaGetErrorString(cudaGetLastError()));
+    if (dh0) {  // no tokens: dh0 = dhT
+      const size_t sb = (size_t)p->num_seqs * p->num_heads * p->head_dim * p->head_dim * sizeof(float);
+      const cudaError_t e = dhT ? cudaMemcpyAsync(dh0, dhT, sb, cudaMemcpyDeviceToDevice, s)
+                                : cudaMemsetAsync(dh0, 0, sb, s);
+      if (e != cudaSuccess)
+        return kda::set_error(KDA_ERR_CUDA, "state copy failed: %s", cudaGetErrorString(cudaGetLastError()));
+    }
     return KDA_OK;
   }
   void* scratch = nullptr;
@@ -106,6 +115,8 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
   kda::BwdArgs a;
   a.q = q; a.k = k; a.v = v; a.g = g_raw; a.b = beta_raw; a.A_log = A_log; a.dt_bias = dt_bias;
   a.dO = dO;
+  a.dhT = dhT;
+  a.dh0 = dh0;
   a.ckpt = (const float*)((const char*)ctx + kda::kHeaderBytes);
   a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg_raw; a.db = dbeta_raw;
   a.dA_log = dA_log; a.ddt_bias = ddt_bias;

@@ -271,7 +271,9 @@ __global__ void __launch_bounds__(kNT, 1) kda_fwd_simt_kernel(const FwdArgs a) {
   const Tin* b = static_cast<const Tin*>(a.b);
   Tin* o = static_cast<Tin*>(a.o);
   for (int i = tid; i < D; i += kNT) t.dtb[i] = a.dt_bias[h * D + i];
-  for (int x = tid; x < D * V; x += kNT) Hs[x] = 0.f;
+  // initial state h0 [N][H][D][V] (zero when NULL)
+  const float* h0 = a.h0 ? a.h0 + (int64_t)blockIdx.x * (D * V) : nullptr;
+  for (int x = tid; x < D * V; x += kNT) Hs[x] = h0 ? h0[x] : 0.f;
   const float expA = expf(a.A_log[h]);
   __syncthreads();
   for (int64_t t0 = bos; t0 < eos; t0 += C) {
@@ -286,6 +288,11 @@ __global__ void __launch_bounds__(kNT, 1) kda_fwd_simt_kernel(const FwdArgs a) {
     state_residual<D, C>(t, Hs, V);
     chunk_output<Tin, D, C>(t, Hs, V, o, t0, rows, h, a.H);
     state_update<D, C>(t, Hs, V);
+  }
+  if (a.hT != nullptr) {  // final state
+    __syncthreads();
+    float* dst = a.hT + (int64_t)blockIdx.x * (D * V);
+    for (int x = tid; x < D * V; x += kNT) dst[x] = Hs[x];
   }
 }
 
@@ -346,7 +353,12 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
     const int nseg = (int)((T + kCkptTokens - 1) / kCkptTokens);
     const float expA = expf(a.A_log[h]);
     for (int i = tid; i < D; i += kNT) t.dtb[i] = a.dt_bias[h * D + i];
-    for (int x = tid; x < D * LDH; x += kNT) u.dH[x] = 0.f;
+    // dH = dhT, the gradient of the final state (zero when NULL)
+    const float* dhT = a.dhT ? a.dhT + (int64_t)item * (D * V) : nullptr;
+    for (int x = tid; x < D * LDH; x += kNT) {
+      const int i = x / LDH, j = x % LDH;
+      u.dH[x] = (dhT != nullptr && j < V) ? dhT[i * V + j] : 0.f;
+    }
     float acc_dtb = 0.f, acc_alog = 0.f;  // thread owns column tid % D
     __syncthreads();
 
@@ -612,6 +624,10 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
       __syncthreads();
     }
     if (tid == 0) a.partial[(int64_t)item * (D + 1) + D] = u.red[0];
+    if (a.dh0 != nullptr) {  // the gradient of the initial state
+      float* dst = a.dh0 + (int64_t)item * (D * V);
+      for (int x = tid; x < D * V; x += kNT) dst[x] = u.dH[(x / V) * LDH + (x % V)];
+    }
     __syncthreads();
   }
 }

@@ -100,6 +100,8 @@ struct TcBwdArgs {
   const float* A_log;
   const float* dt_bias;
   const float* ckpt;
+  const float* dhT;  // gradient of the final states [N][H][D][D] (NULL: zero)
+  float* dh0;        // gradient of the initial states (NULL: not written)
   __nv_bfloat16 *dq, *dk, *dv, *dg, *db;
   float* partial;
   uint8_t* scratch;  // fp16 chunk-start state tiles (per CTA, or per item and level parity)
@@ -285,14 +287,32 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
         acc_alog = 0.f;
         open = true;
         seg = nseg - 1;
-        // dH' = 0 (TMEM state and its fp16 operand copy)
-        float z[32];
+        // dH' = dhT, the gradient of the final state, or zero (TMEM state and its
+        // fp16 operand copy; lane = value channel L, columns = key channel)
+        if (a.dhT != nullptr) {
+          const float* src = a.dhT + static_cast<int64_t>(item) * (kD * kD);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = 0.f;
-        tmem_st32(tmem + tlane + TM_DH + 64 * hh, z);
-        tmem_st32(tmem + tlane + TM_DH + 64 * hh + 32, z);
-        tmem_st_wait();
-        for (int x = tid; x < 32768 / 16; x += kT) reinterpret_cast<uint4*>(sm + OFF_A1D)[x] = make_uint4(0, 0, 0, 0);
+          for (int half = 0; half < 2; ++half) {
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = src[(64 * hh + 32 * half + j) * kD + L];
+            tmem_st32(tmem + tlane + TM_DH + 64 * hh + 32 * half, x);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+              *reinterpret_cast<uint4*>(sm + OFF_A1D + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
+                  make_uint4(pack_h2(x[8 * cc], x[8 * cc + 1]), pack_h2(x[8 * cc + 2], x[8 * cc + 3]),
+                             pack_h2(x[8 * cc + 4], x[8 * cc + 5]), pack_h2(x[8 * cc + 6], x[8 * cc + 7]));
+          }
+          tmem_st_wait();
+        } else {
+          float z[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) z[j] = 0.f;
+          tmem_st32(tmem + tlane + TM_DH + 64 * hh, z);
+          tmem_st32(tmem + tlane + TM_DH + 64 * hh + 32, z);
+          tmem_st_wait();
+          for (int x = tid; x < 32768 / 16; x += kT) reinterpret_cast<uint4*>(sm + OFF_A1D)[x] = make_uint4(0, 0, 0, 0);
+        }
       }
     } else {
       // claim the next job (a counter after the items' hand-off counters): a
@@ -1128,7 +1148,18 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
       --seg;
       continue;
     }
-    // ---- item done: per-(sequence, head) partial sums of the gate-parameter gradients ----
+    // ---- item done: the gradient of the initial state (dH of the first chunk's start) ----
+    if (a.dh0 != nullptr) {
+      float* dst = a.dh0 + static_cast<int64_t>(item) * (kD * kD);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float x[32];
+        tmem_ld32(tmem + tlane + TM_DH + 64 * hh + 32 * half, x);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dst[(64 * hh + 32 * half + j) * kD + L] = x[j];
+      }
+    }
+    // ---- and per-(sequence, head) partial sums of the gate-parameter gradients ----
     float* R = S + S_TOT;  // 256 floats
     R[tid] = acc_dtb;
     __syncthreads();
@@ -1187,6 +1218,8 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   t.A_log = a.A_log;
   t.dt_bias = a.dt_bias;
   t.ckpt = a.ckpt;
+  t.dhT = a.dhT;
+  t.dh0 = a.dh0;
   t.dq = static_cast<__nv_bfloat16*>(a.dq);
   t.dk = static_cast<__nv_bfloat16*>(a.dk);
   t.dv = static_cast<__nv_bfloat16*>(a.dv);

@@ -111,6 +111,8 @@ struct TcFwdArgs {
   const float* A_log;
   const float* dt_bias;
   __nv_bfloat16* o;
+  const float* h0;  // initial states [N][H][D][D] (NULL: zero)
+  float* hT;        // final states (NULL: not written)
   float* ckpt;
   int* status;
   const int32_t* cu;
@@ -287,9 +289,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // row-major role (operand tiles): k rows (q4 < 2) or q rows (q4 >= 2)
   const bool krole = q4 < 2;
   const int prow = 32 * (q4 & 1) + lane, pI = prow >> 4;
-  float Hst[64];
+  float Hst[64];  // H[64 hh + j][lrow]
 #pragma unroll
   for (int j = 0; j < 64; ++j) Hst[j] = 0.f;
+  if (!helper && a.h0 != nullptr) {  // initial state: registers and its fp16 operand tile
+    const float* src = a.h0 + static_cast<int64_t>(item) * (kD * kD);
+#pragma unroll
+    for (int j = 0; j < 64; ++j) Hst[j] = src[(64 * hh + j) * kD + lrow];
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc)
+      *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(lrow, 8 * hh + cc, 128)) =
+          make_uint4(pack_h2(Hst[8 * cc], Hst[8 * cc + 1]), pack_h2(Hst[8 * cc + 2], Hst[8 * cc + 3]),
+                     pack_h2(Hst[8 * cc + 4], Hst[8 * cc + 5]), pack_h2(Hst[8 * cc + 6], Hst[8 * cc + 7]));
+  }
   uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0, ph_odd = 0, ph_r2 = 0, ph_x = 0;
   bool x_pending = false;  // a hand-over load into shared memory is in flight
 
@@ -807,6 +819,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_before_sync();
     KDA_SYNC_OR_BAIL();
   }
+  if (!helper && a.hT != nullptr) {  // final state
+    float* dst = a.hT + static_cast<int64_t>(item) * (kD * kD);
+#pragma unroll
+    for (int j = 0; j < 64; ++j) dst[(64 * hh + j) * kD + lrow] = Hst[j];
+  }
 #undef KDA_WAIT
 #undef KDA_SYNC_OR_BAIL
 teardown:
@@ -872,6 +889,8 @@ kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s)
   t.A_log = a.A_log;
   t.dt_bias = a.dt_bias;
   t.o = static_cast<__nv_bfloat16*>(a.o);
+  t.h0 = a.h0;
+  t.hT = a.hT;
   t.ckpt = a.ckpt;
   t.status = a.status;
   t.cu = a.cu;

@@ -112,3 +112,19 @@ def make_inputs(w: Workload, device="cpu", with_dO: bool = True) -> dict:
         out["dt_bias"] = torch.zeros((H, D), device=dev)
     out["cu_seqlens"] = cu_seqlens_of(w.lengths, dev)
     return out
+
+
+def make_states(w: Workload, device="cpu", seed_offset: int = 1000, dht_std: float = 0.05) -> dict:
+    """Seeded initial states h0 ~ N(0, 0.5^2) and final-state gradients
+    dht ~ N(0, dht_std^2), both [N, H, D, D] float32 (rows: key channel),
+    drawn from their own generator (seed = workload seed + seed_offset).
+    0.05 is the size of the state gradient inside a sequence at these
+    workloads (entries of order 0.01 - 0.1), i.e. what a following segment's
+    initial-state gradient hands back."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(w.seed) + seed_offset)
+    shape = (w.num_seqs, w.H, w.D, w.D)
+    h0 = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * 0.5
+    dht = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * dht_std
+    return {"h0": h0, "dht": dht}

@@ -58,11 +58,11 @@ def load_library(path: str = LIB_PATH):
             lib.kda_bwd_workspace_bytes.restype = ctypes.c_size_t
             lib.kda_bwd_workspace_bytes.argtypes = [P]
             lib.kda_fwd.restype = ctypes.c_int
-            lib.kda_fwd.argtypes = [P] + [vp] * 10
+            lib.kda_fwd.argtypes = [P] + [vp] * 12
             lib.kda_bwd.restype = ctypes.c_int
-            lib.kda_bwd.argtypes = [P] + [vp] * 18
+            lib.kda_bwd.argtypes = [P] + [vp] * 20
             lib.kda_bwd_noalloc.restype = ctypes.c_int
-            lib.kda_bwd_noalloc.argtypes = [P] + [vp] * 17
+            lib.kda_bwd_noalloc.argtypes = [P] + [vp] * 19
             lib.kda_query_device_status.restype = ctypes.c_int
             lib.kda_query_device_status.argtypes = [vp, vp]
             lib.kda_status_string.restype = ctypes.c_char_p
@@ -137,13 +137,37 @@ def _check_tensors(q, *others, params=()):
             raise ValueError("A_log and dt_bias must be contiguous float32 CUDA tensors")
 
 
+def _check_state(t, q, cu_seqlens, name):
+    """States are fp32 [N, H, D, D] (rows: key channel), contiguous, on q's device."""
+    if t is None:
+        return
+    S, H, D = q.shape
+    want = (cu_seqlens.numel() - 1, H, D, D)
+    if (not t.is_cuda or not t.is_contiguous() or t.dtype != torch.float32 or t.device != q.device
+            or tuple(t.shape) != want):
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape {want}")
+
+
+def _state_like(q, cu_seqlens):
+    S, H, D = q.shape
+    return torch.empty((cu_seqlens.numel() - 1, H, D, D), dtype=torch.float32, device=q.device)
+
+
 def kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
             lower_bound: float = -5.0, eps: float = 1e-6, save_ctx: bool = True, out=None,
-            ctx=None, flags: int = 0):
+            ctx=None, flags: int = 0, h0=None, final_state=False):
     """Forward. Returns (o, ctx); ctx is None when save_ctx is False. ``out``
-    and ``ctx`` may be preallocated (ctx of at least ctx_bytes(problem))."""
+    and ``ctx`` may be preallocated (ctx of at least ctx_bytes(problem)).
+    h0: initial states [N, H, D, D] fp32 (zero when None). With final_state
+    True (or a preallocated [N, H, D, D] fp32 tensor) the final states are
+    returned too: (o, ctx, hT)."""
     _check_tensors(q, k, v, g, beta, params=(A_log, dt_bias))
+    _check_state(h0, q, cu_seqlens, "h0")
     p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps, flags)
+    hT = None
+    if final_state is not False and final_state is not None:
+        hT = _state_like(q, cu_seqlens) if final_state is True else final_state
+        _check_state(hT, q, cu_seqlens, "final_state")
     o = torch.empty_like(q) if out is None else out
     if not save_ctx:
         ctx = None
@@ -152,50 +176,63 @@ def kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
     elif ctx.numel() * ctx.element_size() < ctx_bytes(p):
         raise ValueError("ctx buffer too small")
     st = load_library().kda_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                                _ptr(A_log), _ptr(dt_bias), _ptr(o), _ptr(ctx), _stream_handle(q.device))
+                                _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(o), _ptr(hT), _ptr(ctx),
+                                _stream_handle(q.device))
     _check(st, "kda_fwd")
-    return o, ctx
+    return (o, ctx) if hT is None else (o, ctx, hT)
 
 
-def kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO, ctx, *, scale: float = 1.0,
-            lower_bound: float = -5.0, eps: float = 1e-6, workspace=None, outs=None,
-            flags: int = 0):
-    """Backward. Returns dict dq, dk, dv, dg, dbeta, dA_log, ddt_bias."""
-    _check_tensors(q, k, v, g, beta, dO, params=(A_log, dt_bias))
-    p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps, flags)
+def _grad_outs(outs, q, k, v, g, beta, A_log, dt_bias, cu_seqlens, want_dh0):
     if outs is None:
         outs = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                     dg=torch.empty_like(g), dbeta=torch.empty_like(beta),
                     dA_log=torch.empty_like(A_log), ddt_bias=torch.empty_like(dt_bias))
+    if want_dh0 and outs.get("dh0") is None:
+        outs["dh0"] = _state_like(q, cu_seqlens)
+    _check_state(outs.get("dh0"), q, cu_seqlens, "dh0")
+    return outs
+
+
+def kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO, ctx, *, scale: float = 1.0,
+            lower_bound: float = -5.0, eps: float = 1e-6, workspace=None, outs=None,
+            flags: int = 0, dht=None, want_dh0: bool = False):
+    """Backward. Returns dict dq, dk, dv, dg, dbeta, dA_log, ddt_bias, and dh0
+    (the initial-state gradient) when want_dh0. dht: gradient of the final
+    states [N, H, D, D] fp32 (zero when None). ctx must come from a forward
+    with the same h0."""
+    _check_tensors(q, k, v, g, beta, dO, params=(A_log, dt_bias))
+    _check_state(dht, q, cu_seqlens, "dht")
+    p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps, flags)
+    outs = _grad_outs(outs, q, k, v, g, beta, A_log, dt_bias, cu_seqlens, want_dh0)
     if workspace is None:
         workspace = torch.empty(workspace_bytes(p), dtype=torch.uint8, device=q.device)
     elif workspace.numel() * workspace.element_size() < workspace_bytes(p):
         raise ValueError("workspace buffer too small")
     st = load_library().kda_bwd(
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
-        _ptr(dO), _ptr(ctx), _ptr(outs["dq"]), _ptr(outs["dk"]), _ptr(outs["dv"]), _ptr(outs["dg"]),
-        _ptr(outs["dbeta"]), _ptr(outs["dA_log"]), _ptr(outs["ddt_bias"]), _ptr(workspace),
-        _stream_handle(q.device))
+        _ptr(dO), _ptr(dht), _ptr(ctx), _ptr(outs["dq"]), _ptr(outs["dk"]), _ptr(outs["dv"]),
+        _ptr(outs["dg"]), _ptr(outs["dbeta"]), _ptr(outs["dA_log"]), _ptr(outs["ddt_bias"]),
+        _ptr(outs.get("dh0")), _ptr(workspace), _stream_handle(q.device))
     _check(st, "kda_bwd")
     return outs
 
 
 def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO, ctx, *, scale: float = 1.0,
-                    lower_bound: float = -5.0, eps: float = 1e-6, outs=None):
+                    lower_bound: float = -5.0, eps: float = 1e-6, outs=None, dht=None,
+                    want_dh0: bool = False):
     """Backward through kda_bwd_noalloc: no workspace, the library's fixed
     scratch array is used instead (for callers that cannot allocate device
     memory at this point; calls must not overlap on the GPU). Returns the
     same dict as kda_bwd."""
     _check_tensors(q, k, v, g, beta, dO, params=(A_log, dt_bias))
+    _check_state(dht, q, cu_seqlens, "dht")
     p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps)
-    if outs is None:
-        outs = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
-                    dg=torch.empty_like(g), dbeta=torch.empty_like(beta),
-                    dA_log=torch.empty_like(A_log), ddt_bias=torch.empty_like(dt_bias))
+    outs = _grad_outs(outs, q, k, v, g, beta, A_log, dt_bias, cu_seqlens, want_dh0)
     st = load_library().kda_bwd_noalloc(
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
-        _ptr(dO), _ptr(ctx), _ptr(outs["dq"]), _ptr(outs["dk"]), _ptr(outs["dv"]), _ptr(outs["dg"]),
-        _ptr(outs["dbeta"]), _ptr(outs["dA_log"]), _ptr(outs["ddt_bias"]), _stream_handle(q.device))
+        _ptr(dO), _ptr(dht), _ptr(ctx), _ptr(outs["dq"]), _ptr(outs["dk"]), _ptr(outs["dv"]),
+        _ptr(outs["dg"]), _ptr(outs["dbeta"]), _ptr(outs["dA_log"]), _ptr(outs["ddt_bias"]),
+        _ptr(outs.get("dh0")), _stream_handle(q.device))
     _check(st, "kda_bwd_noalloc")
     return outs
 
@@ -209,24 +246,31 @@ class KDAFunction(torch.autograd.Function):
     """Autograd wrapper: forward saves the inputs and the checkpoint ctx only."""
 
     @staticmethod
-    def forward(actx, q, k, v, g, beta, A_log, dt_bias, cu_seqlens, scale, lower_bound, eps):
-        o, ctx = kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, scale=scale,
-                         lower_bound=lower_bound, eps=eps, save_ctx=True)
+    def forward(actx, q, k, v, g, beta, A_log, dt_bias, cu_seqlens, h0, output_final_state, scale,
+                lower_bound, eps):
+        r = kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, scale=scale, lower_bound=lower_bound,
+                    eps=eps, save_ctx=True, h0=h0, final_state=bool(output_final_state))
+        o, ctx = r[0], r[1]
         actx.save_for_backward(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, ctx)
-        actx.args = (scale, lower_bound, eps)
-        return o
+        actx.args = (scale, lower_bound, eps, h0 is not None, bool(output_final_state))
+        return (o, r[2]) if output_final_state else o
 
     @staticmethod
-    def backward(actx, dO):
+    def backward(actx, dO, dht=None):
         q, k, v, g, beta, A_log, dt_bias, cu_seqlens, ctx = actx.saved_tensors
-        scale, lower_bound, eps = actx.args
+        scale, lower_bound, eps, has_h0, _ = actx.args
         r = kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO.contiguous(), ctx,
-                    scale=scale, lower_bound=lower_bound, eps=eps)
+                    scale=scale, lower_bound=lower_bound, eps=eps,
+                    dht=None if dht is None else dht.contiguous(), want_dh0=has_h0)
         return (r["dq"], r["dk"], r["dv"], r["dg"], r["dbeta"], r["dA_log"], r["ddt_bias"],
-                None, None, None, None)
+                None, r.get("dh0"), None, None, None, None)
 
 
 def kda(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, scale: float = 1.0,
-        lower_bound: float = -5.0, eps: float = 1e-6):
-    """Differentiable KDA over packed sequences (see include/kda.h)."""
-    return KDAFunction.apply(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, scale, lower_bound, eps)
+        lower_bound: float = -5.0, eps: float = 1e-6, initial_state=None,
+        output_final_state: bool = False):
+    """Differentiable KDA over packed sequences (see include/kda.h). With
+    initial_state ([N, H, D, D] fp32) the recurrences start from it; with
+    output_final_state the call returns (o, final_state)."""
+    return KDAFunction.apply(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, initial_state,
+                             output_final_state, scale, lower_bound, eps)

@@ -65,25 +65,34 @@ def test_invalid_arguments_are_rejected_on_host(lib):
     cu = torch.tensor([0, 16], dtype=torch.int32)  # host tensor: never dereferenced
     p = K.make_problem(16, 1, 2, 64, torch.bfloat16, cu)
     nul = ctypes.c_void_p(0)
-    st = lib.kda_fwd(ctypes.byref(p), nul, nul, nul, nul, nul, nul, nul, nul, nul, nul)
+    # kda_fwd(p, q, k, v, g, beta, A_log, dt_bias, h0, o, hT, ctx, stream)
+    st = lib.kda_fwd(ctypes.byref(p), *([nul] * 12))
     assert st == 1  # KDA_ERR_INVALID_ARG
     assert b"NULL" in lib.kda_last_error_message()
     mis = ctypes.c_void_p(0x1008)  # not 16-byte aligned
     al = ctypes.c_void_p(0x1000)
-    st = lib.kda_fwd(ctypes.byref(p), mis, al, al, al, al, al, al, al, nul, nul)
+    st = lib.kda_fwd(ctypes.byref(p), mis, *([al] * 6), nul, al, nul, nul, nul)
     assert st == 1 and b"aligned" in lib.kda_last_error_message()
+    st = lib.kda_fwd(ctypes.byref(p), *([al] * 7), mis, al, nul, nul, nul)  # misaligned h0
+    assert st == 1 and b"h0" in lib.kda_last_error_message()
+    st = lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, mis, nul, nul)  # misaligned hT
+    assert st == 1 and b"hT" in lib.kda_last_error_message()
     p.gate_lower_bound = -8.0
-    st = lib.kda_fwd(ctypes.byref(p), al, al, al, al, al, al, al, al, nul, nul)
+    st = lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, nul, nul)
     assert st == 2  # KDA_ERR_UNSUPPORTED
     p.gate_lower_bound = -5.0
     p.num_seqs = 0
-    assert lib.kda_bwd(ctypes.byref(p), *([al] * 17), nul) == 1
+    # kda_bwd(p, q, k, v, g, beta, A_log, dt_bias, dO, dhT, ctx, dq, dk, dv, dg, dbeta,
+    #         dA_log, ddt_bias, dh0, workspace, stream)
+    assert lib.kda_bwd(ctypes.byref(p), *([al] * 19), nul) == 1
     p.num_seqs = 1
+    st = lib.kda_bwd(ctypes.byref(p), *([al] * 8), mis, *([al] * 10), nul)  # misaligned dhT
+    assert st == 1 and b"dhT" in lib.kda_last_error_message()
     p.dtype = 7
-    assert lib.kda_fwd(ctypes.byref(p), *([al] * 8), nul, nul) == 2
+    assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, nul, nul) == 2
     p.dtype = 0
     p.flags = 4  # no such flag
-    assert lib.kda_fwd(ctypes.byref(p), *([al] * 8), nul, nul) == 1
+    assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, nul, nul) == 1
     assert b"unknown flags" in lib.kda_last_error_message()
     p.flags = K.KDA_FLAG_FORCE_SIMT | K.KDA_FLAG_TEST_TIMEOUT  # both known: sizes still answer
     assert lib.kda_ctx_bytes(ctypes.byref(p)) > 0
@@ -92,4 +101,4 @@ def test_invalid_arguments_are_rejected_on_host(lib):
 def test_status_strings(lib):
     for i, name in enumerate(K.STATUS_NAMES):
         assert lib.kda_status_string(i).decode() == name
-    assert lib.kda_version() >= 100
+    assert lib.kda_version() >= 200

@@ -46,6 +46,8 @@ def test_noalloc_rejects_problems_beyond_its_buffer():
     import ctypes
     lib = K.load_library()
     al = ctypes.c_void_p(1 << 20)
-    st = lib.kda_bwd_noalloc(ctypes.byref(p), *([al] * 16), None)
+    # (p, q, k, v, g, beta, A_log, dt_bias, dO, dhT, ctx, dq, dk, dv, dg, dbeta, dA_log,
+    #  ddt_bias, dh0, stream)
+    st = lib.kda_bwd_noalloc(ctypes.byref(p), *([al] * 8), None, al, *([al] * 7), None, None)
     assert st == 3  # KDA_ERR_WORKSPACE
     assert b"fixed buffer" in lib.kda_last_error_message()
