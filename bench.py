@@ -217,6 +217,94 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+FWD_METRIC = "KDA forward (inference, no checkpoints) tokens/sec"
+
+
+def run_gb300_fwd(args, w, rank, world, local):
+    """Forward-only inference: kda_fwd with KDA_FLAG_NO_CHECKPOINTS (the ctx
+    holds only the status word and the helper hand-off area)."""
+    import torch
+    from recompute_kda_chunkwise_gb300 import make_inputs
+    from recompute_kda_chunkwise_gb300 import kda as K
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    K.load_library()
+    inp = make_inputs(w, device=dev, with_dO=False)
+    q, k, v, g, beta, A_log, dt_bias, cu = (inp[n] for n in
+                                            ["q", "k", "v", "g", "beta", "A_log", "dt_bias", "cu_seqlens"])
+    prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale,
+                          flags=K.KDA_FLAG_NO_CHECKPOINTS)
+    kname = {0: "simt", 1: "tc"}.get(K.kernel_family(prob), "unknown")
+    scratch = torch.empty(K.ctx_bytes(prob), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        K.kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu, scale=w.scale, save_ctx=False, out=o, ctx=scratch)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms_step = max_over_ranks(start.elapsed_time(end)) / args.steps
+    tokens = w.total_tokens * world
+    fwd_b, _ = algorithmic_bytes(w)
+    peak_gbs, peak_kind = measured_peaks()
+    achieved = fwd_b / (ms_step / 1e3) / 1e9
+    e2e = None
+    if args.e2e_steps > 0:  # pinned host inputs -> device -> forward -> host o
+        names_in = ["q", "k", "v", "g", "beta"]
+        host_in = {n: torch.empty(inp[n].shape, dtype=inp[n].dtype, pin_memory=True) for n in names_in}
+        for n in names_in:
+            host_in[n].copy_(inp[n])
+        host_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+
+        def e2e_step():
+            for n in names_in:
+                inp[n].copy_(host_in[n], non_blocking=True)
+            step()
+            host_o.copy_(o, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        dt = max_over_ranks(time.perf_counter() - t0) / args.e2e_steps
+        e2e = {"value": tokens / dt, "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in.values()),
+               "d2h_bytes_per_step": host_o.numel() * host_o.element_size()}
+    if rank == 0:
+        line = {"metric": FWD_METRIC, "value": tokens / (ms_step / 1e3), "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+                "data": "synthetic",
+                "config": {"workload": w.name, "num_seqs": w.num_seqs, "seq_lens": list(w.lengths)[:16],
+                           "heads": w.H, "head_dim": w.D, "pass": "forward (inference)",
+                           "l2_flush": "none needed: inputs (%.1f GB) exceed L2" % (fwd_b / 1e9)
+                           if fwd_b > 2 * 129e6 else "inputs below L2 size: not flushed (context only)",
+                           "parallelism": f"replicas{world}", "kernel_family": kname},
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
+                             "frac": achieved / peak_gbs, "traffic": None, "kernel": f"kda_fwd ({kname} kernels)",
+                             "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": fwd_b,
+                             "ms_per_launch": ms_step},
+                "cpu_baseline": None, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk.summary(),
+                "device_status_ok": K.query_device_status(scratch) == 0}
+        print(json.dumps(line), flush=True)
+
+
 def run_gb300(args, w, rank, world, local):
     import torch
     from recompute_kda_chunkwise_gb300 import make_inputs
@@ -356,6 +444,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default=None)
+    ap.add_argument("--pass", dest="pass_", choices=["fwdbwd", "fwd"], default="fwdbwd",
+                    help="fwd: forward-only inference (no checkpoints); the default times fwd+bwd")
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--sample-tokens", type=int, default=65536)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -365,6 +455,8 @@ def main(argv=None):
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, w, rank)
+    elif args.pass_ == "fwd":
+        run_gb300_fwd(args, w, rank, world, local)
     else:
         run_gb300(args, w, rank, world, local)
     import torch.distributed as dist

@@ -83,6 +83,13 @@ typedef enum {
  * o is not written. kda_query_device_status(ctx) then reports the timeout and
  * the context stays usable. Ignored by the CUDA-core kernels. */
 #define KDA_FLAG_TEST_TIMEOUT 2
+/* Inference: kda_fwd writes no state checkpoints. ctx (optional, of
+ * kda_ctx_bytes(p) bytes with this flag set, which leaves the checkpoints
+ * out) then only holds the status word and, when the tensor-core forward
+ * runs with helper CTAs, their hand-off area, so the forward keeps that
+ * speed-up without a checkpoint buffer. Such a ctx cannot feed kda_bwd, which
+ * rejects the flag. */
+#define KDA_FLAG_NO_CHECKPOINTS 4
 
 /* Problem description. cu_seqlens is a DEVICE pointer; the library never
  * reads it on the host (so no synchronisation), and trusts that it is

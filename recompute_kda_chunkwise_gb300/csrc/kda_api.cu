@@ -34,7 +34,7 @@ kda_status validate(const kda_problem* p, bool need_ptrs = true) {
   if (p->num_seqs < 1) return fail(KDA_ERR_INVALID_ARG, "num_seqs must be >= 1 (got %d)", p->num_seqs);
   if (p->num_heads < 1) return fail(KDA_ERR_INVALID_ARG, "num_heads must be >= 1 (got %d)", p->num_heads);
   if (p->total_tokens < 0) return fail(KDA_ERR_INVALID_ARG, "total_tokens must be >= 0");
-  if ((p->flags & ~(KDA_FLAG_FORCE_SIMT | KDA_FLAG_TEST_TIMEOUT)) != 0)
+  if ((p->flags & ~(KDA_FLAG_FORCE_SIMT | KDA_FLAG_TEST_TIMEOUT | KDA_FLAG_NO_CHECKPOINTS)) != 0)
     return fail(KDA_ERR_INVALID_ARG, "unknown flags 0x%x", p->flags);
   if (need_ptrs && !p->cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is NULL");
   if (p->dtype != KDA_DTYPE_BF16 && p->dtype != KDA_DTYPE_F32)
@@ -63,6 +63,7 @@ size_t ckpt_slots(const kda_problem* p) {
 }
 
 size_t ckpt_bytes(const kda_problem* p) {
+  if (p->flags & KDA_FLAG_NO_CHECKPOINTS) return 0;
   const size_t D = (size_t)p->head_dim;
   return ckpt_slots(p) * (size_t)p->num_heads * D * D * sizeof(float);
 }
@@ -188,7 +189,7 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
   a.o = o;
   a.h0 = h0;
   a.hT = hT;
-  a.ckpt = ctx ? (float*)((char*)ctx + kda::kHeaderBytes) : nullptr;
+  a.ckpt = (ctx && ckpt_bytes(p)) ? (float*)((char*)ctx + kda::kHeaderBytes) : nullptr;
   a.status = ctx ? (int*)ctx : nullptr;
   a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
@@ -214,6 +215,8 @@ kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const voi
   kda_status st = validate(p);
   if (st != KDA_OK) return st;
   CHECK_OPT(dhT); CHECK_OPT(dh0);
+  if (p->flags & KDA_FLAG_NO_CHECKPOINTS)
+    return fail(KDA_ERR_INVALID_ARG, "KDA_FLAG_NO_CHECKPOINTS: a forward without checkpoints cannot feed kda_bwd");
   cudaStream_t s = (cudaStream_t)stream;
   if (p->total_tokens == 0) {  // no tokens: zero parameter gradients, dh0 = dhT
     CHECK_PTR(dA_log); CHECK_PTR(ddt_bias);

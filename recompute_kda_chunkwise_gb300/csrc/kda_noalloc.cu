@@ -66,6 +66,9 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
   if (st != KDA_OK) return st;
   if ((dhT && !aligned16(dhT)) || (dh0 && !aligned16(dh0)))
     return kda::set_error(KDA_ERR_INVALID_ARG, "dhT / dh0 is not 16-byte aligned");
+  if (p->flags & KDA_FLAG_NO_CHECKPOINTS)
+    return kda::set_error(KDA_ERR_INVALID_ARG,
+                          "KDA_FLAG_NO_CHECKPOINTS: a forward without checkpoints cannot feed the backward");
   const void* ptrs[] = {q, k, v, g_raw, beta_raw, A_log, dt_bias, dO, ctx, dq, dk, dv, dg_raw, dbeta_raw,
                         dA_log, ddt_bias};
   const char* names[] = {"q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias", "dO", "ctx", "dq", "dk", "dv",

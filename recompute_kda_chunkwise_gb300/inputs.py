@@ -70,6 +70,11 @@ WORKLOADS = {
     # The long-context shape cut to 8192 tokens: the same launch configuration
     # (96 sequence-heads) for profiler captures that must stay small.
     "mbs1_8k_h96_d128_bf16": Workload("mbs1_8k_h96_d128_bf16", _equal(1, 8192), 96, 128, "bf16", 20266),
+    # Unequal-length packing: 8 sequences of mean length 1024 (8192 tokens),
+    # the shape of the pages' varlen forward comparisons, at H = 96.
+    "varlen8_8k_h96_d128_bf16": Workload("varlen8_8k_h96_d128_bf16",
+                                         (512, 1536, 768, 1280, 256, 1792, 1024, 1024), 96, 128,
+                                         "bf16", 20267),
 }
 HEADLINE = "mbs1_128k_h96_d128_bf16"
 

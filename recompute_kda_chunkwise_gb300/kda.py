@@ -85,6 +85,7 @@ def _check(status: int, where: str):
 
 KDA_FLAG_FORCE_SIMT = 1
 KDA_FLAG_TEST_TIMEOUT = 2  # test only: the forward's bounded wait runs out (see include/kda.h)
+KDA_FLAG_NO_CHECKPOINTS = 4  # inference: ctx holds no checkpoints (scratch for the forward only)
 
 
 def make_problem(total_tokens: int, num_seqs: int, num_heads: int, head_dim: int, dtype,
@@ -158,20 +159,23 @@ def kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
             ctx=None, flags: int = 0, h0=None, final_state=False):
     """Forward. Returns (o, ctx); ctx is None when save_ctx is False. ``out``
     and ``ctx`` may be preallocated (ctx of at least ctx_bytes(problem)).
+    Without save_ctx the forward runs as inference (KDA_FLAG_NO_CHECKPOINTS):
+    no checkpoints are written, and a small scratch ctx (``ctx`` when given)
+    carries only the status word and the helper hand-off area.
     h0: initial states [N, H, D, D] fp32 (zero when None). With final_state
     True (or a preallocated [N, H, D, D] fp32 tensor) the final states are
     returned too: (o, ctx, hT)."""
     _check_tensors(q, k, v, g, beta, params=(A_log, dt_bias))
     _check_state(h0, q, cu_seqlens, "h0")
+    if not save_ctx:
+        flags |= KDA_FLAG_NO_CHECKPOINTS
     p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps, flags)
     hT = None
     if final_state is not False and final_state is not None:
         hT = _state_like(q, cu_seqlens) if final_state is True else final_state
         _check_state(hT, q, cu_seqlens, "final_state")
     o = torch.empty_like(q) if out is None else out
-    if not save_ctx:
-        ctx = None
-    elif ctx is None:
+    if ctx is None:
         ctx = torch.empty(ctx_bytes(p), dtype=torch.uint8, device=q.device)
     elif ctx.numel() * ctx.element_size() < ctx_bytes(p):
         raise ValueError("ctx buffer too small")
@@ -179,6 +183,8 @@ def kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
                                 _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(o), _ptr(hT), _ptr(ctx),
                                 _stream_handle(q.device))
     _check(st, "kda_fwd")
+    if not save_ctx:
+        ctx = None
     return (o, ctx) if hT is None else (o, ctx, hT)
 
 

@@ -91,11 +91,17 @@ def test_invalid_arguments_are_rejected_on_host(lib):
     p.dtype = 7
     assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, nul, nul) == 2
     p.dtype = 0
-    p.flags = 4  # no such flag
+    p.flags = 8  # no such flag
     assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, nul, nul) == 1
     assert b"unknown flags" in lib.kda_last_error_message()
     p.flags = K.KDA_FLAG_FORCE_SIMT | K.KDA_FLAG_TEST_TIMEOUT  # both known: sizes still answer
     assert lib.kda_ctx_bytes(ctypes.byref(p)) > 0
+    # inference: no checkpoints, so ctx shrinks to the status header; the
+    # backward refuses a problem flagged that way
+    p.flags = K.KDA_FLAG_NO_CHECKPOINTS
+    assert lib.kda_ctx_bytes(ctypes.byref(p)) == 256
+    assert lib.kda_bwd(ctypes.byref(p), *([al] * 8), nul, *([al] * 8), nul, al, nul) == 1
+    assert b"NO_CHECKPOINTS" in lib.kda_last_error_message()
 
 
 def test_status_strings(lib):

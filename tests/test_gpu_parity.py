@@ -35,6 +35,7 @@ def _check_workload(w: Workload, heads=None, device_inputs=False, scale=None):
     "mbs1_8k_h64_d128_bf16_gate2",
     "mbs1_8k_h128_d128_bf16_gate2",
     "mbs1_8k_h96_d128_bf16",
+    "varlen8_8k_h96_d128_bf16",
 ])
 def test_workload_parity_all_heads(name):
     _check_workload(WORKLOADS[name])
@@ -105,6 +106,24 @@ def test_deterministic_and_inference_forward_matches():
                            inp["dt_bias"], inp["cu_seqlens"], save_ctx=False)
     assert ctx is None
     assert torch.equal(o_inf, a["o"])
+
+
+def test_inference_forward_keeps_split_mode_and_matches():
+    # 96 (sequence, head) items: the inference forward (no checkpoints, ctx as
+    # scratch for the helper hand-off) gives the training forward's o bit for bit
+    from recompute_kda_chunkwise_gb300 import kda as K
+    w = Workload("infer_split", (1024,), 96, 128, "bf16", seed=7550, param_std=0.3)
+    inp = make_inputs(w, device="cuda")
+    args = [inp[n] for n in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "cu_seqlens")]
+    o_train, _ = K.kda_fwd(*args)
+    o_inf, ctx = K.kda_fwd(*args, save_ctx=False)
+    torch.cuda.synchronize()
+    assert ctx is None
+    assert torch.equal(o_inf, o_train)
+    p = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, torch.bfloat16,
+                       flags=K.KDA_FLAG_NO_CHECKPOINTS)
+    p_train = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, torch.bfloat16)
+    assert 256 < K.ctx_bytes(p) < K.ctx_bytes(p_train)  # hand-off area only
 
 
 def test_autograd_function_matches_direct_calls():
