@@ -67,7 +67,7 @@ constexpr int OFF_V = OFF_R;           //   then staged v (bf16 -> fp16 in place
 constexpr int OFF_ABAR = OFF_R + 16384;//   then Abar fp32 [64][65]
 constexpr int OFF_TF = OFF_R + 33024;  //        T fp32 [64][65]
 constexpr int OFF_TP = OFF_R + 50176;  //        T' fp16 [64 r][64 s]
-constexpr int OFF_X = OFF_R + 58368;   //        fp32 scratch [6][16][9]
+constexpr int OFF_X = OFF_R + 58368;   //        fp32 scratch [8][16][9]
 constexpr int OFF_TPL = OFF_R + 16384; //   after the inverse (Abar dead): T' low part fp16 [64 r][64 s]
 constexpr int OFF_ML = OFF_R + 24576;  //                                  M low part fp16 [64 r][64 s]
 constexpr int OFF_UL = OFF_R;          //   after the U product (v dead): U~^T low part fp16 [128 v][64 r]
@@ -134,30 +134,61 @@ __device__ __forceinline__ uint32_t xs_off(int r, int c) {
   return static_cast<uint32_t>(r * 512 + (c >> 5) * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + ((c & 3) << 2));
 }
 
-// T = (I + diag(beta) Abar)^-1 (fp32) on 16 x 16 blocks: the diagonal blocks
-// by right-looking forward substitution (one warp per block, one lane per
-// column), then level by level T_IJ = -T_II diag(beta_I) sum_{K=J}^{I-1}
-// Abar_IK T_KJ on warp-level tf32 tiles split into hi + lo parts (about fp32
-// accuracy); finally T' = T diag(beta) as fp16 hi + lo parts. The Abar tile
-// already holds diag(beta) Abar (rows scaled when it is written).
+// T = (I + N)^-1, N = diag(beta) Abar strictly lower (fp32; the Abar tile
+// already holds N, rows scaled when it is written), in 16 x 16 blocks:
+//  * each diagonal block by one warp, itself in 8 x 8 halves: lane j < 16
+//    solves column j of its half by right-looking forward substitution, then
+//    lanes 0-7 form the lower-left 8 x 8 part as -T22 N21 T11;
+//  * T_10 and T_32 = -T_II N_IJ T_JJ (level A), then the lower-left 32 x 32
+//    part as -T_hi (N_21 T_lo) in two product phases on all eight warps;
+// products on warp-level tf32 tiles split into hi + lo parts (about fp32
+// accuracy); finally T' = T diag(beta) as fp16 hi + lo parts.
 __device__ __forceinline__ void tri_inverse(uint8_t* sm, const float* s_beta, int tid) {
   float* Ab = reinterpret_cast<float*>(sm + OFF_ABAR);
   float* Tf = reinterpret_cast<float*>(sm + OFF_TF);
   float* X = reinterpret_cast<float*>(sm + OFF_X);
   const int warp = tid >> 5, lane = tid & 31, fg = lane >> 2, ft = lane & 3;
   if (warp < 4) {
-    const int base = 16 * warp, j = lane & 15;
-    float x[16];
+    const int base = 16 * warp, j = lane & 15, b8 = 8 * (j >> 3);
+    float x[8];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
+    for (int k = 0; k < 8; ++k) x[k] = (b8 + k == j) ? 1.f : 0.f;
 #pragma unroll
-    for (int s2 = 0; s2 < 15; ++s2) {
+    for (int s2 = 0; s2 < 7; ++s2) {
 #pragma unroll
-      for (int r = s2 + 1; r < 16; ++r) x[r] -= Ab[(base + r) * 65 + base + s2] * x[s2];
+      for (int k = s2 + 1; k < 8; ++k) x[k] -= Ab[(base + b8 + k) * 65 + base + b8 + s2] * x[s2];
     }
     if (lane < 16) {
 #pragma unroll
-      for (int r = 0; r < 16; ++r) Tf[(base + r) * 65 + base + j] = x[r];
+      for (int k = 0; k < 8; ++k) Tf[(base + b8 + k) * 65 + base + j] = x[k];
+    }
+    __syncwarp();
+    float z[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) z[k] = 0.f;
+    if (lane < 8) {
+      float y[8];  // (N21 T11)[., j] within the block
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float acc = 0.f;
+#pragma unroll
+        for (int s3 = 0; s3 < 8; ++s3) acc += Ab[(base + 8 + k) * 65 + base + s3] * x[s3];
+        y[k] = acc;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m <= k; ++m) acc += Tf[(base + 8 + k) * 65 + base + 8 + m] * y[m];
+        z[k] = -acc;
+      }
+    }
+    if (lane < 16) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const float t = ((r >> 3) == (j >> 3)) ? x[r & 7] : ((r >= 8) ? z[r - 8] : 0.f);
+        Tf[(base + r) * 65 + base + j] = t;
+      }
     }
   } else {  // the six blocks above the diagonal are zero
     for (int x = tid - 128; x < 6 * 256; x += 128) {
@@ -167,42 +198,54 @@ __device__ __forceinline__ void tri_inverse(uint8_t* sm, const float* s_beta, in
     }
   }
   __syncthreads();
-#pragma unroll 1
-  for (int d = 1; d <= 3; ++d) {
-    if (warp < 2 * (4 - d)) {  // two warps (8-column halves) per block (I, J = I - d)
-      const int J = warp >> 1, nt = warp & 1, I = J + d;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int K = J; K < I; ++K) {
+  // product of a 16-row block tile (A: 16 x 16 at A0, stride lda) with this
+  // warp's 8 columns of B (16 x 8 at B0, stride ldb), accumulated into acc
+  auto mma_block = [&](float (&acc)[4], const float* A0, int lda, const float* B0, int ldb) {
 #pragma unroll
-        for (int k0 = 0; k0 < 16; k0 += 8) {
-          float fa[4], fb[2];
-          ldA(fa, Ab + (16 * I) * 65 + 16 * K, 65, k0, fg, ft);
-          ldBr(fb, Tf + (16 * K) * 65 + 16 * J, 65, 8 * nt, k0, fg, ft);
-          mma3(acc, fa, fb);
-        }
-      }
-      float* Xw = X + warp * (16 * 9);  // diag(beta_I) sum_K Abar_IK T_KJ, this warp's 8 columns
-      Xw[fg * 9 + 2 * ft] = acc[0];
-      Xw[fg * 9 + 2 * ft + 1] = acc[1];
-      Xw[(fg + 8) * 9 + 2 * ft] = acc[2];
-      Xw[(fg + 8) * 9 + 2 * ft + 1] = acc[3];
-      __syncwarp();
-      float t2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int k0 = 0; k0 < 16; k0 += 8) {
-        float fa[4], fb[2];
-        ldA(fa, Tf + (16 * I) * 65 + 16 * I, 65, k0, fg, ft);
-        ldBr(fb, Xw, 9, 0, k0, fg, ft);
-        mma3(t2, fa, fb);
-      }
-      float* dst = Tf + (16 * I) * 65 + 16 * J + 8 * nt + 2 * ft;
-      dst[fg * 65] = -t2[0];
-      dst[fg * 65 + 1] = -t2[1];
-      dst[(fg + 8) * 65] = -t2[2];
-      dst[(fg + 8) * 65 + 1] = -t2[3];
+    for (int k0 = 0; k0 < 16; k0 += 8) {
+      float fa[4], fb[2];
+      ldA(fa, A0, lda, k0, fg, ft);
+      ldBr(fb, B0, ldb, 0, k0, fg, ft);
+      mma3(acc, fa, fb);
     }
-    __syncthreads();
+  };
+  auto store_tile = [&](float* dst, int ld, const float (&v)[4], float sgn) {
+    dst[fg * ld + 2 * ft] = sgn * v[0];
+    dst[fg * ld + 2 * ft + 1] = sgn * v[1];
+    dst[(fg + 8) * ld + 2 * ft] = sgn * v[2];
+    dst[(fg + 8) * ld + 2 * ft + 1] = sgn * v[3];
+  };
+  // level A: T_10 and T_32 (warps 0-3: block J = 2 (w >> 1), 8-column half nt)
+  if (warp < 4) {
+    const int J = 2 * (warp >> 1), I = J + 1, nt = warp & 1;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_block(acc, Ab + (16 * I) * 65 + 16 * J, 65, Tf + (16 * J) * 65 + 16 * J + 8 * nt, 65);
+    float* Xw = X + warp * (16 * 9);  // N_IJ T_JJ, this warp's 8 columns
+    store_tile(Xw, 9, acc, 1.f);
+    __syncwarp();
+    float t2[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_block(t2, Tf + (16 * I) * 65 + 16 * I, 65, Xw, 9);
+    store_tile(Tf + (16 * I) * 65 + 16 * J + 8 * nt, 65, t2, -1.f);
   }
+  __syncthreads();
+  // level B: Y_IJ = sum_{K=J..1} N_IK T_KJ for I in {2, 3}, J in {0, 1}
+  // (warp w: I = 2 + (w >> 2), J = (w >> 1) & 1, half nt = w & 1)
+  const int I = 2 + (warp >> 2), J = (warp >> 1) & 1, nt = warp & 1;
+  {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int K = J; K < 2; ++K)
+      mma_block(acc, Ab + (16 * I) * 65 + 16 * K, 65, Tf + (16 * K) * 65 + 16 * J + 8 * nt, 65);
+    store_tile(X + warp * (16 * 9), 9, acc, 1.f);
+  }
+  __syncthreads();
+  // T_IJ = -sum_{K=2..I} T_IK Y_KJ (Y_KJ: warp (K - 2) * 4 + J * 2 + nt's tile)
+  {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int K = 2; K <= I; ++K)
+      mma_block(acc, Tf + (16 * I) * 65 + 16 * K, 65, X + ((K - 2) * 4 + J * 2 + nt) * (16 * 9), 9);
+    store_tile(Tf + (16 * I) * 65 + 16 * J + 8 * nt, 65, acc, -1.f);
+  }
+  __syncthreads();
   for (int x = tid; x < 64 * 32; x += kThreads) {
     const int r = x >> 5, s = 2 * (x & 31);
     const float t0 = Tf[r * 65 + s] * s_beta[s], t1 = Tf[r * 65 + s + 1] * s_beta[s + 1];
