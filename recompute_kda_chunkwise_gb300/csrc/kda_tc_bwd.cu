@@ -1029,7 +1029,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                 const int n0 = 16 * warp + 8 * nt;
                 float fb[2];
                 ldBr(fb, DUT, kLd, n0, k0, fg, ft);
-                mma3(dvv[nt], tpt, fb);  // dV = T'^T dU~
+                mma1(dvv[nt], tpt, fb);  // dV = T'^T dU~ (feeds only dv: plain tf32)
                 ldBr(fb, WT, kLd, n0, k0, fg, ft);
                 mma3(dkg[nt], tpt, fb);  // d(Kh Gamma) += T'^T dW
                 ldBr(fb, KI, kLd, n0, k0, fg, ft);

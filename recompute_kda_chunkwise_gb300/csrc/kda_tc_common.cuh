@@ -262,6 +262,16 @@ __device__ __forceinline__ void mma3(float (&d)[4], const float (&a)[4], const f
   mma_tf32_16x8(d, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
   mma_tf32_16x8(d, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
 }
+// d += A B in plain tf32 (both operands rounded to tf32 once): about 2^-11
+// relative per product, for results that feed nothing more sensitive.
+__device__ __forceinline__ void mma1(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
+  uint32_t ah[4], bh[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(ah[i]) : "f"(a[i]));
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(bh[0]) : "f"(b[0]));
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(bh[1]) : "f"(b[1]));
+  mma_tf32_16x8(d, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
+}
 // d += A B where B is exact in tf32 (bf16 / fp16 values): A split only.
 __device__ __forceinline__ void mma2_bexact(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
   uint32_t ah[4], al[4];
