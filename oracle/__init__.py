@@ -14,7 +14,11 @@ Parity status of each part (what pins it is listed in the tests):
     differences, fp64 autograd of an independent explicit-matrix forward);
   * gate formula g = L*sigmoid(exp(A_log)*(a + dt_bias)) and the shapes
     A_log[H], dt_bias[H,D] -- parity unpinned: the pages name only a
-    "safe gate with lower bound -5" built from these three inputs.
+    "safe gate with lower bound -5" built from these three inputs;
+  * GDN-2 channel-wise erase / write gates (``gdn2_reference``) -- recurrence
+    and backward pinned (explicit-matrix autograd, finite differences, the
+    KDA special case b = w = beta, the closed form with no erasing); the
+    sigmoid activation of the two raw gates is a reading (unpinned).
 """
 from __future__ import annotations
 
@@ -60,6 +64,12 @@ def _load():
                           ctypes.c_int, dp, dp, dp, dp, dp, dp, dp,
                           ctypes.c_double, ctypes.c_double, ctypes.c_double, dp,
                           dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
+            f2 = lib.gdn2_oracle_run
+            f2.restype = ctypes.c_int
+            f2.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                           ctypes.c_int, dp, dp, dp, dp, dp, dp, dp, dp,
+                           ctypes.c_double, ctypes.c_double, ctypes.c_double, dp,
+                           dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -166,4 +176,63 @@ def kda_reference_heads(inputs: dict, heads, dO=True, *, scale=1.0, lower_bound=
     for key in parts[0]:
         axis = 0 if key in ("dA_log", "ddt_bias") else 1
         out[key] = np.concatenate([p[key] for p in parts], axis=axis)
+    return out
+
+
+def gdn2_reference(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, dO=None, *,
+                   scale: float = 1.0, lower_bound: float = -5.0, eps: float = 1e-6,
+                   threads: int | None = None, want_o: bool = True, h0=None, dht=None,
+                   want_state: bool = False) -> dict:
+    """Run the GDN-2 oracle: KDA with the scalar beta replaced by channel-wise
+    gates, erase b_t = sigmoid(erase_t) on key channels and write
+    w_t = sigmoid(write_t) on value channels (see gdn2_oracle_run in
+    kda_oracle.c). erase and write are [S,H,D]; everything else as in
+    kda_reference. Returns 'o' and, when dO is given, 'dq','dk','dv','dg',
+    'derase','dwrite','dA_log','ddt_bias' (plus 'hT' / 'dh0' with states)."""
+    q = _f64(q)
+    if q.ndim != 3:
+        raise ValueError("q must be [S,H,D]")
+    S, H, D = q.shape
+    k = _f64(k, (S, H, D)); v = _f64(v, (S, H, D)); g = _f64(g, (S, H, D))
+    erase = _f64(erase, (S, H, D)); write = _f64(write, (S, H, D))
+    A_log = _f64(A_log, (H,)); dt_bias = _f64(dt_bias, (H, D))
+    if hasattr(cu_seqlens, "detach"):
+        cu_seqlens = cu_seqlens.detach().to("cpu").numpy()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    if cu.ndim != 1 or cu.size < 1 or cu[0] != 0 or cu[-1] != S:
+        raise ValueError("cu_seqlens must start at 0 and end at S")
+    N = cu.size - 1
+    want_state = want_state or h0 is not None or dht is not None
+    h0 = None if h0 is None else _f64(h0, (N, H, D, D))
+    dht = None if dht is None else _f64(dht, (N, H, D, D))
+    out = {}
+    hT = dh0 = None
+    if want_state:
+        hT = out["hT"] = np.zeros((N, H, D, D))
+        if dO is not None:
+            dh0 = out["dh0"] = np.zeros((N, H, D, D))
+    o = np.zeros((S, H, D), np.float64) if want_o else None
+    if want_o:
+        out["o"] = o
+    G = {}
+    if dO is not None:
+        dO = _f64(dO, (S, H, D))
+        G = dict(dq=np.zeros((S, H, D)), dk=np.zeros((S, H, D)), dv=np.zeros((S, H, D)),
+                 dg=np.zeros((S, H, D)), derase=np.zeros((S, H, D)), dwrite=np.zeros((S, H, D)),
+                 dA_log=np.zeros((H,)), ddt_bias=np.zeros((H, D)))
+        out.update(G)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    lib = _load()
+    fp = ctypes.c_double
+    rc = lib.gdn2_oracle_run(
+        N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), H, D,
+        _ptr(q, fp), _ptr(k, fp), _ptr(v, fp), _ptr(g, fp), _ptr(erase, fp), _ptr(write, fp),
+        _ptr(A_log, fp), _ptr(dt_bias, fp), float(scale), float(lower_bound), float(eps),
+        _ptr(dO, fp), _ptr(o, fp), _ptr(G.get("dq"), fp), _ptr(G.get("dk"), fp),
+        _ptr(G.get("dv"), fp), _ptr(G.get("dg"), fp), _ptr(G.get("derase"), fp),
+        _ptr(G.get("dwrite"), fp), _ptr(G.get("dA_log"), fp), _ptr(G.get("ddt_bias"), fp),
+        _ptr(h0, fp), _ptr(hT, fp), _ptr(dht, fp), _ptr(dh0, fp), int(threads))
+    if rc != 0:
+        raise RuntimeError(f"gdn2_oracle_run failed with code {rc}")
     return out
