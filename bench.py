@@ -4,7 +4,8 @@
                     [--workload NAME] [--e2e-steps E] [--no-cpu-baseline]
 
 A step is one kda_fwd + kda_bwd over the whole workload (every hot-path kernel
-runs once per step). Inputs are seeded synthetic tensors already resident in
+runs once per step); for a GDN-2 workload (gdn2_*: channel-wise erase / write
+gates) it is one kda_gdn2_fwd + kda_gdn2_bwd. Inputs are seeded synthetic tensors already resident in
 HBM; they total far more than the 129 MB L2, so no flush is needed between
 steps. The value is whole-job tokens/s (all ranks' tokens / max-over-ranks
 time). Under torchrun every rank runs an independent replica of the workload
@@ -28,6 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "KDA fwd+bwd tokens/sec at MBS1·128K·H96·D128; % HBM roofline; peak alloc GiB"
+GDN2_METRIC = "GDN-2 (channel-wise erase / write gates) fwd+bwd tokens/sec"
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -39,9 +41,19 @@ def algorithmic_bytes(w):
     e = 2 if w.dtype == "bf16" else 4
     D = w.D
     th = w.total_tokens * w.H
+    if w.gates == "channel":  # GDN-2: erase and write gates are D wide each
+        fwd = th * e * 7 * D         # q,k,v,g,erase,write,o
+        bwd = th * e * 13 * D        # q,k,v,g,erase,write,dO + dq,dk,dv,dg,derase,dwrite
+        return fwd, bwd
     fwd = th * e * (5 * D + 1)       # q,k,v,g,o (D each) + beta
     bwd = th * e * (9 * D + 2)       # q,k,v,g,dO + dq,dk,dv,dg (D each) + beta, dbeta
     return fwd, bwd
+
+
+def gate_names(w):
+    """Input names of the write-strength gates: raw beta (KDA) or the raw
+    erase and write gates (GDN-2)."""
+    return ["erase", "write"] if w.gates == "channel" else ["beta"]
 
 
 def measured_peaks():
@@ -165,7 +177,10 @@ def oracle_sample(w, inp_cpu_slices, cores):
     """Times the fp64 oracle on a bounded sample; returns token-heads/s."""
     import oracle
     t0 = time.perf_counter()
-    oracle.kda_reference(**inp_cpu_slices, threads=cores)
+    if "erase" in inp_cpu_slices:
+        oracle.gdn2_reference(**inp_cpu_slices, threads=cores)
+    else:
+        oracle.kda_reference(**inp_cpu_slices, threads=cores)
     dt = time.perf_counter() - t0
     th = inp_cpu_slices["q"].shape[0] * inp_cpu_slices["q"].shape[1]
     return th / dt, dt
@@ -177,10 +192,13 @@ def make_sample(w, inp, sample_tokens, sample_heads):
     T = min(sample_tokens, w.lengths[0])
     hs = slice(0, sample_heads)
     cpu = lambda x: x.detach().to("cpu")
-    return dict(q=cpu(inp["q"][:T, hs]), k=cpu(inp["k"][:T, hs]), v=cpu(inp["v"][:T, hs]),
-                g=cpu(inp["g"][:T, hs]), beta=cpu(inp["beta"][:T, hs]), A_log=cpu(inp["A_log"][hs]),
-                dt_bias=cpu(inp["dt_bias"][hs]), cu_seqlens=[0, T], dO=cpu(inp["dO"][:T, hs]),
-                scale=w.scale)
+    out = dict(q=cpu(inp["q"][:T, hs]), k=cpu(inp["k"][:T, hs]), v=cpu(inp["v"][:T, hs]),
+               g=cpu(inp["g"][:T, hs]))
+    for n in gate_names(w):
+        out[n] = cpu(inp[n][:T, hs])
+    out.update(A_log=cpu(inp["A_log"][hs]), dt_bias=cpu(inp["dt_bias"][hs]), cu_seqlens=[0, T],
+               dO=cpu(inp["dO"][:T, hs]), scale=w.scale)
+    return out
 
 
 def run_reference(args, w, rank):
@@ -205,7 +223,8 @@ def run_reference(args, w, rank):
     value = th_per_s / w.H  # tokens/s of the full-H workload
     desc = (f"first {sl['q'].shape[0]} tokens x {heads} heads of {w.name} per step "
             f"(fwd+bwd, fp64), scaled to tokens/s over all {w.H} heads")
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+    metric = GDN2_METRIC if w.gates == "channel" else METRIC
+    line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
@@ -315,17 +334,20 @@ def run_gb300(args, w, rank, world, local):
     torch.cuda.set_device(dev)
     K.load_library()
     inp = make_inputs(w, device=dev)
-    q, k, v, g, beta, A_log, dt_bias, cu, dO = (inp[n] for n in
-                                                  ["q", "k", "v", "g", "beta", "A_log", "dt_bias",
-                                                   "cu_seqlens", "dO"])
-    prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale)
+    gates = gate_names(w)
+    gdn2 = w.gates == "channel"
+    args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
+    q, cu, dO = inp["q"], inp["cu_seqlens"], inp["dO"]
+    fwd_fn, bwd_fn = (K.gdn2_fwd, K.gdn2_bwd) if gdn2 else (K.kda_fwd, K.kda_bwd)
+    prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale,
+                          flags=K.KDA_FLAG_CHANNEL_GATES if gdn2 else 0)
     family = K.kernel_family(prob)
     torch.cuda.synchronize()
 
     # peak allocated memory of one fwd+bwd (inputs, dO, o, grads, ctx, workspace)
     torch.cuda.reset_peak_memory_stats(dev)
-    o, ctx = K.kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu, scale=w.scale)
-    grads = K.kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu, dO, ctx, scale=w.scale)
+    o, ctx = fwd_fn(*args_in, scale=w.scale)
+    grads = bwd_fn(*args_in, dO, ctx, scale=w.scale)
     torch.cuda.synchronize()
     peak_gib = torch.cuda.max_memory_allocated(dev) / 2 ** 30
     ws = torch.empty(K.workspace_bytes(prob), dtype=torch.uint8, device=dev)
@@ -335,10 +357,10 @@ def run_gb300(args, w, rank, world, local):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        K.kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu, scale=w.scale, out=o, ctx=ctx)
+        fwd_fn(*args_in, scale=w.scale, out=o, ctx=ctx)
         if ev is not None:
             ev[1].record(stream)
-        K.kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu, dO, ctx, scale=w.scale, workspace=ws, outs=grads)
+        bwd_fn(*args_in, dO, ctx, scale=w.scale, workspace=ws, outs=grads)
         if ev is not None:
             ev[2].record(stream)
 
@@ -367,7 +389,8 @@ def run_gb300(args, w, rank, world, local):
     value = tokens / (ms_step / 1e3)
     fwd_b, bwd_b = algorithmic_bytes(w)
     peak_gbs, peak_kind = measured_peaks()
-    dominant = "kda_bwd" if bwd_ms >= fwd_ms else "kda_fwd"
+    prefix = "kda_gdn2" if gdn2 else "kda"
+    dominant = f"{prefix}_bwd" if bwd_ms >= fwd_ms else f"{prefix}_fwd"
     dom_ms, dom_b = (bwd_ms, bwd_b) if dominant == "kda_bwd" else (fwd_ms, fwd_b)
     achieved = dom_b / (dom_ms / 1e3) / 1e9
     step_gbs = (fwd_b + bwd_b) / (ms_step / 1e3) / 1e9
@@ -382,11 +405,11 @@ def run_gb300(args, w, rank, world, local):
     # end to end through the public API: pinned host inputs -> device -> fwd+bwd -> host outputs
     e2e = None
     if args.e2e_steps > 0:
-        names_in = ["q", "k", "v", "g", "beta", "dO"]
+        names_in = ["q", "k", "v", "g"] + gates + ["dO"]
         host_in = {n: torch.empty(inp[n].shape, dtype=inp[n].dtype, pin_memory=True) for n in names_in}
         for n in names_in:
             host_in[n].copy_(inp[n])
-        names_out = ["dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias"]
+        names_out = ["dq", "dk", "dv", "dg"] + ["d" + n for n in gates] + ["dA_log", "ddt_bias"]
         host_out = {n: torch.empty(grads[n].shape, dtype=grads[n].dtype, pin_memory=True) for n in names_out}
         host_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -421,8 +444,8 @@ def run_gb300(args, w, rank, world, local):
                                f"(fwd+bwd, fp64, {dt:.1f} s wall), scaled to tokens/s over all {w.H} heads")}
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        line = {"metric": GDN2_METRIC if gdn2 else METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
                 "config": {"workload": w.name, "num_seqs": w.num_seqs, "seq_len": w.lengths[0],
                            "heads": w.H, "head_dim": w.D, "scale": w.scale, "gate_lower_bound": -5.0,
@@ -456,6 +479,8 @@ def main(argv=None):
     if args.impl == "reference":
         run_reference(args, w, rank)
     elif args.pass_ == "fwd":
+        if w.gates == "channel":
+            raise SystemExit("--pass fwd times KDA workloads; GDN-2 workloads run fwd+bwd")
         run_gb300_fwd(args, w, rank, world, local)
     else:
         run_gb300(args, w, rank, world, local)

@@ -90,6 +90,12 @@ typedef enum {
  * speed-up without a checkpoint buffer. Such a ctx cannot feed kda_bwd, which
  * rejects the flag. */
 #define KDA_FLAG_NO_CHECKPOINTS 4
+/* GDN-2 problem: the operator with channel-wise erase and write gates
+ * (kda_gdn2_fwd / kda_gdn2_bwd below). Set it before the size queries so
+ * that they size ctx and workspace for the GDN-2 kernels; kda_fwd, kda_bwd
+ * and kda_bwd_noalloc reject it, and kda_gdn2_fwd / kda_gdn2_bwd require it.
+ * GDN-2 runs on the fp32 CUDA-core kernels for every dtype and head_dim. */
+#define KDA_FLAG_CHANNEL_GATES 8
 
 /* Problem description. cu_seqlens is a DEVICE pointer; the library never
  * reads it on the host (so no synchronisation), and trusts that it is
@@ -190,6 +196,40 @@ kda_status kda_bwd_noalloc(const kda_problem* p,
                            void* dq, void* dk, void* dv, void* dg_raw, void* dbeta_raw,
                            float* dA_log, float* ddt_bias, float* dh0, void* stream);
 
+/* GDN-2: the same operator with the scalar beta replaced by two channel-wise
+ * gates ("KDA at the production shape ...", section 1.6, which names GDN-2
+ * as this generalisation with KDA its special case, and the section 2.1 op
+ * table: akk = (b*k*Gamma)(k/Gamma)^T, w = M^-1 (b k*Gamma), u = M^-1 (w*v)):
+ *     b_t = sigmoid(erase_raw_t)   (per key channel)
+ *     w_t = sigmoid(write_raw_t)   (per value channel)
+ *     S_t = (I - kh_t (b_t * kh_t)^T) Diag(exp(g_t)) S_{t-1} + kh_t (w_t * v_t)^T
+ *     o_t = S_t^T qh_t
+ * with qh, kh, g, scale, states and sequence packing exactly as for KDA
+ * (b_t = w_t = beta_t on every channel gives KDA). The sigmoid of the two raw
+ * gates mirrors beta's; the pages print no activation for them.
+ * erase_raw, write_raw, derase_raw, dwrite_raw: [S, H, D] in problem->dtype.
+ * p->flags must include KDA_FLAG_CHANNEL_GATES (KDA_ERR_INVALID_ARG
+ * otherwise), and ctx / workspace must then hold kda_ctx_bytes(p) /
+ * kda_bwd_workspace_bytes(p) bytes of that problem. Every other argument,
+ * ownership rule and error behaviour is that of kda_fwd / kda_bwd;
+ * KDA_FLAG_NO_CHECKPOINTS works as for kda_fwd. */
+kda_status kda_gdn2_fwd(const kda_problem* p,
+                        const void* q, const void* k, const void* v,
+                        const void* g_raw, const void* erase_raw, const void* write_raw,
+                        const float* A_log, const float* dt_bias,
+                        const float* h0,
+                        void* o, float* hT, void* ctx, void* stream);
+
+kda_status kda_gdn2_bwd(const kda_problem* p,
+                        const void* q, const void* k, const void* v,
+                        const void* g_raw, const void* erase_raw, const void* write_raw,
+                        const float* A_log, const float* dt_bias,
+                        const void* dO, const float* dhT, const void* ctx,
+                        void* dq, void* dk, void* dv, void* dg_raw,
+                        void* derase_raw, void* dwrite_raw,
+                        float* dA_log, float* ddt_bias, float* dh0,
+                        void* workspace, void* stream);
+
 /* Reads the device status word at the head of a ctx or workspace buffer.
  * Synchronises `stream` first. Returns KDA_OK, KDA_ERR_TIMEOUT or
  * KDA_ERR_DEVICE_CHECK as recorded by the kernels, or KDA_ERR_CUDA if the
@@ -209,7 +249,7 @@ const char* kda_last_error_message(void);
  * Host only. */
 int kda_kernel_family(const kda_problem* p);
 
-/* Library ABI version (major * 10000 + minor * 100 + patch). */
+/* Library ABI version, major * 100 + minor * 10 (210 = 2.1: the GDN-2 entry points). */
 int kda_version(void);
 
 #ifdef __cplusplus

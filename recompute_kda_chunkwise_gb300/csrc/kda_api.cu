@@ -34,7 +34,8 @@ kda_status validate(const kda_problem* p, bool need_ptrs = true) {
   if (p->num_seqs < 1) return fail(KDA_ERR_INVALID_ARG, "num_seqs must be >= 1 (got %d)", p->num_seqs);
   if (p->num_heads < 1) return fail(KDA_ERR_INVALID_ARG, "num_heads must be >= 1 (got %d)", p->num_heads);
   if (p->total_tokens < 0) return fail(KDA_ERR_INVALID_ARG, "total_tokens must be >= 0");
-  if ((p->flags & ~(KDA_FLAG_FORCE_SIMT | KDA_FLAG_TEST_TIMEOUT | KDA_FLAG_NO_CHECKPOINTS)) != 0)
+  if ((p->flags & ~(KDA_FLAG_FORCE_SIMT | KDA_FLAG_TEST_TIMEOUT | KDA_FLAG_NO_CHECKPOINTS |
+                    KDA_FLAG_CHANNEL_GATES)) != 0)
     return fail(KDA_ERR_INVALID_ARG, "unknown flags 0x%x", p->flags);
   if (need_ptrs && !p->cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is NULL");
   if (p->dtype != KDA_DTYPE_BF16 && p->dtype != KDA_DTYPE_F32)
@@ -53,9 +54,11 @@ kda_status validate(const kda_problem* p, bool need_ptrs = true) {
   return KDA_OK;
 }
 
-// Kernel family of both passes: tcgen05 kernels for bf16 D = 128, else fp32 SIMT.
+// Kernel family of both passes: tcgen05 kernels for bf16 D = 128, else fp32
+// SIMT. GDN-2 problems (channel-wise gates) always run the SIMT kernels.
 int family_of(const kda_problem* p) {
-  return (p->dtype == KDA_DTYPE_BF16 && p->head_dim == 128 && !(p->flags & KDA_FLAG_FORCE_SIMT)) ? 1 : 0;
+  return (p->dtype == KDA_DTYPE_BF16 && p->head_dim == 128 &&
+          !(p->flags & (KDA_FLAG_FORCE_SIMT | KDA_FLAG_CHANNEL_GATES))) ? 1 : 0;
 }
 
 size_t ckpt_slots(const kda_problem* p) {
@@ -156,7 +159,7 @@ size_t kda_bwd_workspace_bytes(const kda_problem* p) {
 
 int kda_kernel_family(const kda_problem* p) { return validate(p, false) == KDA_OK ? family_of(p) : -1; }
 
-int kda_version(void) { return 200; }
+int kda_version(void) { return 210; }
 
 const char* kda_status_string(kda_status s) {
   switch (s) {
@@ -173,9 +176,15 @@ const char* kda_status_string(kda_status s) {
 
 const char* kda_last_error_message(void) { return g_msg; }
 
-kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
-                   const void* beta_raw, const float* A_log, const float* dt_bias, const float* h0, void* o,
-                   float* hT, void* ctx, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Forward of both operators: write_raw is NULL for KDA (beta_raw [S,H]) and
+// set for GDN-2 (beta_raw is then the erase gate [S,H,D]).
+kda_status forward(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
+                   const void* beta_raw, const void* write_raw, const float* A_log, const float* dt_bias,
+                   const float* h0, void* o, float* hT, void* ctx, void* stream) {
   kda_status st = validate(p);
   if (st != KDA_OK) return st;
   CHECK_OPT(h0); CHECK_OPT(hT);
@@ -196,6 +205,7 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
   a.test_timeout = (p->flags & KDA_FLAG_TEST_TIMEOUT) ? 1 : 0;
   a.xflags = nullptr;
   a.xbuf = nullptr;
+  a.w = write_raw;
   if (ctx && fwd_handoff(p)) {
     a.xflags = (uint32_t*)((char*)ctx + kda::kHeaderBytes + ckpt_bytes(p));
     a.xbuf = (uint8_t*)a.xflags + round_up((size_t)p->num_seqs * p->num_heads * 5 * sizeof(uint32_t), 256);
@@ -207,11 +217,13 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
   return KDA_OK;
 }
 
-kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
-                   const void* beta_raw, const float* A_log, const float* dt_bias, const void* dO,
-                   const float* dhT, const void* ctx, void* dq, void* dk, void* dv, void* dg_raw,
-                   void* dbeta_raw, float* dA_log, float* ddt_bias, float* dh0, void* workspace,
-                   void* stream) {
+// Backward of both operators: write_raw / dwrite_raw are NULL for KDA and set
+// for GDN-2 (beta_raw / dbeta_raw are then the erase gate and its gradient).
+kda_status backward(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
+                    const void* beta_raw, const void* write_raw, const float* A_log, const float* dt_bias,
+                    const void* dO, const float* dhT, const void* ctx, void* dq, void* dk, void* dv,
+                    void* dg_raw, void* dbeta_raw, void* dwrite_raw, float* dA_log, float* ddt_bias,
+                    float* dh0, void* workspace, void* stream) {
   kda_status st = validate(p);
   if (st != KDA_OK) return st;
   CHECK_OPT(dhT); CHECK_OPT(dh0);
@@ -243,11 +255,60 @@ kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const voi
   a.scratch = (float*)((char*)workspace + kda::kHeaderBytes + partial_bytes(p) + flag_bytes(p));
   a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
+  a.w = write_raw;
+  a.dw = dwrite_raw;
   if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess)
     return fail(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
   st = family_of(p) == 1 ? kda::launch_bwd_tc(p, a, s, tc_bwd_ctas(p)) : kda::launch_bwd_simt(p, a, s);
   if (st != KDA_OK) return fail(st, "backward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
+                   const void* beta_raw, const float* A_log, const float* dt_bias, const float* h0, void* o,
+                   float* hT, void* ctx, void* stream) {
+  if (p && (p->flags & KDA_FLAG_CHANNEL_GATES))
+    return fail(KDA_ERR_INVALID_ARG, "KDA_FLAG_CHANNEL_GATES: a GDN-2 problem runs through kda_gdn2_fwd");
+  return forward(p, q, k, v, g_raw, beta_raw, nullptr, A_log, dt_bias, h0, o, hT, ctx, stream);
+}
+
+kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
+                   const void* beta_raw, const float* A_log, const float* dt_bias, const void* dO,
+                   const float* dhT, const void* ctx, void* dq, void* dk, void* dv, void* dg_raw,
+                   void* dbeta_raw, float* dA_log, float* ddt_bias, float* dh0, void* workspace,
+                   void* stream) {
+  if (p && (p->flags & KDA_FLAG_CHANNEL_GATES))
+    return fail(KDA_ERR_INVALID_ARG, "KDA_FLAG_CHANNEL_GATES: a GDN-2 problem runs through kda_gdn2_bwd");
+  return backward(p, q, k, v, g_raw, beta_raw, nullptr, A_log, dt_bias, dO, dhT, ctx, dq, dk, dv, dg_raw,
+                  dbeta_raw, nullptr, dA_log, ddt_bias, dh0, workspace, stream);
+}
+
+kda_status kda_gdn2_fwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
+                        const void* erase_raw, const void* write_raw, const float* A_log, const float* dt_bias,
+                        const float* h0, void* o, float* hT, void* ctx, void* stream) {
+  if (p && !(p->flags & KDA_FLAG_CHANNEL_GATES))
+    return fail(KDA_ERR_INVALID_ARG, "kda_gdn2_fwd needs KDA_FLAG_CHANNEL_GATES in the problem's flags");
+  if (p && p->total_tokens > 0) CHECK_PTR(write_raw);
+  return forward(p, q, k, v, g_raw, erase_raw, write_raw, A_log, dt_bias, h0, o, hT, ctx, stream);
+}
+
+kda_status kda_gdn2_bwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* g_raw,
+                        const void* erase_raw, const void* write_raw, const float* A_log, const float* dt_bias,
+                        const void* dO, const float* dhT, const void* ctx, void* dq, void* dk, void* dv,
+                        void* dg_raw, void* derase_raw, void* dwrite_raw, float* dA_log, float* ddt_bias,
+                        float* dh0, void* workspace, void* stream) {
+  if (p && !(p->flags & KDA_FLAG_CHANNEL_GATES))
+    return fail(KDA_ERR_INVALID_ARG, "kda_gdn2_bwd needs KDA_FLAG_CHANNEL_GATES in the problem's flags");
+  if (p && p->total_tokens > 0) {
+    CHECK_PTR(write_raw);
+    CHECK_PTR(dwrite_raw);
+  }
+  return backward(p, q, k, v, g_raw, erase_raw, write_raw, A_log, dt_bias, dO, dhT, ctx, dq, dk, dv, dg_raw,
+                  derase_raw, dwrite_raw, dA_log, ddt_bias, dh0, workspace, stream);
 }
 
 kda_status kda_query_device_status(const void* buf, void* stream) {

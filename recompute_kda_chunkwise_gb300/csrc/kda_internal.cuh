@@ -39,6 +39,9 @@ struct FwdArgs {
   // ctx (NULL: no helper CTAs)
   uint32_t* xflags;
   uint8_t* xbuf;
+  // GDN-2 (KDA_FLAG_CHANNEL_GATES, CUDA-core kernels only): raw write gate
+  // [S,H,D]; b is then the raw erase gate [S,H,D]
+  const void* w = nullptr;
 };
 
 struct BwdArgs {
@@ -67,6 +70,11 @@ struct BwdArgs {
   const int32_t* cu;
   int N, H;
   float scale, lower, eps;
+  // GDN-2 (KDA_FLAG_CHANNEL_GATES, CUDA-core kernels only): raw write gate
+  // and its gradient [S,H,D]; b / db are then the raw erase gate and its
+  // gradient [S,H,D]
+  const void* w = nullptr;
+  void* dw = nullptr;
 };
 
 // Index of the checkpoint slot of (sequence n, segment j) relative to slot 0:

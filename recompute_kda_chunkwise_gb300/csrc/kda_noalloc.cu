@@ -66,6 +66,8 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
   if (st != KDA_OK) return st;
   if ((dhT && !aligned16(dhT)) || (dh0 && !aligned16(dh0)))
     return kda::set_error(KDA_ERR_INVALID_ARG, "dhT / dh0 is not 16-byte aligned");
+  if (p->flags & KDA_FLAG_CHANNEL_GATES)
+    return kda::set_error(KDA_ERR_INVALID_ARG, "KDA_FLAG_CHANNEL_GATES: kda_bwd_noalloc runs KDA only");
   if (p->flags & KDA_FLAG_NO_CHECKPOINTS)
     return kda::set_error(KDA_ERR_INVALID_ARG,
                           "KDA_FLAG_NO_CHECKPOINTS: a forward without checkpoints cannot feed the backward");

@@ -21,6 +21,16 @@
 // 17 tokens); these kernels use C = 16 (D = 64)
 // and C = 8 (D = 128, to fit the backward's tiles in shared memory).
 //
+// GDN-2 (template flag CG, "KDA at the production shape ...", section 1.6
+// and the section 2.1 op table): the scalar beta becomes a channel-wise erase
+// gate Be[r,i] = sigmoid(erase_raw) on key channels and a write gate
+// Wr[r,j] = sigmoid(write_raw) on value channels, so with Xw = Be*Kg and
+// Xu = Wr*V the intra products read
+//   Abar[r,s] = sum_i Xw_ri Ki_si (s < r),  T = (I + Abar)^-1,
+//   W = T Xw,  U = T Xu,
+// and everything after U~ = U - W H is unchanged (the state update writes
+// kh r^T). KDA is the case Be = Wr = beta.
+//
 // Backward (recompute policy): the forward stores fp32 states every 1024
 // tokens. For each such segment, in reverse order, the backward rebuilds the
 // chunk-start states of the segment into per-CTA scratch with the same code
@@ -57,16 +67,21 @@ struct Tiles {
   float *Abar, *Aqk, *Tm;
   float *bet, *nq, *nk;
   float *gam, *dtb;
-  __device__ float* carve(float* p) {
+  float *Be, *Wr;  // GDN-2 only: erase gates [C][LD] (key channels), write gates [C][LD] (value channels)
+  __device__ float* carve(float* p, bool cg = false) {
     Qh = p; p += TILE; Kh = p; p += TILE; Gc = p; p += TILE; Vv = p; p += TILE;
     Qg = p; p += TILE; Kg = p; p += TILE; Ki = p; p += TILE; Kb = p; p += TILE;
     Ww = p; p += TILE; Uu = p; p += TILE;
     Abar = p; p += SQ; Aqk = p; p += SQ; Tm = p; p += SQ;
     bet = p; p += C; nq = p; p += C; nk = p; p += C;
     gam = p; p += D; dtb = p; p += D;
+    Be = Wr = nullptr;
+    if (cg) {
+      Be = p; p += TILE; Wr = p; p += TILE;
+    }
     return p;
   }
-  static constexpr int floats() { return 10 * TILE + 3 * SQ + 3 * C + 2 * D; }
+  static constexpr int floats(bool cg = false) { return 10 * TILE + 3 * SQ + 3 * C + 2 * D + (cg ? 2 * TILE : 0); }
 };
 
 // Loads rows [t0, t0 + rows) of head h (zeros beyond `rows`, which makes the
@@ -75,10 +90,13 @@ struct Tiles {
 //   Gc = chunk-local inclusive cumsum of g*log2(e), gam = 2^Gc[C-1],
 //   Qg = scale*Qh*2^G, Kg = Kh*2^G, Ki = Kh*2^-G, Kb = Kh*2^(G[C-1]-G).
 // The gate is g = lower * sigmoid(exp(A_log) * (g_raw + dt_bias)).
-template <typename Tin, int D, int C>
+// With CG (GDN-2), b is the raw erase gate and w the raw write gate, both
+// [S,H,D]: Be = sigmoid(b), Wr = sigmoid(w) (zero on padded rows) and bet is
+// not used.
+template <typename Tin, int D, int C, bool CG = false>
 __device__ void chunk_prologue(const Tiles<D, C>& t, const Tin* q, const Tin* k, const Tin* v,
-                               const Tin* g, const Tin* b, int64_t t0, int rows, int h, int H,
-                               float expA, float scale, float lower, float eps) {
+                               const Tin* g, const Tin* b, const Tin* w, int64_t t0, int rows, int h,
+                               int H, float expA, float scale, float lower, float eps) {
   constexpr int LD = D + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int x = tid; x < C * D; x += kNT) {
@@ -95,8 +113,18 @@ __device__ void chunk_prologue(const Tiles<D, C>& t, const Tin* q, const Tin* k,
     t.Kh[r * LD + i] = kv;
     t.Gc[r * LD + i] = gv;
     t.Vv[r * LD + i] = vv;
+    if constexpr (CG) {
+      float be = 0.f, wr = 0.f;
+      if (r < rows) {
+        const int64_t off = ((t0 + r) * H + h) * (int64_t)D + i;
+        be = sigmoidf_(ldf(b + off));
+        wr = sigmoidf_(ldf(w + off));
+      }
+      t.Be[r * LD + i] = be;
+      t.Wr[r * LD + i] = wr;
+    }
   }
-  if (tid < C) t.bet[tid] = tid < rows ? sigmoidf_(ldf(b + (t0 + tid) * H + h)) : 0.f;
+  if (!CG && tid < C) t.bet[tid] = tid < rows ? sigmoidf_(ldf(b + (t0 + tid) * H + h)) : 0.f;
   __syncthreads();
   for (int r = warp; r < C; r += kNT / 32) {
     float sq = 0.f, sk = 0.f;
@@ -141,8 +169,10 @@ __device__ void chunk_prologue(const Tiles<D, C>& t, const Tin* q, const Tin* k,
 }
 
 // Abar (strictly lower), Aqk (lower incl. diagonal), T = (I + diag(beta)Abar)^-1,
-// W = T diag(beta) Kg, U = T diag(beta) V.
-template <int D, int C>
+// W = T diag(beta) Kg, U = T diag(beta) V. With CG (GDN-2) Abar carries the
+// erase gates, Abar[r,s] = sum_i Be_ri Kg_ri Ki_si, T = (I + Abar)^-1,
+// W = T (Be*Kg) and U = T (Wr*V).
+template <int D, int C, bool CG = false>
 __device__ void chunk_intra(const Tiles<D, C>& t) {
   constexpr int LD = D + 1, CP = C + 1;
   const int tid = threadIdx.x;
@@ -152,7 +182,10 @@ __device__ void chunk_intra(const Tiles<D, C>& t) {
     if (s <= r) {
       for (int i = 0; i < D; ++i) {
         const float ki = t.Ki[s * LD + i];
-        akk += t.Kg[r * LD + i] * ki;
+        if constexpr (CG)
+          akk += t.Be[r * LD + i] * t.Kg[r * LD + i] * ki;
+        else
+          akk += t.Kg[r * LD + i] * ki;
         aqk += t.Qg[r * LD + i] * ki;
       }
     }
@@ -171,7 +204,7 @@ __device__ void chunk_intra(const Tiles<D, C>& t) {
           val = 0.f;
         } else {
           val = 0.f;
-          const float br = t.bet[r];
+          const float br = CG ? 1.f : t.bet[r];
           for (int s = j; s < r; ++s) val -= br * t.Abar[r * CP + s] * t.Tm[s * CP + j];
         }
         t.Tm[r * CP + j] = val;
@@ -183,10 +216,18 @@ __device__ void chunk_intra(const Tiles<D, C>& t) {
   for (int x = tid; x < C * D; x += kNT) {
     const int r = x / D, i = x % D;
     float w = 0.f, u = 0.f;
-    for (int s = 0; s <= r; ++s) {
-      const float ts = t.Tm[r * CP + s] * t.bet[s];
-      w += ts * t.Kg[s * LD + i];
-      u += ts * t.Vv[s * LD + i];
+    if constexpr (CG) {
+      for (int s = 0; s <= r; ++s) {
+        const float ts = t.Tm[r * CP + s];
+        w += ts * (t.Be[s * LD + i] * t.Kg[s * LD + i]);
+        u += ts * (t.Wr[s * LD + i] * t.Vv[s * LD + i]);
+      }
+    } else {
+      for (int s = 0; s <= r; ++s) {
+        const float ts = t.Tm[r * CP + s] * t.bet[s];
+        w += ts * t.Kg[s * LD + i];
+        u += ts * t.Vv[s * LD + i];
+      }
     }
     t.Ww[r * LD + i] = w;
     t.Uu[r * LD + i] = u;
@@ -255,12 +296,12 @@ __device__ void chunk_output(const Tiles<D, C>& t, const float* Hs, int ldh, Tin
   __syncthreads();
 }
 
-template <typename Tin, int D>
+template <typename Tin, int D, bool CG>
 __global__ void __launch_bounds__(kNT, 1) kda_fwd_simt_kernel(const FwdArgs a) {
   constexpr int C = SimtChunk<D>::C, V = D;
   extern __shared__ float sm[];
   Tiles<D, C> t;
-  float* Hs = t.carve(sm);  // [D][V]
+  float* Hs = t.carve(sm, CG);  // [D][V]
   const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
   const int64_t bos = a.cu[n], eos = a.cu[n + 1];
   const int tid = threadIdx.x;
@@ -269,6 +310,7 @@ __global__ void __launch_bounds__(kNT, 1) kda_fwd_simt_kernel(const FwdArgs a) {
   const Tin* v = static_cast<const Tin*>(a.v);
   const Tin* g = static_cast<const Tin*>(a.g);
   const Tin* b = static_cast<const Tin*>(a.b);
+  const Tin* w = static_cast<const Tin*>(a.w);
   Tin* o = static_cast<Tin*>(a.o);
   for (int i = tid; i < D; i += kNT) t.dtb[i] = a.dt_bias[h * D + i];
   // initial state h0 [N][H][D][V] (zero when NULL)
@@ -283,8 +325,8 @@ __global__ void __launch_bounds__(kNT, 1) kda_fwd_simt_kernel(const FwdArgs a) {
       for (int x = tid; x < D * V; x += kNT) dst[x] = Hs[x];
     }
     const int rows = (int)min((int64_t)C, eos - t0);
-    chunk_prologue<Tin, D, C>(t, q, k, v, g, b, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
-    chunk_intra<D, C>(t);
+    chunk_prologue<Tin, D, C, CG>(t, q, k, v, g, b, w, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
+    chunk_intra<D, C, CG>(t);
     state_residual<D, C>(t, Hs, V);
     chunk_output<Tin, D, C>(t, Hs, V, o, t0, rows, h, a.H);
     state_update<D, C>(t, Hs, V);
@@ -321,7 +363,7 @@ struct BwdTiles {
   static constexpr int floats() { return 6 * TILE + 3 * SQ + 3 * C + D + 2 * kNT + 2 * D * LDH; }
 };
 
-template <typename Tin, int D>
+template <typename Tin, int D, bool CG>
 __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
   constexpr int C = SimtChunk<D>::C, V = D, LD = D + 1, CP = C + 1, LDH = V + 1;
   constexpr int CPS = kCkptTokens / C;  // chunks per checkpoint segment
@@ -329,19 +371,21 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
   extern __shared__ float sm[];
   Tiles<D, C> t;
   BwdTiles<D, C> u;
-  u.carve(t.carve(sm));
+  u.carve(t.carve(sm, CG));
   const int tid = threadIdx.x;
   const Tin* q = static_cast<const Tin*>(a.q);
   const Tin* k = static_cast<const Tin*>(a.k);
   const Tin* v = static_cast<const Tin*>(a.v);
   const Tin* g = static_cast<const Tin*>(a.g);
   const Tin* b = static_cast<const Tin*>(a.b);
+  const Tin* w = static_cast<const Tin*>(a.w);
   const Tin* dO = static_cast<const Tin*>(a.dO);
   Tin* dq = static_cast<Tin*>(a.dq);
   Tin* dk = static_cast<Tin*>(a.dk);
   Tin* dv = static_cast<Tin*>(a.dv);
   Tin* dg = static_cast<Tin*>(a.dg);
-  Tin* db = static_cast<Tin*>(a.db);
+  Tin* db = static_cast<Tin*>(a.db);  // CG: gradient of the raw erase gate [S,H,D]
+  Tin* dw = static_cast<Tin*>(a.dw);  // CG: gradient of the raw write gate [S,H,D]
   float* scratch = a.scratch + (int64_t)blockIdx.x * CPS * D * LDH;
   const int nitems = a.N * a.H;
 
@@ -376,8 +420,8 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
         if (c == c1 - 1) break;
         const int64_t t0 = bos + (int64_t)c * C;
         const int rows = (int)min((int64_t)C, eos - t0);
-        chunk_prologue<Tin, D, C>(t, q, k, v, g, b, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
-        chunk_intra<D, C>(t);
+        chunk_prologue<Tin, D, C, CG>(t, q, k, v, g, b, w, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
+        chunk_intra<D, C, CG>(t);
         state_residual<D, C>(t, u.Hc, LDH);
         state_update<D, C>(t, u.Hc, LDH);
       }
@@ -394,8 +438,8 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
             u.dOt[r * LD + j] = r < rows ? ldf(dO + ((t0 + r) * a.H + h) * (int64_t)V + j) : 0.f;
           }
         }
-        chunk_prologue<Tin, D, C>(t, q, k, v, g, b, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
-        chunk_intra<D, C>(t);
+        chunk_prologue<Tin, D, C, CG>(t, q, k, v, g, b, w, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
+        chunk_intra<D, C, CG>(t);
         state_residual<D, C>(t, u.Hc, LDH);  // t.Uu = U~, t.Ww = W
 
         // dU~[r][j] = sum_{r'>=r} Aqk[r'][r] dO[r'][j] + sum_i Kb[r][i] dH[i][j]
@@ -484,9 +528,15 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
             for (int j = 0; j < V; ++j) dm += u.dOt[r * LD + j] * t.Uu[s * LD + j];
           if (s < r) {
             float d1 = 0.f, d2 = 0.f;
-            for (int i = 0; i < D; ++i) d1 += u.dWt[r * LD + i] * t.Kg[s * LD + i];
-            for (int j = 0; j < V; ++j) d2 += u.dUt[r * LD + j] * t.Vv[s * LD + j];
-            dt = t.bet[s] * (d1 + d2);
+            if constexpr (CG) {  // dW Xw^T + dU~ Xu^T with the channel gates
+              for (int i = 0; i < D; ++i) d1 += u.dWt[r * LD + i] * (t.Be[s * LD + i] * t.Kg[s * LD + i]);
+              for (int j = 0; j < V; ++j) d2 += u.dUt[r * LD + j] * (t.Wr[s * LD + j] * t.Vv[s * LD + j]);
+              dt = d1 + d2;
+            } else {
+              for (int i = 0; i < D; ++i) d1 += u.dWt[r * LD + i] * t.Kg[s * LD + i];
+              for (int j = 0; j < V; ++j) d2 += u.dUt[r * LD + j] * t.Vv[s * LD + j];
+              dt = t.bet[s] * (d1 + d2);
+            }
           }
           u.dM[r * CP + s] = dm;
           u.dT[r * CP + s] = dt;
@@ -524,13 +574,22 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
           }
         }
         __syncthreads();
-        // dv = beta dXu
+        // dv = beta dXu (CG: dv = Wr dXu and the raw write-gate gradient V dXu Wr (1 - Wr))
         for (int x = tid; x < C * V; x += kNT) {
           const int r = x / V, j = x % V;
-          if (r < rows) stf(dv + ((t0 + r) * a.H + h) * (int64_t)V + j, t.bet[r] * u.dOt[r * LD + j]);
+          if (r < rows) {
+            const int64_t off = ((t0 + r) * a.H + h) * (int64_t)V + j;
+            if constexpr (CG) {
+              const float wr = t.Wr[r * LD + j], dxu = u.dOt[r * LD + j];
+              stf(dv + off, wr * dxu);
+              stf(dw + off, t.Vv[r * LD + j] * dxu * wr * (1.f - wr));
+            } else {
+              stf(dv + off, t.bet[r] * u.dOt[r * LD + j]);
+            }
+          }
         }
         // dbeta (before the beta-sigmoid): Xw, Xu and the beta factor of A
-        {
+        if constexpr (!CG) {
           const int warp = tid >> 5, lane = tid & 31;
           for (int r = warp; r < C; r += kNT / 32) {
             float s_ = 0.f;
@@ -545,7 +604,23 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
         for (int x = tid; x < C * D; x += kNT) {
           const int r = x / D, i = x % D;
           const float G = t.Gc[r * LD + i], e = exp2f(G), ei = exp2f(-G);
-          const float br = t.bet[r], dxw = u.dWt[r * LD + i];
+          const float dxw = u.dWt[r * LD + i];
+          if constexpr (CG) {
+            // dXw = T^T dW + dA Ki; Xw = Be*Kg gives dBe = Kg dXw and dKg = Be dXw;
+            // dKi = dA^T Xw
+            float a1 = 0.f, a2 = 0.f, m1 = 0.f, m2 = 0.f;
+            for (int s = 0; s < r; ++s) a1 += u.dT[r * CP + s] * t.Ki[s * LD + i];
+            for (int s = r + 1; s < C; ++s) a2 += u.dT[s * CP + r] * (t.Be[s * LD + i] * t.Kg[s * LD + i]);
+            for (int s = 0; s <= r; ++s) m1 += u.dM[r * CP + s] * t.Ki[s * LD + i];
+            for (int s = r; s < C; ++s) m2 += u.dM[s * CP + r] * t.Qg[s * LD + i];
+            const float be = t.Be[r * LD + i], kg = t.Kg[r * LD + i], dX = dxw + a1;
+            u.dQ[r * LD + i] += m1 * e;
+            u.dK[r * LD + i] += be * e * dX + (a2 + m2) * ei;
+            u.dGt[r * LD + i] += be * dX * kg + m1 * t.Qg[r * LD + i] - (a2 + m2) * t.Ki[r * LD + i];
+            if (r < rows) stf(db + ((t0 + r) * a.H + h) * (int64_t)D + i, kg * dX * be * (1.f - be));
+            continue;
+          }
+          const float br = t.bet[r];
           float a1 = 0.f, a2 = 0.f, m1 = 0.f, m2 = 0.f;
           for (int s = 0; s < r; ++s) a1 += u.dT[r * CP + s] * t.Ki[s * LD + i];
           a1 *= br;
@@ -601,7 +676,7 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
             acc_alog += dz * z;
           }
         }
-        if (tid < C && tid < rows) {
+        if (!CG && tid < C && tid < rows) {
           const float bt = t.bet[tid];
           stf(db + (t0 + tid) * a.H + h, u.dbet[tid] * bt * (1.f - bt));
         }
@@ -647,11 +722,11 @@ __global__ void kda_param_reduce_kernel(const float* partial, int N, int H, int 
   }
 }
 
-template <typename Tin, int D>
+template <typename Tin, int D, bool CG = false>
 kda_status launch_fwd_t(const kda_problem* p, const FwdArgs& a, cudaStream_t s) {
   constexpr int C = SimtChunk<D>::C;
-  const size_t smem = sizeof(float) * (Tiles<D, C>::floats() + D * D);
-  auto kern = kda_fwd_simt_kernel<Tin, D>;
+  const size_t smem = sizeof(float) * (Tiles<D, C>::floats(CG) + D * D);
+  auto kern = kda_fwd_simt_kernel<Tin, D, CG>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KDA_ERR_CUDA;
   const int grid = p->num_seqs * p->num_heads;
@@ -665,11 +740,11 @@ int bwd_ctas(const kda_problem* p) {
   return items < kMaxBwdCtas ? items : kMaxBwdCtas;
 }
 
-template <typename Tin, int D>
+template <typename Tin, int D, bool CG = false>
 kda_status launch_bwd_t(const kda_problem* p, const BwdArgs& a, cudaStream_t s) {
   constexpr int C = SimtChunk<D>::C;
-  const size_t smem = sizeof(float) * (Tiles<D, C>::floats() + BwdTiles<D, C>::floats());
-  auto kern = kda_bwd_simt_kernel<Tin, D>;
+  const size_t smem = sizeof(float) * (Tiles<D, C>::floats(CG) + BwdTiles<D, C>::floats());
+  auto kern = kda_bwd_simt_kernel<Tin, D, CG>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KDA_ERR_CUDA;
   int dev = 0, sms = 0;
@@ -688,6 +763,13 @@ kda_status launch_bwd_t(const kda_problem* p, const BwdArgs& a, cudaStream_t s) 
 
 kda_status launch_fwd_simt(const kda_problem* p, const FwdArgs& a, cudaStream_t s) {
   const bool bf = p->dtype == KDA_DTYPE_BF16;
+  if (p->flags & KDA_FLAG_CHANNEL_GATES) {
+    if (p->head_dim == 64)
+      return bf ? launch_fwd_t<__nv_bfloat16, 64, true>(p, a, s) : launch_fwd_t<float, 64, true>(p, a, s);
+    if (p->head_dim == 128)
+      return bf ? launch_fwd_t<__nv_bfloat16, 128, true>(p, a, s) : launch_fwd_t<float, 128, true>(p, a, s);
+    return KDA_ERR_UNSUPPORTED;
+  }
   if (p->head_dim == 64) return bf ? launch_fwd_t<__nv_bfloat16, 64>(p, a, s) : launch_fwd_t<float, 64>(p, a, s);
   if (p->head_dim == 128) return bf ? launch_fwd_t<__nv_bfloat16, 128>(p, a, s) : launch_fwd_t<float, 128>(p, a, s);
   return KDA_ERR_UNSUPPORTED;
@@ -695,6 +777,13 @@ kda_status launch_fwd_simt(const kda_problem* p, const FwdArgs& a, cudaStream_t 
 
 kda_status launch_bwd_simt(const kda_problem* p, const BwdArgs& a, cudaStream_t s) {
   const bool bf = p->dtype == KDA_DTYPE_BF16;
+  if (p->flags & KDA_FLAG_CHANNEL_GATES) {
+    if (p->head_dim == 64)
+      return bf ? launch_bwd_t<__nv_bfloat16, 64, true>(p, a, s) : launch_bwd_t<float, 64, true>(p, a, s);
+    if (p->head_dim == 128)
+      return bf ? launch_bwd_t<__nv_bfloat16, 128, true>(p, a, s) : launch_bwd_t<float, 128, true>(p, a, s);
+    return KDA_ERR_UNSUPPORTED;
+  }
   if (p->head_dim == 64) return bf ? launch_bwd_t<__nv_bfloat16, 64>(p, a, s) : launch_bwd_t<float, 64>(p, a, s);
   if (p->head_dim == 128) return bf ? launch_bwd_t<__nv_bfloat16, 128>(p, a, s) : launch_bwd_t<float, 128>(p, a, s);
   return KDA_ERR_UNSUPPORTED;
@@ -711,7 +800,7 @@ kda_status launch_bwd_simt_ctas(const kda_problem* p, const BwdArgs& a, cudaStre
     constexpr int D = decltype(d_tag)::value;
     constexpr int C = SimtChunk<D>::C;
     const size_t smem = sizeof(float) * (Tiles<D, C>::floats() + BwdTiles<D, C>::floats());
-    auto kern = kda_bwd_simt_kernel<Tin, D>;
+    auto kern = kda_bwd_simt_kernel<Tin, D, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return KDA_ERR_CUDA;
     kern<<<ctas, kNT, smem, s>>>(a);

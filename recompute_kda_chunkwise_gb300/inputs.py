@@ -13,6 +13,11 @@ seed, draws in this fixed order: Q, K, V, raw gate, raw beta, dO (each in
 fp32, then cast to the workload dtype), then -- only when ``param_std`` > 0 --
 A_log and dt_bias (fp32). Otherwise A_log and dt_bias are zeros. The raw gate
 is N(gate_mean, gate_std); everything else is N(0, 1).
+
+GDN-2 workloads (``gates == "channel"``, the channel-wise erase / write gate
+form of "KDA at the production shape ...", section 1.6) draw the raw erase
+gate and the raw write gate, both [S,H,D] N(0, 1), in place of raw beta:
+Q, K, V, raw gate, raw erase, raw write, dO, then A_log / dt_bias as above.
 """
 from __future__ import annotations
 
@@ -35,6 +40,7 @@ class Workload:
     gate_std: float = 1.0
     param_std: float = 0.0  # std of A_log / dt_bias draws (0 -> zeros)
     scale: float = 1.0
+    gates: str = "scalar"   # "scalar" (KDA beta) or "channel" (GDN-2 erase / write gates)
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
     @property
@@ -75,6 +81,13 @@ WORKLOADS = {
     "varlen8_8k_h96_d128_bf16": Workload("varlen8_8k_h96_d128_bf16",
                                          (512, 1536, 768, 1280, 256, 1792, 1024, 1024), 96, 128,
                                          "bf16", 20267),
+    # GDN-2 (channel-wise erase / write gates): the pages' own fp32 preset
+    # shape (b=10 t=512 h=12 K=V=64) and a bf16 D = 128 shape of the
+    # MBS8 x 8K x H16 workload.
+    "gdn2_b10_t512_h12_d64_f32": Workload("gdn2_b10_t512_h12_d64_f32", _equal(10, 512), 12, 64, "f32",
+                                          20268, gates="channel"),
+    "gdn2_mbs8_8k_h16_d128_bf16": Workload("gdn2_mbs8_8k_h16_d128_bf16", _equal(8, 8192), 16, 128,
+                                           "bf16", 20269, gates="channel"),
 }
 HEADLINE = "mbs1_128k_h96_d128_bf16"
 
@@ -107,7 +120,11 @@ def make_inputs(w: Workload, device="cpu", with_dO: bool = True) -> dict:
     out["k"] = normal((S, H, D))
     out["v"] = normal((S, H, D))
     out["g"] = normal((S, H, D), w.gate_mean, w.gate_std)
-    out["beta"] = normal((S, H))
+    if w.gates == "channel":
+        out["erase"] = normal((S, H, D))
+        out["write"] = normal((S, H, D))
+    else:
+        out["beta"] = normal((S, H))
     out["dO"] = normal((S, H, D)) if with_dO else None
     if w.param_std > 0:
         out["A_log"] = torch.randn((H,), generator=gen, device=dev) * w.param_std

@@ -63,6 +63,10 @@ def load_library(path: str = LIB_PATH):
             lib.kda_bwd.argtypes = [P] + [vp] * 20
             lib.kda_bwd_noalloc.restype = ctypes.c_int
             lib.kda_bwd_noalloc.argtypes = [P] + [vp] * 19
+            lib.kda_gdn2_fwd.restype = ctypes.c_int
+            lib.kda_gdn2_fwd.argtypes = [P] + [vp] * 13
+            lib.kda_gdn2_bwd.restype = ctypes.c_int
+            lib.kda_gdn2_bwd.argtypes = [P] + [vp] * 22
             lib.kda_query_device_status.restype = ctypes.c_int
             lib.kda_query_device_status.argtypes = [vp, vp]
             lib.kda_status_string.restype = ctypes.c_char_p
@@ -86,6 +90,7 @@ def _check(status: int, where: str):
 KDA_FLAG_FORCE_SIMT = 1
 KDA_FLAG_TEST_TIMEOUT = 2  # test only: the forward's bounded wait runs out (see include/kda.h)
 KDA_FLAG_NO_CHECKPOINTS = 4  # inference: ctx holds no checkpoints (scratch for the forward only)
+KDA_FLAG_CHANNEL_GATES = 8  # GDN-2 problem (channel-wise erase / write gates)
 
 
 def make_problem(total_tokens: int, num_seqs: int, num_heads: int, head_dim: int, dtype,
@@ -243,9 +248,102 @@ def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO, ctx, *, sc
     return outs
 
 
+def gdn2_fwd(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
+             lower_bound: float = -5.0, eps: float = 1e-6, save_ctx: bool = True, out=None,
+             ctx=None, h0=None, final_state=False):
+    """GDN-2 forward (kda_gdn2_fwd): KDA with the scalar beta replaced by the
+    channel-wise erase gate sigmoid(erase) on key channels and write gate
+    sigmoid(write) on value channels; erase and write are [S, H, D] in q's
+    dtype. Returns (o, ctx) or (o, ctx, hT) as kda_fwd does."""
+    _check_tensors(q, k, v, g, erase, write, params=(A_log, dt_bias))
+    _check_state(h0, q, cu_seqlens, "h0")
+    flags = KDA_FLAG_CHANNEL_GATES | (0 if save_ctx else KDA_FLAG_NO_CHECKPOINTS)
+    p = _problem_from(q, None, cu_seqlens, scale, lower_bound, eps, flags)
+    hT = None
+    if final_state is not False and final_state is not None:
+        hT = _state_like(q, cu_seqlens) if final_state is True else final_state
+        _check_state(hT, q, cu_seqlens, "final_state")
+    o = torch.empty_like(q) if out is None else out
+    if ctx is None:
+        ctx = torch.empty(ctx_bytes(p), dtype=torch.uint8, device=q.device)
+    elif ctx.numel() * ctx.element_size() < ctx_bytes(p):
+        raise ValueError("ctx buffer too small")
+    st = load_library().kda_gdn2_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(erase),
+                                     _ptr(write), _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(o), _ptr(hT),
+                                     _ptr(ctx), _stream_handle(q.device))
+    _check(st, "kda_gdn2_fwd")
+    if not save_ctx:
+        ctx = None
+    return (o, ctx) if hT is None else (o, ctx, hT)
+
+
+def gdn2_bwd(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, dO, ctx, *, scale: float = 1.0,
+             lower_bound: float = -5.0, eps: float = 1e-6, workspace=None, outs=None, dht=None,
+             want_dh0: bool = False):
+    """GDN-2 backward (kda_gdn2_bwd). Returns dict dq, dk, dv, dg, derase,
+    dwrite, dA_log, ddt_bias, and dh0 when want_dh0."""
+    _check_tensors(q, k, v, g, erase, write, dO, params=(A_log, dt_bias))
+    _check_state(dht, q, cu_seqlens, "dht")
+    p = _problem_from(q, None, cu_seqlens, scale, lower_bound, eps, KDA_FLAG_CHANNEL_GATES)
+    if outs is None:
+        outs = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                    dg=torch.empty_like(g), derase=torch.empty_like(erase),
+                    dwrite=torch.empty_like(write), dA_log=torch.empty_like(A_log),
+                    ddt_bias=torch.empty_like(dt_bias))
+    if want_dh0 and outs.get("dh0") is None:
+        outs["dh0"] = _state_like(q, cu_seqlens)
+    _check_state(outs.get("dh0"), q, cu_seqlens, "dh0")
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(p), dtype=torch.uint8, device=q.device)
+    elif workspace.numel() * workspace.element_size() < workspace_bytes(p):
+        raise ValueError("workspace buffer too small")
+    st = load_library().kda_gdn2_bwd(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(erase), _ptr(write), _ptr(A_log),
+        _ptr(dt_bias), _ptr(dO), _ptr(dht), _ptr(ctx), _ptr(outs["dq"]), _ptr(outs["dk"]),
+        _ptr(outs["dv"]), _ptr(outs["dg"]), _ptr(outs["derase"]), _ptr(outs["dwrite"]),
+        _ptr(outs["dA_log"]), _ptr(outs["ddt_bias"]), _ptr(outs.get("dh0")), _ptr(workspace),
+        _stream_handle(q.device))
+    _check(st, "kda_gdn2_bwd")
+    return outs
+
+
 def query_device_status(buf) -> int:
     """Status word written by the kernels into a ctx or workspace buffer."""
     return int(load_library().kda_query_device_status(_ptr(buf), _stream_handle(buf.device)))
+
+
+class GDN2Function(torch.autograd.Function):
+    """Autograd wrapper of the GDN-2 operator (saves the inputs and ctx only)."""
+
+    @staticmethod
+    def forward(actx, q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, h0, output_final_state,
+                scale, lower_bound, eps):
+        r = gdn2_fwd(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, scale=scale,
+                     lower_bound=lower_bound, eps=eps, save_ctx=True, h0=h0,
+                     final_state=bool(output_final_state))
+        actx.save_for_backward(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, r[1])
+        actx.args = (scale, lower_bound, eps, h0 is not None)
+        return (r[0], r[2]) if output_final_state else r[0]
+
+    @staticmethod
+    def backward(actx, dO, dht=None):
+        q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, ctx = actx.saved_tensors
+        scale, lower_bound, eps, has_h0 = actx.args
+        r = gdn2_bwd(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, dO.contiguous(), ctx,
+                     scale=scale, lower_bound=lower_bound, eps=eps,
+                     dht=None if dht is None else dht.contiguous(), want_dh0=has_h0)
+        return (r["dq"], r["dk"], r["dv"], r["dg"], r["derase"], r["dwrite"], r["dA_log"],
+                r["ddt_bias"], None, r.get("dh0"), None, None, None, None)
+
+
+def gdn2(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, scale: float = 1.0,
+         lower_bound: float = -5.0, eps: float = 1e-6, initial_state=None,
+         output_final_state: bool = False):
+    """Differentiable GDN-2 (channel-wise erase / write gates) over packed
+    sequences; arguments as for ``kda`` with erase / write [S, H, D] in place
+    of beta."""
+    return GDN2Function.apply(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, initial_state,
+                              output_final_state, scale, lower_bound, eps)
 
 
 class KDAFunction(torch.autograd.Function):

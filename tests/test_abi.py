@@ -91,7 +91,7 @@ def test_invalid_arguments_are_rejected_on_host(lib):
     p.dtype = 7
     assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, nul, nul) == 2
     p.dtype = 0
-    p.flags = 8  # no such flag
+    p.flags = 16  # no such flag
     assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, nul, nul) == 1
     assert b"unknown flags" in lib.kda_last_error_message()
     p.flags = K.KDA_FLAG_FORCE_SIMT | K.KDA_FLAG_TEST_TIMEOUT  # both known: sizes still answer
@@ -102,6 +102,39 @@ def test_invalid_arguments_are_rejected_on_host(lib):
     assert lib.kda_ctx_bytes(ctypes.byref(p)) == 256
     assert lib.kda_bwd(ctypes.byref(p), *([al] * 8), nul, *([al] * 8), nul, al, nul) == 1
     assert b"NO_CHECKPOINTS" in lib.kda_last_error_message()
+
+
+def test_gdn2_entry_points_and_flag_on_host(lib):
+    cu = torch.tensor([0, 16], dtype=torch.int32)  # host tensor: never dereferenced
+    nul = ctypes.c_void_p(0)
+    al = ctypes.c_void_p(0x1000)
+    # GDN-2 problems size ctx / workspace for the CUDA-core kernels
+    g = K.make_problem(131072, 1, 96, 128, torch.bfloat16, flags=K.KDA_FLAG_CHANNEL_GATES)
+    simt = K.make_problem(131072, 1, 96, 128, torch.bfloat16, flags=K.KDA_FLAG_FORCE_SIMT)
+    assert K.kernel_family(g) == 0
+    assert K.ctx_bytes(g) == K.ctx_bytes(simt) and K.workspace_bytes(g) == K.workspace_bytes(simt)
+    p = K.make_problem(16, 1, 2, 64, torch.bfloat16, cu, flags=K.KDA_FLAG_CHANNEL_GATES)
+    # the KDA entry points refuse a GDN-2 problem ...
+    assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, al, nul) == 1
+    assert b"kda_gdn2_fwd" in lib.kda_last_error_message()
+    assert lib.kda_bwd(ctypes.byref(p), *([al] * 8), nul, *([al] * 8), nul, al, nul) == 1
+    assert b"kda_gdn2_bwd" in lib.kda_last_error_message()
+    assert lib.kda_bwd_noalloc(ctypes.byref(p), *([al] * 8), nul, *([al] * 8), nul, nul) == 1
+    # ... and the GDN-2 entry points refuse a problem without the flag
+    # kda_gdn2_fwd(p, q, k, v, g, erase, write, A_log, dt_bias, h0, o, hT, ctx, stream)
+    p.flags = 0
+    assert lib.kda_gdn2_fwd(ctypes.byref(p), *([al] * 8), nul, al, nul, al, nul) == 1
+    assert b"KDA_FLAG_CHANNEL_GATES" in lib.kda_last_error_message()
+    # kda_gdn2_bwd(p, q, k, v, g, erase, write, A_log, dt_bias, dO, dhT, ctx, dq, dk, dv, dg,
+    #              derase, dwrite, dA_log, ddt_bias, dh0, workspace, stream)
+    assert lib.kda_gdn2_bwd(ctypes.byref(p), *([al] * 9), nul, *([al] * 10), nul, al, nul) == 1
+    p.flags = K.KDA_FLAG_CHANNEL_GATES
+    # a missing write gate is an argument error found on the host
+    assert lib.kda_gdn2_fwd(ctypes.byref(p), *([al] * 5), nul, *([al] * 2), nul, al, nul, al, nul) == 1
+    assert b"write_raw" in lib.kda_last_error_message()
+    assert lib.kda_gdn2_bwd(ctypes.byref(p), *([al] * 9), nul, *([al] * 6), nul, *([al] * 2), nul, al,
+                            nul) == 1
+    assert b"dwrite_raw" in lib.kda_last_error_message()
 
 
 def test_status_strings(lib):
