@@ -237,11 +237,13 @@ def run_reference(args, w, rank):
 
 
 FWD_METRIC = "KDA forward (inference, no checkpoints) tokens/sec"
+GDN2_FWD_METRIC = "GDN-2 forward (inference, no checkpoints) tokens/sec"
 
 
 def run_gb300_fwd(args, w, rank, world, local):
-    """Forward-only inference: kda_fwd with KDA_FLAG_NO_CHECKPOINTS (the ctx
-    holds only the status word and the helper hand-off area)."""
+    """Forward-only inference: kda_fwd (kda_gdn2_fwd for a GDN-2 workload)
+    with KDA_FLAG_NO_CHECKPOINTS (the ctx holds only the status word and the
+    helper hand-off area)."""
     import torch
     from recompute_kda_chunkwise_gb300 import make_inputs
     from recompute_kda_chunkwise_gb300 import kda as K
@@ -250,17 +252,20 @@ def run_gb300_fwd(args, w, rank, world, local):
     torch.cuda.set_device(dev)
     K.load_library()
     inp = make_inputs(w, device=dev, with_dO=False)
-    q, k, v, g, beta, A_log, dt_bias, cu = (inp[n] for n in
-                                            ["q", "k", "v", "g", "beta", "A_log", "dt_bias", "cu_seqlens"])
+    gates = gate_names(w)
+    gdn2 = w.gates == "channel"
+    args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
+    q, cu = inp["q"], inp["cu_seqlens"]
+    fwd_fn = K.gdn2_fwd if gdn2 else K.kda_fwd
     prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale,
-                          flags=K.KDA_FLAG_NO_CHECKPOINTS)
+                          flags=K.KDA_FLAG_NO_CHECKPOINTS | (K.KDA_FLAG_CHANNEL_GATES if gdn2 else 0))
     kname = {0: "simt", 1: "tc"}.get(K.kernel_family(prob), "unknown")
     scratch = torch.empty(K.ctx_bytes(prob), dtype=torch.uint8, device=dev)
     o = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        K.kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu, scale=w.scale, save_ctx=False, out=o, ctx=scratch)
+        fwd_fn(*args_in, scale=w.scale, save_ctx=False, out=o, ctx=scratch)
 
     for _ in range(args.warmup):
         step()
@@ -282,7 +287,7 @@ def run_gb300_fwd(args, w, rank, world, local):
     achieved = fwd_b / (ms_step / 1e3) / 1e9
     e2e = None
     if args.e2e_steps > 0:  # pinned host inputs -> device -> forward -> host o
-        names_in = ["q", "k", "v", "g", "beta"]
+        names_in = ["q", "k", "v", "g"] + gates
         host_in = {n: torch.empty(inp[n].shape, dtype=inp[n].dtype, pin_memory=True) for n in names_in}
         for n in names_in:
             host_in[n].copy_(inp[n])
@@ -306,7 +311,7 @@ def run_gb300_fwd(args, w, rank, world, local):
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in.values()),
                "d2h_bytes_per_step": host_o.numel() * host_o.element_size()}
     if rank == 0:
-        line = {"metric": FWD_METRIC, "value": tokens / (ms_step / 1e3), "unit": "tokens/s", "n_gpus": world,
+        line = {"metric": GDN2_FWD_METRIC if gdn2 else FWD_METRIC, "value": tokens / (ms_step / 1e3), "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
                 "data": "synthetic",
@@ -316,7 +321,7 @@ def run_gb300_fwd(args, w, rank, world, local):
                            if fwd_b > 2 * 129e6 else "inputs below L2 size: not flushed (context only)",
                            "parallelism": f"replicas{world}", "kernel_family": kname},
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
-                             "frac": achieved / peak_gbs, "traffic": None, "kernel": f"kda_fwd ({kname} kernels)",
+                             "frac": achieved / peak_gbs, "traffic": None, "kernel": f"{'kda_gdn2_fwd' if gdn2 else 'kda_fwd'} ({kname} kernels)",
                              "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": fwd_b,
                              "ms_per_launch": ms_step},
                 "cpu_baseline": None, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk.summary(),
@@ -479,8 +484,6 @@ def main(argv=None):
     if args.impl == "reference":
         run_reference(args, w, rank)
     elif args.pass_ == "fwd":
-        if w.gates == "channel":
-            raise SystemExit("--pass fwd times KDA workloads; GDN-2 workloads run fwd+bwd")
         run_gb300_fwd(args, w, rank, world, local)
     else:
         run_gb300(args, w, rank, world, local)

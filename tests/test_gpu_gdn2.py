@@ -137,3 +137,17 @@ def test_autograd_function_matches_direct_calls():
                  dt_bias="ddt_bias")
     for leaf, gname in pairs.items():
         assert torch.equal(leaves[leaf].grad, r[gname]), gname
+
+
+def test_inference_forward_matches_the_training_forward():
+    # without checkpoints (KDA_FLAG_NO_CHECKPOINTS, no ctx kept) the forward
+    # writes the same o, bit for bit, and the same final states
+    w = Workload("gdn2_infer", (1500, 33, 1), 3, 128, "bf16", seed=7800, param_std=0.3,
+                 gates="channel")
+    inp = to_dev(make_inputs(w, device="cpu"))
+    args = [inp[n] for n in ARGS]
+    o, ctx, hT = K.gdn2_fwd(*args, final_state=True)
+    o2, ctx2, hT2 = K.gdn2_fwd(*args, save_ctx=False, final_state=True)
+    torch.cuda.synchronize()
+    assert ctx2 is None
+    assert torch.equal(o, o2) and torch.equal(hT, hT2)
