@@ -292,7 +292,10 @@ kda_status kda_gdn2_fwd(const kda_problem* p, const void* q, const void* k, cons
                         const float* h0, void* o, float* hT, void* ctx, void* stream) {
   if (p && !(p->flags & KDA_FLAG_CHANNEL_GATES))
     return fail(KDA_ERR_INVALID_ARG, "kda_gdn2_fwd needs KDA_FLAG_CHANNEL_GATES in the problem's flags");
-  if (p && p->total_tokens > 0) CHECK_PTR(write_raw);
+  if (p && p->total_tokens > 0) {
+    CHECK_PTR(erase_raw);
+    CHECK_PTR(write_raw);
+  }
   return forward(p, q, k, v, g_raw, erase_raw, write_raw, A_log, dt_bias, h0, o, hT, ctx, stream);
 }
 
@@ -304,7 +307,9 @@ kda_status kda_gdn2_bwd(const kda_problem* p, const void* q, const void* k, cons
   if (p && !(p->flags & KDA_FLAG_CHANNEL_GATES))
     return fail(KDA_ERR_INVALID_ARG, "kda_gdn2_bwd needs KDA_FLAG_CHANNEL_GATES in the problem's flags");
   if (p && p->total_tokens > 0) {
+    CHECK_PTR(erase_raw);
     CHECK_PTR(write_raw);
+    CHECK_PTR(derase_raw);
     CHECK_PTR(dwrite_raw);
   }
   return backward(p, q, k, v, g_raw, erase_raw, write_raw, A_log, dt_bias, dO, dhT, ctx, dq, dk, dv, dg_raw,

@@ -135,6 +135,9 @@ def test_gdn2_entry_points_and_flag_on_host(lib):
     assert lib.kda_gdn2_bwd(ctypes.byref(p), *([al] * 9), nul, *([al] * 6), nul, *([al] * 2), nul, al,
                             nul) == 1
     assert b"dwrite_raw" in lib.kda_last_error_message()
+    assert lib.kda_gdn2_bwd(ctypes.byref(p), *([al] * 9), nul, *([al] * 5), nul, *([al] * 3), nul, al,
+                            nul) == 1
+    assert b"derase_raw" in lib.kda_last_error_message()
 
 
 def test_status_strings(lib):
