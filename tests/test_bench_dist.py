@@ -56,3 +56,21 @@ def test_algorithmic_bytes_match_per_token_head_formula():
     f, b = bench.algorithmic_bytes(w)
     # bf16: (10D + 2) forward + (18D + 4) backward bytes per token-head
     assert f + b == w.total_tokens * w.H * (28 * w.D + 6)
+
+
+def test_gdn2_algorithmic_bytes_and_sample():
+    # GDN-2: q, k, v, g, erase, write read and o written forward (14D bytes
+    # per token-head in bf16); the backward re-reads the six inputs, reads dO
+    # and writes six gradients (26D)
+    import bench
+    from recompute_kda_chunkwise_gb300 import WORKLOADS, make_inputs
+    w = WORKLOADS["gdn2_mbs8_8k_h16_d128_bf16"]
+    f, b = bench.algorithmic_bytes(w)
+    assert f == w.total_tokens * w.H * 14 * w.D and b == w.total_tokens * w.H * 26 * w.D
+    assert bench.gate_names(w) == ["erase", "write"]
+    small = WORKLOADS["gdn2_b10_t512_h12_d64_f32"]
+    sl = bench.make_sample(small, make_inputs(small), 100, 3)
+    assert sl["erase"].shape == (100, 3, 64) and sl["write"].shape == (100, 3, 64)
+    assert "beta" not in sl
+    rate, dt = bench.oracle_sample(small, sl, 2)
+    assert rate > 0 and dt > 0
