@@ -420,13 +420,27 @@ def run_gb300(args, w, rank, world, local):
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + host_o.numel() * host_o.element_size()
 
+        copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        names_fwd = [n for n in names_in if n != "dO"]
+
         def e2e_step():
-            for n in names_in:
+            # Every copy of the step stays inside the step. dO, which only the
+            # backward reads, uploads on its own stream while the forward
+            # runs, and o downloads while the backward runs.
+            for n in names_fwd:
                 inp[n].copy_(host_in[n], non_blocking=True)
-            step()
-            host_o.copy_(o, non_blocking=True)
+            copy_in.wait_stream(stream)  # after the forward's uploads and the previous backward
+            with torch.cuda.stream(copy_in):
+                dO.copy_(host_in["dO"], non_blocking=True)
+            fwd_fn(*args_in, scale=w.scale, out=o, ctx=ctx)
+            copy_out.wait_stream(stream)
+            with torch.cuda.stream(copy_out):
+                host_o.copy_(o, non_blocking=True)
+            stream.wait_stream(copy_in)
+            bwd_fn(*args_in, dO, ctx, scale=w.scale, workspace=ws, outs=grads)
             for n in names_out:
                 host_out[n].copy_(grads[n], non_blocking=True)
+            stream.wait_stream(copy_out)  # the next step's forward overwrites o
 
         e2e_step()
         torch.cuda.synchronize()
