@@ -208,7 +208,7 @@ def run_reference(args, w, rank):
     from recompute_kda_chunkwise_gb300 import make_inputs
     cores = os.cpu_count() or 1
     heads = min(cores, w.H)
-    sample_tokens = args.sample_tokens
+    sample_tokens = args.ref_sample_tokens
     small = w.with_(lengths=(min(sample_tokens, w.lengths[0]),), H=heads)
     inp = make_inputs(small, device="cpu")
     sl = make_sample(small, inp, sample_tokens, heads)
@@ -489,7 +489,10 @@ def main(argv=None):
     ap.add_argument("--pass", dest="pass_", choices=["fwdbwd", "fwd"], default="fwdbwd",
                     help="fwd: forward-only inference (no checkpoints); the default times fwd+bwd")
     ap.add_argument("--e2e-steps", type=int, default=2)
-    ap.add_argument("--sample-tokens", type=int, default=65536)
+    ap.add_argument("--sample-tokens", type=int, default=98304,
+                    help="tokens of the oracle sample behind cpu_baseline (about 10-30 s of host work)")
+    ap.add_argument("--ref-sample-tokens", type=int, default=32768,
+                    help="tokens of the oracle sample per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     from recompute_kda_chunkwise_gb300 import HEADLINE, WORKLOADS
