@@ -2,9 +2,11 @@
  * kda.h -- C ABI of the GB300-native chunk-parallel Kimi Delta Attention
  * (KDA) forward and backward library (libkda_gb300.so).
  *
- * The operation (all entry points compute the same operator; see the page
- * "KDA Memory with Recompute: FLA vs cuDNN Frontend FROST", section
- * "Sources and measurement configuration", for the operator configuration):
+ * The operation (kda_fwd, kda_bwd and kda_bwd_noalloc compute this operator;
+ * kda_gdn2_fwd / kda_gdn2_bwd compute its GDN-2 generalisation, declared
+ * further down; see the page "KDA Memory with Recompute: FLA vs cuDNN
+ * Frontend FROST", section "Sources and measurement configuration", for the
+ * operator configuration):
  *
  *   per packed sequence n (tokens cu_seqlens[n] .. cu_seqlens[n+1]-1) and
  *   per head h, with state S (D x D; S_0 = h0[n][h], zero unless given; the
