@@ -5,9 +5,10 @@
 
 A step is one kda_fwd + kda_bwd over the whole workload (every hot-path kernel
 runs once per step); for a GDN-2 workload (gdn2_*: channel-wise erase / write
-gates) it is one kda_gdn2_fwd + kda_gdn2_bwd. Inputs are seeded synthetic tensors already resident in
-HBM; they total far more than the 129 MB L2, so no flush is needed between
-steps. The value is whole-job tokens/s (all ranks' tokens / max-over-ranks
+gates) it is one kda_gdn2_fwd + kda_gdn2_bwd. By default 20 steps are timed
+after 5 warm-up steps. Inputs are seeded synthetic tensors already resident
+in HBM; they total far more than the 129 MB L2, so no flush is needed
+between steps. The value is whole-job tokens/s (all ranks' tokens / max-over-ranks
 time). Under torchrun every rank runs an independent replica of the workload
 on its own GPU (weak scaling, no collective on the data path).
 
@@ -388,6 +389,7 @@ def run_gb300(args, w, rank, world, local):
     ms_step = ms_total / args.steps
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    step_ms_median = statistics.median(e[0].elapsed_time(e[2]) for e in evs)
     status_ok = K.query_device_status(ctx) == 0 and K.query_device_status(ws) == 0
 
     tokens = w.total_tokens * world
@@ -471,7 +473,7 @@ def run_gb300(args, w, rank, world, local):
                            "l2_flush": "none needed: inputs (%.1f GB) exceed L2" % (
                                (fwd_b + bwd_b) / 1e9 / 2),
                            "parallelism": f"replicas{world}", "kernel_family": kname},
-                "peak_alloc_gib": peak_gib, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                "peak_alloc_gib": peak_gib, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_ms_median": step_ms_median,
                 "hbm_roofline_frac": step_gbs / peak_gbs,
                 "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary(),
@@ -482,8 +484,8 @@ def run_gb300(args, w, rank, world, local):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default=None)
     ap.add_argument("--pass", dest="pass_", choices=["fwdbwd", "fwd"], default="fwdbwd",
