@@ -174,17 +174,31 @@ def barrier():
         dist.barrier()
 
 
-def oracle_sample(w, inp_cpu_slices, cores):
-    """Times the fp64 oracle on a bounded sample; returns token-heads/s."""
+def oracle_sample(w, inp_cpu_slices, cores, want=False):
+    """Times the fp64 oracle on a bounded sample; returns token-heads/s and
+    seconds (and the oracle's outputs when ``want``)."""
     import oracle
     t0 = time.perf_counter()
     if "erase" in inp_cpu_slices:
-        oracle.gdn2_reference(**inp_cpu_slices, threads=cores)
+        out = oracle.gdn2_reference(**inp_cpu_slices, threads=cores)
     else:
-        oracle.kda_reference(**inp_cpu_slices, threads=cores)
+        out = oracle.kda_reference(**inp_cpu_slices, threads=cores)
     dt = time.perf_counter() - t0
     th = inp_cpu_slices["q"].shape[0] * inp_cpu_slices["q"].shape[1]
-    return th / dt, dt
+    return (th / dt, dt, out) if want else (th / dt, dt)
+
+
+def sample_parity(got, ref, bf16: bool):
+    """Error of the device output on the oracle's sample beyond the output's
+    own rounding (half an ulp of the exact value's binade in the stored
+    type), divided by RMS(ref): max(|x - ref| - ulp/2) / RMS(ref)."""
+    import numpy as np
+    x = got.double().cpu().numpy()
+    a = np.abs(ref)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    half = np.where(a > 0, np.ldexp(1.0, (e - (8 if bf16 else 24)).astype(np.int64)), 0.0)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    return max(float(np.max(np.abs(x - ref) - half)), 0.0) / rms if rms > 0 else 0.0
 
 
 def make_sample(w, inp, sample_tokens, sample_heads):
@@ -454,15 +468,21 @@ def run_gb300(args, w, rank, world, local):
         dt = max_over_ranks(time.perf_counter() - t0) / args.e2e_steps
         e2e = {"value": tokens / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    cpu_base = None
+    cpu_base = sample_check = None
     if rank == 0 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         heads = min(cores, w.H)
         sl = make_sample(w, inp, args.sample_tokens, heads)
-        rate, dt = oracle_sample(w, sl, cores)
+        rate, dt, ref = oracle_sample(w, sl, cores, want=True)
         cpu_base = {"value": rate / w.H, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                     "sample": (f"first {sl['q'].shape[0]} tokens x {heads} heads of {w.name} "
                                f"(fwd+bwd, fp64, {dt:.1f} s wall), scaled to tokens/s over all {w.H} heads")}
+        # The forward is causal, so o on the sample's tokens is exactly what
+        # the oracle computed for them: the timed run's own output, checked.
+        T_s = sl["q"].shape[0]
+        sample_check = {"tensor": "o", "tokens": T_s, "heads": heads,
+                        "max_err_over_rms": sample_parity(o[:T_s, :heads], ref["o"], w.dtype == "bf16"),
+                        "tol": 2e-2 if w.dtype == "bf16" else 1e-4}
 
     if rank == 0:
         line = {"metric": GDN2_METRIC if gdn2 else METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -475,7 +495,7 @@ def run_gb300(args, w, rank, world, local):
                            "parallelism": f"replicas{world}", "kernel_family": kname},
                 "peak_alloc_gib": peak_gib, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_ms_median": step_ms_median,
                 "hbm_roofline_frac": step_gbs / peak_gbs,
-                "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
+                "roofline": roofline, "cpu_baseline": cpu_base, "oracle_check": sample_check, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary(),
                 "device_status_ok": status_ok}
         print(json.dumps(line), flush=True)
