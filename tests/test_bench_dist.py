@@ -74,3 +74,18 @@ def test_gdn2_algorithmic_bytes_and_sample():
     assert "beta" not in sl
     rate, dt = bench.oracle_sample(small, sl, 2)
     assert rate > 0 and dt > 0
+
+
+def test_reference_arm_prints_its_line(capsys):
+    # --impl reference times the oracle on host cores only (no GPU): one JSON
+    # line with impl, cpu_baseline and a zero-copy e2e
+    import json
+    import bench
+    for name in ["tiny_t256_h2_d64_bf16", "gdn2_b10_t512_h12_d64_f32"]:
+        bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0", "--ref-sample-tokens", "64",
+                    "--workload", name])
+        line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+        assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
+        assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+        assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+        assert line["config"]["workload"] == name
