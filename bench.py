@@ -18,6 +18,7 @@ bounded sample of the same workload per step (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import functools
 import hashlib
 import json
 import os
@@ -271,9 +272,10 @@ def run_gb300_fwd(args, w, rank, world, local):
     gdn2 = w.gates == "channel"
     args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
     q, cu = inp["q"], inp["cu_seqlens"]
-    fwd_fn = K.gdn2_fwd if gdn2 else K.kda_fwd
+    simt = K.KDA_FLAG_FORCE_SIMT if (args.force_simt and not gdn2) else 0
+    fwd_fn = K.gdn2_fwd if gdn2 else functools.partial(K.kda_fwd, flags=simt)
     prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale,
-                          flags=K.KDA_FLAG_NO_CHECKPOINTS | (K.KDA_FLAG_CHANNEL_GATES if gdn2 else 0))
+                          flags=K.KDA_FLAG_NO_CHECKPOINTS | simt | (K.KDA_FLAG_CHANNEL_GATES if gdn2 else 0))
     kname = {0: "simt", 1: "tc"}.get(K.kernel_family(prob), "unknown")
     scratch = torch.empty(K.ctx_bytes(prob), dtype=torch.uint8, device=dev)
     o = torch.empty_like(q)
@@ -358,9 +360,13 @@ def run_gb300(args, w, rank, world, local):
     gdn2 = w.gates == "channel"
     args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
     q, cu, dO = inp["q"], inp["cu_seqlens"], inp["dO"]
-    fwd_fn, bwd_fn = (K.gdn2_fwd, K.gdn2_bwd) if gdn2 else (K.kda_fwd, K.kda_bwd)
-    prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale,
-                          flags=K.KDA_FLAG_CHANNEL_GATES if gdn2 else 0)
+    if gdn2:  # GDN-2 always runs the CUDA-core kernels
+        fwd_fn, bwd_fn, flags = K.gdn2_fwd, K.gdn2_bwd, K.KDA_FLAG_CHANNEL_GATES
+    else:
+        flags = K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0
+        fwd_fn = functools.partial(K.kda_fwd, flags=flags)
+        bwd_fn = functools.partial(K.kda_bwd, flags=flags)
+    prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale, flags=flags)
     family = K.kernel_family(prob)
     torch.cuda.synchronize()
 
@@ -516,6 +522,8 @@ def main(argv=None):
     ap.add_argument("--ref-sample-tokens", type=int, default=32768,
                     help="tokens of the oracle sample per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--force-simt", action="store_true",
+                    help="KDA workloads: run the fp32 CUDA-core kernels (KDA_FLAG_FORCE_SIMT) instead of tcgen05")
     args = ap.parse_args(argv)
     from recompute_kda_chunkwise_gb300 import HEADLINE, WORKLOADS
     w = WORKLOADS[args.workload or HEADLINE]
