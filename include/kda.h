@@ -100,8 +100,16 @@ typedef enum {
 #define KDA_FLAG_CHANNEL_GATES 8
 
 /* Problem description. cu_seqlens is a DEVICE pointer; the library never
- * reads it on the host (so no synchronisation), and trusts that it is
- * non-decreasing, starts at 0 and ends at total_tokens. */
+ * reads it on the host (so no synchronisation). It must start at 0, be
+ * non-decreasing and end at total_tokens. The kernels check this on the
+ * device before they load anything else: every CTA of every kernel reads the
+ * whole array, and if any of the three conditions fails, it records
+ * KDA_ERR_DEVICE_CHECK in the call's status word (ctx for the forward,
+ * workspace for the backward, the library's array for kda_bwd_noalloc) and
+ * returns without touching inputs, outputs or scratch. The outputs of such a
+ * call are then not written (dA_log / ddt_bias hold stale partial sums); the
+ * status is readable with kda_query_device_status / kda_noalloc_device_status.
+ * A forward given ctx == NULL has no status word and skips silently. */
 typedef struct {
   int64_t total_tokens;       /* S */
   int32_t num_seqs;           /* N >= 1 */
@@ -189,7 +197,8 @@ kda_status kda_bwd(const kda_problem* p,
  *   so it is slower.
  * - Every call shares the array: calls whose GPU work overlaps (other
  *   streams or threads on the same device) race and give wrong results.
- * - Device-side status is not readable for this entry point. */
+ * - Its device-side status word (a bounded wait that ran out, a malformed
+ *   cu_seqlens) sits in the array: read it with kda_noalloc_device_status. */
 kda_status kda_bwd_noalloc(const kda_problem* p,
                            const void* q, const void* k, const void* v,
                            const void* g_raw, const void* beta_raw,
@@ -197,6 +206,14 @@ kda_status kda_bwd_noalloc(const kda_problem* p,
                            const void* dO, const float* dhT, const void* ctx,
                            void* dq, void* dk, void* dv, void* dg_raw, void* dbeta_raw,
                            float* dA_log, float* ddt_bias, float* dh0, void* stream);
+
+/* Device status word of the last kda_bwd_noalloc call on the current
+ * device (the word at the head of the library's fixed scratch array),
+ * copied into a host int without any allocation. Synchronises `stream`
+ * first. Returns KDA_OK, KDA_ERR_TIMEOUT or KDA_ERR_DEVICE_CHECK as recorded
+ * by the kernels, or KDA_ERR_CUDA if the read failed. The paper has no
+ * counterpart: it completes the no-allocation entry point above. */
+kda_status kda_noalloc_device_status(void* stream);
 
 /* GDN-2: the same operator with the scalar beta replaced by two channel-wise
  * gates ("KDA at the production shape ...", section 1.6, which names GDN-2

@@ -200,7 +200,7 @@ kda_status forward(const kda_problem* p, const void* q, const void* k, const voi
   a.hT = hT;
   a.ckpt = (ctx && ckpt_bytes(p)) ? (float*)((char*)ctx + kda::kHeaderBytes) : nullptr;
   a.status = ctx ? (int*)ctx : nullptr;
-  a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
+  a.cu = p->cu_seqlens; a.S = p->total_tokens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   a.test_timeout = (p->flags & KDA_FLAG_TEST_TIMEOUT) ? 1 : 0;
   a.xflags = nullptr;
@@ -253,7 +253,7 @@ kda_status backward(const kda_problem* p, const void* q, const void* k, const vo
   a.partial = (float*)((char*)workspace + kda::kHeaderBytes);
   a.flags = flag_bytes(p) ? (uint32_t*)((char*)workspace + kda::kHeaderBytes + partial_bytes(p)) : nullptr;
   a.scratch = (float*)((char*)workspace + kda::kHeaderBytes + partial_bytes(p) + flag_bytes(p));
-  a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
+  a.cu = p->cu_seqlens; a.S = p->total_tokens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   a.w = write_raw;
   a.dw = dwrite_raw;

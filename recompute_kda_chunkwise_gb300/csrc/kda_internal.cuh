@@ -32,6 +32,7 @@ struct FwdArgs {
   float* ckpt;  // NULL: no checkpoints
   int* status;  // NULL when ckpt is NULL
   const int32_t* cu;
+  int64_t S;  // total tokens (cu[N])
   int N, H;
   float scale, lower, eps;
   int test_timeout;  // KDA_FLAG_TEST_TIMEOUT (tensor-core forward only)
@@ -68,6 +69,7 @@ struct BwdArgs {
   uint32_t* flags;  // tensor-core backward: per-item hand-off counters (NULL: no helper CTAs)
   int* status;
   const int32_t* cu;
+  int64_t S;  // total tokens (cu[N])
   int N, H;
   float scale, lower, eps;
   // GDN-2 (KDA_FLAG_CHANNEL_GATES, CUDA-core kernels only): raw write gate
@@ -101,6 +103,24 @@ __device__ __forceinline__ float warp_sum(float x) {
 // First error wins; later ones are dropped.
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
+}
+
+// Device-side check of the sequence boundaries, run by every CTA of every
+// kernel before any other global load: cu[0] == 0, cu non-decreasing and
+// cu[N] == S (the total token count). Every thread of the block must call it.
+// On failure the caller records KDA_ERR_DEVICE_CHECK and returns at once, so
+// no kernel indexes inputs, outputs, checkpoints or scratch through a
+// malformed cu_seqlens, and no CTA is left waiting for another (all CTAs
+// read the same array and reach the same verdict).
+__device__ __forceinline__ bool cu_seqlens_bad(const int32_t* cu, int N, int64_t S) {
+  int bad = 0;
+  for (int i = static_cast<int>(threadIdx.x); i <= N; i += static_cast<int>(blockDim.x)) {
+    const int64_t c = cu[i];
+    if (i == 0 && c != 0) bad = 1;
+    if (i > 0 && c < static_cast<int64_t>(cu[i - 1])) bad = 1;
+    if (c < 0 || c > S || (i == N && c != S)) bad = 1;
+  }
+  return __syncthreads_or(bad) != 0;
 }
 
 // Host-side launchers (defined in the kernel translation units).

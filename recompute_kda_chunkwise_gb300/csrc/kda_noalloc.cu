@@ -129,7 +129,7 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
   a.partial = (float*)((char*)scratch + kda::kHeaderBytes);
   a.scratch = (float*)((char*)scratch + head);
   a.flags = nullptr;  // no helper CTAs here: few CTAs fit the fixed buffer
-  a.cu = p->cu_seqlens; a.N = p->num_seqs; a.H = p->num_heads;
+  a.cu = p->cu_seqlens; a.S = p->total_tokens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   if (cudaMemsetAsync(scratch, 0, sizeof(int), s) != cudaSuccess)
     return kda::set_error(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
@@ -137,4 +137,18 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
   if (st != KDA_OK)
     return kda::set_error(st, "no-alloc backward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return KDA_OK;
+}
+
+// The status word of the last kda_bwd_noalloc call on the current device: it
+// sits at the head of the library's scratch array, so it is read here with a
+// copy from the symbol into a host int (no allocation). Synchronises `stream`.
+extern "C" kda_status kda_noalloc_device_status(void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  int word = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&word, g_kda_noalloc_scratch, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return kda::set_error(KDA_ERR_CUDA, "no-alloc status read failed: %s", cudaGetErrorString(e));
+  if (word == 0) return KDA_OK;
+  if (word == KDA_ERR_TIMEOUT) return kda::set_error(KDA_ERR_TIMEOUT, "a device-side bounded wait ran out");
+  return kda::set_error(KDA_ERR_DEVICE_CHECK, "device-side check failed (code %d)", word);
 }

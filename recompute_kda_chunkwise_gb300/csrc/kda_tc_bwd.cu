@@ -108,6 +108,7 @@ struct TcBwdArgs {
   uint32_t* flags;   // per item: last level + 1 rebuilt into each buffer, levels consumed (split mode)
   int* status;
   const int32_t* cu;
+  int64_t S;  // total tokens (cu[N])
   int N, H;
   int helpers;  // > 0: CTAs N*H .. N*H+helpers-1 rebuild segment states for the others
   float scale, lower, eps;
@@ -169,6 +170,10 @@ __device__ __forceinline__ void stage_tiles(const TcBwdArgs& a, uint32_t dst, in
 
 __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  if (cu_seqlens_bad(a.cu, a.N, a.S)) {  // before any other load, wait or allocation
+    if (threadIdx.x == 0) set_status(a.status, KDA_ERR_DEVICE_CHECK);
+    return;
+  }
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
   const uint64_t D0 = sdesc(sb, 0);  // base of every tcgen05 shared-memory descriptor
@@ -1230,6 +1235,7 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   t.flags = a.flags;
   t.status = a.status;
   t.cu = a.cu;
+  t.S = a.S;
   t.N = a.N;
   t.H = a.H;
   t.helpers = 0;

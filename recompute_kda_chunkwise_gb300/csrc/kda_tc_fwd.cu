@@ -116,6 +116,7 @@ struct TcFwdArgs {
   float* ckpt;
   int* status;
   const int32_t* cu;
+  int64_t S;  // total tokens (cu[N])
   int N, H;
   float scale, lower, eps;
   int test_timeout;
@@ -261,6 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
                       const TcFwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  if (cu_seqlens_bad(a.cu, a.N, a.S)) {  // before any other load, wait or allocation
+    if (threadIdx.x == 0) set_status(a.status, KDA_ERR_DEVICE_CHECK);
+    return;
+  }
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
   const uint64_t D0 = sdesc(sb, 0);  // base of every tcgen05 shared-memory descriptor
@@ -937,6 +942,7 @@ kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s)
   t.ckpt = a.ckpt;
   t.status = a.status;
   t.cu = a.cu;
+  t.S = a.S;
   t.N = a.N;
   t.H = a.H;
   t.scale = a.scale;

@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH):
             lib.kda_gdn2_bwd.argtypes = [P] + [vp] * 22
             lib.kda_query_device_status.restype = ctypes.c_int
             lib.kda_query_device_status.argtypes = [vp, vp]
+            lib.kda_noalloc_device_status.restype = ctypes.c_int
+            lib.kda_noalloc_device_status.argtypes = [vp]
             lib.kda_status_string.restype = ctypes.c_char_p
             lib.kda_status_string.argtypes = [ctypes.c_int]
             lib.kda_last_error_message.restype = ctypes.c_char_p
@@ -310,6 +312,14 @@ def gdn2_bwd(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, dO, ctx, *, s
 def query_device_status(buf) -> int:
     """Status word written by the kernels into a ctx or workspace buffer."""
     return int(load_library().kda_query_device_status(_ptr(buf), _stream_handle(buf.device)))
+
+
+def noalloc_device_status(device=None) -> int:
+    """Status word of the last kda_bwd_noalloc call on ``device`` (the
+    current CUDA device by default), read without any allocation."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(load_library().kda_noalloc_device_status(_stream_handle(dev)))
 
 
 class GDN2Function(torch.autograd.Function):
