@@ -471,40 +471,73 @@ def run_gb300(args, w, rank, world, local):
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + host_o.numel() * host_o.element_size()
 
-        copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        names_fwd = [n for n in names_in if n != "dO"]
+        # Pipelined steps: two device sets of inputs and of results. Step i
+        # computes on set i % 2 while the uploads of step i+1 (into the other
+        # set) and the downloads of step i-1 (out of the other set) run on
+        # their own streams; o of step i downloads while its backward runs.
+        # Every step's copies, the first upload and the last download
+        # included, lie inside the timed region.
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        sets = [(inp, o, grads)]
+        inp2 = {n: (torch.empty_like(inp[n]) if n in names_in else inp[n]) for n in inp}
+        o2 = torch.empty_like(o)
+        grads2 = {n: torch.empty_like(t) for n, t in grads.items()}
+        sets.append((inp2, o2, grads2))
+        ev = lambda: torch.cuda.Event()
+        up_done, fwd_done, comp_done, down_done = ([ev(), ev()] for _ in range(4))
 
-        def e2e_step():
-            # Every copy of the step stays inside the step. dO, which only the
-            # backward reads, uploads on its own stream while the forward
-            # runs, and o downloads while the backward runs.
-            for n in names_fwd:
-                inp[n].copy_(host_in[n], non_blocking=True)
-            copy_in.wait_stream(stream)  # after the forward's uploads and the previous backward
-            with torch.cuda.stream(copy_in):
-                dO.copy_(host_in["dO"], non_blocking=True)
-            fwd_fn(*args_in, scale=w.scale, out=o, ctx=ctx)
-            copy_out.wait_stream(stream)
-            with torch.cuda.stream(copy_out):
-                host_o.copy_(o, non_blocking=True)
-            stream.wait_stream(copy_in)
-            bwd_fn(*args_in, dO, ctx, scale=w.scale, workspace=ws, outs=grads)
-            for n in names_out:
-                host_out[n].copy_(grads[n], non_blocking=True)
-            stream.wait_stream(copy_out)  # the next step's forward overwrites o
+        def upload(b):
+            up.wait_event(comp_done[b])  # the set's previous step no longer reads these inputs
+            with torch.cuda.stream(up):
+                for n in names_in:
+                    sets[b][0][n].copy_(host_in[n], non_blocking=True)
+                up_done[b].record(up)
 
-        e2e_step()
+        def compute(b):
+            x, ob, gb = sets[b]
+            a_in = [x[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
+            stream.wait_event(up_done[b])
+            stream.wait_event(down_done[b])  # results of step i-2 have left this set
+            fwd_fn(*a_in, scale=w.scale, out=ob, ctx=ctx)
+            fwd_done[b].record(stream)
+            bwd_fn(*a_in, x["dO"], ctx, scale=w.scale, workspace=ws, outs=gb)
+            comp_done[b].record(stream)
+
+        def download(b):
+            _, ob, gb = sets[b]
+            with torch.cuda.stream(down):
+                down.wait_event(fwd_done[b])
+                host_o.copy_(ob, non_blocking=True)
+                down.wait_event(comp_done[b])
+                for n in names_out:
+                    host_out[n].copy_(gb[n], non_blocking=True)
+                down_done[b].record(down)
+
+        def run_pipeline(nsteps):
+            for b in (0, 1):  # nothing is in flight on either set
+                comp_done[b].record(stream)
+                down_done[b].record(stream)
+            upload(0)
+            for i in range(nsteps):
+                if i + 1 < nsteps:
+                    upload((i + 1) % 2)
+                compute(i % 2)
+                download(i % 2)
+
+        run_pipeline(2)
         torch.cuda.synchronize()
         rates = copy_rates(stream, [(inp[n], host_in[n]) for n in names_in],
                            [(host_out[n], grads[n]) for n in names_out] + [(host_o, o)])
         barrier()
         t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        run_pipeline(args.e2e_steps)
         torch.cuda.synchronize()
         dt = max_over_ranks(time.perf_counter() - t0) / args.e2e_steps
         e2e = {"value": tokens / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": args.e2e_steps, "ms_per_step": dt * 1e3, **rates}
+               "steps": args.e2e_steps, "ms_per_step": dt * 1e3, **rates,
+               "overlap": "pipelined: step i+1's uploads and step i-1's downloads run beside step i's "
+                          "compute (two device sets of inputs and results)"}
+        del inp2, o2, grads2, sets
 
     cpu_base = sample_check = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -549,7 +582,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=None)
     ap.add_argument("--pass", dest="pass_", choices=["fwdbwd", "fwd"], default="fwdbwd",
                     help="fwd: forward-only inference (no checkpoints); the default times fwd+bwd")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--sample-tokens", type=int, default=98304,
                     help="tokens of the oracle sample behind cpu_baseline (about 10-30 s of host work)")
     ap.add_argument("--ref-sample-tokens", type=int, default=32768,

@@ -249,6 +249,46 @@ kda_status kda_gdn2_bwd(const kda_problem* p,
                         float* dA_log, float* ddt_bias, float* dh0,
                         void* workspace, void* stream);
 
+/* Affine state prefix: the exchange step that joins the pieces of sequences
+ * cut in time (context parallelism). The recurrence is linear in its state,
+ * so for fixed inputs piece p of a sequence maps its start state to its end
+ * state affinely, H_end = A_p H_start + B_p (A_p: D x D on the key index;
+ * it is the piece's final state when the piece runs from the identity state
+ * with zero values, B_p the final state when it runs from zero with its
+ * values, both from kda_fwd with hT). The backward is the transposed map: a
+ * piece's start-state gradient is A_p^T (its end-state gradient) + C_p,
+ * with C_p the dh0 of the piece's kda_bwd run with dhT = 0. Given every
+ * piece's (A_p, B_p) or (A_p, C_p), this prefix returns each piece's true
+ * start state (forward) or true end-state gradient (backward); the pieces
+ * then run kda_fwd / kda_bwd independently with those h0 / dhT, on one GPU
+ * (the pieces packed as sequences of one launch) or one piece per GPU after
+ * the maps have been gathered from the ranks. The pages measure no such
+ * split ("KDA Memory with Recompute ...", section "Measured peak allocated
+ * memory", leaves every 256K-token case unmeasured); the algebra is the
+ * state recurrence's own.
+ *   num_seqs N, pieces P >= 1, num_heads H, head_dim D (64 or 128).
+ *   A, B, xs: fp32 D x D matrices; the one of (piece p, sequence n, head h)
+ *     starts at element (p * piece_stride + n * seq_stride + h) * D * D.
+ *     piece_stride = H, seq_stride = P * H is the layout kda_fwd / kda_bwd
+ *     give when each sequence's P pieces are packed as P consecutive
+ *     sequences ([N][P][H][D][D]); piece_stride = N * H, seq_stride = H is
+ *     the layout of maps gathered from P ranks ([P][N][H][D][D]). Any other
+ *     strides are rejected.
+ *   x0, x_end: fp32 [N][H][D][D].
+ *   KDA_PREFIX_FORWARD:  x_0 = x0 (zero when NULL), xs[p] = x_p,
+ *                        x_{p+1} = A_p x_p + B_p, x_end = x_P (if not NULL).
+ *   KDA_PREFIX_BACKWARD: x_{P-1} = x0 (zero when NULL), xs[p] = x_p,
+ *                        x_{p-1} = A_p^T x_p + B_p, x_end = A_0^T x_0 + B_0.
+ * Device pointers, 16-byte aligned; fp32 accumulation; asynchronous on
+ * `stream`; one CTA per (sequence, head). Returns KDA_ERR_INVALID_ARG /
+ * KDA_ERR_UNSUPPORTED for bad arguments, KDA_ERR_CUDA if the launch fails. */
+#define KDA_PREFIX_FORWARD 0
+#define KDA_PREFIX_BACKWARD 1
+kda_status kda_state_prefix(int32_t num_seqs, int32_t pieces, int32_t num_heads, int32_t head_dim,
+                            int32_t direction, int64_t piece_stride, int64_t seq_stride,
+                            const float* A, const float* B, const float* x0, float* xs, float* x_end,
+                            void* stream);
+
 /* Reads the device status word at the head of a ctx or workspace buffer.
  * Synchronises `stream` first. Returns KDA_OK, KDA_ERR_TIMEOUT or
  * KDA_ERR_DEVICE_CHECK as recorded by the kernels, or KDA_ERR_CUDA if the
@@ -268,7 +308,8 @@ const char* kda_last_error_message(void);
  * Host only. */
 int kda_kernel_family(const kda_problem* p);
 
-/* Library ABI version, major * 100 + minor * 10 (210 = 2.1: the GDN-2 entry points). */
+/* Library ABI version, major * 100 + minor * 10 (220 = 2.2: the affine state prefix,
+ * the no-allocation status query and the device-side cu_seqlens check). */
 int kda_version(void);
 
 #ifdef __cplusplus

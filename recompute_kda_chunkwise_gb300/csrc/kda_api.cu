@@ -159,7 +159,7 @@ size_t kda_bwd_workspace_bytes(const kda_problem* p) {
 
 int kda_kernel_family(const kda_problem* p) { return validate(p, false) == KDA_OK ? family_of(p) : -1; }
 
-int kda_version(void) { return 210; }
+int kda_version(void) { return 220; }
 
 const char* kda_status_string(kda_status s) {
   switch (s) {

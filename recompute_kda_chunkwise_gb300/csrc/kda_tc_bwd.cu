@@ -52,8 +52,13 @@ constexpr uint32_t kPrepMBytes = 4096;         // M hi + lo tiles
 constexpr uint32_t kPrepWOff = kStateBytes + 8192;  // -W fp16 [16][128]
 constexpr uint32_t kPrepUOff = kPrepWOff + 4096;    // U~ fp16 [16][128]
 constexpr uint32_t kPrepUTOff = kPrepUOff + 4096;   // U~ fp32 [16][kLd]
-constexpr uint32_t kSlotBytesSplit = kPrepUTOff + kC * kLd * 4;
-constexpr uint32_t kSlotBytesInline = kStateBytes;  // the state alone
+// Every slot ends with the fp16 low part of the chunk-start state (the
+// state minus its fp16 value), so that the product of a state and a state
+// gradient (dgamma = rowsum(H .* dH')) sees the fp32 state to ~2^-22.
+constexpr uint32_t kLoOffSplit = kPrepUTOff + kC * kLd * 4;
+constexpr uint32_t kSlotBytesSplit = kLoOffSplit + kStateBytes;
+constexpr uint32_t kLoOffInline = kStateBytes;
+constexpr uint32_t kSlotBytesInline = 2 * kStateBytes;  // the state, high and low parts
 
 // ---- shared memory map (bytes) ----
 constexpr int OFF_A1 = 0;                  // H^T fp16 [128 v][128 i] (SW128)
@@ -353,6 +358,23 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
       const int c0 = seg * kCPS, c1 = min(nchunks, c0 + kCPS);
       const bool rebuild = !split || helper;
       const uint32_t sbytes = split ? kSlotBytesSplit : kSlotBytesInline;
+      const uint32_t looff = split ? kLoOffSplit : kLoOffInline;
+      // low part of 32 state values (columns 64 hh + 32 half ..) of lane L's row, into a slot
+      auto store_lo = [&](uint8_t* slot, int half, const float (&x)[32]) {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = x[8 * cc + 2 * e], x1 = x[8 * cc + 2 * e + 1];
+            const uint32_t hi = pack_h2(x0, x1);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+            w[e] = pack_h2(x0 - hf.x, x1 - hf.y);
+          }
+          *reinterpret_cast<uint4*>(slot + looff + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      };
       uint8_t* segbuf = split ? a.scratch + (static_cast<size_t>(item) * kTcBwdBufs + lv % kTcBwdBufs) * kCPS * sbytes
                               : a.scratch + static_cast<size_t>(blockIdx.x) * kCPS * sbytes;
       if (split) {  // hand-off: the helper waits until the level that last used this
@@ -382,6 +404,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
                 make_uint4(pack_h2(x[8 * cc], x[8 * cc + 1]), pack_h2(x[8 * cc + 2], x[8 * cc + 3]),
                            pack_h2(x[8 * cc + 4], x[8 * cc + 5]), pack_h2(x[8 * cc + 6], x[8 * cc + 7]));
+          store_lo(segbuf, half, x);  // the segment's first chunk-start state
         }
         tmem_st_wait();
         fence_async_smem();
@@ -782,6 +805,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                 *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
                     make_uint4(pack_h2(hv[8 * cc], hv[8 * cc + 1]), pack_h2(hv[8 * cc + 2], hv[8 * cc + 3]),
                                pack_h2(hv[8 * cc + 4], hv[8 * cc + 5]), pack_h2(hv[8 * cc + 6], hv[8 * cc + 7]));
+              store_lo(segbuf + static_cast<size_t>(c + 1 - c0) * sbytes, half, hv);  // next chunk's start state
             }
             tmem_st_wait();
             fence_async_smem();
@@ -853,6 +877,12 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               S[dst + r * kSq + sc] = d[e] + d2[e];
             }
           }
+          // low part of this chunk's start state (written by the rebuild pass
+          // with plain stores; read past L1 in [E]): fetched into L2 now
+          const uint8_t* hlo_src = segbuf + static_cast<size_t>(c - c0) * sbytes + looff;
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(hlo_src + sw128_chunk(L, 8 * hh + x, 128)));
           KDA_WAIT_MMA();
           if (!mbar_wait(bar_g1, ph_g1, a.status)) *s_fail = 1;
           ph_g1 ^= 1u;
@@ -865,17 +895,23 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               float dh[32], inc[32];
+              uint4 hlo[4];
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                hlo[cc] = __ldcg(reinterpret_cast<const uint4*>(hlo_src + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)));
               tmem_ld32(tmem + tlane + TM_DH + 64 * hh + 32 * half, dh);
               tmem_ld32(tmem + tlane + TM_D2 + 64 * hh + 32 * half, inc);
 #pragma unroll
               for (int cc = 0; cc < 4; ++cc) {
                 const uint4 hw = *reinterpret_cast<const uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128));
-                const uint32_t hu[4] = {hw.x, hw.y, hw.z, hw.w};
+                const uint4 lw = hlo[cc];
+                const uint32_t hu[4] = {hw.x, hw.y, hw.z, hw.w}, lu[4] = {lw.x, lw.y, lw.z, lw.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
+                for (int e = 0; e < 4; ++e) {  // (H hi + H lo) * dH'
                   const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hu[e]));
-                  p[32 * half + 8 * cc + 2 * e] = hf.x * dh[8 * cc + 2 * e];
-                  p[32 * half + 8 * cc + 2 * e + 1] = hf.y * dh[8 * cc + 2 * e + 1];
+                  const float2 lf = __half22float2(*reinterpret_cast<const __half2*>(&lu[e]));
+                  p[32 * half + 8 * cc + 2 * e] = (hf.x + lf.x) * dh[8 * cc + 2 * e];
+                  p[32 * half + 8 * cc + 2 * e + 1] = (hf.y + lf.y) * dh[8 * cc + 2 * e + 1];
                 }
               }
               const float4* g4 = reinterpret_cast<const float4*>(S + S_GAM + 64 * hh + 32 * half);
@@ -1135,6 +1171,10 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           fence_async_smem();
           fence_before_sync();
           KDA_SYNC_OR_BAIL();
+        }
+        if (!rev) {  // the low parts went out as plain stores: make them visible before the publish
+          __threadfence();
+          __syncthreads();
         }
         if (!rev && tid == 0) {
           bulk_wait_all();  // scratch states written before pass 1 reads them

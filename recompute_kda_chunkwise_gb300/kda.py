@@ -71,6 +71,9 @@ def load_library(path: str = LIB_PATH):
             lib.kda_query_device_status.argtypes = [vp, vp]
             lib.kda_noalloc_device_status.restype = ctypes.c_int
             lib.kda_noalloc_device_status.argtypes = [vp]
+            i32, i64 = ctypes.c_int32, ctypes.c_int64
+            lib.kda_state_prefix.restype = ctypes.c_int
+            lib.kda_state_prefix.argtypes = [i32, i32, i32, i32, i32, i64, i64, vp, vp, vp, vp, vp, vp]
             lib.kda_status_string.restype = ctypes.c_char_p
             lib.kda_status_string.argtypes = [ctypes.c_int]
             lib.kda_last_error_message.restype = ctypes.c_char_p
@@ -320,6 +323,46 @@ def noalloc_device_status(device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with torch.cuda.device(dev):
         return int(load_library().kda_noalloc_device_status(_stream_handle(dev)))
+
+
+KDA_PREFIX_FORWARD = 0
+KDA_PREFIX_BACKWARD = 1
+
+
+def state_prefix(A, B, x0=None, *, direction: int, layout: str, x_end=None):
+    """kda_state_prefix: the affine prefix over the pieces of each sequence.
+
+    A, B: fp32 CUDA tensors of D x D matrices, either ``layout="seq_major"``
+    [N, P, H, D, D] (each sequence's pieces packed as consecutive sequences,
+    as kda_fwd / kda_bwd return their states) or ``layout="piece_major"``
+    [P, N, H, D, D] (maps gathered from P ranks). x0: [N, H, D, D] or None
+    (zero). Returns (xs, x_end): xs in A's layout holds each piece's start
+    state (KDA_PREFIX_FORWARD) or end-state gradient (KDA_PREFIX_BACKWARD);
+    x_end [N, H, D, D] the final state / the gradient of the first piece's
+    start state."""
+    if A.dim() != 5 or A.shape != B.shape or A.dtype != torch.float32 or B.dtype != torch.float32:
+        raise ValueError("A and B must be fp32 tensors of one 5-d shape")
+    for t in (A, B):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("A and B must be contiguous CUDA tensors")
+    if layout == "seq_major":
+        N, P, H, D, _ = A.shape
+        ps, ss = H, P * H
+    elif layout == "piece_major":
+        P, N, H, D, _ = A.shape
+        ps, ss = N * H, H
+    else:
+        raise ValueError("layout must be 'seq_major' or 'piece_major'")
+    want = (N, H, D, D)
+    if x0 is not None and (tuple(x0.shape) != want or x0.dtype != torch.float32 or not x0.is_contiguous()):
+        raise ValueError(f"x0 must be a contiguous fp32 tensor of shape {want}")
+    xs = torch.empty_like(A)
+    if x_end is None:
+        x_end = torch.empty(want, dtype=torch.float32, device=A.device)
+    st = load_library().kda_state_prefix(N, P, H, D, int(direction), ps, ss, _ptr(A), _ptr(B), _ptr(x0),
+                                         _ptr(xs), _ptr(x_end), _stream_handle(A.device))
+    _check(st, "kda_state_prefix")
+    return xs, x_end
 
 
 class GDN2Function(torch.autograd.Function):
