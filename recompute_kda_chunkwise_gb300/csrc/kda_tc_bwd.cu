@@ -52,9 +52,14 @@ constexpr uint32_t kPrepMBytes = 4096;         // M hi + lo tiles
 constexpr uint32_t kPrepWOff = kStateBytes + 8192;  // -W fp16 [16][128]
 constexpr uint32_t kPrepUOff = kPrepWOff + 4096;    // U~ fp16 [16][128]
 constexpr uint32_t kPrepUTOff = kPrepUOff + 4096;   // U~ fp32 [16][kLd]
-// Every slot ends with the fp16 low part of the chunk-start state (the
-// state minus its fp16 value), so that the product of a state and a state
-// gradient (dgamma = rowsum(H .* dH')) sees the fp32 state to ~2^-22.
+// Every slot ends with room for the fp16 low part of the chunk-start state
+// (the state minus its fp16 value). It is written and read only for the
+// first and the last chunk of a sequence: there the state or the state
+// gradient is the caller's (h0, dhT), and the gate gradient of the chunk's
+// tokens is dominated by dgamma = rowsum(H .* dH'), a direct product of the
+// two, which then needs the state to better than fp16 (~2^-22 with hi + lo).
+// Inside a sequence both factors are the recurrence's own and the fp16
+// state meets the bar.
 constexpr uint32_t kLoOffSplit = kPrepUTOff + kC * kLd * 4;
 constexpr uint32_t kSlotBytesSplit = kLoOffSplit + kStateBytes;
 constexpr uint32_t kLoOffInline = kStateBytes;
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
                 make_uint4(pack_h2(x[8 * cc], x[8 * cc + 1]), pack_h2(x[8 * cc + 2], x[8 * cc + 3]),
                            pack_h2(x[8 * cc + 4], x[8 * cc + 5]), pack_h2(x[8 * cc + 6], x[8 * cc + 7]));
-          store_lo(segbuf, half, x);  // the segment's first chunk-start state
+          if (c0 == 0 || c0 == nchunks - 1) store_lo(segbuf, half, x);  // a sequence-edge chunk starts here
         }
         tmem_st_wait();
         fence_async_smem();
@@ -805,7 +810,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                 *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
                     make_uint4(pack_h2(hv[8 * cc], hv[8 * cc + 1]), pack_h2(hv[8 * cc + 2], hv[8 * cc + 3]),
                                pack_h2(hv[8 * cc + 4], hv[8 * cc + 5]), pack_h2(hv[8 * cc + 6], hv[8 * cc + 7]));
-              store_lo(segbuf + static_cast<size_t>(c + 1 - c0) * sbytes, half, hv);  // next chunk's start state
+              if (c + 1 == nchunks - 1)  // the start state of the sequence's last chunk
+                store_lo(segbuf + static_cast<size_t>(c + 1 - c0) * sbytes, half, hv);
             }
             tmem_st_wait();
             fence_async_smem();
@@ -877,12 +883,11 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               S[dst + r * kSq + sc] = d[e] + d2[e];
             }
           }
-          // low part of this chunk's start state (written by the rebuild pass
-          // with plain stores; read past L1 in [E]): fetched into L2 now
+          // the first and last chunk of a sequence also use the low part of
+          // their start state (written by the rebuild pass with plain stores,
+          // read past L1 in [E])
+          const bool edge = c == 0 || c == nchunks - 1;
           const uint8_t* hlo_src = segbuf + static_cast<size_t>(c - c0) * sbytes + looff;
-#pragma unroll
-          for (int x = 0; x < 8; ++x)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(hlo_src + sw128_chunk(L, 8 * hh + x, 128)));
           KDA_WAIT_MMA();
           if (!mbar_wait(bar_g1, ph_g1, a.status)) *s_fail = 1;
           ph_g1 ^= 1u;
@@ -898,7 +903,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               uint4 hlo[4];
 #pragma unroll
               for (int cc = 0; cc < 4; ++cc)
-                hlo[cc] = __ldcg(reinterpret_cast<const uint4*>(hlo_src + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)));
+                hlo[cc] = edge ? __ldcg(reinterpret_cast<const uint4*>(hlo_src + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)))
+                               : make_uint4(0, 0, 0, 0);
               tmem_ld32(tmem + tlane + TM_DH + 64 * hh + 32 * half, dh);
               tmem_ld32(tmem + tlane + TM_D2 + 64 * hh + 32 * half, inc);
 #pragma unroll
