@@ -98,14 +98,21 @@ size_t flag_bytes(const kda_problem* p) {
   return round_up(((size_t)tc_bwd_ctas(p) * kda::kTcBwdFlags + 1) * sizeof(uint32_t), 256);
 }
 
+// Tensor-core backward: per-item low parts of the sequence-edge chunk states.
+size_t edge_bytes(const kda_problem* p) {
+  if (family_of(p) != 1) return 0;
+  return kda::bwd_edge_bytes_tc((int64_t)p->num_seqs * p->num_heads);
+}
+
 size_t workspace_bytes(const kda_problem* p) {
   size_t scratch = kda::bwd_scratch_bytes_simt(p, nullptr);
   if (family_of(p) == 1) {
     // inline mode: one segment's states per CTA; split mode (items < 152):
     // kTcBwdBufs segment buffers per item
     const int64_t items = (int64_t)p->num_seqs * p->num_heads;
-    scratch = items < kda::kTcBwdCtas ? (size_t)items * kda::kTcBwdBufs * kda::bwd_scratch_bytes_per_buf_split_tc()
-                                      : (size_t)kda::kTcBwdCtas * kda::bwd_scratch_bytes_per_cta_tc();
+    scratch = edge_bytes(p) +
+              (items < kda::kTcBwdCtas ? (size_t)items * kda::kTcBwdBufs * kda::bwd_scratch_bytes_per_buf_split_tc()
+                                       : (size_t)kda::kTcBwdCtas * kda::bwd_scratch_bytes_per_cta_tc());
   }
   return kda::kHeaderBytes + partial_bytes(p) + flag_bytes(p) + scratch;
 }
@@ -252,7 +259,8 @@ kda_status backward(const kda_problem* p, const void* q, const void* k, const vo
   a.status = (int*)workspace;
   a.partial = (float*)((char*)workspace + kda::kHeaderBytes);
   a.flags = flag_bytes(p) ? (uint32_t*)((char*)workspace + kda::kHeaderBytes + partial_bytes(p)) : nullptr;
-  a.scratch = (float*)((char*)workspace + kda::kHeaderBytes + partial_bytes(p) + flag_bytes(p));
+  a.edge = (char*)workspace + kda::kHeaderBytes + partial_bytes(p) + flag_bytes(p);
+  a.scratch = (float*)((char*)a.edge + edge_bytes(p));
   a.cu = p->cu_seqlens; a.S = p->total_tokens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   a.w = write_raw;

@@ -66,6 +66,7 @@ struct BwdArgs {
   float* ddt_bias;
   float* partial;  // [N*H][D+1]
   float* scratch;  // per-CTA segment states
+  void* edge = nullptr;  // tensor-core backward: per-item low parts of the sequence-edge chunk states
   uint32_t* flags;  // tensor-core backward: per-item hand-off counters (NULL: no helper CTAs)
   int* status;
   const int32_t* cu;
@@ -132,6 +133,9 @@ kda_status launch_bwd_simt_ctas(const kda_problem* p, const BwdArgs& a, cudaStre
 size_t bwd_scratch_bytes_per_cta_simt(const kda_problem* p);
 size_t bwd_scratch_bytes_per_cta_tc();
 size_t bwd_scratch_bytes_per_buf_split_tc();
+// Bytes of the tensor-core backward's per-item edge area (low parts of the
+// first and last chunk's start states).
+size_t bwd_edge_bytes_tc(int64_t items);
 // Bytes of the tensor-core forward's hand-off area (counters + slots) for
 // `items` (sequence, head) items.
 size_t fwd_handoff_bytes(int items);

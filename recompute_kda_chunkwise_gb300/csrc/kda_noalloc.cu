@@ -80,10 +80,12 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
     if (!aligned16(ptrs[i])) return kda::set_error(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
   }
   // Scratch plan inside the fixed array: status header, per-(sequence, head)
-  // gate-parameter partials, then as many per-CTA state slots as fit.
-  const size_t head = (size_t)kda::kHeaderBytes + kda::gate_partial_bytes(p);
+  // gate-parameter partials, (tensor-core family) the per-item edge tiles,
+  // then as many per-CTA state slots as fit.
   // Same kernel family as kda_bwd, so both entry points give identical results.
   const bool tc = kda::kernel_family(p) == 1;
+  const size_t edge = tc ? kda::bwd_edge_bytes_tc((int64_t)p->num_seqs * p->num_heads) : 0;
+  const size_t head = (size_t)kda::kHeaderBytes + kda::gate_partial_bytes(p) + edge;
   const size_t per_cta = tc ? kda::bwd_scratch_bytes_per_cta_tc() : kda::bwd_scratch_bytes_per_cta_simt(p);
   const size_t cap = (size_t)KDA_NOALLOC_SCRATCH_BYTES;
   if (head + per_cta > cap)
@@ -127,6 +129,7 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
   a.dA_log = dA_log; a.ddt_bias = ddt_bias;
   a.status = (int*)scratch;
   a.partial = (float*)((char*)scratch + kda::kHeaderBytes);
+  a.edge = (char*)scratch + kda::kHeaderBytes + kda::gate_partial_bytes(p);
   a.scratch = (float*)((char*)scratch + head);
   a.flags = nullptr;  // no helper CTAs here: few CTAs fit the fixed buffer
   a.cu = p->cu_seqlens; a.S = p->total_tokens; a.N = p->num_seqs; a.H = p->num_heads;

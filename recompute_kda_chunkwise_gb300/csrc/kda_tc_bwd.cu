@@ -52,18 +52,17 @@ constexpr uint32_t kPrepMBytes = 4096;         // M hi + lo tiles
 constexpr uint32_t kPrepWOff = kStateBytes + 8192;  // -W fp16 [16][128]
 constexpr uint32_t kPrepUOff = kPrepWOff + 4096;    // U~ fp16 [16][128]
 constexpr uint32_t kPrepUTOff = kPrepUOff + 4096;   // U~ fp32 [16][kLd]
-// Every slot ends with room for the fp16 low part of the chunk-start state
-// (the state minus its fp16 value). It is written and read only for the
-// first and the last chunk of a sequence: there the state or the state
-// gradient is the caller's (h0, dhT), and the gate gradient of the chunk's
-// tokens is dominated by dgamma = rowsum(H .* dH'), a direct product of the
-// two, which then needs the state to better than fp16 (~2^-22 with hi + lo).
-// Inside a sequence both factors are the recurrence's own and the fp16
-// state meets the bar.
-constexpr uint32_t kLoOffSplit = kPrepUTOff + kC * kLd * 4;
-constexpr uint32_t kSlotBytesSplit = kLoOffSplit + kStateBytes;
-constexpr uint32_t kLoOffInline = kStateBytes;
-constexpr uint32_t kSlotBytesInline = 2 * kStateBytes;  // the state, high and low parts
+constexpr uint32_t kSlotBytesSplit = kPrepUTOff + kC * kLd * 4;
+constexpr uint32_t kSlotBytesInline = kStateBytes;  // the state alone
+// The first and the last chunk of a sequence also keep the fp16 low part of
+// their start state (the state minus its fp16 value) in a per-item edge
+// area of the workspace (two 32 KB tiles per (sequence, head)): there the
+// state or the state gradient is the caller's (h0, dhT), and the gate
+// gradient of the chunk's tokens is dominated by dgamma = rowsum(H .* dH'),
+// a direct product of the two, which then needs the state to better than
+// fp16 (~2^-22 with hi + lo). Inside a sequence both factors are the
+// recurrence's own and the fp16 state meets the bar.
+constexpr uint32_t kEdgeBytes = 2 * kStateBytes;
 
 // ---- shared memory map (bytes) ----
 constexpr int OFF_A1 = 0;                  // H^T fp16 [128 v][128 i] (SW128)
@@ -115,6 +114,7 @@ struct TcBwdArgs {
   __nv_bfloat16 *dq, *dk, *dv, *dg, *db;
   float* partial;
   uint8_t* scratch;  // fp16 chunk-start state tiles (per CTA, or per item and level parity)
+  uint8_t* edge;     // per item: low parts of the first and last chunk's start states
   uint32_t* flags;   // per item: last level + 1 rebuilt into each buffer, levels consumed (split mode)
   int* status;
   const int32_t* cu;
@@ -363,9 +363,10 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
       const int c0 = seg * kCPS, c1 = min(nchunks, c0 + kCPS);
       const bool rebuild = !split || helper;
       const uint32_t sbytes = split ? kSlotBytesSplit : kSlotBytesInline;
-      const uint32_t looff = split ? kLoOffSplit : kLoOffInline;
-      // low part of 32 state values (columns 64 hh + 32 half ..) of lane L's row, into a slot
-      auto store_lo = [&](uint8_t* slot, int half, const float (&x)[32]) {
+      // edge tile of chunk c (0: the sequence's first chunk, 1: its last)
+      uint8_t* edge_buf = a.edge + static_cast<size_t>(item) * kEdgeBytes;
+      // low part of 32 state values (columns 64 hh + 32 half ..) of lane L's row, into an edge tile
+      auto store_lo = [&](uint8_t* tile, int half, const float (&x)[32]) {
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t w[4];
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
             w[e] = pack_h2(x0 - hf.x, x1 - hf.y);
           }
-          *reinterpret_cast<uint4*>(slot + looff + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
+          *reinterpret_cast<uint4*>(tile + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
       };
@@ -409,7 +410,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
                 make_uint4(pack_h2(x[8 * cc], x[8 * cc + 1]), pack_h2(x[8 * cc + 2], x[8 * cc + 3]),
                            pack_h2(x[8 * cc + 4], x[8 * cc + 5]), pack_h2(x[8 * cc + 6], x[8 * cc + 7]));
-          if (c0 == 0 || c0 == nchunks - 1) store_lo(segbuf, half, x);  // a sequence-edge chunk starts here
+          if (c0 == 0 || c0 == nchunks - 1)  // a sequence-edge chunk starts here
+            store_lo(edge_buf + (c0 == 0 ? 0 : kStateBytes), half, x);
         }
         tmem_st_wait();
         fence_async_smem();
@@ -811,7 +813,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                     make_uint4(pack_h2(hv[8 * cc], hv[8 * cc + 1]), pack_h2(hv[8 * cc + 2], hv[8 * cc + 3]),
                                pack_h2(hv[8 * cc + 4], hv[8 * cc + 5]), pack_h2(hv[8 * cc + 6], hv[8 * cc + 7]));
               if (c + 1 == nchunks - 1)  // the start state of the sequence's last chunk
-                store_lo(segbuf + static_cast<size_t>(c + 1 - c0) * sbytes, half, hv);
+                store_lo(edge_buf + kStateBytes, half, hv);
             }
             tmem_st_wait();
             fence_async_smem();
@@ -887,7 +889,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           // their start state (written by the rebuild pass with plain stores,
           // read past L1 in [E])
           const bool edge = c == 0 || c == nchunks - 1;
-          const uint8_t* hlo_src = segbuf + static_cast<size_t>(c - c0) * sbytes + looff;
+          const uint8_t* hlo_src = edge_buf + (c == 0 ? 0 : kStateBytes);
           KDA_WAIT_MMA();
           if (!mbar_wait(bar_g1, ph_g1, a.status)) *s_fail = 1;
           ph_g1 ^= 1u;
@@ -1256,6 +1258,7 @@ __global__ void kda_param_reduce_tc_kernel(const float* partial, int N, int H, i
 
 size_t bwd_scratch_bytes_per_cta_tc() { return static_cast<size_t>(kCPS) * kSlotBytesInline; }
 size_t bwd_scratch_bytes_per_buf_split_tc() { return static_cast<size_t>(kCPS) * kSlotBytesSplit; }
+size_t bwd_edge_bytes_tc(int64_t items) { return static_cast<size_t>(items) * kEdgeBytes; }
 
 kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas) {
   if (p->head_dim != kD || p->dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
@@ -1278,6 +1281,7 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   t.db = static_cast<__nv_bfloat16*>(a.db);
   t.partial = a.partial;
   t.scratch = reinterpret_cast<uint8_t*>(a.scratch);
+  t.edge = reinterpret_cast<uint8_t*>(a.edge);
   t.flags = a.flags;
   t.status = a.status;
   t.cu = a.cu;
