@@ -101,15 +101,18 @@ typedef enum {
 
 /* Problem description. cu_seqlens is a DEVICE pointer; the library never
  * reads it on the host (so no synchronisation). It must start at 0, be
- * non-decreasing and end at total_tokens. The kernels check this on the
- * device before they load anything else: every CTA of every kernel reads the
- * whole array, and if any of the three conditions fails, it records
- * KDA_ERR_DEVICE_CHECK in the call's status word (ctx for the forward,
- * workspace for the backward, the library's array for kda_bwd_noalloc) and
- * returns without touching inputs, outputs or scratch. The outputs of such a
- * call are then not written (dA_log / ddt_bias hold stale partial sums); the
- * status is readable with kda_query_device_status / kda_noalloc_device_status.
- * A forward given ctx == NULL has no status word and skips silently. */
+ * non-decreasing and end at total_tokens. Every call checks this on the
+ * device before its kernels run: a one-CTA kernel copies cu_seqlens into the
+ * call's own buffer (after the 256-byte header of ctx for the forward, of
+ * workspace for the backward, of the library's array for kda_bwd_noalloc),
+ * and the kernels read only that copy. If any of the three conditions fails,
+ * the copy is all zeros instead, so every sequence is empty and no kernel
+ * indexes inputs, outputs, checkpoints or scratch through the malformed
+ * array, and KDA_ERR_DEVICE_CHECK is recorded in the call's status word
+ * (kda_query_device_status / kda_noalloc_device_status). The call then
+ * writes no o or activation gradient; hT = h0, dh0 = dhT, dA_log = ddt_bias
+ * = 0. A forward given ctx == NULL has neither a status word nor a buffer
+ * for the copy: it reads cu_seqlens unchecked. */
 typedef struct {
   int64_t total_tokens;       /* S */
   int32_t num_seqs;           /* N >= 1 */
@@ -123,15 +126,16 @@ typedef struct {
   const int32_t* cu_seqlens;  /* device, num_seqs + 1 entries */
 } kda_problem;
 
-/* Bytes of the forward->backward context: state checkpoints (fp32, one per
- * 1024 tokens of every sequence and head) plus a 256-byte header holding the
- * forward's device status word. Returns 0 for an invalid problem. The size
+/* Bytes of the forward->backward context: a 256-byte header holding the
+ * forward's device status word, the checked copy of cu_seqlens (num_seqs + 1
+ * int32, rounded up to 256 bytes), then the state checkpoints (fp32, one per
+ * 1024 tokens of every sequence and head). Returns 0 for an invalid problem. The size
  * queries ignore cu_seqlens (it may be NULL). */
 size_t kda_ctx_bytes(const kda_problem* p);
 
-/* Bytes of the backward workspace: per-CTA scratch for recomputed chunk
- * states of one checkpoint segment, gate-parameter partial sums and a
- * 256-byte header with the backward's device status word. Returns 0 for an
+/* Bytes of the backward workspace: a 256-byte header with the backward's
+ * device status word, the checked copy of cu_seqlens, gate-parameter partial
+ * sums and scratch for the recomputed chunk states of checkpoint segments. Returns 0 for an
  * invalid problem. */
 size_t kda_bwd_workspace_bytes(const kda_problem* p);
 

@@ -72,8 +72,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     objs = [o for o, _ in results]
     if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        subprocess.run([nvcc, "-shared", *ARCH, "-cudart", "static", "-o", tmp, *objs],
-                       check=True, capture_output=True, text=True)
+        r = subprocess.run([nvcc, "-shared", *ARCH, "-cudart", "static", "-o", tmp, *objs],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)
     return LIB
 

@@ -80,7 +80,9 @@ size_t fwd_handoff(const kda_problem* p) {
   return kda::fwd_handoff_bytes((int)items);
 }
 
-size_t ctx_bytes(const kda_problem* p) { return kda::kHeaderBytes + ckpt_bytes(p) + fwd_handoff(p); }
+size_t cu_bytes(const kda_problem* p) { return kda::cu_copy_bytes(p->num_seqs); }
+
+size_t ctx_bytes(const kda_problem* p) { return kda::kHeaderBytes + cu_bytes(p) + ckpt_bytes(p) + fwd_handoff(p); }
 
 size_t partial_bytes(const kda_problem* p) {
   return round_up((size_t)p->num_seqs * p->num_heads * (p->head_dim + 1) * sizeof(float), 256);
@@ -114,7 +116,7 @@ size_t workspace_bytes(const kda_problem* p) {
               (items < kda::kTcBwdCtas ? (size_t)items * kda::kTcBwdBufs * kda::bwd_scratch_bytes_per_buf_split_tc()
                                        : (size_t)kda::kTcBwdCtas * kda::bwd_scratch_bytes_per_cta_tc());
   }
-  return kda::kHeaderBytes + partial_bytes(p) + flag_bytes(p) + scratch;
+  return kda::kHeaderBytes + cu_bytes(p) + partial_bytes(p) + flag_bytes(p) + scratch;
 }
 
 #define CHECK_PTR(ptr)                                                                   \
@@ -144,6 +146,31 @@ kda_status pass_state(float* dst, const float* src, const kda_problem* p, cudaSt
 }  // namespace
 
 namespace kda {
+
+namespace {
+// One CTA: cu_out = cu if cu[0] == 0, cu is non-decreasing and cu[N] == S,
+// else all zeros (every sequence empty, so no kernel indexes anything
+// through the malformed array) and KDA_ERR_DEVICE_CHECK in *status.
+__global__ void __launch_bounds__(256) kda_check_cu_kernel(const int32_t* cu, int N, int64_t S, int32_t* cu_out,
+                                                          int* status) {
+  int bad = 0;
+  for (int i = static_cast<int>(threadIdx.x); i <= N; i += static_cast<int>(blockDim.x)) {
+    const int64_t c = cu[i];
+    if (i == 0 && c != 0) bad = 1;
+    if (i > 0 && c < static_cast<int64_t>(cu[i - 1])) bad = 1;
+    if (c < 0 || c > S || (i == N && c != S)) bad = 1;
+  }
+  bad = __syncthreads_or(bad);
+  for (int i = static_cast<int>(threadIdx.x); i <= N; i += static_cast<int>(blockDim.x)) cu_out[i] = bad ? 0 : cu[i];
+  if (bad && threadIdx.x == 0) set_status(status, KDA_ERR_DEVICE_CHECK);
+}
+}  // namespace
+
+kda_status launch_check_cu(const int32_t* cu, int N, int64_t S, int32_t* cu_out, int* status, cudaStream_t s) {
+  kda_check_cu_kernel<<<1, 256, 0, s>>>(cu, N, S, cu_out, status);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status validate_problem(const kda_problem* p) { return validate(p); }
 kda_status set_error(kda_status s, const char* fmt, ...) {
   va_list ap;
@@ -205,20 +232,27 @@ kda_status forward(const kda_problem* p, const void* q, const void* k, const voi
   a.o = o;
   a.h0 = h0;
   a.hT = hT;
-  a.ckpt = (ctx && ckpt_bytes(p)) ? (float*)((char*)ctx + kda::kHeaderBytes) : nullptr;
+  char* after_cu = ctx ? (char*)ctx + kda::kHeaderBytes + cu_bytes(p) : nullptr;
+  a.ckpt = (ctx && ckpt_bytes(p)) ? (float*)after_cu : nullptr;
   a.status = ctx ? (int*)ctx : nullptr;
-  a.cu = p->cu_seqlens; a.S = p->total_tokens; a.N = p->num_seqs; a.H = p->num_heads;
+  // with a ctx the kernels read the checked copy of cu_seqlens kept in it
+  a.cu = ctx ? (const int32_t*)((char*)ctx + kda::kHeaderBytes) : p->cu_seqlens;
+  a.S = p->total_tokens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   a.test_timeout = (p->flags & KDA_FLAG_TEST_TIMEOUT) ? 1 : 0;
   a.xflags = nullptr;
   a.xbuf = nullptr;
   a.w = write_raw;
   if (ctx && fwd_handoff(p)) {
-    a.xflags = (uint32_t*)((char*)ctx + kda::kHeaderBytes + ckpt_bytes(p));
+    a.xflags = (uint32_t*)(after_cu + ckpt_bytes(p));
     a.xbuf = (uint8_t*)a.xflags + round_up((size_t)p->num_seqs * p->num_heads * 5 * sizeof(uint32_t), 256);
   }
   if (ctx && cudaMemsetAsync(ctx, 0, sizeof(int), s) != cudaSuccess)
     return fail(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
+  if (ctx) {
+    st = kda::launch_check_cu(p->cu_seqlens, p->num_seqs, p->total_tokens, (int32_t*)a.cu, a.status, s);
+    if (st != KDA_OK) return fail(st, "cu_seqlens check launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  }
   st = family_of(p) == 1 ? kda::launch_fwd_tc(p, a, s) : kda::launch_fwd_simt(p, a, s);
   if (st != KDA_OK) return fail(st, "forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return KDA_OK;
@@ -253,20 +287,24 @@ kda_status backward(const kda_problem* p, const void* q, const void* k, const vo
   a.dO = dO;
   a.dhT = dhT;
   a.dh0 = dh0;
-  a.ckpt = (const float*)((const char*)ctx + kda::kHeaderBytes);
+  a.ckpt = (const float*)((const char*)ctx + kda::kHeaderBytes + cu_bytes(p));
   a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg_raw; a.db = dbeta_raw;
   a.dA_log = dA_log; a.ddt_bias = ddt_bias;
   a.status = (int*)workspace;
-  a.partial = (float*)((char*)workspace + kda::kHeaderBytes);
-  a.flags = flag_bytes(p) ? (uint32_t*)((char*)workspace + kda::kHeaderBytes + partial_bytes(p)) : nullptr;
-  a.edge = (char*)workspace + kda::kHeaderBytes + partial_bytes(p) + flag_bytes(p);
+  char* ws = (char*)workspace + kda::kHeaderBytes;  // checked copy of cu_seqlens, then the rest
+  a.partial = (float*)(ws + cu_bytes(p));
+  a.flags = flag_bytes(p) ? (uint32_t*)(ws + cu_bytes(p) + partial_bytes(p)) : nullptr;
+  a.edge = ws + cu_bytes(p) + partial_bytes(p) + flag_bytes(p);
   a.scratch = (float*)((char*)a.edge + edge_bytes(p));
-  a.cu = p->cu_seqlens; a.S = p->total_tokens; a.N = p->num_seqs; a.H = p->num_heads;
+  a.cu = (const int32_t*)ws;
+  a.S = p->total_tokens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   a.w = write_raw;
   a.dw = dwrite_raw;
   if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess)
     return fail(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
+  st = kda::launch_check_cu(p->cu_seqlens, p->num_seqs, p->total_tokens, (int32_t*)a.cu, a.status, s);
+  if (st != KDA_OK) return fail(st, "cu_seqlens check launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   st = family_of(p) == 1 ? kda::launch_bwd_tc(p, a, s, tc_bwd_ctas(p)) : kda::launch_bwd_simt(p, a, s);
   if (st != KDA_OK) return fail(st, "backward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return KDA_OK;

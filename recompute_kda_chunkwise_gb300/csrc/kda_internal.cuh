@@ -106,23 +106,6 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
-// Device-side check of the sequence boundaries, run by every CTA of every
-// kernel before any other global load: cu[0] == 0, cu non-decreasing and
-// cu[N] == S (the total token count). Every thread of the block must call it.
-// On failure the caller records KDA_ERR_DEVICE_CHECK and returns at once, so
-// no kernel indexes inputs, outputs, checkpoints or scratch through a
-// malformed cu_seqlens, and no CTA is left waiting for another (all CTAs
-// read the same array and reach the same verdict).
-__device__ __forceinline__ bool cu_seqlens_bad(const int32_t* cu, int N, int64_t S) {
-  int bad = 0;
-  for (int i = static_cast<int>(threadIdx.x); i <= N; i += static_cast<int>(blockDim.x)) {
-    const int64_t c = cu[i];
-    if (i == 0 && c != 0) bad = 1;
-    if (i > 0 && c < static_cast<int64_t>(cu[i - 1])) bad = 1;
-    if (c < 0 || c > S || (i == N && c != S)) bad = 1;
-  }
-  return __syncthreads_or(bad) != 0;
-}
 
 // Host-side launchers (defined in the kernel translation units).
 kda_status launch_fwd_simt(const kda_problem* p, const FwdArgs& a, cudaStream_t s);
@@ -147,6 +130,15 @@ constexpr int kTcBwdCtas = 152;
 // item (one "rebuilt" counter per buffer, then one "consumed" counter).
 constexpr int kTcBwdBufs = 3;
 constexpr int kTcBwdFlags = kTcBwdBufs + 1;
+
+// Bytes of the checked copy of cu_seqlens that follows the header of ctx
+// and workspace (and of the no-allocation scratch array).
+inline size_t cu_copy_bytes(int num_seqs) { return ((size_t)(num_seqs + 1) * sizeof(int32_t) + 255) / 256 * 256; }
+// Enqueues the device-side check of cu_seqlens: cu_out = cu when cu[0] == 0,
+// cu is non-decreasing and cu[N] == S; otherwise cu_out = all zeros (every
+// sequence empty) and KDA_ERR_DEVICE_CHECK in *status. The kernels then read
+// cu_out only.
+kda_status launch_check_cu(const int32_t* cu, int N, int64_t S, int32_t* cu_out, int* status, cudaStream_t s);
 
 // Host helpers shared by the entry points (defined in kda_api.cu).
 kda_status validate_problem(const kda_problem* p);

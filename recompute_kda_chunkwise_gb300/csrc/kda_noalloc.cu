@@ -85,7 +85,7 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
   // Same kernel family as kda_bwd, so both entry points give identical results.
   const bool tc = kda::kernel_family(p) == 1;
   const size_t edge = tc ? kda::bwd_edge_bytes_tc((int64_t)p->num_seqs * p->num_heads) : 0;
-  const size_t head = (size_t)kda::kHeaderBytes + kda::gate_partial_bytes(p) + edge;
+  const size_t head = (size_t)kda::kHeaderBytes + kda::cu_copy_bytes(p->num_seqs) + kda::gate_partial_bytes(p) + edge;
   const size_t per_cta = tc ? kda::bwd_scratch_bytes_per_cta_tc() : kda::bwd_scratch_bytes_per_cta_simt(p);
   const size_t cap = (size_t)KDA_NOALLOC_SCRATCH_BYTES;
   if (head + per_cta > cap)
@@ -124,18 +124,22 @@ extern "C" kda_status kda_bwd_noalloc(const kda_problem* p, const void* q, const
   a.dO = dO;
   a.dhT = dhT;
   a.dh0 = dh0;
-  a.ckpt = (const float*)((const char*)ctx + kda::kHeaderBytes);
+  a.ckpt = (const float*)((const char*)ctx + kda::kHeaderBytes + kda::cu_copy_bytes(p->num_seqs));
   a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg_raw; a.db = dbeta_raw;
   a.dA_log = dA_log; a.ddt_bias = ddt_bias;
   a.status = (int*)scratch;
-  a.partial = (float*)((char*)scratch + kda::kHeaderBytes);
-  a.edge = (char*)scratch + kda::kHeaderBytes + kda::gate_partial_bytes(p);
+  char* ws = (char*)scratch + kda::kHeaderBytes;  // checked copy of cu_seqlens, then the rest
+  a.partial = (float*)(ws + kda::cu_copy_bytes(p->num_seqs));
+  a.edge = ws + kda::cu_copy_bytes(p->num_seqs) + kda::gate_partial_bytes(p);
   a.scratch = (float*)((char*)scratch + head);
   a.flags = nullptr;  // no helper CTAs here: few CTAs fit the fixed buffer
-  a.cu = p->cu_seqlens; a.S = p->total_tokens; a.N = p->num_seqs; a.H = p->num_heads;
+  a.cu = (const int32_t*)ws;
+  a.S = p->total_tokens; a.N = p->num_seqs; a.H = p->num_heads;
   a.scale = p->scale; a.lower = p->gate_lower_bound; a.eps = p->l2_eps;
   if (cudaMemsetAsync(scratch, 0, sizeof(int), s) != cudaSuccess)
     return kda::set_error(KDA_ERR_CUDA, "status reset failed: %s", cudaGetErrorString(cudaGetLastError()));
+  if (kda::launch_check_cu(p->cu_seqlens, p->num_seqs, p->total_tokens, (int32_t*)ws, a.status, s) != KDA_OK)
+    return kda::set_error(KDA_ERR_CUDA, "cu_seqlens check launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   st = tc ? kda::launch_bwd_tc(p, a, s, (int)ctas) : kda::launch_bwd_simt_ctas(p, a, s, (int)ctas);
   if (st != KDA_OK)
     return kda::set_error(st, "no-alloc backward launch failed: %s", cudaGetErrorString(cudaGetLastError()));

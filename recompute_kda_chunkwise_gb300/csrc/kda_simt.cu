@@ -300,10 +300,6 @@ template <typename Tin, int D, bool CG>
 __global__ void __launch_bounds__(kNT, 1) kda_fwd_simt_kernel(const FwdArgs a) {
   constexpr int C = SimtChunk<D>::C, V = D;
   extern __shared__ float sm[];
-  if (cu_seqlens_bad(a.cu, a.N, a.S)) {
-    if (threadIdx.x == 0) set_status(a.status, KDA_ERR_DEVICE_CHECK);
-    return;
-  }
   Tiles<D, C> t;
   float* Hs = t.carve(sm, CG);  // [D][V]
   const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
@@ -373,10 +369,6 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
   constexpr int CPS = kCkptTokens / C;  // chunks per checkpoint segment
   constexpr int RGD = kNT / D, RPTD = C / RGD;
   extern __shared__ float sm[];
-  if (cu_seqlens_bad(a.cu, a.N, a.S)) {
-    if (threadIdx.x == 0) set_status(a.status, KDA_ERR_DEVICE_CHECK);
-    return;
-  }
   Tiles<D, C> t;
   BwdTiles<D, C> u;
   u.carve(t.carve(sm, CG));

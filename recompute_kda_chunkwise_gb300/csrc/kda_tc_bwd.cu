@@ -178,12 +178,39 @@ __device__ __forceinline__ void stage_tiles(const TcBwdArgs& a, uint32_t dst, in
   if (dO) cp_async16(dst_dO + so, a.dO + off, n);
 }
 
+// dgamma's low-part term of a sequence-edge chunk, sum_v Hlo[i][v] dH'[i][v]:
+// thread (lane L, column half hh) multiplies the fp16 low part of the chunk's
+// start state (edge tile `lo`, read past L1) with dH' (TMEM, columns of
+// `dh_tmem`), reduces the 64 products over the warp's lanes and writes its
+// two totals to red[base], red[base + 1]. Kept out of line: it runs for two
+// chunks per sequence and must not weigh on the hot loop's registers.
+__device__ __noinline__ void edge_dgamma_lo(const uint8_t* lo, uint32_t dh_tmem, int L, int hh, int lane, float* red) {
+  float p[64];
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float dh[32];
+    tmem_ld32(dh_tmem + 32 * half, dh);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const uint4 lw = __ldcg(reinterpret_cast<const uint4*>(lo + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)));
+      const uint32_t lu[4] = {lw.x, lw.y, lw.z, lw.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 lf = __half22float2(*reinterpret_cast<const __half2*>(&lu[e]));
+        p[32 * half + 8 * cc + 2 * e] = lf.x * dh[8 * cc + 2 * e];
+        p[32 * half + 8 * cc + 2 * e + 1] = lf.y * dh[8 * cc + 2 * e + 1];
+      }
+    }
+  }
+  warp_reduce_scatter64(p, lane);
+  const int base = 32 * ((lane >> 4) & 1) + 16 * ((lane >> 3) & 1) + 8 * ((lane >> 2) & 1) + 4 * ((lane >> 1) & 1) +
+                   2 * (lane & 1);
+  red[base] = p[0];
+  red[base + 1] = p[1];
+}
+
 __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  if (cu_seqlens_bad(a.cu, a.N, a.S)) {  // before any other load, wait or allocation
-    if (threadIdx.x == 0) set_status(a.status, KDA_ERR_DEVICE_CHECK);
-    return;
-  }
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
   const uint64_t D0 = sdesc(sb, 0);  // base of every tcgen05 shared-memory descriptor
@@ -365,7 +392,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
       const uint32_t sbytes = split ? kSlotBytesSplit : kSlotBytesInline;
       // edge tile of chunk c (0: the sequence's first chunk, 1: its last)
       uint8_t* edge_buf = a.edge + static_cast<size_t>(item) * kEdgeBytes;
-      // low part of 32 state values (columns 64 hh + 32 half ..) of lane L's row, into an edge tile
+      // low part (value minus its fp16 rounding) of 32 state values of lane
+      // L's row (columns 64 hh + 32 half ..) into an SW128 edge tile
       auto store_lo = [&](uint8_t* tile, int half, const float (&x)[32]) {
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -812,8 +840,6 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                 *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
                     make_uint4(pack_h2(hv[8 * cc], hv[8 * cc + 1]), pack_h2(hv[8 * cc + 2], hv[8 * cc + 3]),
                                pack_h2(hv[8 * cc + 4], hv[8 * cc + 5]), pack_h2(hv[8 * cc + 6], hv[8 * cc + 7]));
-              if (c + 1 == nchunks - 1)  // the start state of the sequence's last chunk
-                store_lo(edge_buf + kStateBytes, half, hv);
             }
             tmem_st_wait();
             fence_async_smem();
@@ -889,37 +915,32 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           // their start state (written by the rebuild pass with plain stores,
           // read past L1 in [E])
           const bool edge = c == 0 || c == nchunks - 1;
-          const uint8_t* hlo_src = edge_buf + (c == 0 ? 0 : kStateBytes);
           KDA_WAIT_MMA();
           if (!mbar_wait(bar_g1, ph_g1, a.status)) *s_fail = 1;
           ph_g1 ^= 1u;
           if (!mbar_wait(bar_g2, ph_g2, a.status)) *s_fail = 1;
           ph_g2 ^= 1u;
           fence_after_sync();
+          if (edge)  // dgamma's low-part term for a sequence-edge chunk
+            edge_dgamma_lo(edge_buf + (c == 0 ? 0 : kStateBytes), tmem + tlane + TM_DH + 64 * hh, L, hh, lane,
+                           RED + 512 + q4 * 128 + 64 * hh);
           // ---- [E] dH update, dgamma (lane = v); dQG, dW, dKbar (lane = i) ----
           {
             float p[64];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               float dh[32], inc[32];
-              uint4 hlo[4];
-#pragma unroll
-              for (int cc = 0; cc < 4; ++cc)
-                hlo[cc] = edge ? __ldcg(reinterpret_cast<const uint4*>(hlo_src + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)))
-                               : make_uint4(0, 0, 0, 0);
               tmem_ld32(tmem + tlane + TM_DH + 64 * hh + 32 * half, dh);
               tmem_ld32(tmem + tlane + TM_D2 + 64 * hh + 32 * half, inc);
 #pragma unroll
               for (int cc = 0; cc < 4; ++cc) {
                 const uint4 hw = *reinterpret_cast<const uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128));
-                const uint4 lw = hlo[cc];
-                const uint32_t hu[4] = {hw.x, hw.y, hw.z, hw.w}, lu[4] = {lw.x, lw.y, lw.z, lw.w};
+                const uint32_t hu[4] = {hw.x, hw.y, hw.z, hw.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {  // (H hi + H lo) * dH'
+                for (int e = 0; e < 4; ++e) {
                   const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hu[e]));
-                  const float2 lf = __half22float2(*reinterpret_cast<const __half2*>(&lu[e]));
-                  p[32 * half + 8 * cc + 2 * e] = (hf.x + lf.x) * dh[8 * cc + 2 * e];
-                  p[32 * half + 8 * cc + 2 * e + 1] = (hf.y + lf.y) * dh[8 * cc + 2 * e + 1];
+                  p[32 * half + 8 * cc + 2 * e] = hf.x * dh[8 * cc + 2 * e];
+                  p[32 * half + 8 * cc + 2 * e + 1] = hf.y * dh[8 * cc + 2 * e + 1];
                 }
               }
               const float4* g4 = reinterpret_cast<const float4*>(S + S_GAM + 64 * hh + 32 * half);
@@ -980,7 +1001,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           // ---- [D1] d(chunk-end log decay); dW (Kh Gamma)^T on tf32 tiles ----
           if (tid >= kD) {
             const int i = tid - kD;
-            const float dgam = RED[i] + RED[128 + i] + RED[256 + i] + RED[384 + i];
+            float dgam = RED[i] + RED[128 + i] + RED[256 + i] + RED[384 + i];
+            if (edge) dgam += (RED[512 + i] + RED[640 + i]) + (RED[768 + i] + RED[896 + i]);
             S[S_DGE + i] = S[S_PART + i] + S[S_PART + 128 + i] + dgam * S[S_GAM + i];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {  // fold the second contraction halves of dM and dU~ V^T
@@ -1180,8 +1202,20 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           fence_before_sync();
           KDA_SYNC_OR_BAIL();
         }
-        if (!rev) {  // the low parts went out as plain stores: make them visible before the publish
-          __threadfence();
+        if (!rev) {
+          // the rebuild pass leaves the start state of chunk c1 - 1 in TMEM:
+          // when that is the sequence's last chunk, its low part goes to the
+          // edge area (the first chunk's was stored with the checkpoint)
+          if (c1 == nchunks && c1 - 1 > c0) {
+            fence_after_sync();
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              float x[32];
+              tmem_ld32(tmem + tlane + TM_H + 64 * hh + 32 * half, x);
+              store_lo(edge_buf + kStateBytes, half, x);
+            }
+          }
+          __threadfence();  // the low parts went out as plain stores: visible before the publish
           __syncthreads();
         }
         if (!rev && tid == 0) {

@@ -262,10 +262,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
                       const TcFwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  if (cu_seqlens_bad(a.cu, a.N, a.S)) {  // before any other load, wait or allocation
-    if (threadIdx.x == 0) set_status(a.status, KDA_ERR_DEVICE_CHECK);
-    return;
-  }
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
   const uint64_t D0 = sdesc(sb, 0);  // base of every tcgen05 shared-memory descriptor

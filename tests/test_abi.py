@@ -45,7 +45,9 @@ def test_problem_struct_layout_matches_header():
 def test_size_queries(lib):
     p = K.make_problem(131072, 1, 96, 128, torch.bfloat16)
     ckpts = 131072 // 1024 + 1
-    states = 256 + ckpts * 96 * 128 * 128 * 4
+    # 256-byte header (status word), the checked copy of cu_seqlens (N + 1
+    # int32 rounded up to 256 bytes), then the fp32 checkpoints
+    states = 256 + 256 + ckpts * 96 * 128 * 128 * 4
     # tensor-core family with fewer items than the 152-CTA grid: the forward's
     # hand-off area (5 counters per item, 4 slots of 98816 bytes) follows
     handoff = (96 * 5 * 4 + 255) // 256 * 256 + 96 * 4 * 98816
@@ -53,7 +55,7 @@ def test_size_queries(lib):
     simt = K.make_problem(131072, 1, 96, 128, torch.bfloat16, flags=K.KDA_FLAG_FORCE_SIMT)
     assert K.ctx_bytes(simt) == states
     many = K.make_problem(131072, 2, 96, 128, torch.bfloat16)  # 192 items: no helpers
-    assert K.ctx_bytes(many) == 256 + (131072 // 1024 + 2) * 96 * 128 * 128 * 4
+    assert K.ctx_bytes(many) == 256 + 256 + (131072 // 1024 + 2) * 96 * 128 * 128 * 4
     assert K.workspace_bytes(p) > 256 + 96 * 129 * 4
     assert K.kernel_family(p) in (0, 1)
     bad = K.make_problem(16, 1, 2, 96, torch.bfloat16)
@@ -96,10 +98,10 @@ def test_invalid_arguments_are_rejected_on_host(lib):
     assert b"unknown flags" in lib.kda_last_error_message()
     p.flags = K.KDA_FLAG_FORCE_SIMT | K.KDA_FLAG_TEST_TIMEOUT  # both known: sizes still answer
     assert lib.kda_ctx_bytes(ctypes.byref(p)) > 0
-    # inference: no checkpoints, so ctx shrinks to the status header; the
-    # backward refuses a problem flagged that way
+    # inference: no checkpoints, so ctx shrinks to the status header and the
+    # checked copy of cu_seqlens; the backward refuses a problem flagged that way
     p.flags = K.KDA_FLAG_NO_CHECKPOINTS
-    assert lib.kda_ctx_bytes(ctypes.byref(p)) == 256
+    assert lib.kda_ctx_bytes(ctypes.byref(p)) == 256 + 256
     assert lib.kda_bwd(ctypes.byref(p), *([al] * 8), nul, *([al] * 8), nul, al, nul) == 1
     assert b"NO_CHECKPOINTS" in lib.kda_last_error_message()
 
