@@ -143,7 +143,13 @@ size_t kda_bwd_workspace_bytes(const kda_problem* p);
  * gradients dh0, dhT): fp32 [N][H][D][D], contiguous, row index = key
  * channel i, column index = value channel j, so that one sequence's state is
  * the D x V matrix S of the recurrence. Every state pointer is optional:
- * NULL h0 / dhT mean zero, NULL hT / dh0 are not written. */
+ * NULL h0 / dhT mean zero, NULL hT / dh0 are not written.
+ * On the tensor-core backward, when dhT is given or dh0 asked for, the gate
+ * gradient of each sequence's first and last chunk uses the chunk-start
+ * state to fp32 accuracy (there h0 or dhT meet it in one product); without
+ * either, those chunks use the same fp16 state operand as the others, which
+ * is exact when h0 is zero. A caller that starts the forward from h0 should
+ * therefore ask the backward for dh0. */
 
 /* Forward. Writes o [S,H,D] and, when hT is not NULL, the final states;
  * the recurrence of sequence n, head h starts from h0[n][h] (zero when h0 is

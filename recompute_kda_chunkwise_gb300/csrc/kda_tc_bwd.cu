@@ -178,6 +178,47 @@ __device__ __forceinline__ void stage_tiles(const TcBwdArgs& a, uint32_t dst, in
   if (dO) cp_async16(dst_dO + so, a.dO + off, n);
 }
 
+// Low part (value minus its fp16 rounding) of lane L's 64 state values
+// (columns 64 hh ..) into an SW128 edge tile, from an fp32 [i][v] state in
+// global memory (a checkpoint) or from the TMEM state (lane L, 64 columns at
+// taddr). Out of line: they run once per sequence edge and must not weigh
+// on the hot loop's registers.
+__device__ __forceinline__ void lo_tile_store(uint8_t* tile, int L, int hh, int half, const float* x) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x0 = x[8 * cc + 2 * e], x1 = x[8 * cc + 2 * e + 1];
+      const uint32_t hi = pack_h2(x0, x1);
+      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+      w[e] = pack_h2(x0 - hf.x, x1 - hf.y);
+    }
+    *reinterpret_cast<uint4*>(tile + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+__device__ __noinline__ void edge_lo_from_global(uint8_t* tile, const float* src, int L, int hh) {
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = src[(64 * hh + 32 * half + j) * kD + L];
+    lo_tile_store(tile, L, hh, half, x);
+  }
+}
+__device__ __noinline__ void edge_lo_from_tmem(uint8_t* tile, uint32_t taddr, int L, int hh) {
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    float x[32];
+    tmem_ld32(taddr + 32 * half, x);
+    lo_tile_store(tile, L, hh, half, x);
+  }
+}
+// RED[0..511] += RED[512..1023] (the edge chunk's low-part dgamma partials)
+__device__ __noinline__ void edge_fold(float* red) {
+  for (int x = static_cast<int>(threadIdx.x); x < 512; x += static_cast<int>(blockDim.x)) red[x] += red[512 + x];
+}
+
 // dgamma's low-part term of a sequence-edge chunk, sum_v Hlo[i][v] dH'[i][v]:
 // thread (lane L, column half hh) multiplies the fp16 low part of the chunk's
 // start state (edge tile `lo`, read past L1) with dH' (TMEM, columns of
@@ -209,6 +250,10 @@ __device__ __noinline__ void edge_dgamma_lo(const uint8_t* lo, uint32_t dh_tmem,
   red[base + 1] = p[1];
 }
 
+// kEdge: the caller passes dhT or asks for dh0 (states in play), so the
+// first and last chunk of each sequence take dgamma's low-part term (the
+// instantiation without it is the stateless path, free of that code).
+template <bool kEdge>
 __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -392,23 +437,6 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
       const uint32_t sbytes = split ? kSlotBytesSplit : kSlotBytesInline;
       // edge tile of chunk c (0: the sequence's first chunk, 1: its last)
       uint8_t* edge_buf = a.edge + static_cast<size_t>(item) * kEdgeBytes;
-      // low part (value minus its fp16 rounding) of 32 state values of lane
-      // L's row (columns 64 hh + 32 half ..) into an SW128 edge tile
-      auto store_lo = [&](uint8_t* tile, int half, const float (&x)[32]) {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x0 = x[8 * cc + 2 * e], x1 = x[8 * cc + 2 * e + 1];
-            const uint32_t hi = pack_h2(x0, x1);
-            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-            w[e] = pack_h2(x0 - hf.x, x1 - hf.y);
-          }
-          *reinterpret_cast<uint4*>(tile + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      };
       uint8_t* segbuf = split ? a.scratch + (static_cast<size_t>(item) * kTcBwdBufs + lv % kTcBwdBufs) * kCPS * sbytes
                               : a.scratch + static_cast<size_t>(blockIdx.x) * kCPS * sbytes;
       if (split) {  // hand-off: the helper waits until the level that last used this
@@ -438,10 +466,10 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
                 make_uint4(pack_h2(x[8 * cc], x[8 * cc + 1]), pack_h2(x[8 * cc + 2], x[8 * cc + 3]),
                            pack_h2(x[8 * cc + 4], x[8 * cc + 5]), pack_h2(x[8 * cc + 6], x[8 * cc + 7]));
-          if (c0 == 0 || c0 == nchunks - 1)  // a sequence-edge chunk starts here
-            store_lo(edge_buf + (c0 == 0 ? 0 : kStateBytes), half, x);
         }
         tmem_st_wait();
+        if (kEdge && (c0 == 0 || c0 == nchunks - 1))  // a sequence-edge chunk starts at this checkpoint
+          edge_lo_from_global(edge_buf + (c0 == 0 ? 0 : kStateBytes), src, L, hh);
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -914,7 +942,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           // the first and last chunk of a sequence also use the low part of
           // their start state (written by the rebuild pass with plain stores,
           // read past L1 in [E])
-          const bool edge = c == 0 || c == nchunks - 1;
+          const bool edge = kEdge && (c == 0 || c == nchunks - 1);
           KDA_WAIT_MMA();
           if (!mbar_wait(bar_g1, ph_g1, a.status)) *s_fail = 1;
           ph_g1 ^= 1u;
@@ -990,6 +1018,10 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           }
           fence_async_smem();
           __syncthreads();
+          if (edge) {  // add the low-part term of dgamma (RED2) to [E]'s partial sums
+            edge_fold(RED);
+            __syncthreads();
+          }
           // the next chunk's start state into A1 (its last reader was [E])
           if (more) {
             if (tid == 0) {
@@ -1001,8 +1033,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           // ---- [D1] d(chunk-end log decay); dW (Kh Gamma)^T on tf32 tiles ----
           if (tid >= kD) {
             const int i = tid - kD;
-            float dgam = RED[i] + RED[128 + i] + RED[256 + i] + RED[384 + i];
-            if (edge) dgam += (RED[512 + i] + RED[640 + i]) + (RED[768 + i] + RED[896 + i]);
+            const float dgam = RED[i] + RED[128 + i] + RED[256 + i] + RED[384 + i];
             S[S_DGE + i] = S[S_PART + i] + S[S_PART + 128 + i] + dgam * S[S_GAM + i];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {  // fold the second contraction halves of dM and dU~ V^T
@@ -1202,18 +1233,13 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           fence_before_sync();
           KDA_SYNC_OR_BAIL();
         }
-        if (!rev) {
+        if (kEdge && !rev) {
           // the rebuild pass leaves the start state of chunk c1 - 1 in TMEM:
           // when that is the sequence's last chunk, its low part goes to the
           // edge area (the first chunk's was stored with the checkpoint)
           if (c1 == nchunks && c1 - 1 > c0) {
             fence_after_sync();
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-              float x[32];
-              tmem_ld32(tmem + tlane + TM_H + 64 * hh + 32 * half, x);
-              store_lo(edge_buf + kStateBytes, half, x);
-            }
+            edge_lo_from_tmem(edge_buf + kStateBytes, tmem + tlane + TM_H + 64 * hh, L, hh);
           }
           __threadfence();  // the low parts went out as plain stores: visible before the publish
           __syncthreads();
@@ -1326,7 +1352,9 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   t.scale = a.scale;
   t.lower = a.lower;
   t.eps = a.eps;
-  if (cudaFuncSetAttribute(kda_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+  const bool edge = a.dhT != nullptr || a.dh0 != nullptr;
+  void (*kern)(const TcBwdArgs) = edge ? kda_bwd_tc_kernel<true> : kda_bwd_tc_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
     return KDA_ERR_CUDA;
   // Split mode: with fewer (sequence, head) items than SMs, the spare SMs
   // rebuild segment states for the reverse CTAs. Their hand-off waits need
@@ -1336,7 +1364,7 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_bwd_tc_kernel, kT, SMEM_BYTES);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kT, SMEM_BYTES);
   int helpers = 0;
   if (a.flags != nullptr && items < kTcBwdCtas && items < sms) {
     const int spare = sms * per_sm - items;
@@ -1348,14 +1376,14 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
     if (cudaMemsetAsync(a.flags, 0, sizeof(uint32_t) * (kTcBwdFlags * items + 1), s) != cudaSuccess)
       return KDA_ERR_CUDA;
     void* kargs[] = {&t};
-    launched = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kda_bwd_tc_kernel), dim3(items + helpers),
+    launched = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(items + helpers),
                                            dim3(kT), kargs, SMEM_BYTES, s) == cudaSuccess;
     if (!launched) {
       cudaGetLastError();  // clear the refusal; run inline instead
       t.helpers = 0;
     }
   }
-  if (!launched && ctas > 0) kda_bwd_tc_kernel<<<ctas, kT, SMEM_BYTES, s>>>(t);
+  if (!launched && ctas > 0) kern<<<ctas, kT, SMEM_BYTES, s>>>(t);
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   kda_param_reduce_tc_kernel<<<p->num_heads, 128, 0, s>>>(a.partial, p->num_seqs, p->num_heads, kD, a.dA_log,
                                                           a.ddt_bias);
