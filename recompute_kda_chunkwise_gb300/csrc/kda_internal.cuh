@@ -94,6 +94,10 @@ __device__ __forceinline__ void stf(float* p, float x) { *p = x; }
 __device__ __forceinline__ void stf(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
+// sigmoid'(x) = sigmoid(x) sigmoid(-x): both factors are computed directly,
+// so the result keeps its relative accuracy where sigmoid(x) is near 1
+// (1 - sigmoid(x) would cancel there).
+__device__ __forceinline__ float sigmoid_grad(float x) { return sigmoidf_(x) * sigmoidf_(-x); }
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll

@@ -46,6 +46,17 @@ namespace {
 
 constexpr int kNT = 256;
 
+// Accumulator type of the contractions: fp64 for fp32 GDN-2 problems (see
+// the backward kernel), fp32 otherwise.
+template <typename Tin, bool CG>
+struct AccOf {
+  using type = float;
+};
+template <>
+struct AccOf<float, true> {
+  using type = double;
+};
+
 template <int D>
 struct SimtChunk;
 template <>
@@ -176,42 +187,42 @@ __device__ void chunk_prologue(const Tiles<D, C>& t, const Tin* q, const Tin* k,
 // W = T diag(beta) Kg, U = T diag(beta) V. With CG (GDN-2) Abar carries the
 // erase gates, Abar[r,s] = sum_i Be_ri Kg_ri Ki_si, T = (I + Abar)^-1,
 // W = T (Be*Kg) and U = T (Wr*V).
-template <int D, int C, bool CG = false>
+template <int D, int C, bool CG = false, typename Acc = float>
 __device__ void chunk_intra(const Tiles<D, C>& t) {
   constexpr int LD = D + 1, CP = C + 1;
   const int tid = threadIdx.x;
   for (int x = tid; x < C * C; x += kNT) {
     const int r = x / C, s = x % C;
-    float akk = 0.f, aqk = 0.f;
+    Acc akk = 0, aqk = 0;
     if (s <= r) {
       for (int i = 0; i < D; ++i) {
         const float ki = t.Ki[s * LD + i];
         if constexpr (CG)
-          akk += t.Be[r * LD + i] * t.Kg[r * LD + i] * ki;
+          akk += Acc(t.Be[r * LD + i] * t.Kg[r * LD + i]) * ki;
         else
-          akk += t.Kg[r * LD + i] * ki;
-        aqk += t.Qg[r * LD + i] * ki;
+          akk += Acc(t.Kg[r * LD + i]) * ki;
+        aqk += Acc(t.Qg[r * LD + i]) * ki;
       }
     }
-    t.Abar[r * CP + s] = s < r ? akk : 0.f;
-    t.Aqk[r * CP + s] = s <= r ? aqk : 0.f;
+    t.Abar[r * CP + s] = s < r ? static_cast<float>(akk) : 0.f;
+    t.Aqk[r * CP + s] = s <= r ? static_cast<float>(aqk) : 0.f;
   }
   __syncthreads();
   if (tid < 32) {  // forward substitution, one lane per column of T
     const int j = tid;
     for (int r = 0; r < C; ++r) {
       if (j < C) {
-        float val;
+        Acc val;
         if (j == r) {
-          val = 1.f;
+          val = 1;
         } else if (j > r) {
-          val = 0.f;
+          val = 0;
         } else {
-          val = 0.f;
+          val = 0;
           const float br = CG ? 1.f : t.bet[r];
-          for (int s = j; s < r; ++s) val -= br * t.Abar[r * CP + s] * t.Tm[s * CP + j];
+          for (int s = j; s < r; ++s) val -= Acc(br * t.Abar[r * CP + s]) * t.Tm[s * CP + j];
         }
-        t.Tm[r * CP + j] = val;
+        t.Tm[r * CP + j] = static_cast<float>(val);
       }
       __syncwarp();
     }
@@ -219,10 +230,10 @@ __device__ void chunk_intra(const Tiles<D, C>& t) {
   __syncthreads();
   for (int x = tid; x < C * D; x += kNT) {
     const int r = x / D, i = x % D;
-    float w = 0.f, u = 0.f;
+    Acc w = 0, u = 0;
     if constexpr (CG) {
       for (int s = 0; s <= r; ++s) {
-        const float ts = t.Tm[r * CP + s];
+        const Acc ts = t.Tm[r * CP + s];
         w += ts * (t.Be[s * LD + i] * t.Kg[s * LD + i]);
         u += ts * (t.Wr[s * LD + i] * t.Vv[s * LD + i]);
       }
@@ -233,33 +244,33 @@ __device__ void chunk_intra(const Tiles<D, C>& t) {
         u += ts * t.Vv[s * LD + i];
       }
     }
-    t.Ww[r * LD + i] = w;
-    t.Uu[r * LD + i] = u;
+    t.Ww[r * LD + i] = static_cast<float>(w);
+    t.Uu[r * LD + i] = static_cast<float>(u);
   }
   __syncthreads();
 }
 
 // U~ = U - W H (in place in Uu). H is D x V with row stride ldh.
-template <int D, int C>
+template <int D, int C, typename Acc = float>
 __device__ void state_residual(const Tiles<D, C>& t, const float* Hs, int ldh) {
   constexpr int V = D, LD = D + 1, RG = kNT / V, RPT = C / RG;
   static_assert(C % RG == 0, "rows per thread");
   const int tid = threadIdx.x, j = tid % V, rg = tid / V;
-  float acc[RPT];
+  Acc acc[RPT];
 #pragma unroll
   for (int rr = 0; rr < RPT; ++rr) acc[rr] = t.Uu[(rg * RPT + rr) * LD + j];
   for (int i = 0; i < D; ++i) {
     const float hv = Hs[i * ldh + j];
 #pragma unroll
-    for (int rr = 0; rr < RPT; ++rr) acc[rr] -= t.Ww[(rg * RPT + rr) * LD + i] * hv;
+    for (int rr = 0; rr < RPT; ++rr) acc[rr] -= Acc(t.Ww[(rg * RPT + rr) * LD + i]) * hv;
   }
 #pragma unroll
-  for (int rr = 0; rr < RPT; ++rr) t.Uu[(rg * RPT + rr) * LD + j] = acc[rr];
+  for (int rr = 0; rr < RPT; ++rr) t.Uu[(rg * RPT + rr) * LD + j] = static_cast<float>(acc[rr]);
   __syncthreads();
 }
 
 // H = diag(gam) H + Kb^T U~ (in place).
-template <int D, int C>
+template <int D, int C, typename Acc = float>
 __device__ void state_update(const Tiles<D, C>& t, float* Hs, int ldh) {
   constexpr int V = D, LD = D + 1, IG = kNT / V, IPT = D / IG;
   const int tid = threadIdx.x, j = tid % V, ig = tid / V;
@@ -268,10 +279,10 @@ __device__ void state_update(const Tiles<D, C>& t, float* Hs, int ldh) {
   for (int r = 0; r < C; ++r) u[r] = t.Uu[r * LD + j];
   for (int ii = 0; ii < IPT; ++ii) {
     const int i = ig * IPT + ii;
-    float acc = t.gam[i] * Hs[i * ldh + j];
+    Acc acc = Acc(t.gam[i]) * Hs[i * ldh + j];
 #pragma unroll
-    for (int r = 0; r < C; ++r) acc += t.Kb[r * LD + i] * u[r];
-    Hs[i * ldh + j] = acc;
+    for (int r = 0; r < C; ++r) acc += Acc(t.Kb[r * LD + i]) * u[r];
+    Hs[i * ldh + j] = static_cast<float>(acc);
   }
   __syncthreads();
 }
@@ -373,6 +384,12 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
   constexpr int CPS = kCkptTokens / C;  // chunks per checkpoint segment
   constexpr int RGD = kNT / D, RPTD = C / RGD;
   extern __shared__ float sm[];
+  // fp32 GDN-2 problems accumulate every contraction of the backward in fp64
+  // (products of fp32 values are exact there; results are stored in fp32):
+  // the erase-gate gradient takes two large terms through W and through
+  // Abar that nearly cancel, and its 1e-4-of-RMS bar needs them to better
+  // than fp32.
+  using Acc = typename AccOf<Tin, CG>::type;
   Tiles<D, C> t;
   BwdTiles<D, C> u;
   u.carve(t.carve(sm, CG));
@@ -425,9 +442,9 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
         const int64_t t0 = bos + (int64_t)c * C;
         const int rows = (int)min((int64_t)C, eos - t0);
         chunk_prologue<Tin, D, C, CG>(t, q, k, v, g, b, w, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
-        chunk_intra<D, C, CG>(t);
-        state_residual<D, C>(t, u.Hc, LDH);
-        state_update<D, C>(t, u.Hc, LDH);
+        chunk_intra<D, C, CG, Acc>(t);
+        state_residual<D, C, Acc>(t, u.Hc, LDH);
+        state_update<D, C, Acc>(t, u.Hc, LDH);
       }
       __syncthreads();
 
@@ -443,28 +460,28 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
           }
         }
         chunk_prologue<Tin, D, C, CG>(t, q, k, v, g, b, w, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
-        chunk_intra<D, C, CG>(t);
-        state_residual<D, C>(t, u.Hc, LDH);  // t.Uu = U~, t.Ww = W
+        chunk_intra<D, C, CG, Acc>(t);
+        state_residual<D, C, Acc>(t, u.Hc, LDH);  // t.Uu = U~, t.Ww = W
 
         // dU~[r][j] = sum_{r'>=r} Aqk[r'][r] dO[r'][j] + sum_i Kb[r][i] dH[i][j]
         {
           constexpr int RG = kNT / V, RPT = C / RG;
           const int j = tid % V, rg = tid / V;
-          float acc[RPT];
+          Acc acc[RPT];
 #pragma unroll
           for (int rr = 0; rr < RPT; ++rr) {
             const int r = rg * RPT + rr;
-            float s_ = 0.f;
-            for (int r2 = r; r2 < C; ++r2) s_ += t.Aqk[r2 * CP + r] * u.dOt[r2 * LD + j];
+            Acc s_ = 0;
+            for (int r2 = r; r2 < C; ++r2) s_ += Acc(t.Aqk[r2 * CP + r]) * u.dOt[r2 * LD + j];
             acc[rr] = s_;
           }
           for (int i = 0; i < D; ++i) {
             const float dh = u.dH[i * LDH + j];
 #pragma unroll
-            for (int rr = 0; rr < RPT; ++rr) acc[rr] += t.Kb[(rg * RPT + rr) * LD + i] * dh;
+            for (int rr = 0; rr < RPT; ++rr) acc[rr] += Acc(t.Kb[(rg * RPT + rr) * LD + i]) * dh;
           }
 #pragma unroll
-          for (int rr = 0; rr < RPT; ++rr) u.dUt[(rg * RPT + rr) * LD + j] = acc[rr];
+          for (int rr = 0; rr < RPT; ++rr) u.dUt[(rg * RPT + rr) * LD + j] = static_cast<float>(acc[rr]);
         }
         __syncthreads();
 
@@ -472,33 +489,33 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
         //   d(Qg) = dO H^T, dW = -dU~ H^T, dKb = U~ dH^T, dgamma = rowsum(H * dH)
         {
           const int i = tid % D, rg = tid / D;
-          float aQ[RPTD], aW[RPTD], aK[RPTD], ag = 0.f;
+          Acc aQ[RPTD], aW[RPTD], aK[RPTD], ag = 0;
 #pragma unroll
           for (int rr = 0; rr < RPTD; ++rr) aQ[rr] = aW[rr] = aK[rr] = 0.f;
           for (int j = 0; j < V; ++j) {
             const float hv = u.Hc[i * LDH + j], dh = u.dH[i * LDH + j];
-            ag += hv * dh;
+            ag += Acc(hv) * dh;
 #pragma unroll
             for (int rr = 0; rr < RPTD; ++rr) {
               const int r = rg * RPTD + rr;
-              aQ[rr] += u.dOt[r * LD + j] * hv;
-              aW[rr] += u.dUt[r * LD + j] * hv;
-              aK[rr] += t.Uu[r * LD + j] * dh;
+              aQ[rr] += Acc(u.dOt[r * LD + j]) * hv;
+              aW[rr] += Acc(u.dUt[r * LD + j]) * hv;
+              aK[rr] += Acc(t.Uu[r * LD + j]) * dh;
             }
           }
-          float ge = 0.f;
+          Acc ge = 0;
 #pragma unroll
           for (int rr = 0; rr < RPTD; ++rr) {
             const int r = rg * RPTD + rr;
             const float G = t.Gc[r * LD + i], Ge = t.Gc[(C - 1) * LD + i];
-            u.dQ[r * LD + i] = aQ[rr] * expf(G);
-            u.dGt[r * LD + i] = aQ[rr] * t.Qg[r * LD + i] - aK[rr] * t.Kb[r * LD + i];
-            u.dWt[r * LD + i] = -aW[rr];
-            u.dK[r * LD + i] = aK[rr] * expf(Ge - G);
+            u.dQ[r * LD + i] = static_cast<float>(aQ[rr] * expf(G));
+            u.dGt[r * LD + i] = static_cast<float>(aQ[rr] * t.Qg[r * LD + i] - aK[rr] * t.Kb[r * LD + i]);
+            u.dWt[r * LD + i] = static_cast<float>(-aW[rr]);
+            u.dK[r * LD + i] = static_cast<float>(aK[rr] * expf(Ge - G));
             ge += aK[rr] * t.Kb[r * LD + i];
           }
           if (rg == 0) ge += ag * t.gam[i];
-          u.part[tid] = ge;
+          u.part[tid] = static_cast<float>(ge);
         }
         __syncthreads();
         for (int i = tid; i < D; i += kNT) {
@@ -518,23 +535,23 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
           }
           for (int ii = 0; ii < IPT; ++ii) {
             const int i = ig * IPT + ii;
-            float acc = t.gam[i] * u.dH[i * LDH + j];
+            Acc acc = Acc(t.gam[i]) * u.dH[i * LDH + j];
 #pragma unroll
-            for (int r = 0; r < C; ++r) acc += t.Qg[r * LD + i] * o_[r] - t.Ww[r * LD + i] * du[r];
-            u.dH[i * LDH + j] = acc;
+            for (int r = 0; r < C; ++r) acc += Acc(t.Qg[r * LD + i]) * o_[r] - Acc(t.Ww[r * LD + i]) * du[r];
+            u.dH[i * LDH + j] = static_cast<float>(acc);
           }
         }
         // dM = tril(dO U~^T);  dT = strictly-lower part of dW Xw^T + dU~ Xu^T
         for (int x = tid; x < C * C; x += kNT) {
           const int r = x / C, s = x % C;
-          float dm = 0.f, dt = 0.f;
+          Acc dm = 0, dt = 0;
           if (s <= r)
-            for (int j = 0; j < V; ++j) dm += u.dOt[r * LD + j] * t.Uu[s * LD + j];
+            for (int j = 0; j < V; ++j) dm += Acc(u.dOt[r * LD + j]) * t.Uu[s * LD + j];
           if (s < r) {
-            float d1 = 0.f, d2 = 0.f;
+            Acc d1 = 0, d2 = 0;
             if constexpr (CG) {  // dW Xw^T + dU~ Xu^T with the channel gates
-              for (int i = 0; i < D; ++i) d1 += u.dWt[r * LD + i] * (t.Be[s * LD + i] * t.Kg[s * LD + i]);
-              for (int j = 0; j < V; ++j) d2 += u.dUt[r * LD + j] * (t.Wr[s * LD + j] * t.Vv[s * LD + j]);
+              for (int i = 0; i < D; ++i) d1 += Acc(u.dWt[r * LD + i]) * (Acc(t.Be[s * LD + i]) * t.Kg[s * LD + i]);
+              for (int j = 0; j < V; ++j) d2 += Acc(u.dUt[r * LD + j]) * (Acc(t.Wr[s * LD + j]) * t.Vv[s * LD + j]);
               dt = d1 + d2;
             } else {
               for (int i = 0; i < D; ++i) d1 += u.dWt[r * LD + i] * t.Kg[s * LD + i];
@@ -542,26 +559,26 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
               dt = t.bet[s] * (d1 + d2);
             }
           }
-          u.dM[r * CP + s] = dm;
-          u.dT[r * CP + s] = dt;
+          u.dM[r * CP + s] = static_cast<float>(dm);
+          u.dT[r * CP + s] = static_cast<float>(dt);
         }
         __syncthreads();
         // Y = dT T^T
         for (int x = tid; x < C * C; x += kNT) {
           const int a_ = x / C, s = x % C;
-          float y = 0.f;
+          Acc y = 0;
           const int bmax = min(s, a_ - 1);
-          for (int bb = 0; bb <= bmax; ++bb) y += u.dT[a_ * CP + bb] * t.Tm[s * CP + bb];
-          u.Yt[a_ * CP + s] = y;
+          for (int bb = 0; bb <= bmax; ++bb) y += Acc(u.dT[a_ * CP + bb]) * t.Tm[s * CP + bb];
+          u.Yt[a_ * CP + s] = static_cast<float>(y);
         }
         __syncthreads();
         // dA = -(T^T Y) on the strictly lower part (reuse dT for dA)
         for (int x = tid; x < C * C; x += kNT) {
           const int r = x / C, s = x % C;
-          float da = 0.f;
+          Acc da = 0;
           if (s < r)
-            for (int a_ = r; a_ < C; ++a_) da -= t.Tm[a_ * CP + r] * u.Yt[a_ * CP + s];
-          u.dT[r * CP + s] = da;
+            for (int a_ = r; a_ < C; ++a_) da -= Acc(t.Tm[a_ * CP + r]) * u.Yt[a_ * CP + s];
+          u.dT[r * CP + s] = static_cast<float>(da);
         }
         // dXw = T^T dW (in place, by column); dXu = T^T dU~ (into dOt, free now)
         for (int x = tid; x < D + V; x += kNT) {
@@ -572,9 +589,9 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
           float* out = x < D ? (u.dWt + x) : (u.dOt + (x - D));
 #pragma unroll
           for (int r = 0; r < C; ++r) {
-            float s_ = 0.f;
-            for (int r2 = r; r2 < C; ++r2) s_ += t.Tm[r2 * CP + r] * col[r2];
-            out[r * LD] = s_;
+            Acc s_ = 0;
+            for (int r2 = r; r2 < C; ++r2) s_ += Acc(t.Tm[r2 * CP + r]) * col[r2];
+            out[r * LD] = static_cast<float>(s_);
           }
         }
         __syncthreads();
@@ -586,7 +603,7 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
             if constexpr (CG) {
               const float wr = t.Wr[r * LD + j], dxu = u.dOt[r * LD + j];
               stf(dv + off, wr * dxu);
-              stf(dw + off, t.Vv[r * LD + j] * dxu * wr * (1.f - wr));
+              stf(dw + off, t.Vv[r * LD + j] * dxu * sigmoid_grad(ldf(w + off)));
             } else {
               stf(dv + off, t.bet[r] * u.dOt[r * LD + j]);
             }
@@ -612,16 +629,19 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
           if constexpr (CG) {
             // dXw = T^T dW + dA Ki; Xw = Be*Kg gives dBe = Kg dXw and dKg = Be dXw;
             // dKi = dA^T Xw
-            float a1 = 0.f, a2 = 0.f, m1 = 0.f, m2 = 0.f;
-            for (int s = 0; s < r; ++s) a1 += u.dT[r * CP + s] * t.Ki[s * LD + i];
-            for (int s = r + 1; s < C; ++s) a2 += u.dT[s * CP + r] * (t.Be[s * LD + i] * t.Kg[s * LD + i]);
-            for (int s = 0; s <= r; ++s) m1 += u.dM[r * CP + s] * t.Ki[s * LD + i];
-            for (int s = r; s < C; ++s) m2 += u.dM[s * CP + r] * t.Qg[s * LD + i];
-            const float be = t.Be[r * LD + i], kg = t.Kg[r * LD + i], dX = dxw + a1;
-            u.dQ[r * LD + i] += m1 * e;
-            u.dK[r * LD + i] += be * e * dX + (a2 + m2) * ei;
-            u.dGt[r * LD + i] += be * dX * kg + m1 * t.Qg[r * LD + i] - (a2 + m2) * t.Ki[r * LD + i];
-            if (r < rows) stf(db + ((t0 + r) * a.H + h) * (int64_t)D + i, kg * dX * be * (1.f - be));
+            Acc a1 = 0, a2 = 0, m1 = 0, m2 = 0;
+            for (int s = 0; s < r; ++s) a1 += Acc(u.dT[r * CP + s]) * t.Ki[s * LD + i];
+            for (int s = r + 1; s < C; ++s) a2 += Acc(u.dT[s * CP + r]) * (Acc(t.Be[s * LD + i]) * t.Kg[s * LD + i]);
+            for (int s = 0; s <= r; ++s) m1 += Acc(u.dM[r * CP + s]) * t.Ki[s * LD + i];
+            for (int s = r; s < C; ++s) m2 += Acc(u.dM[s * CP + r]) * t.Qg[s * LD + i];
+            const Acc be = t.Be[r * LD + i], kg = t.Kg[r * LD + i], dX = dxw + a1;
+            u.dQ[r * LD + i] += static_cast<float>(m1 * e);
+            u.dK[r * LD + i] += static_cast<float>(be * e * dX + (a2 + m2) * ei);
+            u.dGt[r * LD + i] += static_cast<float>(be * dX * kg + m1 * t.Qg[r * LD + i] - (a2 + m2) * t.Ki[r * LD + i]);
+            if (r < rows) {
+              const int64_t off = ((t0 + r) * a.H + h) * (int64_t)D + i;
+              stf(db + off, static_cast<float>(kg * dX * Acc(sigmoid_grad(ldf(b + off)))));
+            }
             continue;
           }
           const float br = t.bet[r];
@@ -673,16 +693,14 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
             stf(dq + off, (dxq - t.Qh[r * LD + i] * u.rq[r]) * iq);
             stf(dk + off, (u.dK[r * LD + i] - t.Kh[r * LD + i] * u.rk[r]) * ik);
             const float z = expA * (ldf(g + off) + t.dtb[i]);
-            const float sg = sigmoidf_(z);
-            const float dz = u.dGt[r * LD + i] * a.lower * sg * (1.f - sg);
+            const float dz = u.dGt[r * LD + i] * a.lower * sigmoid_grad(z);
             stf(dg + off, expA * dz);
             acc_dtb += expA * dz;
             acc_alog += dz * z;
           }
         }
         if (!CG && tid < C && tid < rows) {
-          const float bt = t.bet[tid];
-          stf(db + (t0 + tid) * a.H + h, u.dbet[tid] * bt * (1.f - bt));
+          stf(db + (t0 + tid) * a.H + h, u.dbet[tid] * sigmoid_grad(ldf(b + (t0 + tid) * a.H + h)));
         }
         __syncthreads();
       }
