@@ -120,11 +120,10 @@ struct TcFwdArgs {
   int N, H;
   float scale, lower, eps;
   int test_timeout;
-  // split mode (helpers > 0): CTAs N*H .. N*H+helpers-1 prepare a fraction
-  // ha / hb (<= 1/2) of the chunks of every item, chunk c being theirs when
-  // ((c + 1) ha) / hb > (c ha) / hb, and hand them over through xbuf / xflags
-  int helpers, ha, hb;
-  uint32_t* xflags;  // per item: [4] handed-chunk index + 1 written into slot q, [4] consumed count
+  // split mode (helpers > 0): CTAs N*H .. N*H+helpers-1 prepare the odd
+  // chunks of every item and hand them over through xbuf / xflags
+  int helpers;
+  uint32_t* xflags;  // per item: [4] last odd-chunk index + 1 written into slot q, [4] consumed count
   uint8_t* xbuf;     // per item: kXSlots slots of kXSlotBytes
 };
 
@@ -287,13 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Roles. Without helpers, CTA b walks every chunk of item b. In split mode
-  // the main CTA b < items prepares most chunks itself and takes the rest,
-  // a fraction ha / hb spread evenly (never two in a row), prepared by the
-  // helper CTAs, which walk jobs t * items + item (the item's t-th handed
-  // chunk) in order, helper j taking jobs j, j + helpers, ...
-  auto is_handed = [&](int cc) { return ((cc + 1) * a.ha) / a.hb > (cc * a.ha) / a.hb; };
-  auto handed_index = [&](int cc) { return ((cc + 1) * a.ha) / a.hb - 1; };
-  auto handed_chunk = [&](int t) { return ((t + 1) * a.hb + a.ha - 1) / a.ha - 1; };
+  // the main CTA b < items prepares its even chunks itself and takes the odd
+  // ones prepared by the helper CTAs, which walk jobs t * items + item (odd
+  // chunk 2t + 1 of item) in order, helper j taking jobs j, j + helpers, ...
   const int items = a.N * a.H;
   const bool split = a.helpers > 0;
   const bool helper = split && static_cast<int>(blockIdx.x) >= items;
@@ -303,10 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   int nchunks = helper ? 0 : static_cast<int>((eos - bos + kC - 1) / kC);
   int job = static_cast<int>(blockIdx.x) - items, max_jobs = 0;
   if (helper) {
-    int max_handed = 0;
+    int max_odd = 0;
     for (int s2 = 0; s2 < a.N; ++s2)
-      max_handed = max(max_handed, static_cast<int>((a.cu[s2 + 1] - a.cu[s2] + kC - 1) / kC) * a.ha / a.hb);
-    max_jobs = max_handed * items;
+      max_odd = max(max_odd, static_cast<int>((a.cu[s2 + 1] - a.cu[s2] + kC - 1) / kC) / 2);
+    max_jobs = max_odd * items;
   }
 
   if (tid == 0) {
@@ -394,9 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (job < max_jobs) {
       const int tt = job / items, it = job % items, s2 = it / a.H;
       job += a.helpers;
-      if (handed_chunk(tt) < static_cast<int>((a.cu[s2 + 1] - a.cu[s2] + kC - 1) / kC)) {
+      if (2 * tt + 1 < static_cast<int>((a.cu[s2 + 1] - a.cu[s2] + kC - 1) / kC)) {
         nx_item = it;
-        nx_c = handed_chunk(tt);
+        nx_c = 2 * tt + 1;
         return;
       }
     }
@@ -436,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       dtb1 = a.dt_bias[h * kD + c0 + 1];
       find_job();
     }
-    const bool handed = split && !helper && is_handed(c);  // prepared by a helper
+    const bool handed = split && !helper && (c & 1);  // prepared by a helper
     const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
     const int rows = static_cast<int>(min(static_cast<int64_t>(kC), eos - t0));
 
@@ -591,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk (into the offsets' space) and q, k, g of the next chunk
     if (tid == 0) {
       issue_v(static_cast<int>(t0));
-      const int cn = (split && is_handed(c + 1)) ? c + 2 : c + 1;  // the next chunk this CTA prepares itself
+      const int cn = split ? c + 2 : c + 1;  // the next chunk this CTA prepares itself
       if (helper) {
         if (nx_c >= 0) issue_next_job();
       } else if (cn < nchunks) {
@@ -737,11 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     KDA_SYNC_OR_BAIL();
     }  // prepared here
     if (helper) {
-      // ---- hand the prepared chunk over: the operand runs, T' hi and
+      // ---- hand the prepared odd chunk over: the operand runs, T' hi and
       // gamma to the item's slot once the main CTA has drained it; the stores
       // complete, and are published, during the next job ----
       if (tid == 0) {
-        const int tt = handed_index(c);
+        const int tt = c >> 1;
         if (tt >= kXSlots && !wait_flag_geq(a.xflags + 5 * item + 4, static_cast<uint32_t>(tt - kXSlots + 1), a.status))
           *s_fail = 1;
         fence_proxy_global();
@@ -764,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         *s_fail = 1;
       ph_x ^= 1u;
-      if (tid == 0) st_release(a.xflags + 5 * item + 4, static_cast<uint32_t>(handed_index(c) + 1));
+      if (tid == 0) st_release(a.xflags + 5 * item + 4, static_cast<uint32_t>((c >> 1) + 1));
     }
     if (tid == 0) {
       fence_after_sync();
@@ -818,11 +813,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     KDA_WAIT(bar_mma, ph_mma);
     fence_after_sync();
-    if (split && !handed && c + 1 < nchunks && is_handed(c + 1)) {
-      // fetch the helper-prepared next chunk into the tiles this chunk has
-      // finished with (its last product above has completed)
+    if (split && !(c & 1) && c + 1 < nchunks) {
+      // fetch the helper-prepared next (odd) chunk into the tiles this chunk
+      // has finished with (its last product above has completed)
       if (tid == 0) {
-        const int tt = handed_index(c + 1);
+        const int tt = (c + 1) >> 1;
         if (!wait_flag_geq(a.xflags + 5 * item + tt % kXSlots, static_cast<uint32_t>(tt + 1), a.status)) *s_fail = 1;
         fence_proxy_global();
         const uint8_t* slot = a.xbuf + (static_cast<size_t>(item) * kXSlots + tt % kXSlots) * kXSlotBytes;
@@ -951,8 +946,6 @@ kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s)
   t.eps = a.eps;
   t.test_timeout = a.test_timeout;
   t.helpers = 0;
-  t.ha = 1;
-  t.hb = 2;
   t.xflags = a.xflags;
   t.xbuf = a.xbuf;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -970,25 +963,8 @@ kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s)
   bool launched = false;
   if (a.xflags != nullptr && !a.test_timeout && items > 0 && items < sms * per_sm) {
     const int spare = sms * per_sm - items;
-    if (8 * spare >= items) {
+    if (2 * spare >= items) {
       t.helpers = spare < items ? spare : items;
-      // The helpers' share ha / 12 of the chunks balances the main CTAs'
-      // time per chunk, (1 - f) kOwn + f kHanded, against the helpers',
-      // f kJob items / helpers (cycles per chunk measured with stage timers on
-      // the 1 x 131072-token, 96-head launch: a main CTA's own chunk, a
-      // handed chunk, and a helper job with its hand-off).
-      constexpr float kOwn = 27.6f, kHanded = 5.5f, kJob = 26.f;
-      float best = 1e30f;
-      for (int ha = 1; ha <= 6; ++ha) {
-        const float f = ha / 12.f;
-        const float tm = (1.f - f) * kOwn + f * kHanded, th = f * kJob * items / t.helpers;
-        const float tc = tm > th ? tm : th;
-        if (tc < best) {
-          best = tc;
-          t.ha = ha;
-          t.hb = 12;
-        }
-      }
       if (cudaMemsetAsync(a.xflags, 0, sizeof(uint32_t) * 5 * items, s) != cudaSuccess) return KDA_ERR_CUDA;
       void* kargs[] = {&mq, &mk, &mv, &mg, &t};
       launched = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kda_fwd_tc_kernel),
