@@ -632,7 +632,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=None)
     ap.add_argument("--pass", dest="pass_", choices=["fwdbwd", "fwd"], default="fwdbwd",
                     help="fwd: forward-only inference (no checkpoints); the default times fwd+bwd")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=24)
     ap.add_argument("--sample-tokens", type=int, default=98304,
                     help="tokens of the oracle sample behind cpu_baseline (about 10-30 s of host work)")
     ap.add_argument("--ref-sample-tokens", type=int, default=32768,
