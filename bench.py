@@ -596,6 +596,12 @@ def run_gb300(args, w, rank, world, local):
         cpu_base = {"value": rate / w.H, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                     "sample": (f"first {sl['q'].shape[0]} tokens x {heads} heads of {w.name} "
                                f"(fwd+bwd, fp64, {dt:.1f} s wall), scaled to tokens/s over all {w.H} heads")}
+        # the same oracle on one core, on a smaller sample (one head)
+        sl1 = make_sample(w, inp, min(args.sample_tokens, 16384), 1)
+        rate1, dt1 = oracle_sample(w, sl1, 1)
+        cpu_base["one_core"] = {"value": rate1 / w.H, "unit": "tokens/s", "cores": 1,
+                                "sample": (f"first {sl1['q'].shape[0]} tokens x 1 head (fwd+bwd, fp64, "
+                                           f"{dt1:.1f} s), scaled to tokens/s over all {w.H} heads")}
         # The forward is causal, so o on the sample's tokens is exactly what
         # the oracle computed for them: the timed run's own output, checked.
         T_s = sl["q"].shape[0]
