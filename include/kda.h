@@ -96,7 +96,9 @@ typedef enum {
  * (kda_gdn2_fwd / kda_gdn2_bwd below). Set it before the size queries so
  * that they size ctx and workspace for the GDN-2 kernels; kda_fwd, kda_bwd
  * and kda_bwd_noalloc reject it, and kda_gdn2_fwd / kda_gdn2_bwd require it.
- * GDN-2 runs on the fp32 CUDA-core kernels for every dtype and head_dim. */
+ * The GDN-2 forward runs on the tensor-core kernels for bf16 with head_dim
+ * 128 (the CUDA-core kernels otherwise); the GDN-2 backward runs on the
+ * fp32 CUDA-core kernels for every dtype and head_dim. */
 #define KDA_FLAG_CHANNEL_GATES 8
 
 /* Problem description. cu_seqlens is a DEVICE pointer; the library never
@@ -312,10 +314,11 @@ const char* kda_status_string(kda_status s);
  * overwritten by the next failing call on that thread). */
 const char* kda_last_error_message(void);
 
-/* Which kernel family a problem's forward and backward dispatch to: 0 = fp32 CUDA-core
- * (SIMT) kernels, 1 = tcgen05 tensor-core kernels (bf16, head_dim 128,
- * unless KDA_FLAG_FORCE_SIMT); -1 for an invalid or unsupported problem.
- * Host only. */
+/* Which kernel families a problem's forward and backward dispatch to: 0 =
+ * fp32 CUDA-core (SIMT) kernels for both, 1 = tcgen05 tensor-core kernels
+ * for both (bf16, head_dim 128, unless KDA_FLAG_FORCE_SIMT), 2 = tensor-core
+ * forward and CUDA-core backward (GDN-2 problems in bf16 with head_dim 128);
+ * -1 for an invalid or unsupported problem. Host only. */
 int kda_kernel_family(const kda_problem* p);
 
 /* Library ABI version, major * 100 + minor * 10 (220 = 2.2: the affine state prefix,

@@ -54,11 +54,14 @@ kda_status validate(const kda_problem* p, bool need_ptrs = true) {
   return KDA_OK;
 }
 
-// Kernel family of both passes: tcgen05 kernels for bf16 D = 128, else fp32
-// SIMT. GDN-2 problems (channel-wise gates) always run the SIMT kernels.
-int family_of(const kda_problem* p) {
-  return (p->dtype == KDA_DTYPE_BF16 && p->head_dim == 128 &&
-          !(p->flags & (KDA_FLAG_FORCE_SIMT | KDA_FLAG_CHANNEL_GATES))) ? 1 : 0;
+// Kernel family of each pass: tcgen05 kernels for bf16 D = 128 (unless
+// KDA_FLAG_FORCE_SIMT), else fp32 SIMT. GDN-2 problems (channel-wise gates)
+// run the tensor-core forward but the SIMT backward.
+int fwd_family_of(const kda_problem* p) {
+  return (p->dtype == KDA_DTYPE_BF16 && p->head_dim == 128 && !(p->flags & KDA_FLAG_FORCE_SIMT)) ? 1 : 0;
+}
+int family_of(const kda_problem* p) {  // the backward's
+  return (fwd_family_of(p) == 1 && !(p->flags & KDA_FLAG_CHANNEL_GATES)) ? 1 : 0;
 }
 
 size_t ckpt_slots(const kda_problem* p) {
@@ -76,7 +79,7 @@ size_t ckpt_bytes(const kda_problem* p) {
 // the checkpoints in ctx.
 size_t fwd_handoff(const kda_problem* p) {
   const int64_t items = (int64_t)p->num_seqs * p->num_heads;
-  if (family_of(p) != 1 || items <= 0 || items >= kda::kTcBwdCtas) return 0;
+  if (fwd_family_of(p) != 1 || items <= 0 || items >= kda::kTcBwdCtas) return 0;
   return kda::fwd_handoff_bytes((int)items);
 }
 
@@ -191,7 +194,10 @@ size_t kda_bwd_workspace_bytes(const kda_problem* p) {
   return validate(p, false) == KDA_OK ? workspace_bytes(p) : 0;
 }
 
-int kda_kernel_family(const kda_problem* p) { return validate(p, false) == KDA_OK ? family_of(p) : -1; }
+int kda_kernel_family(const kda_problem* p) {
+  if (validate(p, false) != KDA_OK) return -1;
+  return fwd_family_of(p) == family_of(p) ? family_of(p) : 2;
+}
 
 int kda_version(void) { return 220; }
 
@@ -253,7 +259,7 @@ kda_status forward(const kda_problem* p, const void* q, const void* k, const voi
     st = kda::launch_check_cu(p->cu_seqlens, p->num_seqs, p->total_tokens, (int32_t*)a.cu, a.status, s);
     if (st != KDA_OK) return fail(st, "cu_seqlens check launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   }
-  st = family_of(p) == 1 ? kda::launch_fwd_tc(p, a, s) : kda::launch_fwd_simt(p, a, s);
+  st = fwd_family_of(p) == 1 ? kda::launch_fwd_tc(p, a, s) : kda::launch_fwd_simt(p, a, s);
   if (st != KDA_OK) return fail(st, "forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return KDA_OK;
 }

@@ -71,13 +71,14 @@ constexpr int OFF_X = OFF_R + 58368;   //        fp32 scratch [8][16][9]
 constexpr int OFF_TPL = OFF_R + 16384; //   after the inverse (Abar dead): T' low part fp16 [64 r][64 s]
 constexpr int OFF_ML = OFF_R + 24576;  //                                  M low part fp16 [64 r][64 s]
 constexpr int OFF_UL = OFF_R;          //   after the U product (v dead): U~^T low part fp16 [128 v][64 r]
+constexpr int OFF_WG = OFF_R + 33792;  //   GDN-2: after the inverse (T dead), the raw write gate bf16 SW128 [64 s][128 v]
 constexpr int OFF_SMALL = OFF_R + 65536;
 // small fp32 arrays
 constexpr int SM_BETA = 0, SM_IQ = 64, SM_IK = 128, SM_GAM = 192, SM_EB = 320, SM_EK = 832, SM_U = 1344;
 constexpr int SM_GAM2 = 1344 + 6 * 128;  // gamma of a handed-over chunk (split mode)
 constexpr int SMALL_FLOATS = SM_GAM2 + 128;
 constexpr int OFF_BAR = OFF_SMALL + SMALL_FLOATS * 4;
-constexpr int SMEM_USED = OFF_BAR + 64;
+constexpr int SMEM_USED = OFF_BAR + 80;  // 10 mbarrier / flag words
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
 
 // Split-mode hand-off slot (bytes, all 16-byte multiples): the prepared
@@ -257,9 +258,16 @@ __device__ __forceinline__ void tri_inverse(uint8_t* sm, const float* s_beta, in
   }
 }
 
+// CG: the GDN-2 operator (channel-wise erase gate on the key channels, write
+// gate on the value channels, in place of beta): the erase gate scales the
+// k rows of the Abar row operand and the Kh*Gamma operand of W, the write
+// gate scales V before U = T (w * V), and T' = T. tme / tmw map the raw erase
+// and write gates [S,H,D] (unused for KDA).
+template <bool CG>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
+                      const __grid_constant__ CUtensorMap tme, const __grid_constant__ CUtensorMap tmw,
                       const TcFwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -282,6 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_odd = bar_qkg + 5;  // completion of Abar | M round 1
   uint64_t* bar_r2 = bar_qkg + 6;   // completion of Abar | M round 2
   uint64_t* bar_x = bar_qkg + 7;    // split mode: a handed-over odd chunk has landed
+  uint64_t* bar_e = bar_qkg + 8;    // GDN-2: the erase-gate tile has landed
+  uint64_t* bar_w = bar_qkg + 9;    // GDN-2: the write-gate tile has landed
   float* s_gam2 = smf + SM_GAM2;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -311,6 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_odd, 1);
     mbar_init(bar_r2, 1);
     mbar_init(bar_x, 1);
+    mbar_init(bar_e, 1);
+    mbar_init(bar_w, 1);
     *s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -346,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           make_uint4(pack_h2(Hst[8 * cc], Hst[8 * cc + 1]), pack_h2(Hst[8 * cc + 2], Hst[8 * cc + 3]),
                      pack_h2(Hst[8 * cc + 4], Hst[8 * cc + 5]), pack_h2(Hst[8 * cc + 6], Hst[8 * cc + 7]));
   }
-  uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0, ph_odd = 0, ph_r2 = 0, ph_x = 0;
+  uint32_t ph_qkg = 0, ph_v = 0, ph_mma = 0, ph_odd = 0, ph_r2 = 0, ph_x = 0, ph_e = 0, ph_w = 0;
   bool x_pending = false;  // a hand-over load into shared memory is in flight
 
   auto issue_qkg = [&](int hd, int t) {
@@ -443,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (!handed) {
     // raw beta: loaded now, stored once the norms are done (its latency hidden)
-    const unsigned short braw = (tid < rows) ? beta_bits(a.b, (t0 + tid) * a.H + h) : 0;
+    const unsigned short braw = (!CG && tid < rows) ? beta_bits(a.b, (t0 + tid) * a.H + h) : 0;
     KDA_WAIT(bar_qkg, ph_qkg);
     // ---- row norms: warp w handles rows 8w .. 8w+7, four at a time (sums
     // interleaved; lanes 0-3 finish the q rows, lanes 8-11 the k rows) ----
@@ -483,7 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_iq[r] = (ok && nrm > 0.f) ? a.scale / nrm : 0.f;
       }
     }
-    if (tid < kC) s_beta[tid] = tid < rows ? sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
+    if (tid < kC)  // GDN-2: beta = 1 on every valid row (the gates act per channel)
+      s_beta[tid] = tid < rows ? (CG ? 1.f : sigmoidf_(__bfloat162float(__ushort_as_bfloat16(braw)))) : 0.f;
     if (pub_pending) {  // the previous job's stores still read the region the offsets go to
       if (tid == 0) bulk_wait_read();
       __syncthreads();
@@ -509,6 +522,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_tot[Ib * 128 + c0 + 1] = acc1;
     }
     __syncthreads();
+    if (CG && tid == 0) {  // the raw gate is consumed: the erase gate takes its tile
+      mbar_expect_tx(bar_e, 2 * 8192);
+      tma_load_3d(sm + OFF_STG_G, &tme, 0, h, static_cast<int>(t0), bar_e);
+      tma_load_3d(sm + OFF_STG_G + 8192, &tme, 64, h, static_cast<int>(t0), bar_e);
+    }
     // ---- per-channel block references ----
     if (tid < kD) {
       const int ch = tid;
@@ -528,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     // ---- operand tiles, row-major: thread = one row (k or q) x 64 channels ----
+    if (CG) KDA_WAIT(bar_e, ph_e);  // GDN-2: the erase gate (in the raw gate's tile)
     float rowf[64];  // kh e^{G_r - B_{I+1}} (k rows) or qh e^{G_r - B_{I+1}} (q rows)
     {
       // k rows build Kh*Gamma and Kbar, q rows build Qh*Gamma and the tf32 column
@@ -544,6 +563,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4 rawk = raw;
         if (!krole) rawk = *reinterpret_cast<const uint4*>(sm + OFF_STG_K + sw128_chunk(r, 8 * hh + cc, 64));
         const uint32_t rk[4] = {rawk.x, rawk.y, rawk.z, rawk.w};
+        uint32_t re[4] = {0u, 0u, 0u, 0u};  // GDN-2, k rows: the raw erase gate of these channels
+        if (CG && krole) {
+          const uint4 rawe = *reinterpret_cast<const uint4*>(sm + OFF_STG_G + sw128_chunk(r, 8 * hh + cc, 64));
+          re[0] = rawe.x; re[1] = rawe.y; re[2] = rawe.z; re[3] = rawe.w;
+        }
         const float4 x0 = *reinterpret_cast<const float4*>(sm + OFF_XS + xs_off(r, ch0));
         const float4 x1 = *reinterpret_cast<const float4*>(sm + OFF_XS + xs_off(r, ch0 + 4));
         const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -553,7 +577,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const float2 vv = unpack_bf16(rw[e]);
           const int ca = ch0 + 2 * e, cb = ca + 1;
-          const float ha = vv.x * nrm, hb = vv.y * nrm;
+          float ha = vv.x * nrm, hb = vv.y * nrm;
+          float kba = ha, kbb = hb;  // Kbar's k (never gated)
+          if (CG && krole) {  // erase gate b = sigmoid(raw) on the row side of Abar and in W's operand
+            const float2 ee = unpack_bf16(re[e]);
+            ha *= sigmoid_fast(ee.x);
+            hb *= sigmoid_fast(ee.y);
+          }
           const float sa = ex2(xv[2 * e]), sbv = ex2(xv[2 * e + 1]);  // e^{G_r - B_{I+1}} >= 1
           const float ia = ex2(-xv[2 * e]), ib = ex2(-xv[2 * e + 1]);  // e^{B_{I+1} - G_r} <= 1
           rowf[8 * cc + 2 * e] = ha * sa;
@@ -561,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float ga = sa * s_eB[pI * 128 + ca], gb = sbv * s_eB[pI * 128 + cb];  // Gamma_r
           o1[e] = pack_h2(ha * ga, hb * gb);  // Kh*Gamma (k rows) or Qh*Gamma (q rows)
           if (krole) {
-            o2[e] = pack_h2(ha * ia * s_eK[pI * 128 + ca], hb * ib * s_eK[pI * 128 + cb]);  // Kbar
+            o2[e] = pack_h2(kba * ia * s_eK[pI * 128 + ca], kbb * ib * s_eK[pI * 128 + cb]);  // Kbar
           } else {
             const float2 kk = unpack_bf16(rk[e]);
             bk[2 * e] = kk.x * nrmk * ia;  // kh_r e^{B_{I+1} - G_r}
@@ -672,6 +702,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_before_sync();
     __syncthreads();
     tri_inverse(sm, s_beta, tid);
+    if (CG) {  // T is consumed: the write gate takes its space
+      __syncthreads();
+      if (tid == 0) {
+        mbar_expect_tx(bar_w, 2 * 8192);
+        tma_load_3d(sm + OFF_WG, &tmw, 0, h, static_cast<int>(t0), bar_w);
+        tma_load_3d(sm + OFF_WG + 8192, &tmw, 64, h, static_cast<int>(t0), bar_w);
+      }
+    }
     // ---- low part of M (its fp32 values are still in TMEM) ----
     {
       float v[32];
@@ -695,12 +733,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- v (bf16, TMA) -> fp16 in place ----
     KDA_WAIT(bar_v, ph_v);
+    if (CG) KDA_WAIT(bar_w, ph_w);
     {
       uint4* vt = reinterpret_cast<uint4*>(sm + OFF_V);
+      const uint4* wt = reinterpret_cast<const uint4*>(sm + OFF_WG);  // same layout as v
 #pragma unroll
       for (int x = tid; x < 16384 / 16; x += kThreads) {
         uint4 w = vt[x];
-        const float2 a0 = unpack_bf16(w.x), a1 = unpack_bf16(w.y), a2 = unpack_bf16(w.z), a3 = unpack_bf16(w.w);
+        float2 a0 = unpack_bf16(w.x), a1 = unpack_bf16(w.y), a2 = unpack_bf16(w.z), a3 = unpack_bf16(w.w);
+        if (CG) {  // GDN-2: U = T (w * v), write gate w = sigmoid(raw)
+          const uint4 ww = wt[x];
+          const float2 w0 = unpack_bf16(ww.x), w1 = unpack_bf16(ww.y), w2 = unpack_bf16(ww.z), w3 = unpack_bf16(ww.w);
+          a0.x *= sigmoid_fast(w0.x); a0.y *= sigmoid_fast(w0.y);
+          a1.x *= sigmoid_fast(w1.x); a1.y *= sigmoid_fast(w1.y);
+          a2.x *= sigmoid_fast(w2.x); a2.y *= sigmoid_fast(w2.y);
+          a3.x *= sigmoid_fast(w3.x); a3.y *= sigmoid_fast(w3.y);
+        }
         vt[x] = make_uint4(pack_h2(a0.x, a0.y), pack_h2(a1.x, a1.y), pack_h2(a2.x, a2.y), pack_h2(a3.x, a3.y));
       }
     }
@@ -922,12 +970,23 @@ size_t fwd_handoff_bytes(int items) {
 
 kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s) {
   if (p->head_dim != kD || p->dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
-  CUtensorMap mq, mk, mv, mg;
+  const bool cg = a.w != nullptr;  // GDN-2: b is the raw erase gate [S,H,D], w the raw write gate
+  CUtensorMap mq, mk, mv, mg, me, mw;
   if (!make_tma_map_bf16(&mq, a.q, p->total_tokens, p->num_heads) ||
       !make_tma_map_bf16(&mk, a.k, p->total_tokens, p->num_heads) ||
       !make_tma_map_bf16(&mv, a.v, p->total_tokens, p->num_heads) ||
       !make_tma_map_bf16(&mg, a.g, p->total_tokens, p->num_heads))
     return KDA_ERR_CUDA;
+  if (cg) {
+    if (!make_tma_map_bf16(&me, a.b, p->total_tokens, p->num_heads) ||
+        !make_tma_map_bf16(&mw, a.w, p->total_tokens, p->num_heads))
+      return KDA_ERR_CUDA;
+  } else {
+    me = mq;  // unused
+    mw = mq;
+  }
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+               const CUtensorMap, const TcFwdArgs) = cg ? kda_fwd_tc_kernel<true> : kda_fwd_tc_kernel<false>;
   TcFwdArgs t;
   t.b = static_cast<const __nv_bfloat16*>(a.b);
   t.A_log = a.A_log;
@@ -949,7 +1008,7 @@ kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s)
   t.xflags = a.xflags;
   t.xbuf = a.xbuf;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  if (cudaFuncSetAttribute(kda_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
     return KDA_ERR_CUDA;
   const int items = p->num_seqs * p->num_heads;
   // Split mode: with at least half as many spare SMs as items, helper CTAs
@@ -959,15 +1018,15 @@ kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s)
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_fwd_tc_kernel, kThreads, SMEM_BYTES);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, SMEM_BYTES);
   bool launched = false;
   if (a.xflags != nullptr && !a.test_timeout && items > 0 && items < sms * per_sm) {
     const int spare = sms * per_sm - items;
     if (2 * spare >= items) {
       t.helpers = spare < items ? spare : items;
       if (cudaMemsetAsync(a.xflags, 0, sizeof(uint32_t) * 5 * items, s) != cudaSuccess) return KDA_ERR_CUDA;
-      void* kargs[] = {&mq, &mk, &mv, &mg, &t};
-      launched = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kda_fwd_tc_kernel),
+      void* kargs[] = {&mq, &mk, &mv, &mg, &me, &mw, &t};
+      launched = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern),
                                              dim3(items + t.helpers), dim3(kThreads), kargs, SMEM_BYTES,
                                              s) == cudaSuccess;
       if (!launched) {
@@ -976,7 +1035,7 @@ kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s)
       }
     }
   }
-  if (!launched && items > 0) kda_fwd_tc_kernel<<<items, kThreads, SMEM_BYTES, s>>>(mq, mk, mv, mg, t);
+  if (!launched && items > 0) kern<<<items, kThreads, SMEM_BYTES, s>>>(mq, mk, mv, mg, me, mw, t);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

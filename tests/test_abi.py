@@ -110,11 +110,16 @@ def test_gdn2_entry_points_and_flag_on_host(lib):
     cu = torch.tensor([0, 16], dtype=torch.int32)  # host tensor: never dereferenced
     nul = ctypes.c_void_p(0)
     al = ctypes.c_void_p(0x1000)
-    # GDN-2 problems size ctx / workspace for the CUDA-core kernels
+    # bf16 D = 128 GDN-2 problems: tensor-core forward (ctx sized like KDA's,
+    # with the helper hand-off area), CUDA-core backward (workspace sized
+    # like the forced CUDA-core KDA backward's)
     g = K.make_problem(131072, 1, 96, 128, torch.bfloat16, flags=K.KDA_FLAG_CHANNEL_GATES)
+    kda_tc = K.make_problem(131072, 1, 96, 128, torch.bfloat16)
     simt = K.make_problem(131072, 1, 96, 128, torch.bfloat16, flags=K.KDA_FLAG_FORCE_SIMT)
-    assert K.kernel_family(g) == 0
-    assert K.ctx_bytes(g) == K.ctx_bytes(simt) and K.workspace_bytes(g) == K.workspace_bytes(simt)
+    assert K.kernel_family(g) == 2
+    assert K.ctx_bytes(g) == K.ctx_bytes(kda_tc) and K.workspace_bytes(g) == K.workspace_bytes(simt)
+    g64 = K.make_problem(131072, 1, 96, 64, torch.bfloat16, flags=K.KDA_FLAG_CHANNEL_GATES)
+    assert K.kernel_family(g64) == 0
     p = K.make_problem(16, 1, 2, 64, torch.bfloat16, cu, flags=K.KDA_FLAG_CHANNEL_GATES)
     # the KDA entry points refuse a GDN-2 problem ...
     assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, al, nul) == 1
