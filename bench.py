@@ -491,7 +491,7 @@ def run_gb300(args, w, rank, world, local):
     peak_gbs, peak_kind = measured_peaks()
     prefix = "kda_gdn2" if gdn2 else "kda"
     dominant = f"{prefix}_bwd" if bwd_ms >= fwd_ms else f"{prefix}_fwd"
-    dom_ms, dom_b = (bwd_ms, bwd_b) if dominant == "kda_bwd" else (fwd_ms, fwd_b)
+    dom_ms, dom_b = (bwd_ms, bwd_b) if dominant == f"{prefix}_bwd" else (fwd_ms, fwd_b)
     achieved = dom_b / (dom_ms / 1e3) / 1e9
     step_gbs = (fwd_b + bwd_b) / (ms_step / 1e3) / 1e9
     kname = {0: "simt", 1: "tc"}.get(family, "unknown")
