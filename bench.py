@@ -305,7 +305,7 @@ def run_gb300_fwd(args, w, rank, world, local):
     fwd_fn = K.gdn2_fwd if gdn2 else functools.partial(K.kda_fwd, flags=simt)
     prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale,
                           flags=K.KDA_FLAG_NO_CHECKPOINTS | simt | (K.KDA_FLAG_CHANNEL_GATES if gdn2 else 0))
-    kname = {0: "simt", 1: "tc"}.get(K.kernel_family(prob), "unknown")
+    kname = {0: "simt", 1: "tc", 2: "tc fwd, simt bwd"}.get(K.kernel_family(prob), "unknown")
     scratch = torch.empty(K.ctx_bytes(prob), dtype=torch.uint8, device=dev)
     o = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
@@ -494,7 +494,7 @@ def run_gb300(args, w, rank, world, local):
     dom_ms, dom_b = (bwd_ms, bwd_b) if dominant == f"{prefix}_bwd" else (fwd_ms, fwd_b)
     achieved = dom_b / (dom_ms / 1e3) / 1e9
     step_gbs = (fwd_b + bwd_b) / (ms_step / 1e3) / 1e9
-    kname = {0: "simt", 1: "tc"}.get(family, "unknown")
+    kname = {0: "simt", 1: "tc", 2: "tc fwd, simt bwd"}.get(family, "unknown")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
                 "frac": achieved / peak_gbs, "traffic": ncu_traffic(f"{dominant}_{kname}", w.name),
                 "kernel": f"{dominant} ({kname} kernels)", "peak_kind": f"{peak_kind} hbm_gbs",
