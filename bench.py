@@ -301,8 +301,8 @@ def run_gb300_fwd(args, w, rank, world, local):
     gdn2 = w.gates == "channel"
     args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
     q, cu = inp["q"], inp["cu_seqlens"]
-    simt = K.KDA_FLAG_FORCE_SIMT if (args.force_simt and not gdn2) else 0
-    fwd_fn = K.gdn2_fwd if gdn2 else functools.partial(K.kda_fwd, flags=simt)
+    simt = K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0
+    fwd_fn = functools.partial(K.gdn2_fwd if gdn2 else K.kda_fwd, flags=simt)
     prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale,
                           flags=K.KDA_FLAG_NO_CHECKPOINTS | simt | (K.KDA_FLAG_CHANNEL_GATES if gdn2 else 0))
     kname = {0: "simt", 1: "tc", 2: "tc fwd, simt bwd"}.get(K.kernel_family(prob), "unknown")
@@ -388,12 +388,10 @@ def peak_only(args, w, local):
     inp = make_inputs(w, device=dev)
     gates = gate_names(w)
     args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
-    if w.gates == "channel":
-        fwd_fn, bwd_fn = K.gdn2_fwd, K.gdn2_bwd
-    else:
-        flags = K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0
-        fwd_fn = functools.partial(K.kda_fwd, flags=flags)
-        bwd_fn = functools.partial(K.kda_bwd, flags=flags)
+    flags = K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0
+    gdn2 = w.gates == "channel"
+    fwd_fn = functools.partial(K.gdn2_fwd if gdn2 else K.kda_fwd, flags=flags)
+    bwd_fn = functools.partial(K.gdn2_bwd if gdn2 else K.kda_bwd, flags=flags)
     torch.cuda.synchronize()
     torch.cuda.reset_peak_memory_stats(dev)
     o, ctx = fwd_fn(*args_in, scale=w.scale)
@@ -433,10 +431,13 @@ def run_gb300(args, w, rank, world, local):
     gdn2 = w.gates == "channel"
     args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
     q, cu, dO = inp["q"], inp["cu_seqlens"], inp["dO"]
-    if gdn2:  # GDN-2 always runs the CUDA-core kernels
-        fwd_fn, bwd_fn, flags = K.gdn2_fwd, K.gdn2_bwd, K.KDA_FLAG_CHANNEL_GATES
+    simt = K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0
+    if gdn2:
+        fwd_fn = functools.partial(K.gdn2_fwd, flags=simt)
+        bwd_fn = functools.partial(K.gdn2_bwd, flags=simt)
+        flags = simt | K.KDA_FLAG_CHANNEL_GATES
     else:
-        flags = K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0
+        flags = simt
         fwd_fn = functools.partial(K.kda_fwd, flags=flags)
         bwd_fn = functools.partial(K.kda_bwd, flags=flags)
     prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale, flags=flags)

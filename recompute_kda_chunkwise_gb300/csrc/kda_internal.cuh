@@ -40,8 +40,8 @@ struct FwdArgs {
   // ctx (NULL: no helper CTAs)
   uint32_t* xflags;
   uint8_t* xbuf;
-  // GDN-2 (KDA_FLAG_CHANNEL_GATES, CUDA-core kernels only): raw write gate
-  // [S,H,D]; b is then the raw erase gate [S,H,D]
+  // GDN-2 (KDA_FLAG_CHANNEL_GATES): raw write gate [S,H,D]; b is then the
+  // raw erase gate [S,H,D]
   const void* w = nullptr;
 };
 
@@ -73,7 +73,7 @@ struct BwdArgs {
   int64_t S;  // total tokens (cu[N])
   int N, H;
   float scale, lower, eps;
-  // GDN-2 (KDA_FLAG_CHANNEL_GATES, CUDA-core kernels only): raw write gate
+  // GDN-2 (KDA_FLAG_CHANNEL_GATES, CUDA-core backward only): raw write gate
   // and its gradient [S,H,D]; b / db are then the raw erase gate and its
   // gradient [S,H,D]
   const void* w = nullptr;

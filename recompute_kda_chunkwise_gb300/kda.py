@@ -255,14 +255,14 @@ def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO, ctx, *, sc
 
 def gdn2_fwd(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
              lower_bound: float = -5.0, eps: float = 1e-6, save_ctx: bool = True, out=None,
-             ctx=None, h0=None, final_state=False):
+             ctx=None, h0=None, final_state=False, flags: int = 0):
     """GDN-2 forward (kda_gdn2_fwd): KDA with the scalar beta replaced by the
     channel-wise erase gate sigmoid(erase) on key channels and write gate
     sigmoid(write) on value channels; erase and write are [S, H, D] in q's
     dtype. Returns (o, ctx) or (o, ctx, hT) as kda_fwd does."""
     _check_tensors(q, k, v, g, erase, write, params=(A_log, dt_bias))
     _check_state(h0, q, cu_seqlens, "h0")
-    flags = KDA_FLAG_CHANNEL_GATES | (0 if save_ctx else KDA_FLAG_NO_CHECKPOINTS)
+    flags |= KDA_FLAG_CHANNEL_GATES | (0 if save_ctx else KDA_FLAG_NO_CHECKPOINTS)
     p = _problem_from(q, None, cu_seqlens, scale, lower_bound, eps, flags)
     hT = None
     if final_state is not False and final_state is not None:
@@ -284,12 +284,13 @@ def gdn2_fwd(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, *, scale: flo
 
 def gdn2_bwd(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, dO, ctx, *, scale: float = 1.0,
              lower_bound: float = -5.0, eps: float = 1e-6, workspace=None, outs=None, dht=None,
-             want_dh0: bool = False):
+             want_dh0: bool = False, flags: int = 0):
     """GDN-2 backward (kda_gdn2_bwd). Returns dict dq, dk, dv, dg, derase,
-    dwrite, dA_log, ddt_bias, and dh0 when want_dh0."""
+    dwrite, dA_log, ddt_bias, and dh0 when want_dh0. ``flags`` must match
+    the forward's (KDA_FLAG_FORCE_SIMT)."""
     _check_tensors(q, k, v, g, erase, write, dO, params=(A_log, dt_bias))
     _check_state(dht, q, cu_seqlens, "dht")
-    p = _problem_from(q, None, cu_seqlens, scale, lower_bound, eps, KDA_FLAG_CHANNEL_GATES)
+    p = _problem_from(q, None, cu_seqlens, scale, lower_bound, eps, flags | KDA_FLAG_CHANNEL_GATES)
     if outs is None:
         outs = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                     dg=torch.empty_like(g), derase=torch.empty_like(erase),

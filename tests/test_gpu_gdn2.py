@@ -3,7 +3,10 @@ kda_gdn2_fwd / kda_gdn2_bwd through the C ABI) against the fp64 oracle's
 GDN-2 mode, element by element, with the same tolerances as KDA:
 max|x - ref| (beyond the output's own rounding) <= 2e-2 * RMS(ref) for bf16
 inputs and <= 1e-4 * RMS(ref) for fp32 inputs, for o, every gradient
-(dq, dk, dv, dg, derase, dwrite, dA_log, ddt_bias) and the states."""
+(dq, dk, dv, dg, derase, dwrite, dA_log, ddt_bias) and the states. bf16
+problems with D = 128 run the tensor-core forward (with and without helper
+CTAs) and the fp32 CUDA-core backward; the rest, and the forced cases, the
+CUDA-core kernels in both directions."""
 import pytest
 import torch
 
@@ -19,13 +22,13 @@ NAMES = ["o", "dq", "dk", "dv", "dg", "derase", "dwrite", "dA_log", "ddt_bias"]
 ARGS = ["q", "k", "v", "g", "erase", "write", "A_log", "dt_bias", "cu_seqlens"]
 
 
-def run_gpu(inp, scale, states=None):
+def run_gpu(inp, scale, states=None, flags=0):
     h0 = dht = None
     if states is not None:
         h0, dht = states["h0"], states["dht"]
     args = [inp[n] for n in ARGS]
-    r = K.gdn2_fwd(*args, scale=scale, h0=h0, final_state=states is not None)
-    out = K.gdn2_bwd(*args, inp["dO"], r[1], scale=scale, dht=dht, want_dh0=states is not None)
+    r = K.gdn2_fwd(*args, scale=scale, h0=h0, final_state=states is not None, flags=flags)
+    out = K.gdn2_bwd(*args, inp["dO"], r[1], scale=scale, dht=dht, want_dh0=states is not None, flags=flags)
     torch.cuda.synchronize()
     out["o"] = r[0]
     if states is not None:
@@ -47,10 +50,10 @@ def run_oracle(inp, scale, heads=None, states=None):
     return oracle.gdn2_reference(*[cpu[n] for n in ARGS], cpu["dO"], scale=scale, **kw)
 
 
-def check(w: Workload, heads=None, states=False):
+def check(w: Workload, heads=None, states=False, flags=0):
     inp = to_dev(make_inputs(w, device="cpu"))
     st = to_dev(make_states(w)) if states else None
-    gpu = run_gpu(inp, w.scale, st)
+    gpu = run_gpu(inp, w.scale, st, flags)
     ref = run_oracle(inp, w.scale, heads, st)
     names = NAMES + (["hT", "dh0"] if states else [])
     return compare(gpu, ref, TOL[_DT[w.dtype]], heads=heads, names=names)
@@ -61,22 +64,46 @@ def test_pages_preset_all_heads():
     check(WORKLOADS["gdn2_b10_t512_h12_d64_f32"])
 
 
-def test_mbs8_8k_h16_d128_bf16_sampled_heads():
-    # 8 x 8192 tokens, 16 heads, bf16 D = 128: the whole launch runs, the
-    # oracle checks three heads end to end (heads are independent)
-    check(WORKLOADS["gdn2_mbs8_8k_h16_d128_bf16"], heads=[0, 7, 15])
+def test_kernel_family_dispatch():
+    # 2: tensor-core forward, CUDA-core backward
+    g = K.KDA_FLAG_CHANNEL_GATES
+    assert K.kernel_family(K.make_problem(64, 1, 2, 128, torch.bfloat16, flags=g)) == 2
+    assert K.kernel_family(K.make_problem(64, 1, 2, 128, torch.bfloat16, flags=g | K.KDA_FLAG_FORCE_SIMT)) == 0
+    assert K.kernel_family(K.make_problem(64, 1, 2, 64, torch.bfloat16, flags=g)) == 0
+    assert K.kernel_family(K.make_problem(64, 1, 2, 128, torch.float32, flags=g)) == 0
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("D", [64, 128])
-def test_ragged_lengths_states_and_parameters(dtype, D):
+def test_mbs8_8k_h16_d128_bf16_all_heads():
+    # 8 x 8192 tokens, 16 heads, bf16 D = 128: 128 sequence-heads, too many
+    # for the forward's helper CTAs; every head against the oracle
+    check(WORKLOADS["gdn2_mbs8_8k_h16_d128_bf16"])
+
+
+@pytest.mark.parametrize("dtype,D,flags", [("bf16", 64, 0), ("f32", 64, 0), ("f32", 128, 0), ("bf16", 128, 0),
+                                           ("bf16", 128, K.KDA_FLAG_FORCE_SIMT)])
+def test_ragged_lengths_states_and_parameters(dtype, D, flags):
     # partial chunks, an empty sequence, single tokens, checkpoint-segment
     # crossings, nonzero A_log / dt_bias, scale 1/sqrt(D), initial states and
-    # final-state gradients
+    # final-state gradients (bf16 D = 128: 24 sequence-heads, so the
+    # tensor-core forward runs with helper CTAs; forced: the CUDA-core forward)
     lengths = (1, 15, 0, 17, 100, 1029, 2049, 3)
     w = Workload(f"gdn2_ragged_d{D}_{dtype}", lengths, 3, D, dtype, seed=7400 + D, param_std=0.5,
                  scale=D ** -0.5, gates="channel")
-    check(w, states=True)
+    check(w, states=True, flags=flags)
+
+
+def test_tensor_core_forward_long_memory_and_saturated_gates():
+    # bf16 D = 128 (tensor-core forward): a long-memory decay gate
+    # (N(-6, 1)) over sequences that cross checkpoint segments, and a second
+    # problem whose raw gates sit far in both tails (erase / write near 0 and 1)
+    w = Workload("gdn2_tc_long", (2100, 700, 5), 4, 128, "bf16", seed=7450, gate_mean=-6.0,
+                 param_std=0.3, gates="channel")
+    check(w)
+    inp = to_dev(make_inputs(w, device="cpu"))
+    inp["erase"] = inp["erase"] * 6.0
+    inp["write"] = inp["write"] * 6.0
+    gpu = run_gpu(inp, w.scale)
+    compare(gpu, run_oracle(inp, w.scale), TOL[torch.bfloat16], names=NAMES)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
