@@ -177,8 +177,9 @@ def barrier():
 
 def copy_rates(stream, h2d_pairs, d2h_pairs, reps: int = 3):
     """Pinned-memory copy rates of the e2e step's own tensors on this machine:
-    host->device alone, device->host alone (best of ``reps``, CUDA events),
-    in GB/s."""
+    host->device alone, device->host alone, and both at once on two streams
+    (best of ``reps``, CUDA events), in GB/s. A pipelined e2e step cannot beat
+    max(device step, both_directions_ms)."""
     import torch
 
     def timed(pairs):
@@ -195,9 +196,35 @@ def copy_rates(stream, h2d_pairs, d2h_pairs, reps: int = 3):
             best = ms if best is None else min(best, ms)
         return nbytes / (best / 1e3) / 1e9, best
 
+    def both():  # uploads and downloads at once, on two streams
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        best = None
+        nbytes = sum(d.numel() * d.element_size() for d, _ in h2d_pairs + d2h_pairs)
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            bu, bd = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            up.wait_event(a)
+            down.wait_event(a)
+            with torch.cuda.stream(up):
+                for dst, src in h2d_pairs:
+                    dst.copy_(src, non_blocking=True)
+                bu.record(up)
+            with torch.cuda.stream(down):
+                for dst, src in d2h_pairs:
+                    dst.copy_(src, non_blocking=True)
+                bd.record(down)
+            bu.synchronize()
+            bd.synchronize()
+            ms = max(a.elapsed_time(bu), a.elapsed_time(bd))
+            best = ms if best is None else min(best, ms)
+        return nbytes / (best / 1e3) / 1e9, best
+
     h2d_gbs, h2d_ms = timed(h2d_pairs)
     d2h_gbs, d2h_ms = timed(d2h_pairs)
-    return {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "h2d_ms": h2d_ms, "d2h_ms": d2h_ms}
+    both_gbs, both_ms = both()
+    return {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "h2d_ms": h2d_ms, "d2h_ms": d2h_ms,
+            "both_directions_gbs": both_gbs, "both_directions_ms": both_ms}
 
 
 def oracle_sample(w, inp_cpu_slices, cores, want=False):
@@ -370,8 +397,76 @@ def run_gb300_fwd(args, w, rank, world, local):
                              "frac": achieved / peak_gbs, "traffic": None, "kernel": f"{'kda_gdn2_fwd' if gdn2 else 'kda_fwd'} ({kname} kernels)",
                              "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": fwd_b,
                              "ms_per_launch": ms_step},
-                "cpu_baseline": None, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk.summary(),
+                "cpu_baseline": None, "e2e": e2e, "gpu_launches": 2 * args.steps,  # check + forward
+                "clocks": clk.summary(),
                 "device_status_ok": K.query_device_status(scratch) == 0}
+        print(json.dumps(line), flush=True)
+
+
+def run_gb300_pieces(args, w, rank, world, local):
+    """The one-GPU split of recompute_kda_chunkwise_gb300.cp: every sequence cut
+    into ``--pieces`` pieces that run as packed sequences, joined by the affine
+    state prefix (three forward launches, two backward launches and two prefix
+    launches per step). Same workload, metric and timing as the default line;
+    the line adds the largest difference from the unsplit path's outputs."""
+    import torch
+    from recompute_kda_chunkwise_gb300 import make_inputs, cp
+    from recompute_kda_chunkwise_gb300 import kda as K
+    if w.gates == "channel":
+        raise SystemExit("--pieces covers KDA workloads")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    K.load_library()
+    inp = make_inputs(w, device=dev)
+    a = [inp[n] for n in ["q", "k", "v", "g", "beta", "A_log", "dt_bias"]]
+    stream = torch.cuda.current_stream(dev)
+    P = args.pieces
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        o, _, pctx = cp.kda_fwd_pieces(*a, w.lengths, P, scale=w.scale)
+        if ev is not None:
+            ev[1].record(stream)
+        r = cp.kda_bwd_pieces(*a, inp["dO"], pctx, scale=w.scale)
+        if ev is not None:
+            ev[2].record(stream)
+        return o, r
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            o, r = step(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms_step = max_over_ranks(start.elapsed_time(end)) / args.steps
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    # the unsplit path on the same inputs
+    o1, ctx1 = K.kda_fwd(*a, inp["cu_seqlens"], scale=w.scale)
+    r1 = K.kda_bwd(*a, inp["cu_seqlens"], inp["dO"], ctx1, scale=w.scale)
+    torch.cuda.synchronize()
+    diff = {}
+    for n, x, y in [("o", o, o1)] + [(n, r[n], r1[n]) for n in ["dq", "dk", "dv", "dg", "dbeta"]]:
+        y = y.float()
+        diff[n] = float((x.float() - y).abs().max() / y.pow(2).mean().sqrt())
+    if rank == 0:
+        line = {"metric": METRIC, "value": w.total_tokens * world / (ms_step / 1e3), "unit": "tokens/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": w.name, "num_seqs": w.num_seqs, "seq_len": w.lengths[0], "heads": w.H,
+                           "head_dim": w.D, "pieces": P, "parallelism": f"replicas{world}"},
+                "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                "max_diff_vs_unsplit_over_rms": diff, "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
 
 
@@ -496,12 +591,16 @@ def run_gb300(args, w, rank, world, local):
     achieved = dom_b / (dom_ms / 1e3) / 1e9
     step_gbs = (fwd_b + bwd_b) / (ms_step / 1e3) / 1e9
     kname = {0: "simt", 1: "tc", 2: "tc fwd, simt bwd"}.get(family, "unknown")
+    # the family that runs the dominant pass (family 2: tensor-core forward, CUDA-core backward)
+    dom_family = "tc" if family == 1 or (family == 2 and dominant.endswith("_fwd")) else "simt"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
-                "frac": achieved / peak_gbs, "traffic": ncu_traffic(f"{dominant}_{kname}", w.name),
+                "frac": achieved / peak_gbs, "traffic": ncu_traffic(f"{dominant}_{dom_family}", w.name),
                 "kernel": f"{dominant} ({kname} kernels)", "peak_kind": f"{peak_kind} hbm_gbs",
                 "algorithmic_bytes_per_launch": dom_b, "ms_per_launch": dom_ms,
                 "step_frac": step_gbs / peak_gbs}
-    launches_per_step = 1 + 2  # forward kernel; backward kernel + gate-parameter reduction
+    # per step: the cu_seqlens check and the forward kernel; the check, the
+    # backward kernel and the gate-parameter reduction
+    launches_per_step = 2 + 3
 
     # end to end through the public API: pinned host inputs -> device -> fwd+bwd -> host outputs
     e2e = None
@@ -640,6 +739,8 @@ def main(argv=None):
     ap.add_argument("--pass", dest="pass_", choices=["fwdbwd", "fwd"], default="fwdbwd",
                     help="fwd: forward-only inference (no checkpoints); the default times fwd+bwd")
     ap.add_argument("--e2e-steps", type=int, default=24)
+    ap.add_argument("--pieces", type=int, default=1,
+                    help="time the one-GPU split of every sequence into this many pieces instead")
     ap.add_argument("--sample-tokens", type=int, default=98304,
                     help="tokens of the oracle sample behind cpu_baseline (about 10-30 s of host work)")
     ap.add_argument("--ref-sample-tokens", type=int, default=32768,
@@ -660,6 +761,8 @@ def main(argv=None):
         run_reference(args, w, rank)
     elif args.pass_ == "fwd":
         run_gb300_fwd(args, w, rank, world, local)
+    elif args.pieces > 1:
+        run_gb300_pieces(args, w, rank, world, local)
     else:
         run_gb300(args, w, rank, world, local)
     import torch.distributed as dist
