@@ -412,23 +412,24 @@ def run_gb300_pieces(args, w, rank, world, local):
     import torch
     from recompute_kda_chunkwise_gb300 import make_inputs, cp
     from recompute_kda_chunkwise_gb300 import kda as K
-    if w.gates == "channel":
-        raise SystemExit("--pieces covers KDA workloads")
+    gdn2 = w.gates == "channel"
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     K.load_library()
     inp = make_inputs(w, device=dev)
-    a = [inp[n] for n in ["q", "k", "v", "g", "beta", "A_log", "dt_bias"]]
+    a = [inp[n] for n in ["q", "k", "v", "g"] + gate_names(w) + ["A_log", "dt_bias"]]
+    fwd_p, bwd_p = (cp.gdn2_fwd_pieces, cp.gdn2_bwd_pieces) if gdn2 else (cp.kda_fwd_pieces, cp.kda_bwd_pieces)
+    fwd1, bwd1 = (K.gdn2_fwd, K.gdn2_bwd) if gdn2 else (K.kda_fwd, K.kda_bwd)
     stream = torch.cuda.current_stream(dev)
     P = args.pieces
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        o, _, pctx = cp.kda_fwd_pieces(*a, w.lengths, P, scale=w.scale)
+        o, _, pctx = fwd_p(*a, w.lengths, P, scale=w.scale)
         if ev is not None:
             ev[1].record(stream)
-        r = cp.kda_bwd_pieces(*a, inp["dO"], pctx, scale=w.scale)
+        r = bwd_p(*a, inp["dO"], pctx, scale=w.scale)
         if ev is not None:
             ev[2].record(stream)
         return o, r
@@ -451,17 +452,19 @@ def run_gb300_pieces(args, w, rank, world, local):
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     # the unsplit path on the same inputs
-    o1, ctx1 = K.kda_fwd(*a, inp["cu_seqlens"], scale=w.scale)
-    r1 = K.kda_bwd(*a, inp["cu_seqlens"], inp["dO"], ctx1, scale=w.scale)
+    o1, ctx1 = fwd1(*a, inp["cu_seqlens"], scale=w.scale)
+    r1 = bwd1(*a, inp["cu_seqlens"], inp["dO"], ctx1, scale=w.scale)
     torch.cuda.synchronize()
     diff = {}
-    for n, x, y in [("o", o, o1)] + [(n, r[n], r1[n]) for n in ["dq", "dk", "dv", "dg", "dbeta"]]:
+    grad_names = ["dq", "dk", "dv", "dg"] + ["d" + n for n in gate_names(w)]
+    for n, x, y in [("o", o, o1)] + [(n, r[n], r1[n]) for n in grad_names]:
         y = y.float()
         diff[n] = float((x.float() - y).abs().max() / y.pow(2).mean().sqrt())
     if rank == 0:
-        line = {"metric": METRIC, "value": w.total_tokens * world / (ms_step / 1e3), "unit": "tokens/s",
-                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        line = {"metric": GDN2_METRIC if gdn2 else METRIC, "value": w.total_tokens * world / (ms_step / 1e3),
+                "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.dtype == "bf16" else "f32",
                 "data": "synthetic",
                 "config": {"workload": w.name, "num_seqs": w.num_seqs, "seq_len": w.lengths[0], "heads": w.H,
                            "head_dim": w.D, "pieces": P, "parallelism": f"replicas{world}"},

@@ -13,9 +13,12 @@ cuts token ranges, allocates buffers, calls the C ABI in order and, across
 ranks, gathers the maps.
 
 Two forms:
-* ``kda_fwd_pieces`` / ``kda_bwd_pieces``: one GPU, each sequence cut into P
-  pieces that run as P packed sequences of one launch (the split is checked
-  against the whole-sequence oracle in the tests).
+* ``kda_fwd_pieces`` / ``kda_bwd_pieces`` (and ``gdn2_fwd_pieces`` /
+  ``gdn2_bwd_pieces``): one GPU, each sequence cut into P pieces that run as
+  P packed sequences of one launch (the split is checked against the
+  whole-sequence oracle in the tests). GDN-2's recurrence is affine in its
+  state in the same way; with zero values its write term vanishes, so its
+  pieces' transitions come out of the same runs.
 * ``kda_fwd_cp`` / ``kda_bwd_cp``: one piece of every sequence per rank of a
   ``torch.distributed`` group (rank r holds piece r); the maps are
   all-gathered, which is the split's one exchange step. ``fwd`` / ``bwd`` /
@@ -67,8 +70,37 @@ class PiecesContext:
     pieces: int
     cu: torch.Tensor          # [N * P + 1] piece boundaries (device)
     A: torch.Tensor           # [N, P, H, D, D] piece transitions
-    ctx: torch.Tensor         # kda_fwd ctx of the pieces' forward
+    ctx: torch.Tensor         # ctx of the pieces' forward
     has_h0: bool
+
+
+def _fwd_pieces(fwd, q, k, v, g, gates, A_log, dt_bias, lengths, pieces, h0, kw):
+    N, P = len(lengths), int(pieces)
+    S, H, D = q.shape
+    cu = _cu(piece_lengths(lengths, P), q.device)
+    # 1. every piece's map: transition (identity start, zero values) and offset (zero start)
+    _, _, A = fwd(q, k, torch.zeros_like(v), g, *gates, A_log, dt_bias, cu, save_ctx=False,
+                  h0=_identity_states(N * P, H, D, q.device), final_state=True, **kw)
+    _, _, B = fwd(q, k, v, g, *gates, A_log, dt_bias, cu, save_ctx=False, final_state=True, **kw)
+    # 2. the prefix: each piece's true start state, and the sequences' final states
+    starts, hT = K.state_prefix(A.view(N, P, H, D, D), B.view(N, P, H, D, D), h0,
+                                direction=K.KDA_PREFIX_FORWARD, layout="seq_major")
+    # 3. the pieces from their true start states
+    o, ctx = fwd(q, k, v, g, *gates, A_log, dt_bias, cu, h0=starts.view(N * P, H, D, D), **kw)
+    return o, hT, PiecesContext(P, cu, A.view(N, P, H, D, D), ctx, h0 is not None)
+
+
+def _bwd_pieces(bwd, q, k, v, g, gates, A_log, dt_bias, dO, pctx, dht, kw):
+    N, P, H, D = pctx.A.shape[0], pctx.pieces, q.shape[1], q.shape[2]
+    # 1. every piece's own start-state gradient (zero end-state gradient)
+    C = bwd(q, k, v, g, *gates, A_log, dt_bias, pctx.cu, dO, pctx.ctx, want_dh0=True, **kw)["dh0"]
+    # 2. the prefix backwards: each piece's true end-state gradient, and dh0
+    ends, dh0 = K.state_prefix(pctx.A, C.view(N, P, H, D, D), dht, direction=K.KDA_PREFIX_BACKWARD,
+                               layout="seq_major")
+    # 3. the pieces' backward from their true end-state gradients
+    r = bwd(q, k, v, g, *gates, A_log, dt_bias, pctx.cu, dO, pctx.ctx, dht=ends.view(N * P, H, D, D), **kw)
+    r["dh0"] = dh0
+    return r
 
 
 def kda_fwd_pieces(q, k, v, g, beta, A_log, dt_bias, lengths, pieces: int, *, h0=None,
@@ -77,20 +109,8 @@ def kda_fwd_pieces(q, k, v, g, beta, A_log, dt_bias, lengths, pieces: int, *, h0
     into ``pieces`` pieces that run as independent sequences after the
     affine state prefix has given every piece its start state. Returns
     (o, hT, PiecesContext); hT [N, H, D, D] are the sequences' final states."""
-    N, P = len(lengths), int(pieces)
-    S, H, D = q.shape
-    cu = _cu(piece_lengths(lengths, P), q.device)
     kw = dict(scale=scale, lower_bound=lower_bound, eps=eps)
-    # 1. every piece's map: transition (identity start, zero values) and offset (zero start)
-    _, _, A = K.kda_fwd(q, k, torch.zeros_like(v), g, beta, A_log, dt_bias, cu, save_ctx=False,
-                        h0=_identity_states(N * P, H, D, q.device), final_state=True, **kw)
-    _, _, B = K.kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu, save_ctx=False, final_state=True, **kw)
-    # 2. the prefix: each piece's true start state, and the sequences' final states
-    starts, hT = K.state_prefix(A.view(N, P, H, D, D), B.view(N, P, H, D, D), h0,
-                                direction=K.KDA_PREFIX_FORWARD, layout="seq_major")
-    # 3. the pieces from their true start states
-    o, ctx = K.kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu, h0=starts.view(N * P, H, D, D), **kw)
-    return o, hT, PiecesContext(P, cu, A.view(N, P, H, D, D), ctx, h0 is not None)
+    return _fwd_pieces(K.kda_fwd, q, k, v, g, (beta,), A_log, dt_bias, lengths, pieces, h0, kw)
 
 
 def kda_bwd_pieces(q, k, v, g, beta, A_log, dt_bias, dO, pctx: PiecesContext, *, dht=None,
@@ -98,18 +118,24 @@ def kda_bwd_pieces(q, k, v, g, beta, A_log, dt_bias, dO, pctx: PiecesContext, *,
     """Backward matching ``kda_fwd_pieces``. Returns the dict of kda_bwd
     (dq, dk, dv, dg, dbeta, dA_log, ddt_bias) plus dh0 [N, H, D, D], the
     gradient of the sequences' initial states."""
-    N, P, H, D = pctx.A.shape[0], pctx.pieces, q.shape[1], q.shape[2]
     kw = dict(scale=scale, lower_bound=lower_bound, eps=eps)
-    # 1. every piece's own start-state gradient (zero end-state gradient)
-    C = K.kda_bwd(q, k, v, g, beta, A_log, dt_bias, pctx.cu, dO, pctx.ctx, want_dh0=True, **kw)["dh0"]
-    # 2. the prefix backwards: each piece's true end-state gradient, and dh0
-    ends, dh0 = K.state_prefix(pctx.A, C.view(N, P, H, D, D), dht, direction=K.KDA_PREFIX_BACKWARD,
-                               layout="seq_major")
-    # 3. the pieces' backward from their true end-state gradients
-    r = K.kda_bwd(q, k, v, g, beta, A_log, dt_bias, pctx.cu, dO, pctx.ctx,
-                  dht=ends.view(N * P, H, D, D), **kw)
-    r["dh0"] = dh0
-    return r
+    return _bwd_pieces(K.kda_bwd, q, k, v, g, (beta,), A_log, dt_bias, dO, pctx, dht, kw)
+
+
+def gdn2_fwd_pieces(q, k, v, g, erase, write, A_log, dt_bias, lengths, pieces: int, *, h0=None,
+                    scale: float = 1.0, lower_bound: float = -5.0, eps: float = 1e-6):
+    """``kda_fwd_pieces`` for GDN-2 (channel-wise erase and write gates, as in
+    kda.gdn2_fwd)."""
+    kw = dict(scale=scale, lower_bound=lower_bound, eps=eps)
+    return _fwd_pieces(K.gdn2_fwd, q, k, v, g, (erase, write), A_log, dt_bias, lengths, pieces, h0, kw)
+
+
+def gdn2_bwd_pieces(q, k, v, g, erase, write, A_log, dt_bias, dO, pctx: PiecesContext, *, dht=None,
+                    scale: float = 1.0, lower_bound: float = -5.0, eps: float = 1e-6):
+    """Backward matching ``gdn2_fwd_pieces``: the dict of kda.gdn2_bwd plus
+    dh0."""
+    kw = dict(scale=scale, lower_bound=lower_bound, eps=eps)
+    return _bwd_pieces(K.gdn2_bwd, q, k, v, g, (erase, write), A_log, dt_bias, dO, pctx, dht, kw)
 
 
 # ---- one piece per rank ----------------------------------------------------
@@ -129,18 +155,28 @@ def _prefix_default(A_all, B_all, x0, direction):
     return K.state_prefix(A_all, B_all, x0, direction=direction, layout="piece_major")
 
 
+def _gates(inp):
+    """The problem's gate tensors and its entry points: GDN-2's erase and
+    write gates when ``inp`` has them, else KDA's beta."""
+    if "erase" in inp:
+        return (inp["erase"], inp["write"]), K.gdn2_fwd, K.gdn2_bwd
+    return (inp["beta"],), K.kda_fwd, K.kda_bwd
+
+
 def _fwd_default(inp, h0, zero_values, kw):
     """This rank's piece forward: (o, ctx, hT); with zero_values the piece
     runs with v = 0 and no ctx (its transition)."""
+    gates, fwd, _ = _gates(inp)
     v = torch.zeros_like(inp["v"]) if zero_values else inp["v"]
-    r = K.kda_fwd(inp["q"], inp["k"], v, inp["g"], inp["beta"], inp["A_log"], inp["dt_bias"],
-                  inp["cu_seqlens"], save_ctx=not zero_values, h0=h0, final_state=True, **kw)
+    r = fwd(inp["q"], inp["k"], v, inp["g"], *gates, inp["A_log"], inp["dt_bias"],
+            inp["cu_seqlens"], save_ctx=not zero_values, h0=h0, final_state=True, **kw)
     return r[0], r[1], r[2]
 
 
 def _bwd_default(inp, ctx, dht, kw):
-    return K.kda_bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["A_log"], inp["dt_bias"],
-                     inp["cu_seqlens"], inp["dO"], ctx, dht=dht, want_dh0=True, **kw)
+    gates, _, bwd = _gates(inp)
+    return bwd(inp["q"], inp["k"], inp["v"], inp["g"], *gates, inp["A_log"], inp["dt_bias"],
+               inp["cu_seqlens"], inp["dO"], ctx, dht=dht, want_dh0=True, **kw)
 
 
 def kda_fwd_cp(inp: dict, group=None, *, h0=None, scale: float = 1.0, lower_bound: float = -5.0,
@@ -148,7 +184,8 @@ def kda_fwd_cp(inp: dict, group=None, *, h0=None, scale: float = 1.0, lower_boun
                identity=None):
     """Forward with one piece of every sequence on each rank of ``group``
     (rank r holds piece r: the r-th contiguous token range of each of the N
-    sequences, packed with its own cu_seqlens in ``inp``). h0 [N, H, D, D]
+    sequences, packed with its own cu_seqlens in ``inp``; GDN-2 when ``inp``
+    holds "erase" and "write" instead of "beta"). h0 [N, H, D, D]
     is the sequences' initial state (the same tensor on every rank, or
     None). Returns (o, ctx, state) where state carries the gathered
     transitions for the backward and the sequences' final states."""

@@ -41,6 +41,29 @@ def test_pieces_match_the_whole_sequence_oracle(dtype, D, pieces, states):
     compare(r, ref, TOL[inp["q"].dtype], names=OUT_NAMES + ["hT", "dh0"])
 
 
+@pytest.mark.parametrize("dtype,D,pieces,states", [("bf16", 128, 3, True), ("f32", 64, 2, True)])
+def test_gdn2_pieces_match_the_whole_sequence_oracle(dtype, D, pieces, states):
+    # GDN-2 (channel-wise erase / write gates) cut the same way; bf16 D = 128
+    # runs the tensor-core forward, fp32 D = 64 the CUDA-core kernels
+    lengths = (1029, 700, 2049)
+    w = Workload(f"cp_gdn2_{dtype}_d{D}_p{pieces}", lengths, 3, D, dtype, seed=8350 + D + pieces,
+                 param_std=0.5, scale=D ** -0.5, gate_mean=-2.0, gates="channel")
+    inp = to_dev(make_inputs(w))
+    st = to_dev(make_states(w)) if states else {"h0": None, "dht": None}
+    names = ("q", "k", "v", "g", "erase", "write", "A_log", "dt_bias")
+    args = [inp[n] for n in names]
+    o, hT, pctx = CP.gdn2_fwd_pieces(*args, list(lengths), pieces, h0=st["h0"], scale=w.scale)
+    r = CP.gdn2_bwd_pieces(*args, inp["dO"], pctx, dht=st["dht"], scale=w.scale)
+    torch.cuda.synchronize()
+    r["o"], r["hT"] = o, hT
+    cpu = {k_: (v_.cpu() if v_ is not None else None) for k_, v_ in inp.items()}
+    ref = oracle.gdn2_reference(*[cpu[n] for n in names], cpu["cu_seqlens"], cpu["dO"], scale=w.scale,
+                                h0=None if st["h0"] is None else st["h0"].cpu(),
+                                dht=None if st["dht"] is None else st["dht"].cpu(), want_state=True)
+    gnames = ["o", "dq", "dk", "dv", "dg", "derase", "dwrite", "dA_log", "ddt_bias", "hT", "dh0"]
+    compare(r, ref, TOL[inp["q"].dtype], names=gnames)
+
+
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("layout", ["seq_major", "piece_major"])
 def test_state_prefix_kernel_against_float64(D, layout):
