@@ -267,7 +267,9 @@ kda_status kda_gdn2_bwd(const kda_problem* p,
  * state affinely, H_end = A_p H_start + B_p (A_p: D x D on the key index;
  * it is the piece's final state when the piece runs from the identity state
  * with zero values, B_p the final state when it runs from zero with its
- * values, both from kda_fwd with hT). The backward is the transposed map: a
+ * values, both from kda_fwd with hT; GDN-2's recurrence is affine in its
+ * state in the same way, so kda_gdn2_fwd / kda_gdn2_bwd give its maps). The
+ * backward is the transposed map: a
  * piece's start-state gradient is A_p^T (its end-state gradient) + C_p,
  * with C_p the dh0 of the piece's kda_bwd run with dhT = 0. Given every
  * piece's (A_p, B_p) or (A_p, C_p), this prefix returns each piece's true
@@ -284,8 +286,11 @@ kda_status kda_gdn2_bwd(const kda_problem* p,
  *     piece_stride = H, seq_stride = P * H is the layout kda_fwd / kda_bwd
  *     give when each sequence's P pieces are packed as P consecutive
  *     sequences ([N][P][H][D][D]); piece_stride = N * H, seq_stride = H is
- *     the layout of maps gathered from P ranks ([P][N][H][D][D]). Any other
- *     strides are rejected.
+ *     the layout of maps gathered from P ranks ([P][N][H][D][D]). Padded
+ *     strides are accepted as long as the matrices cannot overlap: either
+ *     piece_stride >= H and seq_stride >= P * piece_stride, or
+ *     seq_stride >= H and piece_stride >= N * seq_stride. Any other pair
+ *     returns KDA_ERR_INVALID_ARG.
  *   x0, x_end: fp32 [N][H][D][D].
  *   KDA_PREFIX_FORWARD:  x_0 = x0 (zero when NULL), xs[p] = x_p,
  *                        x_{p+1} = A_p x_p + B_p, x_end = x_P (if not NULL).
