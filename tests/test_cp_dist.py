@@ -126,3 +126,19 @@ def test_cp_protocol_two_ranks_matches_the_whole_sequence():
     for rank in (0, 1):
         for n in ("dA_log", "ddt_bias", "dh0", "hT"):
             np.testing.assert_allclose(got[rank][n], ref[n], rtol=1e-9, atol=1e-10, err_msg=n)
+
+
+def test_piece_lengths_cover_each_sequence_in_order():
+    # every sequence's tokens, cut into contiguous pieces sequence-major; the
+    # first T % P pieces take one token more, and empty pieces are allowed
+    import pytest
+    from recompute_kda_chunkwise_gb300 import cp as CP
+    assert CP.piece_lengths([10, 3, 0], 4) == [3, 3, 2, 2, 1, 1, 1, 0, 0, 0, 0, 0]
+    assert CP.piece_lengths([7], 1) == [7]
+    for lengths, P in [([1029, 700, 2049, 3], 5), ([131072], 2), ([1], 3)]:
+        pl = CP.piece_lengths(lengths, P)
+        assert len(pl) == len(lengths) * P
+        assert [sum(pl[n * P:(n + 1) * P]) for n in range(len(lengths))] == list(lengths)
+        assert all(max(pl[n * P:(n + 1) * P]) - min(pl[n * P:(n + 1) * P]) <= 1 for n in range(len(lengths)))
+    with pytest.raises(ValueError):
+        CP.piece_lengths([4], 0)
