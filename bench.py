@@ -632,12 +632,19 @@ def run_gb300(args, w, rank, world, local):
         sets.append((inp2, o2, grads2))
         ev = lambda: torch.cuda.Event()
         up_done, fwd_done, comp_done, down_done = ([ev(), ev()] for _ in range(4))
+        # per-step spans of each stream's own work inside the pipeline
+        tev = lambda: torch.cuda.Event(enable_timing=True)
+        spans = {"upload": [], "compute": [], "download": []}
 
         def upload(b):
             up.wait_event(comp_done[b])  # the set's previous step no longer reads these inputs
             with torch.cuda.stream(up):
+                e0, e1 = tev(), tev()
+                e0.record(up)
                 for n in names_in:
                     sets[b][0][n].copy_(host_in[n], non_blocking=True)
+                e1.record(up)
+                spans["upload"].append((e0, e1))
                 up_done[b].record(up)
 
         def compute(b):
@@ -645,19 +652,29 @@ def run_gb300(args, w, rank, world, local):
             a_in = [x[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
             stream.wait_event(up_done[b])
             stream.wait_event(down_done[b])  # results of step i-2 have left this set
+            e0, e1 = tev(), tev()
+            e0.record(stream)
             fwd_fn(*a_in, scale=w.scale, out=ob, ctx=ctx)
             fwd_done[b].record(stream)
             bwd_fn(*a_in, x["dO"], ctx, scale=w.scale, workspace=ws, outs=gb)
+            e1.record(stream)
+            spans["compute"].append((e0, e1))
             comp_done[b].record(stream)
 
         def download(b):
             _, ob, gb = sets[b]
             with torch.cuda.stream(down):
                 down.wait_event(fwd_done[b])
+                e0, e1, e2, e3 = tev(), tev(), tev(), tev()
+                e0.record(down)
                 host_o.copy_(ob, non_blocking=True)
+                e1.record(down)
                 down.wait_event(comp_done[b])
+                e2.record(down)
                 for n in names_out:
                     host_out[n].copy_(gb[n], non_blocking=True)
+                e3.record(down)
+                spans["download"].append((e0, e1, e2, e3))
                 down_done[b].record(down)
 
         def run_pipeline(nsteps):
@@ -676,12 +693,19 @@ def run_gb300(args, w, rank, world, local):
         rates = copy_rates(stream, [(inp[n], host_in[n]) for n in names_in],
                            [(host_out[n], grads[n]) for n in names_out] + [(host_o, o)])
         barrier()
+        for v_ in spans.values():
+            v_.clear()
         t0 = time.perf_counter()
         run_pipeline(args.e2e_steps)
         torch.cuda.synchronize()
         dt = max_over_ranks(time.perf_counter() - t0) / args.e2e_steps
+        # mean span of each stream's work per step: a compute span above the
+        # device-resident step means the copies slowed the kernels; an upload
+        # or download span above its standalone time means the reverse
+        span_ms = lambda e: sum(e[i].elapsed_time(e[i + 1]) for i in range(0, len(e), 2))
+        pipe = {f"{k}_ms_in_pipeline": statistics.mean(span_ms(e) for e in v_) for k, v_ in spans.items()}
         e2e = {"value": tokens / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": args.e2e_steps, "ms_per_step": dt * 1e3, **rates,
+               "steps": args.e2e_steps, "ms_per_step": dt * 1e3, **rates, **pipe,
                "overlap": "pipelined: step i+1's uploads and step i-1's downloads run beside step i's "
                           "compute (two device sets of inputs and results)"}
         del inp2, o2, grads2, sets

@@ -91,8 +91,52 @@ struct Tiles {
     }
     return p;
   }
-  static constexpr int floats(bool cg = false) { return 10 * TILE + 3 * SQ + 3 * C + 2 * D + (cg ? 2 * TILE : 0); }
+  __host__ __device__ static constexpr int floats(bool cg = false) {
+    return 10 * TILE + 3 * SQ + 3 * C + 2 * D + (cg ? 2 * TILE : 0);
+  }
 };
+
+// dst[di(x)] = src[x] for x in [0, n): each thread issues kB of its global
+// loads before any of its shared-memory stores, so their latencies overlap
+// (in a plain copy loop every load waits behind the previous iteration's
+// store, which the compiler cannot tell apart from the loaded address).
+template <int kB, typename DstIdx>
+__device__ __forceinline__ void load_batched(float* dst, const float* src, int n, DstIdx di) {
+  for (int base = static_cast<int>(threadIdx.x); base < n; base += kNT * kB) {
+    float tmp[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int x = base + j * kNT;
+      tmp[j] = x < n ? src[x] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int x = base + j * kNT;
+      if (x < n) dst[di(x)] = tmp[j];
+    }
+  }
+}
+
+// dst = src for n4 float4s (both 16-byte aligned), kB loads in flight per
+// thread before its stores.
+template <int kB>
+__device__ __forceinline__ void copy4_batched(float* dst, const float* src, int n4) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+  float4* d4 = reinterpret_cast<float4*>(dst);
+  for (int base = static_cast<int>(threadIdx.x); base < n4; base += kNT * kB) {
+    float4 tmp[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int x = base + j * kNT;
+      if (x < n4) tmp[j] = s4[x];
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int x = base + j * kNT;
+      if (x < n4) d4[x] = tmp[j];
+    }
+  }
+}
 
 // Loads rows [t0, t0 + rows) of head h (zeros beyond `rows`, which makes the
 // padded rows inert: k = 0, beta = 0, g = 0) and builds
@@ -113,30 +157,36 @@ __device__ void chunk_prologue(const Tiles<D, C>& t, const Tin* q, const Tin* k,
                                const Tin* g, const Tin* b, const Tin* w, int64_t t0, int rows, int h,
                                int H, float expA, float scale, float lower, float eps) {
   constexpr int LD = D + 1;
+  constexpr int IT = C * D / kNT;  // elements per thread
+  static_assert(C * D % kNT == 0, "the chunk tile must split evenly over the threads");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int x = tid; x < C * D; x += kNT) {
-    const int r = x / D, i = x % D;
-    float qv = 0.f, kv = 0.f, gv = 0.f, vv = 0.f;
-    if (r < rows) {
-      const int64_t off = ((t0 + r) * H + h) * (int64_t)D + i;
-      qv = ldf(q + off);
-      kv = ldf(k + off);
-      vv = ldf(v + off);
-      gv = lower * sigmoidf_(expA * (ldf(g + off) + t.dtb[i]));
-    }
-    t.Qh[r * LD + i] = qv;
-    t.Kh[r * LD + i] = kv;
-    t.Gc[r * LD + i] = gv;
-    t.Vv[r * LD + i] = vv;
+  // all of this thread's global loads first, then the arithmetic and stores
+  float qv[IT], kv[IT], vv[IT], gr[IT], br[CG ? IT : 1], wr[CG ? IT : 1];
+#pragma unroll
+  for (int it = 0; it < IT; ++it) {
+    const int x = tid + it * kNT, r = x / D, i = x % D;
+    const int64_t off = ((t0 + r) * H + h) * (int64_t)D + i;
+    const bool ok = r < rows;
+    qv[it] = ok ? ldf(q + off) : 0.f;
+    kv[it] = ok ? ldf(k + off) : 0.f;
+    vv[it] = ok ? ldf(v + off) : 0.f;
+    gr[it] = ok ? ldf(g + off) : 0.f;
     if constexpr (CG) {
-      float be = 0.f, wr = 0.f;
-      if (r < rows) {
-        const int64_t off = ((t0 + r) * H + h) * (int64_t)D + i;
-        be = sigmoidf_(ldf(b + off));
-        wr = sigmoidf_(ldf(w + off));
-      }
-      t.Be[r * LD + i] = be;
-      t.Wr[r * LD + i] = wr;
+      br[it] = ok ? ldf(b + off) : 0.f;
+      wr[it] = ok ? ldf(w + off) : 0.f;
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < IT; ++it) {
+    const int x = tid + it * kNT, r = x / D, i = x % D;
+    const bool ok = r < rows;
+    t.Qh[r * LD + i] = qv[it];
+    t.Kh[r * LD + i] = kv[it];
+    t.Gc[r * LD + i] = ok ? lower * sigmoidf_(expA * (gr[it] + t.dtb[i])) : 0.f;
+    t.Vv[r * LD + i] = vv[it];
+    if constexpr (CG) {
+      t.Be[r * LD + i] = ok ? sigmoidf_(br[it]) : 0.f;
+      t.Wr[r * LD + i] = ok ? sigmoidf_(wr[it]) : 0.f;
     }
   }
   if (!CG && tid < C) t.bet[tid] = tid < rows ? sigmoidf_(ldf(b + (t0 + tid) * H + h)) : 0.f;
@@ -190,12 +240,14 @@ __device__ void chunk_prologue(const Tiles<D, C>& t, const Tin* q, const Tin* k,
 template <int D, int C, bool CG = false, typename Acc = float>
 __device__ void chunk_intra(const Tiles<D, C>& t) {
   constexpr int LD = D + 1, CP = C + 1;
+  constexpr int SP = kNT / (C * C);  // lanes per C x C output (contraction split over them)
+  static_assert(SP >= 1 && C * C * SP == kNT && 32 % SP == 0, "one output per SP adjacent lanes");
   const int tid = threadIdx.x;
-  for (int x = tid; x < C * C; x += kNT) {
-    const int r = x / C, s = x % C;
+  {
+    const int o = tid / SP, part = tid % SP, r = o / C, s = o % C;
     Acc akk = 0, aqk = 0;
     if (s <= r) {
-      for (int i = 0; i < D; ++i) {
+      for (int i = part; i < D; i += SP) {
         const float ki = t.Ki[s * LD + i];
         if constexpr (CG)
           akk += Acc(t.Be[r * LD + i] * t.Kg[r * LD + i]) * ki;
@@ -204,8 +256,15 @@ __device__ void chunk_intra(const Tiles<D, C>& t) {
         aqk += Acc(t.Qg[r * LD + i]) * ki;
       }
     }
-    t.Abar[r * CP + s] = s < r ? static_cast<float>(akk) : 0.f;
-    t.Aqk[r * CP + s] = s <= r ? static_cast<float>(aqk) : 0.f;
+#pragma unroll
+    for (int m = 1; m < SP; m <<= 1) {
+      akk += __shfl_xor_sync(0xffffffffu, akk, m);
+      aqk += __shfl_xor_sync(0xffffffffu, aqk, m);
+    }
+    if (part == 0) {
+      t.Abar[r * CP + s] = s < r ? static_cast<float>(akk) : 0.f;
+      t.Aqk[r * CP + s] = s <= r ? static_cast<float>(aqk) : 0.f;
+    }
   }
   __syncthreads();
   if (tid < 32) {  // forward substitution, one lane per column of T
@@ -330,7 +389,10 @@ __global__ void __launch_bounds__(kNT, 1) kda_fwd_simt_kernel(const FwdArgs a) {
   for (int i = tid; i < D; i += kNT) t.dtb[i] = a.dt_bias[h * D + i];
   // initial state h0 [N][H][D][V] (zero when NULL)
   const float* h0 = a.h0 ? a.h0 + (int64_t)blockIdx.x * (D * V) : nullptr;
-  for (int x = tid; x < D * V; x += kNT) Hs[x] = h0 ? h0[x] : 0.f;
+  if (h0 != nullptr)
+    load_batched<8>(Hs, h0, D * V, [](int x) { return x; });
+  else
+    for (int x = tid; x < D * V; x += kNT) Hs[x] = 0.f;
   const float expA = expf(a.A_log[h]);
   __syncthreads();
   for (int64_t t0 = bos; t0 < eos; t0 += C) {
@@ -376,6 +438,11 @@ struct BwdTiles {
     return p;
   }
   static constexpr int floats() { return 6 * TILE + 3 * SQ + 3 * C + D + 2 * kNT + 2 * D * LDH; }
+  // Hc's offset in floats behind the chunk tiles: a multiple of 4, so that
+  // Hc takes 16-byte copies (as does each D x LDH scratch slot)
+  __host__ __device__ static constexpr int hc_offset(int tiles_floats) {
+    return tiles_floats + 6 * TILE + 3 * SQ + 3 * C + D + kNT;
+  }
 };
 
 template <typename Tin, int D, bool CG>
@@ -390,6 +457,8 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
   // Abar that nearly cancel, and its 1e-4-of-RMS bar needs them to better
   // than fp32.
   using Acc = typename AccOf<Tin, CG>::type;
+  static_assert(BwdTiles<D, C>::hc_offset(Tiles<D, C>::floats(CG)) % 4 == 0 && (D * LDH) % 4 == 0,
+                "the state tile and its scratch slots must take 16-byte copies");
   Tiles<D, C> t;
   BwdTiles<D, C> u;
   u.carve(t.carve(sm, CG));
@@ -420,9 +489,11 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
     for (int i = tid; i < D; i += kNT) t.dtb[i] = a.dt_bias[h * D + i];
     // dH = dhT, the gradient of the final state (zero when NULL)
     const float* dhT = a.dhT ? a.dhT + (int64_t)item * (D * V) : nullptr;
-    for (int x = tid; x < D * LDH; x += kNT) {
-      const int i = x / LDH, j = x % LDH;
-      u.dH[x] = (dhT != nullptr && j < V) ? dhT[i * V + j] : 0.f;
+    if (dhT != nullptr) {
+      for (int i = tid; i < D; i += kNT) u.dH[i * LDH + V] = 0.f;  // the padding column
+      load_batched<8>(u.dH, dhT, D * V, [](int x) { return (x / V) * LDH + x % V; });
+    } else {
+      for (int x = tid; x < D * LDH; x += kNT) u.dH[x] = 0.f;
     }
     float acc_dtb = 0.f, acc_alog = 0.f;  // thread owns column tid % D
     __syncthreads();
@@ -431,13 +502,13 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
       const int c0 = seg * CPS, c1 = min(nchunks, c0 + CPS);
       {  // checkpoint -> Hc
         const float* src = a.ckpt + (ckpt_slot(bos, n, seg) * a.H + h) * (int64_t)(D * V);
-        for (int x = tid; x < D * V; x += kNT) u.Hc[(x / V) * LDH + (x % V)] = src[x];
+        load_batched<8>(u.Hc, src, D * V, [](int x) { return (x / V) * LDH + x % V; });
       }
       __syncthreads();
       // rebuild the chunk-start states of this segment
       for (int c = c0; c < c1; ++c) {
         float* dst = scratch + (int64_t)(c - c0) * D * LDH;
-        for (int x = tid; x < D * LDH; x += kNT) dst[x] = u.Hc[x];
+        copy4_batched<4>(dst, u.Hc, D * LDH / 4);
         if (c == c1 - 1) break;
         const int64_t t0 = bos + (int64_t)c * C;
         const int rows = (int)min((int64_t)C, eos - t0);
@@ -453,10 +524,19 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
         const int rows = (int)min((int64_t)C, eos - t0);
         {
           const float* src = scratch + (int64_t)(c - c0) * D * LDH;
-          for (int x = tid; x < D * LDH; x += kNT) u.Hc[x] = src[x];
-          for (int x = tid; x < C * V; x += kNT) {
-            const int r = x / V, j = x % V;
-            u.dOt[r * LD + j] = r < rows ? ldf(dO + ((t0 + r) * a.H + h) * (int64_t)V + j) : 0.f;
+          copy4_batched<9>(u.Hc, src, D * LDH / 4);
+          constexpr int ITO = C * V / kNT;
+          static_assert(C * V % kNT == 0, "the dO tile must split evenly over the threads");
+          float dov[ITO];
+#pragma unroll
+          for (int it = 0; it < ITO; ++it) {
+            const int x = tid + it * kNT, r = x / V, j = x % V;
+            dov[it] = r < rows ? ldf(dO + ((t0 + r) * a.H + h) * (int64_t)V + j) : 0.f;
+          }
+#pragma unroll
+          for (int it = 0; it < ITO; ++it) {
+            const int x = tid + it * kNT, r = x / V, j = x % V;
+            u.dOt[r * LD + j] = dov[it];
           }
         }
         chunk_prologue<Tin, D, C, CG>(t, q, k, v, g, b, w, t0, rows, h, a.H, expA, a.scale, a.lower, a.eps);
@@ -542,25 +622,37 @@ __global__ void __launch_bounds__(kNT, 1) kda_bwd_simt_kernel(const BwdArgs a) {
           }
         }
         // dM = tril(dO U~^T);  dT = strictly-lower part of dW Xw^T + dU~ Xu^T
-        for (int x = tid; x < C * C; x += kNT) {
-          const int r = x / C, s = x % C;
-          Acc dm = 0, dt = 0;
+        // (each output's contractions split over SP adjacent lanes)
+        {
+          constexpr int SP = kNT / (C * C);
+          static_assert(SP >= 1 && C * C * SP == kNT && 32 % SP == 0, "one output per SP adjacent lanes");
+          const int o = tid / SP, part = tid % SP, r = o / C, s = o % C;
+          Acc dm = 0, d1 = 0, d2 = 0;
           if (s <= r)
-            for (int j = 0; j < V; ++j) dm += Acc(u.dOt[r * LD + j]) * t.Uu[s * LD + j];
+            for (int j = part; j < V; j += SP) dm += Acc(u.dOt[r * LD + j]) * t.Uu[s * LD + j];
           if (s < r) {
-            Acc d1 = 0, d2 = 0;
             if constexpr (CG) {  // dW Xw^T + dU~ Xu^T with the channel gates
-              for (int i = 0; i < D; ++i) d1 += Acc(u.dWt[r * LD + i]) * (Acc(t.Be[s * LD + i]) * t.Kg[s * LD + i]);
-              for (int j = 0; j < V; ++j) d2 += Acc(u.dUt[r * LD + j]) * (Acc(t.Wr[s * LD + j]) * t.Vv[s * LD + j]);
-              dt = d1 + d2;
+              for (int i = part; i < D; i += SP)
+                d1 += Acc(u.dWt[r * LD + i]) * (Acc(t.Be[s * LD + i]) * t.Kg[s * LD + i]);
+              for (int j = part; j < V; j += SP)
+                d2 += Acc(u.dUt[r * LD + j]) * (Acc(t.Wr[s * LD + j]) * t.Vv[s * LD + j]);
             } else {
-              for (int i = 0; i < D; ++i) d1 += u.dWt[r * LD + i] * t.Kg[s * LD + i];
-              for (int j = 0; j < V; ++j) d2 += u.dUt[r * LD + j] * t.Vv[s * LD + j];
-              dt = t.bet[s] * (d1 + d2);
+              for (int i = part; i < D; i += SP) d1 += u.dWt[r * LD + i] * t.Kg[s * LD + i];
+              for (int j = part; j < V; j += SP) d2 += u.dUt[r * LD + j] * t.Vv[s * LD + j];
             }
           }
-          u.dM[r * CP + s] = static_cast<float>(dm);
-          u.dT[r * CP + s] = static_cast<float>(dt);
+#pragma unroll
+          for (int m = 1; m < SP; m <<= 1) {
+            dm += __shfl_xor_sync(0xffffffffu, dm, m);
+            d1 += __shfl_xor_sync(0xffffffffu, d1, m);
+            d2 += __shfl_xor_sync(0xffffffffu, d2, m);
+          }
+          if (part == 0) {
+            Acc dt = 0;
+            if (s < r) dt = CG ? d1 + d2 : Acc(t.bet[s]) * (d1 + d2);
+            u.dM[r * CP + s] = static_cast<float>(dm);
+            u.dT[r * CP + s] = static_cast<float>(dt);
+          }
         }
         __syncthreads();
         // Y = dT T^T
