@@ -17,6 +17,10 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkda_gb300.so")
+# tracing build: the same sources with the kernels' stage timers compiled in
+# (-DKDA_STAGE_TIMERS), in a directory of its own
+STAGE_BUILD = os.path.join(HERE, "_build_stage_timers")
+STAGE_LIB = os.path.join(STAGE_BUILD, "libkda_gb300.so")
 INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -38,8 +42,13 @@ def _headers():
     return hs
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), stage_timers: bool = False) -> str:
+    """Compiles the library (the tracing build with stage_timers=True) and
+    returns its path."""
+    out_dir, lib = (STAGE_BUILD, STAGE_LIB) if stage_timers else (BUILD, LIB)
+    if stage_timers:
+        extra_flags = (*extra_flags, "-DKDA_STAGE_TIMERS")
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     srcs = sources()
     newest_hdr = max(os.path.getmtime(h) for h in _headers())
@@ -49,7 +58,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         common += ["-Xptxas", "-v"]
 
     def obj_of(src):
-        return os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        return os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
 
     def compile_one(src):
         obj = obj_of(src)
@@ -70,14 +79,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             if log:
                 print(log)
     objs = [o for o, _ in results]
-    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs):
+        tmp = lib + f".tmp{os.getpid()}"
         r = subprocess.run([nvcc, "-shared", *ARCH, "-cudart", "static", "-o", tmp, *objs],
                            capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

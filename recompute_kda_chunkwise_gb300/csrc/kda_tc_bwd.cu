@@ -30,6 +30,17 @@
 //   dA = -T^T (dT' diag(beta)) T^T,  then Abar / M / gate / L2-norm chain rules.
 #include "kda_tc_common.cuh"
 
+#ifdef KDA_STAGE_TIMERS
+// per-CTA stage counters of the tensor-core backward (tracing build)
+__device__ unsigned long long g_bwd_stage[kStageCtas * 32];
+extern "C" int kda_bwd_stage_timers(unsigned long long* host, int clear) {
+  static unsigned long long zero[kStageCtas * 32];
+  if (host != nullptr && cudaMemcpyFromSymbol(host, g_bwd_stage, sizeof(g_bwd_stage)) != cudaSuccess) return 1;
+  if (clear && cudaMemcpyToSymbol(g_bwd_stage, zero, sizeof(zero)) != cudaSuccess) return 1;
+  return 0;
+}
+#endif
+
 namespace kda {
 namespace {
 using namespace tc;
@@ -64,6 +75,41 @@ constexpr uint32_t kSlotBytesInline = kStateBytes;  // the state alone
 // recurrence's own and the fp16 state meets the bar.
 constexpr uint32_t kEdgeBytes = 2 * kStateBytes;
 
+// Stages of a chunk step, as the stage timers of a tracing build count them
+// (each mark closes the stage named by it).
+enum BwdStage {
+  BS_JOB,           // a helper claims a job
+  BS_HANDOFF,       // split mode: wait for a rebuilt segment / a free buffer
+  BS_CKPT,          // segment start state from its checkpoint
+  BS_TILES_ISSUE,   // the next chunk's q / k / v / g copies issued
+  BS_STATE_STORE,   // rebuild pass: the chunk-start state's bulk store issued
+  BS_TILES_WAIT,    // this chunk's tiles landed
+  BS_TOP_BARRIER,   // barrier at the top of the step
+  BS_NORM_GATE,     // row norms, gate, per-half cumulative sums
+  BS_OPERANDS,      // full cumulative sum, gated operand tiles
+  BS_SLOT_WAIT,     // split mode: the helper's matrices landed
+  BS_DO_ISSUE,      // reverse pass: the next chunk's dO copies issued
+  BS_ABAR_M,        // Abar / M tf32 tiles (and the dU~ MMA issue)
+  BS_INVERSE,       // T = (I + diag(beta) Abar)^-1
+  BS_WU,            // W, U
+  BS_UT_MMA,        // U~ = U - W H (tcgen05) completed
+  BS_DUT_MMA,       // dU~ (tcgen05) completed
+  BS_READOUT,       // U~ / dU~ out of TMEM
+  BS_REBUILD_MMA,   // rebuild pass: Kbar^T U~ (tcgen05) completed
+  BS_STATE_UPDATE,  // rebuild pass: H <- diag(gamma) H + Kbar^T U~
+  BS_DM,            // state MMAs issued; dM and dU~ V^T tiles
+  BS_STATE_MMA,     // state MMAs completed
+  BS_E,             // [E] dH update, dgamma, dQG / dW / dKbar readout
+  BS_D1,            // [D1]
+  BS_D2,            // [D2]
+  BS_F,             // [F]
+  BS_DG_CUMSUM,     // dG reverse cumulative sum
+  BS_NORM_DOTS,     // L2-norm chain rule row dots
+  BS_OUTPUTS,       // dq, dk, dg, dbeta out
+  BS_COUNT
+};
+static_assert(BS_COUNT <= 31, "stage slots");
+
 // ---- shared memory map (bytes) ----
 constexpr int OFF_A1 = 0;                  // H^T fp16 [128 v][128 i] (SW128)
 constexpr int OFF_A1D = 32768;             // dH'^T fp16 [128 v][128 i]
@@ -87,7 +133,8 @@ constexpr int S_BETA = 2560, S_IQ0 = 2576, S_IK0 = 2592, S_DB = 2608, S_RQ = 262
 constexpr int S_GEND = 2656, S_DGE = 2784, S_TOT = 2912, S_PART = 3168, S_GAM = 3424, S_PR = 3552;
 constexpr int SMALL_FLOATS = 3872;
 constexpr int OFF_BAR = OFF_SMALL + SMALL_FLOATS * 4;
-constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
+constexpr int OFF_STAGE = OFF_BAR + 64;  // stage counters (tracing build only)
+constexpr int SMEM_BYTES = OFF_STAGE + KDA_STAGE_BYTES + 1024;  // + alignment slack
 // The dgamma reduce-scatter lands in the M hi / lo tiles (free by then).
 constexpr int OFF_RED = OFF_FM;
 static_assert(OFF_STG % 1024 == 0 && OFF_F32 % 16 == 0, "alignment");
@@ -305,6 +352,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *s_tmem;
+  KDA_STAGE_INIT(sm + OFF_STAGE);
   uint32_t ph = 0, ph_a1 = 0, ph_du = 0, ph_g1 = 0, ph_g2 = 0, ph_sm = 0;
   bool sm_pending = false;  // a bulk load of a chunk's small matrices is in flight
   bool a1_pending = false;  // a bulk load into A1 is in flight (same value in every thread)
@@ -407,6 +455,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
       bool found = false;
       while (true) {
         if (tid == 0) *s_job = static_cast<int>(atomicAdd(a.flags + kTcBwdFlags * items, 1u));
+        KDA_STAGE(BS_JOB);
         __syncthreads();
         const int jb = *s_job;
         __syncthreads();
@@ -451,6 +500,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           fence_proxy_global();
         }
         KDA_SYNC_OR_BAIL();
+        KDA_STAGE(BS_HANDOFF);
       }
       if (rebuild) {
         // ---- segment start state: checkpoint (fp32 [i][v]) -> TMEM H^T and fp16 A1 ----
@@ -470,6 +520,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
         tmem_st_wait();
         if (kEdge && (c0 == 0 || c0 == nchunks - 1))  // a sequence-edge chunk starts at this checkpoint
           edge_lo_from_global(edge_buf + (c0 == 0 ? 0 : kStateBytes), src, L, hh);
+        KDA_STAGE(BS_CKPT);
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -526,9 +577,14 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             if (tid < kC && tid < rn) braw_next = beta_bits(a.b, (tn + tid) * a.H + h);
           }
           cp_async_commit();
+          KDA_STAGE(BS_TILES_ISSUE);
           if (!rev && tid == 0) bulk_store(segbuf + static_cast<size_t>(c - c0) * sbytes, sb + OFF_A1, kStateBytes);
+          KDA_STAGE(BS_STATE_STORE);
           cp_async_wait_prev();
+          KDA_STAGE(BS_TILES_WAIT);
           __syncthreads();
+          KDA_STAGE(BS_TOP_BARRIER);
+          KDA_STAGE_STEP();
 
           // ================= chunk prologue =================
           if (tid < kC) S[S_BETA + tid] = tid < rows ? sigm(__bfloat162float(__ushort_as_bfloat16(braw))) : 0.f;
@@ -575,6 +631,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             S[S_TOT + rh * 128 + ci] = acc;
           }
           __syncthreads();
+          KDA_STAGE(BS_NORM_GATE);
           {  // full cumsum, gated operands
             const float carry = rh ? S[S_TOT + ci] : 0.f;
             const float gend = S[S_TOT + ci] + S[S_TOT + 128 + ci];
@@ -615,15 +672,18 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           // Abar / M, inverse and W/U stages and their barriers are the helper's)
           if (!prep) fence_async_smem();
           __syncthreads();
+          KDA_STAGE(BS_OPERANDS);
           if (!prep) {  // split mode: this chunk's Abar, T, T', M come from the helper
             if (!mbar_wait(bar_sm, ph_sm, a.status)) *s_fail = 1;
             ph_sm ^= 1u;
             sm_pending = false;
           }
+          KDA_STAGE(BS_SLOT_WAIT);
           if (rev) {  // next chunk's dO (the dO staging tile has been consumed)
             if (more) stage_tiles(a, 0, h, t0 - kC, kC, tid, false, true, sb + OFF_SDO);
             cp_async_commit();
           }
+          KDA_STAGE(BS_DO_ISSUE);
           // ================= Abar (and M) on tf32 tensor tiles =================
           // warp w: column block nt = w & 1, contraction half kh = (w >> 1) & 1, Abar (w < 4) or
           // M (w >= 4); the kh = 1 warps hand their partial sums over in S_DT1 / S_DT2 (free here)
@@ -670,6 +730,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             fence_before_sync();
             __syncthreads();
           }
+          KDA_STAGE(BS_ABAR_M);
           // dU~^T = dO^T (Mhi + Mlo) + dH'^T Kbar^T needs no U~: issue it now (warp 4 is idle
           // during the inverse) so it runs under the inverse and the W/U stage
           if (rev && warp == 4 && lane == 0) {
@@ -733,6 +794,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               }
             }
           }
+          KDA_STAGE(BS_INVERSE);
           // -W and U~ are rewritten next: the previous step's copies of them (all
           // but this step's state copy) have been read out
           if (helper && tid == 0) bulk_wait_read_but<1>();
@@ -780,6 +842,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             fence_before_sync();
             KDA_SYNC_OR_BAIL();
           }
+          KDA_STAGE(BS_WU);
           // ================= U~ = U - W H (tcgen05) =================
           if (a1_pending) {  // this chunk's start state, loaded during the prologue
             if (!mbar_wait(bar_a1, ph_a1, a.status)) *s_fail = 1;
@@ -796,10 +859,12 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               mma_commit(bar);
             }
             KDA_WAIT_MMA();
+            KDA_STAGE(BS_UT_MMA);
           }
           if (rev) {
             if (!mbar_wait(bar_du, ph_du, a.status)) *s_fail = 1;
             ph_du ^= 1u;
+            KDA_STAGE(BS_DUT_MMA);
           }
           fence_after_sync();
           {
@@ -828,6 +893,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           fence_before_sync();
           KDA_SYNC_OR_BAIL();
 
+          KDA_STAGE(BS_READOUT);
           if (!rev) {
             if (helper) {  // hand -W and U~ over; the segment's last chunk advances no state
               if (tid == 0) ship_wu(segbuf + static_cast<size_t>(c - c0) * sbytes);
@@ -847,6 +913,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               mma_commit(bar);
             }
             KDA_WAIT_MMA();
+            KDA_STAGE(BS_REBUILD_MMA);
             fence_after_sync();
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -873,6 +940,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             fence_async_smem();
             fence_before_sync();
             KDA_SYNC_OR_BAIL();
+            KDA_STAGE(BS_STATE_UPDATE);
             continue;
           }
 
@@ -943,7 +1011,9 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           // their start state (written by the rebuild pass with plain stores,
           // read past L1 in [E])
           const bool edge = kEdge && (c == 0 || c == nchunks - 1);
+          KDA_STAGE(BS_DM);
           KDA_WAIT_MMA();
+          KDA_STAGE(BS_STATE_MMA);
           if (!mbar_wait(bar_g1, ph_g1, a.status)) *s_fail = 1;
           ph_g1 ^= 1u;
           if (!mbar_wait(bar_g2, ph_g2, a.status)) *s_fail = 1;
@@ -1022,6 +1092,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             edge_fold(RED);
             __syncthreads();
           }
+          KDA_STAGE(BS_E);
           // the next chunk's start state into A1 (its last reader was [E])
           if (more) {
             if (tid == 0) {
@@ -1061,6 +1132,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             }
           }
           __syncthreads();
+          KDA_STAGE(BS_D1);
           // ---- [D2] dT = dT' diag(beta) (strictly lower; dT' = DT1 + Y + DT2 partials),
           // Y = dT T^T and dA = -T^T Y on tf32 tiles, warp nt: columns 8nt .. 8nt+7 ----
           if (warp < 2) {
@@ -1110,6 +1182,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             S[S_DB + lane] = db;
           }
           __syncthreads();
+          KDA_STAGE(BS_D2);
           if (tid < kC) {  // dbeta of rows: A = diag(beta) Abar
             float db = S[S_DB + tid];
 #pragma unroll
@@ -1166,6 +1239,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           }
           fence_async_smem();
           __syncthreads();
+          KDA_STAGE(BS_F);
           if (!prep && more) {  // the next chunk's Abar, T, T', M (last read in [D2] and [F])
             if (tid == 0) load_prep(segbuf + static_cast<size_t>(c - 1 - c0) * sbytes);
             sm_pending = true;
@@ -1186,6 +1260,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               AG[r * kLd + ci] = acc;
             }
           }
+          KDA_STAGE(BS_DG_CUMSUM);
           {  // L2-norm chain rule row dots: warp w -> rows 2w, 2w+1
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
@@ -1206,6 +1281,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
             }
           }
           __syncthreads();
+          KDA_STAGE(BS_NORM_DOTS);
           {  // outputs dq, dk, dg (raw gate), parameter partials
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -1232,6 +1308,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           fence_async_smem();
           fence_before_sync();
           KDA_SYNC_OR_BAIL();
+          KDA_STAGE(BS_OUTPUTS);
         }
         if (kEdge && !rev) {
           // the rebuild pass leaves the start state of chunk c1 - 1 in TMEM:
@@ -1299,6 +1376,7 @@ teardown:
   asm volatile("cp.async.wait_all;" ::: "memory");
   fence_before_sync();
   __syncthreads();
+  KDA_STAGE_FLUSH(g_bwd_stage);
   if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 

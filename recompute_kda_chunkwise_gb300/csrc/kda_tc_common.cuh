@@ -19,6 +19,54 @@
 
 #include "kda_internal.cuh"
 
+// Stage timers, for a tracing build only (compiled with -DKDA_STAGE_TIMERS).
+// Thread 0 of each CTA adds the clock64 cycles since its previous mark to a
+// per-stage counter in KDA_STAGE_BYTES of shared memory (slot 31 counts the
+// steps); the counters go to the CTA's row of a device array when the CTA
+// exits. In the default build every mark compiles to nothing and no shared
+// memory is set aside.
+#ifdef KDA_STAGE_TIMERS
+#define KDA_STAGE_BYTES 128
+#define KDA_STAGE_INIT(smem_ptr)                                            \
+  unsigned* const kda_stage_sm = reinterpret_cast<unsigned*>(smem_ptr);     \
+  long long kda_stage_t = clock64();                                        \
+  if (threadIdx.x == 0)                                                     \
+    for (int i_ = 0; i_ < 32; ++i_) kda_stage_sm[i_] = 0u
+#define KDA_STAGE(id)                                                       \
+  do {                                                                      \
+    if (threadIdx.x == 0) {                                                 \
+      const long long t_ = clock64();                                       \
+      kda_stage_sm[(id)] += static_cast<unsigned>(t_ - kda_stage_t);        \
+      kda_stage_t = t_;                                                     \
+    }                                                                       \
+  } while (0)
+#define KDA_STAGE_STEP()                                                    \
+  do {                                                                      \
+    if (threadIdx.x == 0) kda_stage_sm[31] += 1u;                           \
+  } while (0)
+#define KDA_STAGE_FLUSH(dev_array)                                          \
+  do {                                                                      \
+    if (threadIdx.x == 0 && blockIdx.x < kStageCtas)                        \
+      for (int i_ = 0; i_ < 32; ++i_) (dev_array)[blockIdx.x * 32 + i_] += kda_stage_sm[i_]; \
+  } while (0)
+#else
+#define KDA_STAGE_BYTES 0
+#define KDA_STAGE_INIT(smem_ptr) \
+  do {                           \
+  } while (0)
+#define KDA_STAGE(id) \
+  do {                \
+  } while (0)
+#define KDA_STAGE_STEP() \
+  do {                   \
+  } while (0)
+#define KDA_STAGE_FLUSH(dev_array) \
+  do {                             \
+  } while (0)
+#endif
+// CTAs whose stage counters a tracing build keeps (rows of its device array)
+constexpr int kStageCtas = 512;
+
 namespace kda {
 namespace tc {
 

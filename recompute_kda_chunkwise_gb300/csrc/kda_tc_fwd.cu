@@ -41,6 +41,17 @@
 // H^T products -> U~^T tile -> Kbar, M products -> state update and output.
 #include "kda_tc_common.cuh"
 
+#ifdef KDA_STAGE_TIMERS
+// per-CTA stage counters of the tensor-core forward (tracing build)
+__device__ unsigned long long g_fwd_stage[kStageCtas * 32];
+extern "C" int kda_fwd_stage_timers(unsigned long long* host, int clear) {
+  static unsigned long long zero[kStageCtas * 32];
+  if (host != nullptr && cudaMemcpyFromSymbol(host, g_fwd_stage, sizeof(g_fwd_stage)) != cudaSuccess) return 1;
+  if (clear && cudaMemcpyToSymbol(g_fwd_stage, zero, sizeof(zero)) != cudaSuccess) return 1;
+  return 0;
+}
+#endif
+
 namespace kda {
 namespace {
 using namespace tc;
@@ -49,6 +60,31 @@ constexpr int kC = 64;
 constexpr int kD = 128;
 constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Stages of a chunk step, as the stage timers of a tracing build count them
+// (each mark closes the stage named by it; FS_UPDATE, at the loop top, closes
+// the previous chunk's state update and output).
+enum FwdStage {
+  FS_UPDATE,        // state update (fp32 registers), next H^T operand, output
+  FS_TOP,           // loop top: next helper job / checkpoint store
+  FS_QKG_WAIT,      // q / k / raw gate tiles landed (TMA)
+  FS_NORMS,         // row norms (and a helper's wait for its previous stores)
+  FS_GATE,          // gate, cumulative log2-decay
+  FS_REFS,          // per-channel block references
+  FS_OPERANDS,      // operand tiles
+  FS_ROUNDS,        // Abar | M tf32 rounds (row operands to TMEM, four MMA rounds)
+  FS_ROUND_READOUT, // Abar and M out of TMEM
+  FS_INVERSE,       // T by blocked forward substitution
+  FS_WU,            // v -> fp16, W / U products
+  FS_NEG_W,         // -W tile
+  FS_HANDOFF,       // helper: the prepared chunk's bulk stores issued
+  FS_SLOT_WAIT,     // main CTA: a handed chunk's operands landed
+  FS_UT_O,          // U~ and the H^T part of O (tcgen05)
+  FS_KBAR_M,        // U~ tile, Kbar^T U~ and M U~ (tcgen05)
+  FS_NEXT_SLOT,     // split mode: wait for, and fetch, the next handed chunk
+  FS_COUNT
+};
+static_assert(FS_COUNT <= 31, "stage slots");
 
 // Shared-memory map (bytes from a 1024-byte aligned base).
 constexpr int OFF_STG_Q = 0;           // staged q        [64 r][128 c] bf16 SW128 (TMA)
@@ -79,7 +115,8 @@ constexpr int SM_GAM2 = 1344 + 6 * 128;  // gamma of a handed-over chunk (split 
 constexpr int SMALL_FLOATS = SM_GAM2 + 128;
 constexpr int OFF_BAR = OFF_SMALL + SMALL_FLOATS * 4;
 constexpr int SMEM_USED = OFF_BAR + 80;  // 10 mbarrier / flag words
-constexpr int SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
+constexpr int OFF_STAGE = SMEM_USED;  // stage counters (tracing build only)
+constexpr int SMEM_BYTES = SMEM_USED + KDA_STAGE_BYTES + 1024;  // alignment slack
 
 // Split-mode hand-off slot (bytes, all 16-byte multiples): the prepared
 // operands of one odd chunk as the main CTA's shared memory holds them, in
@@ -333,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *s_tmem;
+  KDA_STAGE_INIT(sm + OFF_STAGE);
 
   // channel-major role: channel pair (c0, c0+1), rows 16*Ib .. 16*Ib+15 (sub-block Ib)
   const int pp = tid & 63, Ib = tid >> 6, c0 = 2 * pp;
@@ -427,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int c = -1;
   while (true) {
+    KDA_STAGE(FS_UPDATE);
     if (!helper) {
       if (++c >= nchunks) break;
     } else {  // the job found ahead, whose q, k, g are in flight
@@ -443,6 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       dtb1 = a.dt_bias[h * kD + c0 + 1];
       find_job();
     }
+    KDA_STAGE(FS_TOP);
+    KDA_STAGE_STEP();
     const bool handed = split && !helper && (c & 1);  // prepared by a helper
     const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
     const int rows = static_cast<int>(min(static_cast<int64_t>(kC), eos - t0));
@@ -457,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // raw beta: loaded now, stored once the norms are done (its latency hidden)
     const unsigned short braw = (!CG && tid < rows) ? beta_bits(a.b, (t0 + tid) * a.H + h) : 0;
     KDA_WAIT(bar_qkg, ph_qkg);
+    KDA_STAGE(FS_QKG_WAIT);
     // ---- row norms: warp w handles rows 8w .. 8w+7, four at a time (sums
     // interleaved; lanes 0-3 finish the q rows, lanes 8-11 the k rows) ----
 #pragma unroll
@@ -501,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 0) bulk_wait_read();
       __syncthreads();
     }
+    KDA_STAGE(FS_NORMS);
     // ---- gate and cumulative log2-decay of the thread's 16-row block ----
     {
       float gl0[16], gl1[16], acc0 = 0.f, acc1 = 0.f;
@@ -527,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sm + OFF_STG_G, &tme, 0, h, static_cast<int>(t0), bar_e);
       tma_load_3d(sm + OFF_STG_G + 8192, &tme, 64, h, static_cast<int>(t0), bar_e);
     }
+    KDA_STAGE(FS_GATE);
     // ---- per-channel block references ----
     if (tid < kD) {
       const int ch = tid;
@@ -545,6 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
+    KDA_STAGE(FS_REFS);
     // ---- operand tiles, row-major: thread = one row (k or q) x 64 channels ----
     if (CG) KDA_WAIT(bar_e, ph_e);  // GDN-2: the erase gate (in the raw gate's tile)
     float rowf[64];  // kh e^{G_r - B_{I+1}} (k rows) or qh e^{G_r - B_{I+1}} (q rows)
@@ -612,6 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_async_smem();
     KDA_SYNC_OR_BAIL();
+    KDA_STAGE(FS_OPERANDS);
     // staged q, k, g and the decay offsets are consumed: fetch v of this
     // chunk (into the offsets' space) and q, k, g of the next chunk
     if (tid == 0) {
@@ -670,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     KDA_WAIT(bar_odd, ph_odd);  // round 1
     KDA_WAIT(bar_r2, ph_r2);    // round 2
     KDA_WAIT(bar_mma, ph_mma);  // round 3
+    KDA_STAGE(FS_ROUNDS);
     fence_after_sync();
 
     // ---- Abar (fp32, for the inverse) and M (fp16 operand) out of TMEM ----
@@ -701,7 +748,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_before_sync();
     __syncthreads();
+    KDA_STAGE(FS_ROUND_READOUT);
     tri_inverse(sm, s_beta, tid);
+    KDA_STAGE(FS_INVERSE);
     if (CG) {  // T is consumed: the write gate takes its space
       __syncthreads();
       if (tid == 0) {
@@ -767,6 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     KDA_WAIT(bar_mma, ph_mma);
     fence_after_sync();
 
+    KDA_STAGE(FS_WU);
     // ---- -W into rows 0..63 of B1 ----
     {
       float v[32];
@@ -778,6 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_async_smem();
     fence_before_sync();
     KDA_SYNC_OR_BAIL();
+    KDA_STAGE(FS_NEG_W);
     }  // prepared here
     if (helper) {
       // ---- hand the prepared odd chunk over: the operand runs, T' hi and
@@ -797,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pub_tt = tt;
       }
       pub_pending = true;
+      KDA_STAGE(FS_HANDOFF);
       continue;
     }
     if (handed) {
@@ -808,6 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *s_fail = 1;
       ph_x ^= 1u;
       if (tid == 0) st_release(a.xflags + 5 * item + 4, static_cast<uint32_t>((c >> 1) + 1));
+      KDA_STAGE(FS_SLOT_WAIT);
     }
     if (tid == 0) {
       fence_after_sync();
@@ -824,6 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     KDA_WAIT(bar_mma, ph_mma);
     fence_after_sync();
 
+    KDA_STAGE(FS_UT_O);
     // ---- U~^T (fp16) as the A operand of the Kbar and M products ----
     {
       float v[32];
@@ -861,6 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     KDA_WAIT(bar_mma, ph_mma);
     fence_after_sync();
+    KDA_STAGE(FS_KBAR_M);
     if (split && !(c & 1) && c + 1 < nchunks) {
       // fetch the helper-prepared next (odd) chunk into the tiles this chunk
       // has finished with (its last product above has completed)
@@ -878,6 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       x_pending = true;
     }
 
+    KDA_STAGE(FS_NEXT_SLOT);
     // ---- state update (fp32 registers), next H^T operand, output ----
     {
       float v[32];
@@ -929,6 +985,7 @@ teardown:
   }
   fence_before_sync();
   __syncthreads();
+  KDA_STAGE_FLUSH(g_fwd_stage);
   if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
