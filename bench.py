@@ -78,9 +78,28 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+# the sources each kernel family of a traffic record is compiled from
+KERNEL_SOURCES = {
+    "kda_fwd_tc": ("kda_tc_fwd.cu", "kda_tc_common.cuh", "kda_internal.cuh"),
+    "kda_bwd_tc": ("kda_tc_bwd.cu", "kda_tc_common.cuh", "kda_internal.cuh"),
+    "kda_gdn2_fwd_tc": ("kda_tc_fwd.cu", "kda_tc_common.cuh", "kda_internal.cuh"),
+    "kda_gdn2_bwd_simt": ("kda_simt.cu", "kda_internal.cuh"),
+}
+
+
+def kernel_files_hash(kernel: str):
+    """Hash of the source files a kernel family is compiled from."""
+    csrc = os.path.join(ROOT, "recompute_kda_chunkwise_gb300", "csrc")
+    h = hashlib.sha256()
+    for fn in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
 def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json),
-    valid only while the kernel sources are unchanged since the capture."""
+    valid only while the kernel's own source files are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -88,7 +107,7 @@ def ncu_traffic(kernel: str, workload: str):
     except Exception:
         return None
     ent = rec.get(kernel, {}).get(workload)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or kernel not in KERNEL_SOURCES or ent.get("source_hash") != kernel_files_hash(kernel):
         return None
     return float(ent["dram_bytes_per_launch"])
 
