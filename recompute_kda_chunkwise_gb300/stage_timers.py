@@ -51,8 +51,11 @@ def _table(title, rows, names):
         return []
     steps = rows[:, 31].sum()
     tot = rows[:, :31].sum()
+    per_cta = rows[:, :31].sum(axis=1)  # cycles each CTA spent from its first mark to its last
     out = [f"{title}: {len(rows)} CTAs, {steps / len(rows):.0f} steps per CTA, "
-           f"{tot / steps:.0f} cycles per step", "", "| stage | cycles per step | share |", "|---|---:|---:|"]
+           f"{tot / steps:.0f} cycles per step; cycles per CTA min / mean / max "
+           f"{per_cta.min() / 1e6:.1f} / {per_cta.mean() / 1e6:.1f} / {per_cta.max() / 1e6:.1f} M",
+           "", "| stage | cycles per step | share |", "|---|---:|---:|"]
     for i, n in enumerate(names):
         v = rows[:, i].sum()
         if v > 0:
