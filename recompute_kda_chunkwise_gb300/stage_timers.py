@@ -12,7 +12,7 @@ Thread 0 of every CTA reads clock64 at each stage mark and adds the cycles since
 its previous mark to that stage (shared-memory counters, written out once when
 the CTA exits). Each mark closes the stage it names, so waits are counted in
 the stage that ends with them. The marks add a few instructions per stage to
-thread 0; the kernels run somewhat slower in this build, so compare the
+thread 0; the kernels run somewhat slower in the tracing build, so compare the
 shares, not the absolute times.
 
 Roles: forward main CTAs (one per (sequence, head) item) and helper CTAs
