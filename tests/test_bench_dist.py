@@ -89,3 +89,21 @@ def test_reference_arm_prints_its_line(capsys):
         assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
         assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
         assert line["config"]["workload"] == name
+
+
+def test_traffic_records_follow_their_kernels_sources(monkeypatch):
+    import bench
+    # every recorded kernel family names its own sources, and each record is
+    # keyed by those files' current hash
+    rec = bench.ncu_traffic("kda_bwd_tc", "mbs1_128k_h96_d128_bf16")
+    assert rec is not None and rec > 29e9  # above the algorithmic 29.04 GB per launch
+    assert bench.ncu_traffic("kda_gdn2_bwd_simt", "gdn2_mbs8_8k_h16_d128_bf16") is not None
+    # a change to a kernel's own sources voids its record, and only its record
+    real = bench.kernel_files_hash
+    monkeypatch.setattr(bench, "kernel_files_hash",
+                        lambda k: "changed" if k == "kda_bwd_tc" else real(k))
+    assert bench.ncu_traffic("kda_bwd_tc", "mbs1_128k_h96_d128_bf16") is None
+    assert bench.ncu_traffic("kda_fwd_tc", "mbs1_128k_h96_d128_bf16") is not None
+    # unknown kernels and workloads have no record
+    assert bench.ncu_traffic("kda_bwd_tc", "no_such_workload") is None
+    assert bench.ncu_traffic("no_such_kernel", "mbs1_128k_h96_d128_bf16") is None
