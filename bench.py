@@ -97,10 +97,10 @@ def kernel_files_hash(kernel: str):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
+def ncu_traffic(kernel: str, workload: str, path: str = None):
     """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json),
     valid only while the kernel's own source files are unchanged since the capture."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = path or os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -347,7 +347,7 @@ def run_gb300_fwd(args, w, rank, world, local):
     gdn2 = w.gates == "channel"
     args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
     q, cu = inp["q"], inp["cu_seqlens"]
-    simt = K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0
+    simt = (K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0) | (K.KDA_FLAG_CHUNK16 if args.chunk16 else 0)
     fwd_fn = functools.partial(K.gdn2_fwd if gdn2 else K.kda_fwd, flags=simt)
     prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale,
                           flags=K.KDA_FLAG_NO_CHECKPOINTS | simt | (K.KDA_FLAG_CHANNEL_GATES if gdn2 else 0))
@@ -411,7 +411,8 @@ def run_gb300_fwd(args, w, rank, world, local):
                            "heads": w.H, "head_dim": w.D, "pass": "forward (inference)",
                            "l2_flush": "none needed: inputs (%.1f GB) exceed L2" % (fwd_b / 1e9)
                            if fwd_b > 2 * 129e6 else "inputs below L2 size: not flushed (context only)",
-                           "parallelism": f"replicas{world}", "kernel_family": kname},
+                           "parallelism": f"replicas{world}", "kernel_family": kname,
+                           "forward_chunk": 16 if args.chunk16 else (64 if kname.startswith("tc") else None)},
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
                              "frac": achieved / peak_gbs, "traffic": None, "kernel": f"{'kda_gdn2_fwd' if gdn2 else 'kda_fwd'} ({kname} kernels)",
                              "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": fwd_b,
@@ -505,7 +506,7 @@ def peak_only(args, w, local):
     inp = make_inputs(w, device=dev)
     gates = gate_names(w)
     args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
-    flags = K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0
+    flags = (K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0) | (K.KDA_FLAG_CHUNK16 if args.chunk16 else 0)
     gdn2 = w.gates == "channel"
     fwd_fn = functools.partial(K.gdn2_fwd if gdn2 else K.kda_fwd, flags=flags)
     bwd_fn = functools.partial(K.gdn2_bwd if gdn2 else K.kda_bwd, flags=flags)
@@ -523,6 +524,8 @@ def fresh_peaks(args, w, runs: int):
     cmd = [sys.executable, os.path.abspath(__file__), "--peak-only", "--workload", w.name]
     if args.force_simt:
         cmd.append("--force-simt")
+    if args.chunk16:
+        cmd.append("--chunk16")
     env = dict(os.environ, PYTORCH_CUDA_ALLOC_CONF="expandable_segments:False")
     for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
         env.pop(k, None)
@@ -554,7 +557,7 @@ def run_gb300(args, w, rank, world, local):
         bwd_fn = functools.partial(K.gdn2_bwd, flags=simt)
         flags = simt | K.KDA_FLAG_CHANNEL_GATES
     else:
-        flags = simt
+        flags = simt | (K.KDA_FLAG_CHUNK16 if args.chunk16 else 0)
         fwd_fn = functools.partial(K.kda_fwd, flags=flags)
         bwd_fn = functools.partial(K.kda_bwd, flags=flags)
     prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale, flags=flags)
@@ -764,7 +767,8 @@ def run_gb300(args, w, rank, world, local):
                            "heads": w.H, "head_dim": w.D, "scale": w.scale, "gate_lower_bound": -5.0,
                            "l2_flush": "none needed: inputs (%.1f GB) exceed L2" % (
                                (fwd_b + bwd_b) / 1e9 / 2),
-                           "parallelism": f"replicas{world}", "kernel_family": kname},
+                           "parallelism": f"replicas{world}", "kernel_family": kname,
+                           "forward_chunk": 16 if args.chunk16 else (64 if kname.startswith("tc") else None)},
                 "peak_alloc_gib": statistics.median(peaks), "peak_alloc_gib_runs": peaks,
                 "peak_alloc_protocol": "median over fresh processes, one fwd+bwd each, expandable_segments:False",
                 "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_ms_median": step_ms_median,
@@ -797,6 +801,8 @@ def main(argv=None):
     ap.add_argument("--peak-only", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--force-simt", action="store_true",
                     help="KDA workloads: run the fp32 CUDA-core kernels (KDA_FLAG_FORCE_SIMT) instead of tcgen05")
+    ap.add_argument("--chunk16", action="store_true",
+                    help="KDA workloads: the forward with 16-token chunks (KDA_FLAG_CHUNK16)")
     args = ap.parse_args(argv)
     from recompute_kda_chunkwise_gb300 import HEADLINE, WORKLOADS
     w = WORKLOADS[args.workload or HEADLINE]

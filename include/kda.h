@@ -100,6 +100,16 @@ typedef enum {
  * 128 (the CUDA-core kernels otherwise); the GDN-2 backward runs on the
  * fp32 CUDA-core kernels for every dtype and head_dim. */
 #define KDA_FLAG_CHANNEL_GATES 8
+/* kda_fwd with 16-token chunks ("KDA at the production shape ...", section
+ * 1.3: the chunk size of the FlashKDA and FLA forwards it compares) instead
+ * of the default 64-token chunks with 16-token sub-block references. It runs
+ * on the tensor cores for bf16 with head_dim 128 (KDA_ERR_UNSUPPORTED for
+ * other problems, with KDA_FLAG_FORCE_SIMT, or for GDN-2): one CTA per
+ * (sequence, head) at a time walks the chunks in order, with O = (Qh Gamma) H
+ * + M U~ per chunk, and stores the same checkpoints as the default forward
+ * (none with KDA_FLAG_NO_CHECKPOINTS), so its ctx feeds kda_bwd. Same outputs
+ * to within rounding. kda_bwd ignores the flag. */
+#define KDA_FLAG_CHUNK16 16
 
 /* Problem description. cu_seqlens is a DEVICE pointer; the library never
  * reads it on the host (so no synchronisation). It must start at 0, be
@@ -326,7 +336,7 @@ const char* kda_last_error_message(void);
  * -1 for an invalid or unsupported problem. Host only. */
 int kda_kernel_family(const kda_problem* p);
 
-/* Library ABI version, major * 100 + minor * 10 (220 = 2.2: the affine state prefix,
+/* Library ABI version, major * 100 + minor * 10 (230 = 2.3: KDA_FLAG_CHUNK16; 220 = 2.2: the affine state prefix,
  * the no-allocation status query and the device-side cu_seqlens check). */
 int kda_version(void);
 

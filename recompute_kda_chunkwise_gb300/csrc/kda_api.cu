@@ -35,7 +35,7 @@ kda_status validate(const kda_problem* p, bool need_ptrs = true) {
   if (p->num_heads < 1) return fail(KDA_ERR_INVALID_ARG, "num_heads must be >= 1 (got %d)", p->num_heads);
   if (p->total_tokens < 0) return fail(KDA_ERR_INVALID_ARG, "total_tokens must be >= 0");
   if ((p->flags & ~(KDA_FLAG_FORCE_SIMT | KDA_FLAG_TEST_TIMEOUT | KDA_FLAG_NO_CHECKPOINTS |
-                    KDA_FLAG_CHANNEL_GATES)) != 0)
+                    KDA_FLAG_CHANNEL_GATES | KDA_FLAG_CHUNK16)) != 0)
     return fail(KDA_ERR_INVALID_ARG, "unknown flags 0x%x", p->flags);
   if (need_ptrs && !p->cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is NULL");
   if (p->dtype != KDA_DTYPE_BF16 && p->dtype != KDA_DTYPE_F32)
@@ -199,7 +199,7 @@ int kda_kernel_family(const kda_problem* p) {
   return fwd_family_of(p) == family_of(p) ? family_of(p) : 2;
 }
 
-int kda_version(void) { return 220; }
+int kda_version(void) { return 230; }
 
 const char* kda_status_string(kda_status s) {
   switch (s) {
@@ -259,7 +259,13 @@ kda_status forward(const kda_problem* p, const void* q, const void* k, const voi
     st = kda::launch_check_cu(p->cu_seqlens, p->num_seqs, p->total_tokens, (int32_t*)a.cu, a.status, s);
     if (st != KDA_OK) return fail(st, "cu_seqlens check launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   }
-  st = fwd_family_of(p) == 1 ? kda::launch_fwd_tc(p, a, s) : kda::launch_fwd_simt(p, a, s);
+  if (p->flags & KDA_FLAG_CHUNK16) {  // 16-token chunks: tensor-core KDA problems only
+    if (fwd_family_of(p) != 1 || write_raw != nullptr)
+      return fail(KDA_ERR_UNSUPPORTED, "KDA_FLAG_CHUNK16 needs a KDA problem in bf16 with head_dim 128");
+    st = kda::launch_fwd16_tc(p, a, s);
+  } else {
+    st = fwd_family_of(p) == 1 ? kda::launch_fwd_tc(p, a, s) : kda::launch_fwd_simt(p, a, s);
+  }
   if (st != KDA_OK) return fail(st, "forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return KDA_OK;
 }

@@ -114,6 +114,8 @@ __device__ __forceinline__ void set_status(int* status, int code) {
 // Host-side launchers (defined in the kernel translation units).
 kda_status launch_fwd_simt(const kda_problem* p, const FwdArgs& a, cudaStream_t s);
 kda_status launch_fwd_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s);
+// the forward with 16-token chunks (KDA_FLAG_CHUNK16), on the backward kernel's stages
+kda_status launch_fwd16_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s);
 kda_status launch_bwd_simt(const kda_problem* p, const BwdArgs& a, cudaStream_t s);
 size_t bwd_scratch_bytes_simt(const kda_problem* p, int* nctas);
 kda_status launch_bwd_simt_ctas(const kda_problem* p, const BwdArgs& a, cudaStream_t s, int ctas);

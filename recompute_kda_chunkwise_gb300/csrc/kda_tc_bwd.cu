@@ -169,6 +169,11 @@ struct TcBwdArgs {
   int N, H;
   int helpers;  // > 0: CTAs N*H .. N*H+helpers-1 rebuild segment states for the others
   float scale, lower, eps;
+  // forward with 16-token chunks (kFwd): output, initial / final states
+  __nv_bfloat16* o;
+  const float* h0;   // [N][H][D][D] (NULL: zero)
+  float* hT;         // (NULL: not written)
+  float* ckpt_out;   // checkpoints written (NULL: inference, none)
 };
 
 __device__ __forceinline__ float sigm(float x) { return __fdividef(1.f, 1.f + ex2(-x * kLog2e)); }
@@ -300,7 +305,12 @@ __device__ __noinline__ void edge_dgamma_lo(const uint8_t* lo, uint32_t dh_tmem,
 // kEdge: the caller passes dhT or asks for dh0 (states in play), so the
 // first and last chunk of each sequence take dgamma's low-part term (the
 // instantiation without it is the stateless path, free of that code).
-template <bool kEdge>
+// kFwd: the forward with 16-token chunks. Each CTA walks its items' chunks in
+// order from h0 with the rebuild pass's stages, and per chunk also forms
+// O = (Qh Gamma) H + M U~ (the first product on tcgen05 beside the state
+// update, the second with 3xTF32 warp tiles) and, at every checkpoint
+// boundary, stores the chunk-start state.
+template <bool kEdge, bool kFwd>
 __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -421,10 +431,26 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
         acc_dtb = 0.f;
         acc_alog = 0.f;
         open = true;
-        seg = nseg - 1;
+        seg = kFwd ? 0 : nseg - 1;
         // dH' = dhT, the gradient of the final state, or zero (TMEM state and its
-        // fp16 operand copy; lane = value channel L, columns = key channel)
-        if (a.dhT != nullptr) {
+        // fp16 operand copy; lane = value channel L, columns = key channel); the
+        // forward starts H from h0 or zero instead
+        if constexpr (kFwd) {
+          const float* src = a.h0 != nullptr ? a.h0 + static_cast<int64_t>(item) * (kD * kD) : nullptr;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = src != nullptr ? src[(64 * hh + 32 * half + j) * kD + L] : 0.f;
+            tmem_st32(tmem + tlane + TM_H + 64 * hh + 32 * half, x);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+              *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
+                  make_uint4(pack_h2(x[8 * cc], x[8 * cc + 1]), pack_h2(x[8 * cc + 2], x[8 * cc + 3]),
+                             pack_h2(x[8 * cc + 4], x[8 * cc + 5]), pack_h2(x[8 * cc + 6], x[8 * cc + 7]));
+          }
+          tmem_st_wait();
+        } else if (a.dhT != nullptr) {
           const float* src = a.dhT + static_cast<int64_t>(item) * (kD * kD);
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
@@ -481,7 +507,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
 
     if (seg >= 0) {
       const int lv = nseg - 1 - seg;  // level: segments counted from the end
-      const int c0 = seg * kCPS, c1 = min(nchunks, c0 + kCPS);
+      // (the forward walks the whole sequence as one stretch)
+      const int c0 = kFwd ? 0 : seg * kCPS, c1 = kFwd ? nchunks : min(nchunks, c0 + kCPS);
       const bool rebuild = !split || helper;
       const uint32_t sbytes = split ? kSlotBytesSplit : kSlotBytesInline;
       // edge tile of chunk c (0: the sequence's first chunk, 1: its last)
@@ -502,25 +529,32 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
         KDA_SYNC_OR_BAIL();
         KDA_STAGE(BS_HANDOFF);
       }
-      if (rebuild) {
-        // ---- segment start state: checkpoint (fp32 [i][v]) -> TMEM H^T and fp16 A1 ----
-        const float* src = a.ckpt + (ckpt_slot(bos, n, seg) * a.H + h) * static_cast<int64_t>(kD * kD);
+      if constexpr (!kFwd) {  // (the forward starts from h0, set up at the item's start)
+        if (rebuild) {
+          // ---- segment start state: checkpoint (fp32 [i][v]) -> TMEM H^T and fp16 A1 ----
+          const float* src = a.ckpt + (ckpt_slot(bos, n, seg) * a.H + h) * static_cast<int64_t>(kD * kD);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float x[32];
+          for (int half = 0; half < 2; ++half) {
+            float x[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = src[(64 * hh + 32 * half + j) * kD + L];
-          tmem_st32(tmem + tlane + TM_H + 64 * hh + 32 * half, x);
+            for (int j = 0; j < 32; ++j) x[j] = src[(64 * hh + 32 * half + j) * kD + L];
+            tmem_st32(tmem + tlane + TM_H + 64 * hh + 32 * half, x);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
-                make_uint4(pack_h2(x[8 * cc], x[8 * cc + 1]), pack_h2(x[8 * cc + 2], x[8 * cc + 3]),
-                           pack_h2(x[8 * cc + 4], x[8 * cc + 5]), pack_h2(x[8 * cc + 6], x[8 * cc + 7]));
+            for (int cc = 0; cc < 4; ++cc)
+              *reinterpret_cast<uint4*>(sm + OFF_A1 + sw128_chunk(L, 8 * hh + 4 * half + cc, 128)) =
+                  make_uint4(pack_h2(x[8 * cc], x[8 * cc + 1]), pack_h2(x[8 * cc + 2], x[8 * cc + 3]),
+                             pack_h2(x[8 * cc + 4], x[8 * cc + 5]), pack_h2(x[8 * cc + 6], x[8 * cc + 7]));
+          }
+          tmem_st_wait();
+          if (kEdge && (c0 == 0 || c0 == nchunks - 1))  // a sequence-edge chunk starts at this checkpoint
+            edge_lo_from_global(edge_buf + (c0 == 0 ? 0 : kStateBytes), src, L, hh);
+          KDA_STAGE(BS_CKPT);
+          fence_async_smem();
+          fence_before_sync();
+          __syncthreads();
         }
-        tmem_st_wait();
-        if (kEdge && (c0 == 0 || c0 == nchunks - 1))  // a sequence-edge chunk starts at this checkpoint
-          edge_lo_from_global(edge_buf + (c0 == 0 ? 0 : kStateBytes), src, L, hh);
-        KDA_STAGE(BS_CKPT);
+      }
+      if constexpr (kFwd) {  // the state set up at the item's start feeds the first chunk's MMAs
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -530,12 +564,13 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
       // to scratch slot c - c0 before chunk c advances it); pass 1 walks the
       // chunks c1-1 .. c0 in reverse.
 #pragma unroll 1
-      for (int pass = rebuild ? 0 : 1; pass < (helper ? 1 : 2); ++pass) {
+      for (int pass = rebuild ? 0 : 1; pass < ((helper || kFwd) ? 1 : 2); ++pass) {
         const bool rev = pass == 1;
-        // a helper also walks the segment's last chunk (its Abar, T, T', M only)
-        const int nsteps = (rev || helper) ? c1 - c0 : c1 - c0 - 1;
+        // a helper also walks the segment's last chunk (its Abar, T, T', M only);
+        // the forward advances the state through every chunk
+        const int nsteps = (rev || helper || kFwd) ? c1 - c0 : c1 - c0 - 1;
         const bool prep = !(rev && split);  // this CTA builds Abar / M / T itself
-        const bool need_m = rev || helper;   // M is needed (reverse pass, or for it)
+        const bool need_m = rev || helper || kFwd;  // M is needed (reverse pass, or for it, or O)
         if (rev && !rebuild) {  // split mode: the last chunk's start state comes from scratch too
           if (tid == 0) {
             const uint8_t* slot = segbuf + static_cast<size_t>(c1 - 1 - c0) * sbytes;
@@ -578,7 +613,9 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
           }
           cp_async_commit();
           KDA_STAGE(BS_TILES_ISSUE);
-          if (!rev && tid == 0) bulk_store(segbuf + static_cast<size_t>(c - c0) * sbytes, sb + OFF_A1, kStateBytes);
+          if constexpr (!kFwd) {
+            if (!rev && tid == 0) bulk_store(segbuf + static_cast<size_t>(c - c0) * sbytes, sb + OFF_A1, kStateBytes);
+          }
           KDA_STAGE(BS_STATE_STORE);
           cp_async_wait_prev();
           KDA_STAGE(BS_TILES_WAIT);
@@ -664,6 +701,8 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                   st_h(sm + OFF_FQG, sw128_off(r, ci, 16), qg);
                   // bf16 -> fp16 is exact for these magnitudes
                   st_h(sm + OFF_FDO, sw128_off(r, ci, 16), stg(SDO, r, ci));
+                } else if constexpr (kFwd) {
+                  st_h(sm + OFF_FQG, sw128_off(r, ci, 16), qg);
                 }
               }
             }
@@ -721,6 +760,7 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
                 const float mv = s <= r ? d[e] : 0.f;
                 st_h(sm + OFF_FM, sw128_off(s, r, 16), mv);  // K-major B of dU~^T: row s, column r
                 st_h(sm + OFF_FML, sw128_off(s, r, 16), lo_part(mv));
+                if constexpr (kFwd) S[S_DM + r * kSq + s] = mv;  // fp32 M for the forward's M U~
               }
             }
             }
@@ -904,22 +944,69 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
               fence_after_sync();
               mma(tmem + TM_D2, desc_mn(D0, OFF_FU, 2048, 0), desc_mn(D0, OFF_FKB, 2048, 0),
                   idesc(128, 128, true, true), 0);
-              // the scratch copy of A1 has been read out (a helper's three -W / U~
-              // copies may still be in flight: the next step waits for those)
-              if (helper)
+              if constexpr (kFwd) {  // O^T's state part, H^T (Qh Gamma)^T (lane = v, columns r)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                  mma(tmem + TM_DQ, desc_k(D0, OFF_A1, 128, 0, ks), desc_k(D0, OFF_FQG, 16, 0, ks),
+                      idesc(128, 16), ks > 0);
+              } else if (helper) {
+                // the scratch copy of A1 has been read out (a helper's three -W / U~
+                // copies may still be in flight: the next step waits for those)
                 bulk_wait_read_but<3>();
-              else
+              } else {
                 bulk_wait_read();
+              }
               mma_commit(bar);
+            }
+            if constexpr (kFwd) {  // O's intra-chunk part M U~ (3xTF32, channels 16w .. 16w+15) into the dU~ tile
+              float mu[2][4] = {};
+#pragma unroll
+              for (int k0 = 0; k0 < kC; k0 += 8) {
+                float fa[4];
+                ldA(fa, S + S_DM, kSq, k0, fg, ft);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                  float fb[2];
+                  ldBr(fb, UT, kLd, 16 * warp + 8 * nt, k0, fg, ft);
+                  mma3(mu[nt], fa, fb);
+                }
+              }
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) {
+                const int i = 16 * warp + 8 * nt + 2 * ft;
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr)
+                  *reinterpret_cast<float2*>(DUT + (fg + 8 * hr) * kLd + i) = make_float2(mu[nt][2 * hr], mu[nt][2 * hr + 1]);
+              }
             }
             KDA_WAIT_MMA();
             KDA_STAGE(BS_REBUILD_MMA);
             fence_after_sync();
+            if constexpr (kFwd) {  // o = H^T (Qh Gamma)^T + (M U~)^T, rows 8 hh .. 8 hh + 7 of value channel L
+              __syncthreads();
+              float x[8];
+              tmem_ld8(tmem + tlane + TM_DQ + 8 * hh, x);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int r = 8 * hh + j;
+                if (r < rows) a.o[((t0 + r) * a.H + h) * kD + L] = __float2bfloat16_rn(x[j] + DUT[r * kLd + L]);
+              }
+            }
+            // the forward's checkpoint: the chunk-start state every kCPS chunks
+            float* ck = nullptr;
+            if constexpr (kFwd) {
+              if (a.ckpt_out != nullptr && c % kCPS == 0)
+                ck = a.ckpt_out + (ckpt_slot(bos, n, c / kCPS) * a.H + h) * static_cast<int64_t>(kD * kD);
+            }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               float hv[32], dv[32];
               tmem_ld32(tmem + tlane + TM_H + 64 * hh + 32 * half, hv);
               tmem_ld32(tmem + tlane + TM_D2 + 64 * hh + 32 * half, dv);
+              if (ck != nullptr) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ck[(64 * hh + 32 * half + j) * kD + L] = hv[j];
+              }
               const float4* g4 = reinterpret_cast<const float4*>(S + S_GAM + 64 * hh + 32 * half);
 #pragma unroll
               for (int j4 = 0; j4 < 8; ++j4) {
@@ -1338,6 +1425,22 @@ __global__ void __launch_bounds__(kT, 1) kda_bwd_tc_kernel(const TcBwdArgs a) {
       --seg;
       continue;
     }
+    if constexpr (kFwd) {  // ---- forward item done: its final state ----
+      if (a.hT != nullptr) {
+        float* dst = a.hT + static_cast<int64_t>(item) * (kD * kD);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float x[32];
+          tmem_ld32(tmem + tlane + TM_H + 64 * hh + 32 * half, x);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dst[(64 * hh + 32 * half + j) * kD + L] = x[j];
+        }
+      }
+      __syncthreads();
+      open = false;
+      item += gridDim.x;
+      continue;
+    }
     // ---- item done: the gradient of the initial state (dH of the first chunk's start) ----
     if (a.dh0 != nullptr) {
       float* dst = a.dh0 + static_cast<int64_t>(item) * (kD * kD);
@@ -1430,8 +1533,12 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   t.scale = a.scale;
   t.lower = a.lower;
   t.eps = a.eps;
+  t.o = nullptr;
+  t.h0 = nullptr;
+  t.hT = nullptr;
+  t.ckpt_out = nullptr;
   const bool edge = a.dhT != nullptr || a.dh0 != nullptr;
-  void (*kern)(const TcBwdArgs) = edge ? kda_bwd_tc_kernel<true> : kda_bwd_tc_kernel<false>;
+  void (*kern)(const TcBwdArgs) = edge ? kda_bwd_tc_kernel<true, false> : kda_bwd_tc_kernel<false, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
     return KDA_ERR_CUDA;
   // Split mode: with fewer (sequence, head) items than SMs, the spare SMs
@@ -1465,6 +1572,43 @@ kda_status launch_bwd_tc(const kda_problem* p, const BwdArgs& a, cudaStream_t s,
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   kda_param_reduce_tc_kernel<<<p->num_heads, 128, 0, s>>>(a.partial, p->num_seqs, p->num_heads, kD, a.dA_log,
                                                           a.ddt_bias);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+// The forward with 16-token chunks: the backward kernel's forward mode, one CTA
+// per SM walking its items' chunks in order (no helper CTAs, no scratch).
+kda_status launch_fwd16_tc(const kda_problem* p, const FwdArgs& a, cudaStream_t s) {
+  if (p->head_dim != kD || p->dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
+  TcBwdArgs t{};
+  t.q = static_cast<const __nv_bfloat16*>(a.q);
+  t.k = static_cast<const __nv_bfloat16*>(a.k);
+  t.v = static_cast<const __nv_bfloat16*>(a.v);
+  t.g = static_cast<const __nv_bfloat16*>(a.g);
+  t.b = static_cast<const __nv_bfloat16*>(a.b);
+  t.A_log = a.A_log;
+  t.dt_bias = a.dt_bias;
+  t.status = a.status;
+  t.cu = a.cu;
+  t.S = a.S;
+  t.N = a.N;
+  t.H = a.H;
+  t.helpers = 0;
+  t.scale = a.scale;
+  t.lower = a.lower;
+  t.eps = a.eps;
+  t.o = static_cast<__nv_bfloat16*>(a.o);
+  t.h0 = a.h0;
+  t.hT = a.hT;
+  t.ckpt_out = a.ckpt;
+  void (*kern)(const TcBwdArgs) = kda_bwd_tc_kernel<false, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  const int items = p->num_seqs * p->num_heads;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int ctas = items < sms ? items : sms;
+  if (ctas > 0) kern<<<ctas, kT, SMEM_BYTES, s>>>(t);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -96,6 +96,7 @@ KDA_FLAG_FORCE_SIMT = 1
 KDA_FLAG_TEST_TIMEOUT = 2  # test only: the forward's bounded wait runs out (see include/kda.h)
 KDA_FLAG_NO_CHECKPOINTS = 4  # inference: ctx holds no checkpoints (scratch for the forward only)
 KDA_FLAG_CHANNEL_GATES = 8  # GDN-2 problem (channel-wise erase / write gates)
+KDA_FLAG_CHUNK16 = 16  # kda_fwd with 16-token chunks (tensor-core KDA problems; see include/kda.h)
 
 
 def make_problem(total_tokens: int, num_seqs: int, num_heads: int, head_dim: int, dtype,

@@ -93,7 +93,7 @@ def test_invalid_arguments_are_rejected_on_host(lib):
     p.dtype = 7
     assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, nul, nul) == 2
     p.dtype = 0
-    p.flags = 16  # no such flag
+    p.flags = 32  # no such flag
     assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, nul, nul) == 1
     assert b"unknown flags" in lib.kda_last_error_message()
     p.flags = K.KDA_FLAG_FORCE_SIMT | K.KDA_FLAG_TEST_TIMEOUT  # both known: sizes still answer

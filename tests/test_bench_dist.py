@@ -91,19 +91,24 @@ def test_reference_arm_prints_its_line(capsys):
         assert line["config"]["workload"] == name
 
 
-def test_traffic_records_follow_their_kernels_sources(monkeypatch):
+def test_traffic_records_follow_their_kernels_sources(tmp_path, monkeypatch):
+    import json
     import bench
-    # every recorded kernel family names its own sources, and each record is
-    # keyed by those files' current hash
-    rec = bench.ncu_traffic("kda_bwd_tc", "mbs1_128k_h96_d128_bf16")
-    assert rec is not None and rec > 29e9  # above the algorithmic 29.04 GB per launch
-    assert bench.ncu_traffic("kda_gdn2_bwd_simt", "gdn2_mbs8_8k_h16_d128_bf16") is not None
+    # a record keyed by the current hash of its kernel family's own sources
+    # is used; every family names its sources
+    rec = {k: {"w": {"dram_bytes_per_launch": 1e9 + i, "source_hash": bench.kernel_files_hash(k)}}
+           for i, k in enumerate(bench.KERNEL_SOURCES)}
+    path = str(tmp_path / "traffic.json")
+    with open(path, "w") as f:
+        json.dump(rec, f)
+    for i, k in enumerate(bench.KERNEL_SOURCES):
+        assert bench.ncu_traffic(k, "w", path) == 1e9 + i
     # a change to a kernel's own sources voids its record, and only its record
     real = bench.kernel_files_hash
     monkeypatch.setattr(bench, "kernel_files_hash",
                         lambda k: "changed" if k == "kda_bwd_tc" else real(k))
-    assert bench.ncu_traffic("kda_bwd_tc", "mbs1_128k_h96_d128_bf16") is None
-    assert bench.ncu_traffic("kda_fwd_tc", "mbs1_128k_h96_d128_bf16") is not None
+    assert bench.ncu_traffic("kda_bwd_tc", "w", path) is None
+    assert bench.ncu_traffic("kda_fwd_tc", "w", path) is not None
     # unknown kernels and workloads have no record
-    assert bench.ncu_traffic("kda_bwd_tc", "no_such_workload") is None
-    assert bench.ncu_traffic("no_such_kernel", "mbs1_128k_h96_d128_bf16") is None
+    assert bench.ncu_traffic("kda_fwd_tc", "no_such_workload", path) is None
+    assert bench.ncu_traffic("no_such_kernel", "w", path) is None
