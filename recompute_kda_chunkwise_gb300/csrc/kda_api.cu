@@ -228,6 +228,9 @@ kda_status forward(const kda_problem* p, const void* q, const void* k, const voi
   kda_status st = validate(p);
   if (st != KDA_OK) return st;
   CHECK_OPT(h0); CHECK_OPT(hT);
+  // 16-token chunks: tensor-core KDA problems only (refused before any launch)
+  if ((p->flags & KDA_FLAG_CHUNK16) && (fwd_family_of(p) != 1 || write_raw != nullptr))
+    return fail(KDA_ERR_UNSUPPORTED, "KDA_FLAG_CHUNK16 needs a KDA problem in bf16 with head_dim 128");
   if (p->total_tokens == 0) return pass_state(hT, h0, p, (cudaStream_t)stream);  // hT = h0
   CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(g_raw); CHECK_PTR(beta_raw);
   CHECK_PTR(A_log); CHECK_PTR(dt_bias); CHECK_PTR(o);
@@ -259,13 +262,10 @@ kda_status forward(const kda_problem* p, const void* q, const void* k, const voi
     st = kda::launch_check_cu(p->cu_seqlens, p->num_seqs, p->total_tokens, (int32_t*)a.cu, a.status, s);
     if (st != KDA_OK) return fail(st, "cu_seqlens check launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   }
-  if (p->flags & KDA_FLAG_CHUNK16) {  // 16-token chunks: tensor-core KDA problems only
-    if (fwd_family_of(p) != 1 || write_raw != nullptr)
-      return fail(KDA_ERR_UNSUPPORTED, "KDA_FLAG_CHUNK16 needs a KDA problem in bf16 with head_dim 128");
+  if (p->flags & KDA_FLAG_CHUNK16)
     st = kda::launch_fwd16_tc(p, a, s);
-  } else {
+  else
     st = fwd_family_of(p) == 1 ? kda::launch_fwd_tc(p, a, s) : kda::launch_fwd_simt(p, a, s);
-  }
   if (st != KDA_OK) return fail(st, "forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return KDA_OK;
 }

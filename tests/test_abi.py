@@ -96,6 +96,13 @@ def test_invalid_arguments_are_rejected_on_host(lib):
     p.flags = 32  # no such flag
     assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, nul, nul) == 1
     assert b"unknown flags" in lib.kda_last_error_message()
+    # 16-token chunks: tensor-core KDA problems only, refused before any launch
+    # (this problem has head_dim 64; then bf16 D = 128 forced onto the CUDA cores)
+    p.flags = K.KDA_FLAG_CHUNK16
+    assert lib.kda_fwd(ctypes.byref(p), *([al] * 7), nul, al, nul, al, nul) == 2
+    assert b"CHUNK16" in lib.kda_last_error_message()
+    p128 = K.make_problem(16, 1, 2, 128, torch.bfloat16, cu, flags=K.KDA_FLAG_CHUNK16 | K.KDA_FLAG_FORCE_SIMT)
+    assert lib.kda_fwd(ctypes.byref(p128), *([al] * 7), nul, al, nul, al, nul) == 2
     p.flags = K.KDA_FLAG_FORCE_SIMT | K.KDA_FLAG_TEST_TIMEOUT  # both known: sizes still answer
     assert lib.kda_ctx_bytes(ctypes.byref(p)) > 0
     # inference: no checkpoints, so ctx shrinks to the status header and the
@@ -132,6 +139,11 @@ def test_gdn2_entry_points_and_flag_on_host(lib):
     p.flags = 0
     assert lib.kda_gdn2_fwd(ctypes.byref(p), *([al] * 8), nul, al, nul, al, nul) == 1
     assert b"KDA_FLAG_CHANNEL_GATES" in lib.kda_last_error_message()
+    # GDN-2 has no 16-token forward
+    g128 = K.make_problem(16, 1, 2, 128, torch.bfloat16, cu,
+                          flags=K.KDA_FLAG_CHANNEL_GATES | K.KDA_FLAG_CHUNK16)
+    assert lib.kda_gdn2_fwd(ctypes.byref(g128), *([al] * 8), nul, al, nul, al, nul) == 2
+    assert b"CHUNK16" in lib.kda_last_error_message()
     # kda_gdn2_bwd(p, q, k, v, g, erase, write, A_log, dt_bias, dO, dhT, ctx, dq, dk, dv, dg,
     #              derase, dwrite, dA_log, ddt_bias, dh0, workspace, stream)
     assert lib.kda_gdn2_bwd(ctypes.byref(p), *([al] * 9), nul, *([al] * 10), nul, al, nul) == 1
