@@ -331,6 +331,13 @@ FWD_METRIC = "KDA forward (inference, no checkpoints) tokens/sec"
 GDN2_FWD_METRIC = "GDN-2 forward (inference, no checkpoints) tokens/sec"
 
 
+def call_flags(args) -> int:
+    """The ABI flags the command line selects for the forward and backward calls
+    (the pass- and operator-specific ones are added where the problem is made)."""
+    from recompute_kda_chunkwise_gb300 import kda as K
+    return (K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0) | (K.KDA_FLAG_CHUNK16 if args.chunk16 else 0)
+
+
 def run_gb300_fwd(args, w, rank, world, local):
     """Forward-only inference: kda_fwd (kda_gdn2_fwd for a GDN-2 workload)
     with KDA_FLAG_NO_CHECKPOINTS (the ctx holds only the status word and the
@@ -347,7 +354,7 @@ def run_gb300_fwd(args, w, rank, world, local):
     gdn2 = w.gates == "channel"
     args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
     q, cu = inp["q"], inp["cu_seqlens"]
-    simt = (K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0) | (K.KDA_FLAG_CHUNK16 if args.chunk16 else 0)
+    simt = call_flags(args)
     fwd_fn = functools.partial(K.gdn2_fwd if gdn2 else K.kda_fwd, flags=simt)
     prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale,
                           flags=K.KDA_FLAG_NO_CHECKPOINTS | simt | (K.KDA_FLAG_CHANNEL_GATES if gdn2 else 0))
@@ -506,7 +513,7 @@ def peak_only(args, w, local):
     inp = make_inputs(w, device=dev)
     gates = gate_names(w)
     args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
-    flags = (K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0) | (K.KDA_FLAG_CHUNK16 if args.chunk16 else 0)
+    flags = call_flags(args)
     gdn2 = w.gates == "channel"
     fwd_fn = functools.partial(K.gdn2_fwd if gdn2 else K.kda_fwd, flags=flags)
     bwd_fn = functools.partial(K.gdn2_bwd if gdn2 else K.kda_bwd, flags=flags)
@@ -551,13 +558,13 @@ def run_gb300(args, w, rank, world, local):
     gdn2 = w.gates == "channel"
     args_in = [inp[n] for n in ["q", "k", "v", "g"] + gates + ["A_log", "dt_bias", "cu_seqlens"]]
     q, cu, dO = inp["q"], inp["cu_seqlens"], inp["dO"]
-    simt = K.KDA_FLAG_FORCE_SIMT if args.force_simt else 0
+    simt = call_flags(args)
     if gdn2:
         fwd_fn = functools.partial(K.gdn2_fwd, flags=simt)
         bwd_fn = functools.partial(K.gdn2_bwd, flags=simt)
         flags = simt | K.KDA_FLAG_CHANNEL_GATES
     else:
-        flags = simt | (K.KDA_FLAG_CHUNK16 if args.chunk16 else 0)
+        flags = simt
         fwd_fn = functools.partial(K.kda_fwd, flags=flags)
         bwd_fn = functools.partial(K.kda_bwd, flags=flags)
     prob = K.make_problem(w.total_tokens, w.num_seqs, w.H, w.D, q.dtype, cu, w.scale, flags=flags)
@@ -808,6 +815,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     from recompute_kda_chunkwise_gb300 import HEADLINE, WORKLOADS
     w = WORKLOADS[args.workload or HEADLINE]
+    if args.chunk16 and (w.gates == "channel" or args.pieces > 1):
+        ap.error("--chunk16 runs KDA workloads without --pieces (GDN-2 and the split have no 16-token forward)")
     rank, world, local = dist_setup()
     if args.peak_only:
         peak_only(args, w, local)

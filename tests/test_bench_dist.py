@@ -112,3 +112,18 @@ def test_traffic_records_follow_their_kernels_sources(tmp_path, monkeypatch):
     # unknown kernels and workloads have no record
     assert bench.ncu_traffic("kda_fwd_tc", "no_such_workload", path) is None
     assert bench.ncu_traffic("no_such_kernel", "w", path) is None
+
+
+def test_bench_flags_from_the_command_line():
+    import argparse
+    import bench
+    from recompute_kda_chunkwise_gb300 import kda as K
+    ns = argparse.Namespace
+    assert bench.call_flags(ns(force_simt=False, chunk16=False)) == 0
+    assert bench.call_flags(ns(force_simt=True, chunk16=False)) == K.KDA_FLAG_FORCE_SIMT
+    assert bench.call_flags(ns(force_simt=False, chunk16=True)) == K.KDA_FLAG_CHUNK16
+    # the 16-token forward exists for KDA only, and not in the context-parallel split
+    for extra in (["--workload", "gdn2_mbs8_8k_h16_d128_bf16"], ["--pieces", "2"]):
+        with pytest.raises(SystemExit) as e:
+            bench.main(["--chunk16", *extra])
+        assert e.value.code == 2
