@@ -406,9 +406,9 @@ class KDAFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(actx, q, k, v, g, beta, A_log, dt_bias, cu_seqlens, h0, output_final_state, scale,
-                lower_bound, eps):
+                lower_bound, eps, fwd_flags=0):
         r = kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, scale=scale, lower_bound=lower_bound,
-                    eps=eps, save_ctx=True, h0=h0, final_state=bool(output_final_state))
+                    eps=eps, save_ctx=True, h0=h0, final_state=bool(output_final_state), flags=fwd_flags)
         o, ctx = r[0], r[1]
         actx.save_for_backward(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, ctx)
         actx.args = (scale, lower_bound, eps, h0 is not None, bool(output_final_state))
@@ -422,14 +422,19 @@ class KDAFunction(torch.autograd.Function):
                     scale=scale, lower_bound=lower_bound, eps=eps,
                     dht=None if dht is None else dht.contiguous(), want_dh0=has_h0)
         return (r["dq"], r["dk"], r["dv"], r["dg"], r["dbeta"], r["dA_log"], r["ddt_bias"],
-                None, r.get("dh0"), None, None, None, None)
+                None, r.get("dh0"), None, None, None, None, None)
 
 
 def kda(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, scale: float = 1.0,
         lower_bound: float = -5.0, eps: float = 1e-6, initial_state=None,
-        output_final_state: bool = False):
+        output_final_state: bool = False, chunk_size: int = 64):
     """Differentiable KDA over packed sequences (see include/kda.h). With
     initial_state ([N, H, D, D] fp32) the recurrences start from it; with
-    output_final_state the call returns (o, final_state)."""
+    output_final_state the call returns (o, final_state). chunk_size 16
+    selects the forward with 16-token chunks (KDA_FLAG_CHUNK16: bf16, head_dim
+    128); the backward is the same either way."""
+    if chunk_size not in (16, 64):
+        raise ValueError(f"chunk_size must be 16 or 64 (got {chunk_size})")
     return KDAFunction.apply(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, initial_state,
-                             output_final_state, scale, lower_bound, eps)
+                             output_final_state, scale, lower_bound, eps,
+                             KDA_FLAG_CHUNK16 if chunk_size == 16 else 0)

@@ -24,6 +24,16 @@ def test_kda_refuses_cpu_tensors():
         K.kda_bwd_noalloc(*args, inp["dO"], None)
 
 
+def test_kda_autograd_checks_its_chunk_size_and_refuses_cpu_tensors():
+    inp = _cpu_inputs()
+    args = [inp[n] for n in ["q", "k", "v", "g", "beta", "A_log", "dt_bias", "cu_seqlens"]]
+    with pytest.raises(ValueError, match="chunk_size"):
+        K.kda(*args, chunk_size=32)
+    for c in (16, 64):
+        with pytest.raises(ValueError, match="CUDA"):
+            K.kda(*args, chunk_size=c)
+
+
 def test_gdn2_refuses_cpu_tensors():
     inp = _cpu_inputs("channel")
     args = [inp[n] for n in ["q", "k", "v", "g", "erase", "write", "A_log", "dt_bias", "cu_seqlens"]]

@@ -56,3 +56,22 @@ def test_chunk16_rejects_other_problems():
     with pytest.raises(K.KdaError) as e:
         K.kda_fwd(*_args(inp), flags=K.KDA_FLAG_CHUNK16 | K.KDA_FLAG_FORCE_SIMT)
     assert e.value.status == 2
+
+
+def test_chunk16_through_the_autograd_wrapper():
+    # kda(..., chunk_size=16) runs the 16-token forward and the default backward:
+    # the same bits as the direct calls
+    w = Workload("chunk16_autograd", (300, 77), 2, 128, "bf16", seed=8400, param_std=0.3)
+    inp = to_dev(make_inputs(w))
+    o_d, ctx = K.kda_fwd(*_args(inp), flags=K.KDA_FLAG_CHUNK16)
+    direct = K.kda_bwd(*_args(inp), inp["dO"], ctx)
+    leaves = {n: inp[n].clone().requires_grad_(True)
+              for n in ["q", "k", "v", "g", "beta", "A_log", "dt_bias"]}
+    o = K.kda(leaves["q"], leaves["k"], leaves["v"], leaves["g"], leaves["beta"], leaves["A_log"],
+              leaves["dt_bias"], inp["cu_seqlens"], chunk_size=16)
+    o.backward(inp["dO"])
+    torch.cuda.synchronize()
+    assert torch.equal(o.detach(), o_d)
+    for n, gname in [("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"),
+                     ("A_log", "dA_log"), ("dt_bias", "ddt_bias")]:
+        assert torch.equal(leaves[n].grad, direct[gname]), n
