@@ -149,6 +149,50 @@ def _check_tensors(q, *others, params=()):
             raise ValueError("A_log and dt_bias must be contiguous float32 CUDA tensors")
 
 
+def _check_shapes(q, same=(), beta=None, params=()):
+    """The kernels index every tensor by q's [S, H, D]: the activations in
+    ``same`` (name, tensor) must have that shape, beta [S, H], and the gate
+    parameters (A_log, dt_bias) [H] and [H, D]."""
+    if q.dim() != 3:
+        raise ValueError("q must be [S, H, D]")
+    S, H, D = q.shape
+    for name, t in same:
+        if tuple(t.shape) != (S, H, D):
+            raise ValueError(f"{name} must have q's shape {(S, H, D)} (got {tuple(t.shape)})")
+    if beta is not None and tuple(beta.shape) != (S, H):
+        raise ValueError(f"beta must be [S, H] = {(S, H)} (got {tuple(beta.shape)})")
+    if params:
+        A_log, dt_bias = params
+        if tuple(A_log.shape) != (H,) or tuple(dt_bias.shape) != (H, D):
+            raise ValueError(f"A_log must be [H] = {(H,)} and dt_bias [H, D] = {(H, D)}")
+
+
+def _check_like(t, ref, name):
+    """A caller-supplied output: the shape, dtype and device of ``ref``, contiguous."""
+    if (tuple(t.shape) != tuple(ref.shape) or t.dtype != ref.dtype or t.device != ref.device
+            or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous {ref.dtype} tensor of shape {tuple(ref.shape)} "
+                         f"on {ref.device}")
+
+
+def _check_buffer(t, nbytes, q, name):
+    """A ctx or workspace buffer: contiguous, on q's device, at least nbytes."""
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if (not t.is_cuda or t.device != q.device or not t.is_contiguous()
+            or t.numel() * t.element_size() < nbytes):
+        raise ValueError(f"{name} must be a contiguous CUDA buffer on {q.device} of at least {nbytes} bytes")
+
+
+def _bwd_ctx_bytes(p) -> int:
+    """Bytes of ctx the backward reads: the status header, the checked
+    cu_seqlens copy and the checkpoints (the CUDA-core family's ctx, which
+    has no forward hand-off area after them)."""
+    simt = KdaProblem.from_buffer_copy(p)
+    simt.flags |= KDA_FLAG_FORCE_SIMT
+    return ctx_bytes(simt)
+
+
 def _check_state(t, q, cu_seqlens, name):
     """States are fp32 [N, H, D, D] (rows: key channel), contiguous, on q's device."""
     if t is None:
@@ -177,6 +221,7 @@ def kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
     True (or a preallocated [N, H, D, D] fp32 tensor) the final states are
     returned too: (o, ctx, hT)."""
     _check_tensors(q, k, v, g, beta, params=(A_log, dt_bias))
+    _check_shapes(q, (("k", k), ("v", v), ("g", g)), beta, (A_log, dt_bias))
     _check_state(h0, q, cu_seqlens, "h0")
     if not save_ctx:
         flags |= KDA_FLAG_NO_CHECKPOINTS
@@ -185,11 +230,13 @@ def kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
     if final_state is not False and final_state is not None:
         hT = _state_like(q, cu_seqlens) if final_state is True else final_state
         _check_state(hT, q, cu_seqlens, "final_state")
+    if out is not None:
+        _check_like(out, q, "out")
     o = torch.empty_like(q) if out is None else out
     if ctx is None:
         ctx = torch.empty(ctx_bytes(p), dtype=torch.uint8, device=q.device)
-    elif ctx.numel() * ctx.element_size() < ctx_bytes(p):
-        raise ValueError("ctx buffer too small")
+    else:
+        _check_buffer(ctx, ctx_bytes(p), q, "ctx")
     st = load_library().kda_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                 _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(o), _ptr(hT), _ptr(ctx),
                                 _stream_handle(q.device))
@@ -200,10 +247,13 @@ def kda_fwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, *, scale: float = 1.0,
 
 
 def _grad_outs(outs, q, k, v, g, beta, A_log, dt_bias, cu_seqlens, want_dh0):
+    like = dict(dq=q, dk=k, dv=v, dg=g, dbeta=beta, dA_log=A_log, ddt_bias=dt_bias)
     if outs is None:
-        outs = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
-                    dg=torch.empty_like(g), dbeta=torch.empty_like(beta),
-                    dA_log=torch.empty_like(A_log), ddt_bias=torch.empty_like(dt_bias))
+        outs = {n: torch.empty_like(t) for n, t in like.items()}
+    for n, t in like.items():
+        if n not in outs:
+            raise ValueError(f"outs is missing {n}")
+        _check_like(outs[n], t, n)
     if want_dh0 and outs.get("dh0") is None:
         outs["dh0"] = _state_like(q, cu_seqlens)
     _check_state(outs.get("dh0"), q, cu_seqlens, "dh0")
@@ -218,13 +268,16 @@ def kda_bwd(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO, ctx, *, scale: flo
     states [N, H, D, D] fp32 (zero when None). ctx must come from a forward
     with the same h0."""
     _check_tensors(q, k, v, g, beta, dO, params=(A_log, dt_bias))
+    _check_shapes(q, (("k", k), ("v", v), ("g", g), ("dO", dO)), beta, (A_log, dt_bias))
     _check_state(dht, q, cu_seqlens, "dht")
     p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps, flags)
+    if q.shape[0] > 0:
+        _check_buffer(ctx, _bwd_ctx_bytes(p), q, "ctx")
     outs = _grad_outs(outs, q, k, v, g, beta, A_log, dt_bias, cu_seqlens, want_dh0)
     if workspace is None:
         workspace = torch.empty(workspace_bytes(p), dtype=torch.uint8, device=q.device)
-    elif workspace.numel() * workspace.element_size() < workspace_bytes(p):
-        raise ValueError("workspace buffer too small")
+    else:
+        _check_buffer(workspace, workspace_bytes(p), q, "workspace")
     st = load_library().kda_bwd(
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
         _ptr(dO), _ptr(dht), _ptr(ctx), _ptr(outs["dq"]), _ptr(outs["dk"]), _ptr(outs["dv"]),
@@ -242,8 +295,11 @@ def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, cu_seqlens, dO, ctx, *, sc
     memory at this point; calls must not overlap on the GPU). Returns the
     same dict as kda_bwd."""
     _check_tensors(q, k, v, g, beta, dO, params=(A_log, dt_bias))
+    _check_shapes(q, (("k", k), ("v", v), ("g", g), ("dO", dO)), beta, (A_log, dt_bias))
     _check_state(dht, q, cu_seqlens, "dht")
     p = _problem_from(q, beta, cu_seqlens, scale, lower_bound, eps)
+    if q.shape[0] > 0:
+        _check_buffer(ctx, _bwd_ctx_bytes(p), q, "ctx")
     outs = _grad_outs(outs, q, k, v, g, beta, A_log, dt_bias, cu_seqlens, want_dh0)
     st = load_library().kda_bwd_noalloc(
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
@@ -262,6 +318,8 @@ def gdn2_fwd(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, *, scale: flo
     sigmoid(write) on value channels; erase and write are [S, H, D] in q's
     dtype. Returns (o, ctx) or (o, ctx, hT) as kda_fwd does."""
     _check_tensors(q, k, v, g, erase, write, params=(A_log, dt_bias))
+    _check_shapes(q, (("k", k), ("v", v), ("g", g), ("erase", erase), ("write", write)), None,
+                  (A_log, dt_bias))
     _check_state(h0, q, cu_seqlens, "h0")
     flags |= KDA_FLAG_CHANNEL_GATES | (0 if save_ctx else KDA_FLAG_NO_CHECKPOINTS)
     p = _problem_from(q, None, cu_seqlens, scale, lower_bound, eps, flags)
@@ -269,11 +327,13 @@ def gdn2_fwd(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, *, scale: flo
     if final_state is not False and final_state is not None:
         hT = _state_like(q, cu_seqlens) if final_state is True else final_state
         _check_state(hT, q, cu_seqlens, "final_state")
+    if out is not None:
+        _check_like(out, q, "out")
     o = torch.empty_like(q) if out is None else out
     if ctx is None:
         ctx = torch.empty(ctx_bytes(p), dtype=torch.uint8, device=q.device)
-    elif ctx.numel() * ctx.element_size() < ctx_bytes(p):
-        raise ValueError("ctx buffer too small")
+    else:
+        _check_buffer(ctx, ctx_bytes(p), q, "ctx")
     st = load_library().kda_gdn2_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(erase),
                                      _ptr(write), _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(o), _ptr(hT),
                                      _ptr(ctx), _stream_handle(q.device))
@@ -290,20 +350,26 @@ def gdn2_bwd(q, k, v, g, erase, write, A_log, dt_bias, cu_seqlens, dO, ctx, *, s
     dwrite, dA_log, ddt_bias, and dh0 when want_dh0. ``flags`` must match
     the forward's (KDA_FLAG_FORCE_SIMT)."""
     _check_tensors(q, k, v, g, erase, write, dO, params=(A_log, dt_bias))
+    _check_shapes(q, (("k", k), ("v", v), ("g", g), ("erase", erase), ("write", write), ("dO", dO)),
+                  None, (A_log, dt_bias))
     _check_state(dht, q, cu_seqlens, "dht")
     p = _problem_from(q, None, cu_seqlens, scale, lower_bound, eps, flags | KDA_FLAG_CHANNEL_GATES)
+    if q.shape[0] > 0:
+        _check_buffer(ctx, _bwd_ctx_bytes(p), q, "ctx")
+    like = dict(dq=q, dk=k, dv=v, dg=g, derase=erase, dwrite=write, dA_log=A_log, ddt_bias=dt_bias)
     if outs is None:
-        outs = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
-                    dg=torch.empty_like(g), derase=torch.empty_like(erase),
-                    dwrite=torch.empty_like(write), dA_log=torch.empty_like(A_log),
-                    ddt_bias=torch.empty_like(dt_bias))
+        outs = {n: torch.empty_like(t) for n, t in like.items()}
+    for n, t in like.items():
+        if n not in outs:
+            raise ValueError(f"outs is missing {n}")
+        _check_like(outs[n], t, n)
     if want_dh0 and outs.get("dh0") is None:
         outs["dh0"] = _state_like(q, cu_seqlens)
     _check_state(outs.get("dh0"), q, cu_seqlens, "dh0")
     if workspace is None:
         workspace = torch.empty(workspace_bytes(p), dtype=torch.uint8, device=q.device)
-    elif workspace.numel() * workspace.element_size() < workspace_bytes(p):
-        raise ValueError("workspace buffer too small")
+    else:
+        _check_buffer(workspace, workspace_bytes(p), q, "workspace")
     st = load_library().kda_gdn2_bwd(
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(erase), _ptr(write), _ptr(A_log),
         _ptr(dt_bias), _ptr(dO), _ptr(dht), _ptr(ctx), _ptr(outs["dq"]), _ptr(outs["dk"]),
