@@ -11,14 +11,20 @@ A_log = dt_bias = 0, scale 1, 8192 tokens):
   U~ and Kbar of the state update);
 - with those plus single-pass tf32 operands in the Abar / M products, formed
   per 16-token column block referenced at the block's end, as the 64-token
-  forward forms them (the 16-token forward forms Abar / M from hi + lo tf32
-  parts, which this emulation takes as exact).
+  forward forms them: its fp32 operands go to the tf32 MMA as they are, and
+  a tf32 MMA reads fp32 data with the low 13 mantissa bits dropped
+  (truncation); rounding them to nearest first is the alternative compared
+  (the 16-token forward forms Abar / M from hi + lo tf32 parts, which this
+  emulation takes as exact).
 Each is stored as bf16 and measured the way the parity tests measure it:
 max(|x - ref| - half an ulp of ref) / RMS(ref).
 
 What it shows: the tf32 Abar / M operands, not the fp16 state operands, set
-the 64-token forward's output error (several times the fp16 share), and the
-16-token forward's scheme stays at the fp16 share; both sit below the 2e-2 bar.
+the 64-token forward's output error. Truncated, they give about 1e-2 of RMS
+on a head, the size the GPU parity runs measure (1.3e-2 on a 16-head sample
+of the long-context run); rounded to nearest they would give less than half
+of that; the fp16 operands together give under 1e-3, the share the 16-token
+forward's scheme stays at. All sit below the 2e-2 bar.
 """
 import numpy as np
 import pytest
@@ -36,6 +42,11 @@ def _tf32(x):
     b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
     r = ((b + 0xFFF + ((b >> 13) & 1)) >> 13) << 13
     return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _tf32_truncated(x):
+    b = np.asarray(x, dtype=np.float32).view(np.uint32)
+    return (b & np.uint32(0xFFFFE000)).view(np.float32).astype(np.float64)
 
 
 def _fp16(x):
@@ -111,8 +122,10 @@ def test_chunk_size_leaves_the_exact_output_unchanged(head):
 def test_tf32_abar_m_operands_set_the_64_token_forwards_output_error(head):
     ref = _forward(head, C64, _exact, _exact)
     fp16_only = _adjusted_error(_bf16(_forward(head, C64, _fp16, _exact)), ref)
-    with_tf32 = _adjusted_error(_bf16(_forward(head, C64, _fp16, _tf32)), ref)
+    rounded = _adjusted_error(_bf16(_forward(head, C64, _fp16, _tf32)), ref)
+    truncated = _adjusted_error(_bf16(_forward(head, C64, _fp16, _tf32_truncated)), ref)
     c16 = _adjusted_error(_bf16(_forward(head, C16, _fp16, _exact)), ref)
-    assert with_tf32 > 3.0 * fp16_only, (with_tf32, fp16_only)
-    assert with_tf32 > 3.0 * c16, (with_tf32, c16)
-    assert max(with_tf32, fp16_only, c16) < 2e-2
+    assert truncated > 1.5 * rounded, (truncated, rounded)
+    assert rounded > 3.0 * fp16_only, (rounded, fp16_only)
+    assert truncated > 5.0 * c16, (truncated, c16)
+    assert 5e-3 < truncated < 2e-2 and fp16_only < 1e-3 and c16 < 1e-3, (truncated, fp16_only, c16)
