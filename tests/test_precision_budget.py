@@ -1,4 +1,4 @@
-"""Error budget of the forward's operand roundings, from an fp64 emulation of
+"""Error budget of the kernels' operand roundings, from an fp64 emulation of
 the chunk algebra (not the kernels; CPU only).
 
 The output o = (Qh Gamma) H + M U~ of a chunk ("KDA at the production shape
@@ -25,6 +25,12 @@ on a head, the size the GPU parity runs measure (1.3e-2 on a 16-head sample
 of the long-context run); rounded to nearest they would give less than half
 of that; the fp16 operands together give under 1e-3, the share the 16-token
 forward's scheme stays at. All sit below the 2e-2 bar.
+
+The backward (16-token chunks) is emulated the same way, with its roundings
+grouped: the rebuilt chunk-start states kept as fp16 tiles, the fp16 copy of
+dH' in its products, the other fp16 state-product operands, the plain-tf32
+dV product, and the fp16 operands of the state rebuild. dv's error is the
+tf32 product's alone; dg's comes from the fp16 state side.
 """
 import numpy as np
 import pytest
@@ -129,3 +135,84 @@ def test_tf32_abar_m_operands_set_the_64_token_forwards_output_error(head):
     assert rounded > 3.0 * fp16_only, (rounded, fp16_only)
     assert truncated > 5.0 * c16, (truncated, c16)
     assert 5e-3 < truncated < 2e-2 and fp16_only < 1e-3 and c16 < 1e-3, (truncated, fp16_only, c16)
+
+
+def _backward(inp, dO_all, rH, rdH, rop, rdv, rupd):
+    """Gradients of the 16-token backward with its operand roundings: the
+    rebuilt chunk-start states as fp16 tiles (rH), the fp16 copy of dH' in
+    its products (rdH), the fp16 operands of the other state products (rop:
+    Kbar, Qh Gamma, -W, U~, dU~), the plain-tf32 dV = T'^T dU~ (rdv), and
+    the fp16 operands of the state rebuild (rupd). Returns dq, dk, dv, dg."""
+    q, k, v, a, b = inp
+    S = q.shape[0]
+
+    def chunk(t0):
+        sl = slice(t0, t0 + C16)
+        nq = np.sqrt((q[sl] ** 2).sum(1) + 1e-6)
+        nk = np.sqrt((k[sl] ** 2).sum(1) + 1e-6)
+        xq, xk = q[sl] / nq[:, None], k[sl] / nk[:, None]
+        sg = 1.0 / (1.0 + np.exp(-a[sl]))
+        beta = 1.0 / (1.0 + np.exp(-b[sl]))
+        G = np.cumsum(-5.0 * sg, axis=0)
+        c = dict(xq=xq, xk=xk, nq=nq, nk=nk, sg=sg, beta=beta, G=G, gam=np.exp(G[-1]), V=v[sl])
+        c["Qg"], c["Kg"] = xq * np.exp(G), xk * np.exp(G)
+        c["Ki"], c["Kb"] = xk * np.exp(-G), xk * np.exp(G[-1] - G)
+        c["Xw"], c["Xu"] = beta[:, None] * c["Kg"], beta[:, None] * c["V"]
+        c["M"] = np.tril(c["Qg"] @ c["Ki"].T)
+        c["T"] = np.linalg.inv(np.eye(C16) + np.tril(c["Xw"] @ c["Ki"].T, -1))
+        c["W"], c["U"] = c["T"] @ c["Xw"], c["T"] @ c["Xu"]
+        return c
+
+    starts, H = [], np.zeros((D, D))
+    for t0 in range(0, S, C16):
+        c = chunk(t0)
+        starts.append(H)
+        Ut = c["U"] + rupd(-c["W"]) @ rupd(H)
+        H = c["gam"][:, None] * H + rupd(c["Kb"]).T @ rupd(Ut)
+    out = {n: np.zeros((S, D)) for n in ("dq", "dk", "dv", "dg")}
+    dH = np.zeros((D, D))
+    for i in reversed(range(len(starts))):
+        t0 = i * C16
+        c, Hc, dO = chunk(t0), rH(starts[i]), dO_all[t0:t0 + C16]
+        Ut = c["U"] + rop(-c["W"]) @ Hc
+        dHo = rdH(dH)
+        dUt = c["M"].T @ dO + rop(c["Kb"]) @ dHo
+        dKb = rop(Ut) @ dHo.T
+        dgam = (Hc * dH).sum(1)
+        dW = -rop(dUt) @ Hc.T
+        dQg = dO @ Hc.T
+        dH = c["gam"][:, None] * dH + rop(c["Qg"]).T @ dO - rop(c["W"]).T @ rop(dUt)
+        dM = np.tril(dO @ Ut.T)
+        dT = np.tril(dW @ c["Xw"].T + dUt @ c["Xu"].T, -1)
+        dA = np.tril(-(c["T"].T @ dT @ c["T"].T), -1)
+        dXw = c["T"].T @ dW + dA @ c["Ki"]
+        dXu = rdv(c["T"].T) @ rdv(dUt)
+        dKi = dA.T @ c["Xw"] + dM.T @ c["Qg"]
+        dQg = dQg + dM @ c["Ki"]
+        dKg = c["beta"][:, None] * dXw
+        e, ei, eb = np.exp(c["G"]), np.exp(-c["G"]), np.exp(c["G"][-1] - c["G"])
+        dxq, dxk = dQg * e, dKg * e + dKi * ei + dKb * eb
+        dG = dQg * c["Qg"] + dKg * c["Kg"] - dKi * c["Ki"] - dKb * c["Kb"]
+        dg = np.cumsum(dG[::-1], 0)[::-1] + (dKb * c["Kb"]).sum(0) + dgam * c["gam"]
+        sl, xq, xk = slice(t0, t0 + C16), c["xq"], c["xk"]
+        out["dq"][sl] = (dxq - xq * (xq * dxq).sum(1, keepdims=True)) / c["nq"][:, None]
+        out["dk"][sl] = (dxk - xk * (xk * dxk).sum(1, keepdims=True)) / c["nk"][:, None]
+        out["dv"][sl] = c["beta"][:, None] * dXu
+        out["dg"][sl] = dg * -5.0 * c["sg"] * (1.0 - c["sg"])
+    return out
+
+
+def test_backward_error_sources(head):
+    # dv's error is its plain-tf32 product's; dg's comes from the fp16 state
+    # side (the rebuilt state tiles and the rebuild's fp16 operands), not
+    # from the tf32 product
+    rng = np.random.default_rng(20261)
+    dO = _bf16(rng.standard_normal((TOKENS, D)))
+    ref = _backward(head, dO, *([_exact] * 5))
+    err = lambda g: {n: _adjusted_error(_bf16(g[n]), ref[n]) for n in ref}
+    full = err(_backward(head, dO, _fp16, _fp16, _fp16, _tf32, _fp16))
+    dv_only = err(_backward(head, dO, _exact, _exact, _exact, _tf32, _exact))
+    no_dv = err(_backward(head, dO, _fp16, _fp16, _fp16, _exact, _fp16))
+    assert dv_only["dv"] > 0.8 * full["dv"] and no_dv["dv"] < 0.5 * full["dv"], (full, dv_only, no_dv)
+    assert no_dv["dg"] > 0.8 * full["dg"] and dv_only["dg"] < 1e-4 * full["dg"], (full, dv_only, no_dv)
+    assert max(full.values()) < 2e-2, full
